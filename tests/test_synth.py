@@ -1,0 +1,37 @@
+"""The seeded generators produce the documented storage formats and distributions."""
+import numpy as np
+
+from block_scaled_bit_gb300 import synth
+
+
+def test_shapes_dtypes_and_ranges():
+    c = synth.make_case("int4", "f16", 32, True, 64, 512, 3, 1)
+    assert c.W.shape == (64, 256) and c.W.dtype == np.uint8
+    assert c.scales.shape == (64, 16) and c.scales.dtype == np.uint16
+    s = c.scales.view(np.float16).astype(np.float64)
+    assert s.min() >= 0.005 * (1 - 2 ** -10) and s.max() <= 0.02 * (1 + 2 ** -10)
+    assert c.zp.shape == (64, 8) and c.A.shape == (3, 512)
+    c8 = synth.make_case("int8", "f16", 128, True, 32, 1024, 1, 2)
+    assert c8.zp.min() >= 120 and c8.zp.max() <= 136 and c8.scales.shape == (32, 8)
+    f8 = synth.make_case("fp8", "f16", 128, False, 16, 512, 1, 3)
+    assert f8.scales.dtype == np.float32 and f8.W.shape == (16, 512)
+    assert not np.isin(f8.W, [0x7F, 0xFF]).any(), "saturated, never NaN"
+    assert np.isin(f8.W, [0x7E, 0xFE]).any(), "N(0,1)*64 saturates at +-448 sometimes"
+    n4 = synth.make_case("nvfp4", "bf16", 16, False, 16, 256, 2, 4)
+    assert n4.scales.min() >= 0x18 and n4.scales.max() <= 0x58 and n4.gscale[0] == 1 / 64
+    assert n4.W.shape == (16, 128) and n4.scales.shape == (16, 16)
+
+
+def test_seeded_and_rows_independent_of_M():
+    a = synth.make_case("int8", "bf16", 32, True, 8, 256, 16, 9)
+    b = synth.make_case("int8", "bf16", 32, True, 8, 256, 4, 9)
+    assert np.array_equal(a.W, b.W) and np.array_equal(a.A[:4], b.A)
+    assert np.array_equal(a.with_M(2).A, a.A[:2])
+
+
+def test_config_enumeration():
+    shapes = synth.all_shapes()
+    assert len(synth.config_shapes(2)) == 10 and len(synth.config_shapes(3)) == 8
+    assert len({s.seed for s in shapes}) == len(shapes)
+    c1 = synth.config_shapes(1)[0]
+    assert (c1.N, c1.K, c1.block_size, c1.has_zp) == (1024, 512, 32, True)
