@@ -1,0 +1,412 @@
+// bsgemv_api.cu -- the C ABI declared in include/bsgemv.h (host code).
+//
+// A plan holds the geometry (fixed per problem and device), the device workspace of the
+// stream-K reduction (partials, arrival counters, error word) and a one-entry cache of the TMA
+// tensor maps for the last (A, W, scales, zp, M) seen.  bsgemv_run validates, encodes tensor
+// maps when the pointers change, and launches one kernel on the caller's stream.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "bsgemv_internal.h"
+
+struct bsgemv_plan_s {
+  bsg::Geometry geo;
+  int format = 0;
+  int device = -1;
+  int sm_count = 0;
+  int variant_override = 0, ctas_override = 0, stages_override = 0;
+  void* ws = nullptr;         // one allocation: partials | counters | error word
+  size_t ws_bytes = 0;
+  float* partials = nullptr;
+  unsigned* counters = nullptr;
+  unsigned* err = nullptr;
+  void* stage = nullptr;      // bsgemv_run_host staging for A and y
+  size_t stage_bytes = 0;
+  // tensor-map cache
+  bool cache_valid = false;
+  const void* c_A = nullptr;
+  const void* c_W = nullptr;
+  const void* c_S = nullptr;
+  const void* c_Z = nullptr;
+  int c_M = 0;
+  bsg::KParams params;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t dim0,
+              uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+              CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return BSGEMV_ERR_CUDA;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BSGEMV_OK : BSGEMV_ERR_CUDA;
+}
+
+int query_device(int* dev, int* sms) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BSGEMV_ERR_UNSUPPORTED;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BSGEMV_ERR_CUDA;
+  }
+  // The kernels are built for sm_103a only.
+  if (major != 10 || minor != 3) return BSGEMV_ERR_UNSUPPORTED;
+  return BSGEMV_OK;
+}
+
+// (Re)allocate the workspace for the plan's current geometry; zeroed.
+int alloc_workspace(bsgemv_plan_s* p) {
+  const bsgemv_geometry& g = p->geo.pub;
+  const size_t partial_bytes = size_t(g.ctas) * 2 * p->geo.slot_floats * sizeof(float);
+  const size_t counter_bytes = size_t(g.tiles) * sizeof(unsigned);
+  const size_t need = partial_bytes + counter_bytes + 256;
+  if (need > p->ws_bytes) {
+    if (p->ws) {
+      cudaDeviceSynchronize();
+      cudaFree(p->ws);
+      p->ws = nullptr;
+      p->ws_bytes = 0;
+    }
+    if (cudaMalloc(&p->ws, need) != cudaSuccess) {
+      cudaGetLastError();
+      return BSGEMV_ERR_CUDA;
+    }
+    p->ws_bytes = need;
+  }
+  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess) return BSGEMV_ERR_CUDA;
+  p->partials = static_cast<float*>(p->ws);
+  p->counters = reinterpret_cast<unsigned*>(static_cast<char*>(p->ws) + partial_bytes);
+  p->err = reinterpret_cast<unsigned*>(static_cast<char*>(p->ws) + partial_bytes + counter_bytes);
+  p->cache_valid = false;
+  return BSGEMV_OK;
+}
+
+int rebuild_geometry(bsgemv_plan_s* p) {
+  bsg::Geometry geo;
+  const int rc = bsg::compute_geometry(p->format, p->geo.block_size, p->geo.has_zp, p->geo.N,
+                                       p->geo.K, p->geo.max_M, p->sm_count, p->ctas_override,
+                                       p->stages_override, &geo);
+  if (rc != BSGEMV_OK) return rc;
+  p->geo = geo;
+  return alloc_workspace(p);
+}
+
+// Fill p->params for this call.  Tensor maps are re-encoded only when a pointer or M changes.
+int prepare_params(bsgemv_plan_s* p, const void* A, const void* W, const void* scales,
+                   const void* zp, void* y, int M) {
+  const bsg::Geometry& g = p->geo;
+  bsg::KParams& k = p->params;
+  const bool int_fmt = (g.fmt == bsg::kInt4 || g.fmt == bsg::kInt8);
+  const int64_t row_bytes = (g.fmt == bsg::kInt4 || g.fmt == bsg::kNvfp4) ? g.K / 2 : g.K;
+  const int scale_pitch = g.nb_s * g.scale_es;
+  const int zp_pitch = (g.fmt == bsg::kInt4) ? (g.nb_s + 1) / 2 : g.nb_s;
+  const bool side_scale = (scale_pitch % 16 == 0) && aligned(scales, 16);
+  const bool side_zp = int_fmt && g.has_zp && (zp_pitch % 16 == 0) && aligned(zp, 16);
+
+  if (!(p->cache_valid && p->c_A == A && p->c_W == W && p->c_S == scales && p->c_Z == zp &&
+        p->c_M == M)) {
+    int rc = encode_2d(&k.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, g.N, row_bytes,
+                       bsg::kStageRowBytes, bsg::kRowsPerTile, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != BSGEMV_OK) return rc;
+    rc = encode_2d(&k.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, A, g.K, M, g.K * 2, 64, M,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != BSGEMV_OK) return rc;
+    if (side_scale) {
+      const CUtensorMapDataType dt = g.scale_es == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : g.scale_es == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+      rc = encode_2d(&k.tm_s, dt, scales, g.nb_s, g.N, scale_pitch, g.sbw, bsg::kRowsPerTile,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc != BSGEMV_OK) return rc;
+    }
+    if (side_zp) {
+      rc = encode_2d(&k.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT8, zp, zp_pitch, g.N, zp_pitch,
+                     g.zbw_bytes, bsg::kRowsPerTile, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc != BSGEMV_OK) return rc;
+    }
+    p->cache_valid = true;
+    p->c_A = A;
+    p->c_W = W;
+    p->c_S = scales;
+    p->c_Z = zp;
+    p->c_M = M;
+  }
+  k.W = static_cast<const uint8_t*>(W);
+  k.scales = static_cast<const uint8_t*>(scales);
+  k.zp = int_fmt ? static_cast<const uint8_t*>(zp) : nullptr;
+  k.gscale = (g.fmt == bsg::kNvfp4) ? static_cast<const float*>(zp) : nullptr;
+  k.y = y;
+  k.partials = p->partials;
+  k.counters = p->counters;
+  k.err = p->err;
+  k.N = g.N;
+  k.K = g.K;
+  k.total_stages = g.pub.total_stages;
+  k.spt = g.pub.stages_per_tile;
+  k.M = M;
+  k.nb_s = g.nb_s;
+  int l2 = 0;
+  while ((1 << l2) < g.block_size) ++l2;
+  k.bs_log2 = l2;
+  k.scale_pitch = scale_pitch;
+  k.zp_pitch = zp_pitch;
+  k.stages = g.pub.stages;
+  k.slot_bytes = g.slot_bytes;
+  k.act_off = g.act_off;
+  k.sc_off = g.sc_off;
+  k.zp_off = g.zp_off;
+  k.act_box_bytes = g.act_box_bytes;
+  k.ring_bytes = g.ring_bytes;
+  k.red_off = g.red_off;
+  k.bar_off = g.bar_off;
+  k.sbw = g.sbw;
+  k.zbw_bytes = g.zbw_bytes;
+  k.zblk = g.zblk;
+  k.side_scale_tma = side_scale ? 1 : 0;
+  k.side_zp_tma = side_zp ? 1 : 0;
+  k.merge_pair = (g.block_size >= 2 * g.kpc) ? 1 : 0;
+  k.slot_floats = g.slot_floats;
+  k.tx_bytes = bsg::kRowsPerTile * bsg::kStageRowBytes + g.nbox * M * 128 +
+               (side_scale ? bsg::kRowsPerTile * g.sbw * g.scale_es : 0) +
+               (side_zp ? bsg::kRowsPerTile * g.zbw_bytes : 0);
+  return BSGEMV_OK;
+}
+
+int check_device(const bsgemv_plan_s* p) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) {
+    cudaGetLastError();
+    return BSGEMV_ERR_CUDA;
+  }
+  return cur == p->device ? BSGEMV_OK : BSGEMV_ERR_WRONG_DEVICE;
+}
+
+int validate_run(const bsgemv_plan_s* p, const void* A, const void* W, const void* scales,
+                 const void* zp, const void* y, int M) {
+  if (p == nullptr) return BSGEMV_ERR_INVALID_ARG;
+  const bsg::Geometry& g = p->geo;
+  if (M < 1) return BSGEMV_ERR_INVALID_ARG;
+  if (M > g.max_M) return BSGEMV_ERR_M_TOO_LARGE;
+  if (!A || !W || !scales || !y) return BSGEMV_ERR_INVALID_ARG;
+  if (g.fmt == bsg::kNvfp4 && zp == nullptr) return BSGEMV_ERR_INVALID_ARG;  // global scale
+  if ((g.fmt == bsg::kInt4 || g.fmt == bsg::kInt8) && g.has_zp && zp == nullptr)
+    return BSGEMV_ERR_INVALID_ARG;
+  if ((g.fmt == bsg::kInt4 || g.fmt == bsg::kInt8) && !g.has_zp && zp != nullptr)
+    return BSGEMV_ERR_INVALID_ARG;
+  if (g.fmt == bsg::kFp8 && zp != nullptr) return BSGEMV_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(y, 16)) return BSGEMV_ERR_MISALIGNED;
+  if (!aligned(scales, g.scale_es)) return BSGEMV_ERR_MISALIGNED;
+  if (g.fmt == bsg::kNvfp4 && !aligned(zp, 4)) return BSGEMV_ERR_MISALIGNED;
+  return BSGEMV_OK;
+}
+
+int launch(bsgemv_plan_s* p, cudaStream_t s) {
+  const bsg::Geometry& g = p->geo;
+  const bsg::KParams& k = p->params;
+  const int mt = k.M > 8 ? 2 : 1;
+  const int ctas = g.pub.ctas, smem = g.pub.smem_bytes;
+  switch (g.fmt) {
+    case bsg::kInt4:
+      return bsg::launch_int4(k, mt, g.bf16, g.has_zp, g.block_size == 16, ctas, smem, s);
+    case bsg::kInt8:
+      return bsg::launch_int8(k, mt, g.bf16, g.has_zp, ctas, smem, s);
+    case bsg::kFp8:
+      return bsg::launch_fp8(k, mt, g.bf16, ctas, smem, s);
+    case bsg::kNvfp4:
+      return bsg::launch_nvfp4(k, mt, g.bf16, ctas, smem, s);
+  }
+  return BSGEMV_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bsgemv_version(void) { return 100; }
+
+const char* bsgemv_status_string(int status) {
+  switch (status) {
+    case BSGEMV_OK: return "ok";
+    case BSGEMV_ERR_INVALID_ARG: return "invalid argument";
+    case BSGEMV_ERR_UNSUPPORTED: return "unsupported problem or device";
+    case BSGEMV_ERR_MISALIGNED: return "misaligned pointer";
+    case BSGEMV_ERR_M_TOO_LARGE: return "M exceeds the plan's max_M";
+    case BSGEMV_ERR_CUDA: return "CUDA error";
+    case BSGEMV_ERR_WRONG_DEVICE: return "current device is not the plan's device";
+    case BSGEMV_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a bounded wait";
+  }
+  return "unknown status";
+}
+
+int bsgemv_plan(bsgemv_plan_t* out, int format, int block_size, int has_zp, int64_t N, int64_t K,
+                int max_M) {
+  if (out == nullptr) return BSGEMV_ERR_INVALID_ARG;
+  *out = nullptr;
+  bsg::Geometry probe;
+  int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, max_M, 1, 0, 0, &probe);
+  if (rc != BSGEMV_OK) return rc;  // argument errors need no GPU
+  int dev = -1, sms = 0;
+  rc = query_device(&dev, &sms);
+  if (rc != BSGEMV_OK) return rc;
+  bsgemv_plan_s* p = new (std::nothrow) bsgemv_plan_s();
+  if (!p) return BSGEMV_ERR_CUDA;
+  p->format = format;
+  p->device = dev;
+  p->sm_count = sms;
+  p->geo = probe;
+  rc = rebuild_geometry(p);
+  if (rc != BSGEMV_OK) {
+    if (p->ws) cudaFree(p->ws);
+    delete p;
+    return rc;
+  }
+  *out = p;
+  return BSGEMV_OK;
+}
+
+int bsgemv_run(bsgemv_plan_t plan, const void* A, const void* W, const void* scales,
+               const void* zp, void* y, int M, void* stream) {
+  int rc = validate_run(plan, A, W, scales, zp, y, M);
+  if (rc != BSGEMV_OK) return rc;
+  rc = check_device(plan);
+  if (rc != BSGEMV_OK) return rc;
+  rc = prepare_params(plan, A, W, scales, zp, y, M);
+  if (rc != BSGEMV_OK) return rc;
+  return launch(plan, static_cast<cudaStream_t>(stream));
+}
+
+int bsgemv_run_host(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
+                    const void* zp, void* y_host, int M, void* stream) {
+  if (plan == nullptr || A_host == nullptr || y_host == nullptr) return BSGEMV_ERR_INVALID_ARG;
+  const bsg::Geometry& g = plan->geo;
+  if (M < 1) return BSGEMV_ERR_INVALID_ARG;
+  if (M > g.max_M) return BSGEMV_ERR_M_TOO_LARGE;
+  int rc = check_device(plan);
+  if (rc != BSGEMV_OK) return rc;
+  const size_t a_bytes = size_t(g.max_M) * g.K * 2;
+  const size_t a_pad = (a_bytes + 255) / 256 * 256;
+  const size_t need = a_pad + size_t(g.max_M) * g.N * 2;
+  if (plan->stage_bytes < need) {
+    if (plan->stage) cudaFree(plan->stage);
+    plan->stage = nullptr;
+    plan->stage_bytes = 0;
+    if (cudaMalloc(&plan->stage, need) != cudaSuccess) {
+      cudaGetLastError();
+      return BSGEMV_ERR_CUDA;
+    }
+    plan->stage_bytes = need;
+  }
+  void* dA = plan->stage;
+  void* dy = static_cast<char*>(plan->stage) + a_pad;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dA, A_host, size_t(M) * g.K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return BSGEMV_ERR_CUDA;
+  rc = bsgemv_run(plan, dA, W, scales, zp, dy, M, stream);
+  if (rc != BSGEMV_OK) return rc;
+  if (cudaMemcpyAsync(y_host, dy, size_t(M) * g.N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return BSGEMV_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
+}
+
+int bsgemv_destroy(bsgemv_plan_t plan) {
+  if (plan == nullptr) return BSGEMV_OK;
+  int rc = BSGEMV_OK;
+  if (plan->ws || plan->stage) {
+    if (cudaDeviceSynchronize() != cudaSuccess) rc = BSGEMV_ERR_CUDA;
+    if (plan->ws) cudaFree(plan->ws);
+    if (plan->stage) cudaFree(plan->stage);
+  }
+  delete plan;
+  return rc;
+}
+
+int bsgemv_debug_dequant(bsgemv_plan_t plan, const void* W, const void* scales, const void* zp,
+                         float* out, void* stream) {
+  if (plan == nullptr || W == nullptr || scales == nullptr || out == nullptr)
+    return BSGEMV_ERR_INVALID_ARG;
+  const bsg::Geometry& g = plan->geo;
+  if ((g.fmt == bsg::kNvfp4 || g.has_zp) && zp == nullptr) return BSGEMV_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(scales, g.scale_es)) return BSGEMV_ERR_MISALIGNED;
+  const int rc = check_device(plan);
+  if (rc != BSGEMV_OK) return rc;
+  return bsg::launch_debug_dequant(
+      g.fmt, g.bf16, g.has_zp, g.block_size, g.N, g.K, static_cast<const uint8_t*>(W),
+      static_cast<const uint8_t*>(scales),
+      (g.fmt == bsg::kInt4 || g.fmt == bsg::kInt8) ? static_cast<const uint8_t*>(zp) : nullptr,
+      g.fmt == bsg::kNvfp4 ? static_cast<const float*>(zp) : nullptr, out,
+      static_cast<cudaStream_t>(stream));
+}
+
+int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows_per_tile,
+                             int stages) {
+  if (plan == nullptr || variant < 0 || ctas < 0 || stages < 0 || rows_per_tile != 0)
+    return BSGEMV_ERR_INVALID_ARG;
+  if (variant == BSGEMV_VARIANT_CUDA_CORE) return BSGEMV_ERR_UNSUPPORTED;
+  if (variant > BSGEMV_VARIANT_CUDA_CORE) return BSGEMV_ERR_INVALID_ARG;
+  const int old_c = plan->ctas_override, old_s = plan->stages_override;
+  if (ctas) plan->ctas_override = ctas;
+  if (stages) plan->stages_override = stages;
+  const int rc = rebuild_geometry(plan);
+  if (rc != BSGEMV_OK) {
+    plan->ctas_override = old_c;
+    plan->stages_override = old_s;
+    rebuild_geometry(plan);
+  }
+  return rc;
+}
+
+int bsgemv_plan_describe(bsgemv_plan_t plan, bsgemv_geometry* g) {
+  if (plan == nullptr || g == nullptr) return BSGEMV_ERR_INVALID_ARG;
+  *g = plan->geo.pub;
+  return BSGEMV_OK;
+}
+
+int bsgemv_device_status(bsgemv_plan_t plan, void* stream) {
+  if (plan == nullptr) return BSGEMV_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BSGEMV_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, plan->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BSGEMV_ERR_CUDA;
+  if (word != 0) {
+    const unsigned zero = 0;
+    cudaMemcpy(plan->err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return BSGEMV_ERR_DEVICE_TIMEOUT;
+  }
+  return BSGEMV_OK;
+}
+
+}  // extern "C"

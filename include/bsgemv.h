@@ -1,0 +1,181 @@
+/*
+ * bsgemv.h -- C ABI of the fused dequantize-and-multiply small-M GEMV for one NVIDIA GB300
+ * (sm_103a):
+ *
+ *     y[M, N] = A[M, K] . deq(W)[N, K]^T,        1 <= M <= 16
+ *
+ * A is fp16 or bf16.  W is block-quantised along K and stored in the [N, blocks, blob] layout
+ * ("[CUDA] Batched small-M GEMV for MatMulNBits (4-bit/8-bit)", Description), in one of:
+ *
+ *   BSGEMV_INT4      4-bit codes, two per byte (low nibble = even k); deq = (q - zp) * s with an
+ *                    fp16 scale per (row, block) and an optional packed 4-bit zero point
+ *                    ("[CUDA] MatMulNBits 8-bit: wide fp16 M=1 kernel for decode GEMVs",
+ *                    Description; batched small-M page, Description and review)
+ *   BSGEMV_INT8      8-bit codes; deq = (q - zp) * s, fp16 scale, optional 8-bit zero point
+ *                    (wide M=1 page, Description)
+ *   BSGEMV_FP8_E4M3  E4M3 codes; deq = e4m3 * s with one fp32 scale per 128 k
+ *                    ("[CUDA] Block-scaled MatMul decode GEMV: tensor cores, packed FP4 decode
+ *                    and M-tiling", description, FP8 tensor-core paragraph)
+ *   BSGEMV_NVFP4     E2M1 codes two per byte (low nibble = even k), one E4M3 scale per 16 k and
+ *                    one fp32 global scale g; deq = e2m1 * e4m3 * g (same page, NVFP4
+ *                    tensor-core paragraph)
+ *
+ * Every call accumulates in fp32 and rounds the result once, round-to-nearest-even, to the
+ * activation dtype.  The library has no CPU fallback: without an sm_103a device every entry
+ * point that needs one returns an error.
+ *
+ * Layouts (all row-major, all tensors caller-owned):
+ *   A       [M, K] fp16/bf16, device memory, 16-byte aligned
+ *   W       int4/nvfp4: [N, K/2] bytes; int8/fp8: [N, K] bytes; device, 16-byte aligned
+ *   scales  int4/int8: fp16 [N, K/bs]; fp8: fp32 [N, K/128]; nvfp4: E4M3 bytes [N, K/16]
+ *   zp      int4: [N, ceil((K/bs)/2)] bytes, block b in nibble (b & 1) of byte b/2 (low nibble =
+ *           even block); int8: [N, K/bs] bytes; NULL when has_zp == 0 (implicit zero point 8
+ *           for int4, 128 for int8).  For NVFP4 this slot carries the device pointer of the one
+ *           fp32 global scale.  For FP8 it must be NULL.
+ *   y       [M, N] in the activation dtype, device memory, 16-byte aligned
+ *
+ * Streams are passed as `void*` holding a cudaStream_t (NULL = the legacy default stream).
+ * All entry points are host functions; bsgemv_run only enqueues work and never synchronises.
+ * A plan may be used by one stream at a time: its cross-CTA reduction workspace is shared by
+ * every call made with it.  Status codes are returned; no exception crosses the ABI.
+ */
+#ifndef BSGEMV_H_
+#define BSGEMV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct bsgemv_plan_s* bsgemv_plan_t; /* opaque; owned by the library */
+
+enum bsgemv_format {
+  BSGEMV_INT4 = 1,
+  BSGEMV_INT8 = 2,
+  BSGEMV_FP8_E4M3 = 3,
+  BSGEMV_NVFP4 = 4
+};
+/* OR-ed into `format`: the activations (and the output) are bf16 instead of fp16. */
+#define BSGEMV_ACT_BF16 0x100
+
+enum bsgemv_status {
+  BSGEMV_OK = 0,
+  BSGEMV_ERR_INVALID_ARG = -1,    /* NULL pointer, M out of range for the call, bad enum ... */
+  BSGEMV_ERR_UNSUPPORTED = -2,    /* shape / block size / format combination not provided,
+                                     or no sm_103a device */
+  BSGEMV_ERR_MISALIGNED = -3,     /* A, W or y not 16-byte aligned */
+  BSGEMV_ERR_M_TOO_LARGE = -4,    /* M > the plan's max_M */
+  BSGEMV_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed */
+  BSGEMV_ERR_WRONG_DEVICE = -6,   /* the current device is not the plan's device */
+  BSGEMV_ERR_DEVICE_TIMEOUT = -7  /* a kernel gave up a bounded wait (reported by
+                                     bsgemv_device_status) */
+};
+
+/* Variants a plan can run (bsgemv_geometry.variant, bsgemv_plan_set_override). */
+enum bsgemv_variant {
+  BSGEMV_VARIANT_AUTO = 0,
+  BSGEMV_VARIANT_MMA = 1,        /* tensor-core mma.sync m16n8k16, fp32 accumulate */
+  BSGEMV_VARIANT_CUDA_CORE = 2   /* CUDA-core fp32 FMA, rows of A tiled in registers */
+};
+
+/* What a plan chose.  Filled by bsgemv_plan_describe / bsgemv_geometry_for. */
+typedef struct {
+  int variant;           /* enum bsgemv_variant */
+  int rows_per_tile;     /* output columns n per CTA tile */
+  int k_per_stage;       /* k elements per pipeline stage */
+  int stages;            /* depth of the shared-memory ring */
+  int consumer_warps;    /* warps that decode and multiply; one more warp issues the copies */
+  int ctas;              /* persistent CTAs launched */
+  int ctas_per_sm;       /* CTAs resident per SM the geometry was sized for */
+  int sm_count;          /* SM count the geometry was derived for */
+  int64_t tiles;         /* ceil(N / rows_per_tile) */
+  int64_t stages_per_tile;
+  int64_t total_stages;  /* tiles * stages_per_tile: the work split evenly over the CTAs */
+  int smem_bytes;        /* dynamic shared memory per CTA */
+  int64_t workspace_bytes;
+} bsgemv_geometry;
+
+/*
+ * Create a plan for one weight shape.  format = enum bsgemv_format, optionally | BSGEMV_ACT_BF16.
+ * block_size: int4/int8 one of 16, 32, 64, 128, 256; fp8 128; nvfp4 16.
+ * has_zp: 0 or 1 (int formats only; must be 0 for fp8 and nvfp4).
+ * N >= 1 (any tail); K >= 64 with K % 64 == 0 and K % block_size == 0; 1 <= max_M <= 16.
+ * Uses the current CUDA device, which must be sm_103 (GB300).  Allocates the plan's own device
+ * workspace (cross-CTA partial sums, arrival counters and an error word, all zeroed here) with
+ * cudaMalloc; every call reuses it and the kernels leave the counters at zero.
+ * On success *out holds the plan; on error *out is NULL and a status < 0 is returned.
+ */
+int bsgemv_plan(bsgemv_plan_t* out, int format, int block_size, int has_zp, int64_t N, int64_t K,
+                int max_M);
+
+/*
+ * Enqueue y = A . deq(W)^T for the first M (1 <= M <= max_M) rows of A on `stream`.
+ * Pointers as in the layout table above (device memory).  Checks arguments, alignment and the
+ * current device, launches one kernel and returns cudaGetLastError's verdict; it does not wait.
+ * Results depend only on the plan and the inputs: the same row of A gives bit-identical
+ * output for every M, and repeated calls are bit-identical.
+ */
+int bsgemv_run(bsgemv_plan_t plan, const void* A, const void* W, const void* scales,
+               const void* zp, void* y, int M, void* stream);
+
+/*
+ * Same as bsgemv_run, but A and y are HOST memory (pinned memory gives asynchronous copies):
+ * A is copied into the plan's device staging buffer, the GEMV runs, y is copied back, and the
+ * call returns after the stream has finished (the host buffers are ready on return).  W,
+ * scales and zp stay device pointers.  The staging buffer (max_M * (K + N) activation
+ * elements) is allocated by the first call and freed by bsgemv_destroy.
+ */
+int bsgemv_run_host(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
+                    const void* zp, void* y_host, int M, void* stream);
+
+/* Free the plan and its device memory (synchronises the device first).  NULL is a no-op. */
+int bsgemv_destroy(bsgemv_plan_t plan);
+
+/* Static, human-readable name of a status code. */
+const char* bsgemv_status_string(int status);
+
+/*
+ * Test hook: write the dequantised weight deq(W) as fp32 [N, K] to `out` (device, caller-owned,
+ * N * K floats), through the same register decoders and fragment mapping as the GEMV.  Each
+ * value is the exact dequantised weight rounded once to fp32 (exact for int4/int8; for fp8 and
+ * nvfp4 one rounding of the exact product).  Enqueued on `stream`.
+ */
+int bsgemv_debug_dequant(bsgemv_plan_t plan, const void* W, const void* scales, const void* zp,
+                         float* out, void* stream);
+
+/*
+ * A/B override for measurements: variant (enum bsgemv_variant, 0 = keep), ctas (persistent
+ * CTAs, 0 = keep), rows_per_tile (reserved, must be 0), stages (ring depth, 0 = keep).
+ * Changes the summation order, so results are bit-identical only between calls made under the
+ * same settings.  Returns BSGEMV_ERR_UNSUPPORTED for a setting the plan cannot run.
+ */
+int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows_per_tile,
+                             int stages);
+
+/* Copy the plan's current geometry into *g. */
+int bsgemv_plan_describe(bsgemv_plan_t plan, bsgemv_geometry* g);
+
+/*
+ * Pure host function, no CUDA call: the geometry bsgemv_plan would choose for this problem on a
+ * device with `sm_count` SMs (and the sm_103 shared-memory budget).  Returns the same status
+ * bsgemv_plan would return for invalid arguments.
+ */
+int bsgemv_geometry_for(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
+                        int sm_count, bsgemv_geometry* g);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device error word.  Returns BSGEMV_OK,
+ * BSGEMV_ERR_DEVICE_TIMEOUT if a kernel of this plan abandoned a bounded wait since the last
+ * check, or BSGEMV_ERR_CUDA if the synchronisation failed.
+ */
+int bsgemv_device_status(bsgemv_plan_t plan, void* stream);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int bsgemv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSGEMV_H_ */

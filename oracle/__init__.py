@@ -175,3 +175,33 @@ def max_threads() -> int:
 
 def set_threads(n: int) -> None:
     lib().orc_set_threads(int(n))
+
+
+# ---------------------------------------------------------------------------- the parity bar
+def ulp(values: np.ndarray, act: str) -> np.ndarray:
+    """Spacing of the activation dtype at |values| (fp16: 10, bf16: 7 stored mantissa bits),
+    never below the smallest subnormal spacing."""
+    v = np.abs(np.asarray(values, dtype=np.float64))
+    mbits, qmin = (10, -24) if act == "f16" else (7, -133)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(v > 0, v, 1.0)))
+    q = np.exp2(np.maximum(e - mbits, qmin))
+    return np.where(v > 0, q, np.exp2(qmin))
+
+
+def tolerance_violations(case, ybits_gpu: np.ndarray, rows=None, M: int | None = None,
+                         rel: float = 1e-3):
+    """Compare GPU output bits [M, R] with the oracle on the same inputs.  The bar:
+        |y - y_ref| <= 1 ulp(|y_ref|) + rel * sum_k |a_k * w_k|
+    with y_ref the oracle's correctly rounded result; infinities must match exactly.
+    Returns (number of violations, max |y - y_ref| / bound, oracle bits)."""
+    ref_bits, _, absdot = gemv(case, rows=rows, M=M)
+    y = act_values(np.asarray(ybits_gpu), case.act)
+    r = act_values(ref_bits, case.act)
+    bound = ulp(r, case.act) + rel * absdot
+    finite = np.isfinite(r)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(y - r)
+    bad = np.where(finite, ~(err <= bound), ~((y == r) | (np.isnan(y) & np.isnan(r))))
+    worst = float(np.max(np.where(finite, err / bound, 0.0))) if r.size else 0.0
+    return int(bad.sum()), worst, ref_bits

@@ -1,0 +1,132 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point include/bsgemv.h
+declares, rejects bad arguments on the host, and its launch geometry (a pure host predicate) is
+a deterministic function of the problem and a fixed SM count."""
+import os
+import re
+
+import pytest
+
+from block_scaled_bit_gb300 import bsgemv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from block_scaled_bit_gb300 import _build
+    _build.build()
+    return bsgemv.lib()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "bsgemv.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsgemv_\w+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(L, name), name
+    assert set(names) == set(bsgemv.EXPORTS)
+
+
+def test_status_strings(L):
+    for code in range(-7, 1):
+        assert bsgemv.status_string(code) not in ("", "unknown status")
+    assert bsgemv.status_string(-99) == "unknown status"
+    assert L.bsgemv_version() >= 100
+
+
+@pytest.mark.parametrize("args,code", [
+    (("int4", "f16", 32, True, 0, 512, 1), bsgemv.ERR_INVALID_ARG),      # N = 0
+    (("int4", "f16", 32, True, 64, 512, 0), bsgemv.ERR_INVALID_ARG),     # max_M = 0
+    (("int4", "f16", 32, True, 64, 512, 17), bsgemv.ERR_INVALID_ARG),    # max_M > 16
+    (("int4", "f16", 48, True, 64, 512, 1), bsgemv.ERR_UNSUPPORTED),     # block size
+    (("int4", "f16", 32, True, 64, 544, 1), bsgemv.ERR_UNSUPPORTED),     # K % 64
+    (("fp8", "f16", 64, False, 64, 512, 1), bsgemv.ERR_UNSUPPORTED),     # fp8 needs 128
+    (("fp8", "f16", 128, True, 64, 512, 1), bsgemv.ERR_UNSUPPORTED),     # fp8 has no zp
+    (("nvfp4", "f16", 32, False, 64, 512, 1), bsgemv.ERR_UNSUPPORTED),   # nvfp4 needs 16
+])
+def test_invalid_problems_rejected_on_host(L, args, code):
+    fmt, act, bs, zp, N, K, mm = args
+    with pytest.raises(bsgemv.BsgemvError) as e:
+        bsgemv.geometry_for(fmt, act, bs, zp, N, K, mm, 152)
+    assert e.value.status == code
+    # bsgemv_plan validates its arguments before it touches CUDA
+    with pytest.raises(bsgemv.BsgemvError) as e:
+        bsgemv.Plan(fmt, act, bs, zp, N, K, mm)
+    assert e.value.status == code
+
+
+def test_bad_format_bits(L):
+    import ctypes
+    g = bsgemv.Geometry()
+    assert L.bsgemv_geometry_for(0x200 | 1, 32, 0, 64, 512, 1, 152, ctypes.byref(g)) == bsgemv.ERR_INVALID_ARG
+    assert L.bsgemv_geometry_for(5, 32, 0, 64, 512, 1, 152, ctypes.byref(g)) == bsgemv.ERR_INVALID_ARG
+    assert L.bsgemv_run(None, None, None, None, None, None, 1, None) == bsgemv.ERR_INVALID_ARG
+    assert L.bsgemv_destroy(None) == bsgemv.OK
+
+
+def test_plan_without_gpu_reports_unsupported(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(bsgemv.BsgemvError) as e:
+        bsgemv.Plan("int8", "f16", 128, True, 4096, 4096, 1)
+    assert e.value.status in (bsgemv.ERR_UNSUPPORTED, bsgemv.ERR_CUDA)
+
+
+# ---------------------------------------------------------------------------- geometry
+SHAPES = [("int4", 32, False, 151936, 4096), ("int8", 128, True, 2048, 4096),
+          ("int8", 32, True, 12288, 4096), ("fp8", 128, False, 512, 2048),
+          ("nvfp4", 16, False, 248320, 2048), ("int4", 32, True, 1024, 512),
+          ("int4", 16, True, 1, 64), ("int8", 256, False, 77, 768)]
+
+
+@pytest.mark.parametrize("fmt,bs,zp,N,K", SHAPES)
+@pytest.mark.parametrize("sms", [132, 148, 152])
+@pytest.mark.parametrize("max_M", [1, 8, 16])
+def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
+    g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, sms)
+    four = fmt in ("int4", "nvfp4")
+    assert g["k_per_stage"] == (256 if four else 128)
+    assert g["rows_per_tile"] == 64 and g["consumer_warps"] == 4
+    assert g["tiles"] == -(-N // 64)
+    assert g["stages_per_tile"] == -(-K // g["k_per_stage"])
+    assert g["total_stages"] == g["tiles"] * g["stages_per_tile"]
+    # persistent grid: never more CTAs than stages or than the resident slots
+    assert 1 <= g["ctas"] <= min(g["total_stages"], sms * g["ctas_per_sm"])
+    if g["total_stages"] >= sms * g["ctas_per_sm"]:
+        assert g["ctas"] == sms * g["ctas_per_sm"]
+    # shared memory fits the residency it was sized for
+    assert g["smem_bytes"] <= 232448
+    assert g["ctas_per_sm"] * (g["smem_bytes"] + 1024) <= 233472
+    assert 2 <= g["stages"] <= 8
+    assert g["sm_count"] == sms
+    # the same inputs give the same geometry; act dtype does not change it
+    assert bsgemv.geometry_for(fmt, "bf16", bs, zp, N, K, max_M, sms) == g
+
+
+def test_geometry_independent_of_call_M(L):
+    """The plan is fixed by max_M; M of a call never enters the geometry (row bit-identity)."""
+    a = bsgemv.geometry_for("int4", "f16", 32, False, 4096, 4096, 16, 152)
+    b = bsgemv.geometry_for("int4", "f16", 32, False, 4096, 4096, 9, 152)
+    assert a == b
+
+
+def test_stream_k_ranges_cover_every_stage_once():
+    """Pure arithmetic of the stream-K split used by the kernel: CTA i owns stages
+    [i*T//G, (i+1)*T//G); the CTA owning stage x is ceil((x+1)*G/T) - 1."""
+    for T in (1, 2, 7, 32, 64, 1000, 37984):
+        for G in sorted({g for g in (1, 2, 3, 304, 296, T) if g <= T}):
+            owner = []
+            for i in range(G):
+                s0, s1 = i * T // G, (i + 1) * T // G
+                assert s1 > s0
+                owner += [i] * (s1 - s0)
+            assert len(owner) == T
+            for x in range(0, T, max(1, T // 97)):
+                assert -(-((x + 1) * G) // T) - 1 == owner[x]

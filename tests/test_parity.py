@@ -1,0 +1,208 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on the same seeded
+inputs.
+
+The bar: the dequantisation stage is bit-exact (bsgemv_debug_dequant runs the GEMV's own
+register decoders); the GEMV output satisfies |y - y_ref| <= 1 ulp(|y_ref|) + 1e-3 sum|a*w| on
+every element; every row is bit-identical for every M of a plan; repeated calls are
+bit-identical.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from block_scaled_bit_gb300 import bsgemv, synth
+
+pytestmark = pytest.mark.gpu
+
+INT_BS = (16, 32, 64, 128, 256)
+DEQ_CASES = ([("int4", a, bs, z) for a in ("f16", "bf16") for bs in INT_BS for z in (True, False)]
+             + [("int8", a, bs, z) for a in ("f16", "bf16") for bs in INT_BS for z in (True, False)]
+             + [("fp8", a, 128, False) for a in ("f16", "bf16")]
+             + [("nvfp4", a, 16, False) for a in ("f16", "bf16")])
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    torch.cuda.set_device(0)
+    bsgemv.lib()
+    return torch
+
+
+def run(case, plan=None, M=None, max_M=16, stream=None):
+    """Upload, run through the C ABI, return output bits [M, N]."""
+    import torch
+    M = case.M if M is None else M
+    own = plan is None
+    if own:
+        plan = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K, max_M)
+    d = bsgemv.upload(case.with_M(M) if M != case.M else case, "cuda")
+    plan.run(d.A, d.W, d.scales, d.zp, d.y, M=M, stream=stream)
+    torch.cuda.synchronize()
+    assert plan.device_status() == bsgemv.OK
+    out = bsgemv.y_bits(d.y)
+    if own:
+        plan.close()
+    return out
+
+
+def assert_parity(case, ybits, rows=None):
+    bad, worst, ref = oracle.tolerance_violations(case, ybits if rows is None else ybits[:, rows], rows=rows)
+    assert bad == 0, f"{bad} outputs outside the bound (worst error/bound {worst:.3g})"
+    return worst
+
+
+# ---------------------------------------------------------------------------- decode stage
+@pytest.mark.parametrize("fmt,act,bs,zp", DEQ_CASES)
+def test_debug_dequant_is_bit_exact(torch_cuda, fmt, act, bs, zp):
+    torch = torch_cuda
+    K = max(1024, 4 * bs)
+    case = synth.make_case(fmt, act, bs, zp, 97, K, 1, 100 + bs)
+    d = bsgemv.upload(case, "cuda")
+    out = torch.full((case.N, case.K), float("nan"), dtype=torch.float32, device="cuda")
+    with bsgemv.Plan(fmt, act, bs, zp, case.N, case.K, 1) as plan:
+        plan.debug_dequant(d.W, d.scales, d.zp, out)
+        torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    want = oracle.dequant(case).astype(np.float32)   # exact value, rounded once to fp32
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------- GEMV parity
+PARITY_CASES = ([("int4", a, bs, z) for a in ("f16", "bf16") for bs in (16, 32, 128) for z in (True, False)]
+                + [("int8", a, bs, z) for a in ("f16", "bf16") for bs in (16, 32, 128, 256) for z in (True, False)]
+                + [("fp8", a, 128, False) for a in ("f16", "bf16")]
+                + [("nvfp4", a, 16, False) for a in ("f16", "bf16")])
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", PARITY_CASES)
+@pytest.mark.parametrize("M", [1, 5, 9, 16])
+def test_gemv_parity_ragged(torch_cuda, fmt, act, bs, zp, M):
+    # several tiles with a ragged last tile, several stages with a ragged last stage
+    K = 1536 if bs <= 256 else 2048
+    case = synth.make_case(fmt, act, bs, zp, 357, K, M, 7 * bs + M)
+    assert_parity(case, run(case))
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", [("int4", "f16", 32, True), ("int8", "bf16", 128, True),
+                                           ("fp8", "f16", 128, False), ("nvfp4", "bf16", 16, False),
+                                           ("int4", "bf16", 16, False)])
+def test_rows_bit_identical_across_M(torch_cuda, fmt, act, bs, zp):
+    case16 = synth.make_case(fmt, act, bs, zp, 300, 2048, 16, 55)
+    with bsgemv.Plan(fmt, act, bs, zp, case16.N, case16.K, 16) as plan:
+        y16 = run(case16, plan)
+        for M in range(1, 16):
+            yM = run(case16.with_M(M), plan)
+            assert np.array_equal(yM, y16[:M]), f"M={M}"
+    assert_parity(case16, y16)
+
+
+def test_repeated_calls_bit_identical_and_counters_reset(torch_cuda):
+    case = synth.make_case("int8", "f16", 32, True, 1000, 4096, 4, 77)
+    with bsgemv.Plan("int8", "f16", 32, True, case.N, case.K, 4) as plan:
+        # few CTAs for many stages: every tile is split over several CTAs
+        assert plan.set_override(ctas=37) == bsgemv.OK
+        first = run(case, plan)
+        for _ in range(3):
+            assert np.array_equal(run(case, plan), first)
+    assert_parity(case, first)
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 17, 64, 150, 10 ** 6])
+def test_every_stream_k_split_is_correct(torch_cuda, ctas):
+    case = synth.make_case("int4", "f16", 32, True, 777, 2048, 3, 91)
+    with bsgemv.Plan("int4", "f16", 32, True, case.N, case.K, 4) as plan:
+        assert plan.set_override(ctas=ctas) == bsgemv.OK
+        g = plan.describe()
+        assert g["ctas"] == min(ctas, g["total_stages"])
+        y = run(case, plan)
+    assert_parity(case, y)
+
+
+@pytest.mark.parametrize("stages", [2, 3, 8])
+def test_ring_depths(torch_cuda, stages):
+    case = synth.make_case("fp8", "bf16", 128, False, 500, 2048, 8, 93)
+    with bsgemv.Plan("fp8", "bf16", 128, False, case.N, case.K, 8) as plan:
+        assert plan.set_override(stages=stages) == bsgemv.OK
+        y = run(case, plan)
+    assert_parity(case, y)
+
+
+@pytest.mark.parametrize("fmt,bs,zp,N,K", [
+    ("int4", 32, True, 1, 64), ("int4", 16, True, 1, 64), ("int8", 64, True, 1, 64),
+    ("fp8", 128, False, 1, 128), ("nvfp4", 16, False, 1, 64), ("int4", 64, False, 65, 320),
+    ("int8", 32, True, 63, 192), ("nvfp4", 16, False, 129, 448), ("int4", 256, True, 2, 768),
+    ("int8", 256, True, 130, 256),
+])
+@pytest.mark.parametrize("M", [1, 16])
+def test_edge_shapes(torch_cuda, fmt, bs, zp, N, K, M):
+    case = synth.make_case(fmt, "f16", bs, zp, N, K, M, N + K)
+    assert_parity(case, run(case))
+
+
+def test_side_data_fallback_matches_tma(torch_cuda):
+    """Scales / zero points that cannot be TMA-tiled (misaligned base) are read from global
+    memory; the arithmetic is the same, so the output is bit-identical."""
+    torch = torch_cuda
+    case = synth.make_case("int8", "f16", 32, True, 300, 2048, 2, 5)
+    d = bsgemv.upload(case, "cuda")
+    with bsgemv.Plan("int8", "f16", 32, True, case.N, case.K, 2) as plan:
+        plan.run(d.A, d.W, d.scales, d.zp, d.y)
+        torch.cuda.synchronize()
+        ref = bsgemv.y_bits(d.y)
+        s2 = torch.empty(d.scales.numel() + 1, dtype=torch.int16, device="cuda")[1:]
+        s2.copy_(d.scales.view(-1))
+        z2 = torch.empty(d.zp.numel() + 3, dtype=torch.uint8, device="cuda")[3:]
+        z2.copy_(d.zp.view(-1))
+        assert s2.data_ptr() % 16 != 0 and z2.data_ptr() % 16 != 0
+        y2 = torch.empty_like(d.y)
+        plan.run(d.A, d.W, s2, z2, y2)
+        torch.cuda.synchronize()
+        assert plan.device_status() == bsgemv.OK
+    assert np.array_equal(bsgemv.y_bits(y2), ref)
+    assert_parity(case, ref)
+
+
+def test_run_host_matches_device_run(torch_cuda):
+    torch = torch_cuda
+    case = synth.make_case("nvfp4", "f16", 16, False, 2048, 2048, 3, 17)
+    d = bsgemv.upload(case, "cuda")
+    A_host = torch.from_numpy(case.A.view(np.int16)).pin_memory()
+    y_host = torch.empty((3, case.N), dtype=torch.int16).pin_memory()
+    with bsgemv.Plan("nvfp4", "f16", 16, False, case.N, case.K, 4) as plan:
+        plan.run_host(A_host, d.W, d.scales, d.zp, y_host, M=3)
+        plan.run(d.A, d.W, d.scales, d.zp, d.y)
+        torch.cuda.synchronize()
+    assert np.array_equal(y_host.numpy().view(np.uint16), bsgemv.y_bits(d.y))
+    assert_parity(case, bsgemv.y_bits(d.y))
+
+
+def test_errors_on_device(torch_cuda):
+    torch = torch_cuda
+    case = synth.make_case("int4", "f16", 32, True, 128, 512, 4, 3)
+    d = bsgemv.upload(case, "cuda")
+    with bsgemv.Plan("int4", "f16", 32, True, case.N, case.K, 4) as plan:
+        raw = torch.empty(d.A.numel() + 8, dtype=torch.int16, device="cuda")
+        A_mis = raw[1:1 + d.A.numel()].view(d.A.shape)
+        assert plan.run_status(A_mis, d.W, d.scales, d.zp, d.y) == bsgemv.ERR_MISALIGNED
+        assert plan.run_status(d.A, d.W, d.scales, d.zp, d.y, M=5) == bsgemv.ERR_M_TOO_LARGE
+        assert plan.run_status(d.A, d.W, d.scales, d.zp, d.y, M=0) == bsgemv.ERR_INVALID_ARG
+        assert plan.run_status(d.A, d.W, d.scales, None, d.y) == bsgemv.ERR_INVALID_ARG
+        assert plan.run_status(d.A, None, d.scales, d.zp, d.y) == bsgemv.ERR_INVALID_ARG
+        assert plan.set_override(variant=7) == bsgemv.ERR_INVALID_ARG
+        assert plan.device_status() == bsgemv.OK
+    with bsgemv.Plan("int8", "f16", 32, False, 64, 512, 1) as plan:
+        c8 = synth.make_case("int8", "f16", 32, False, 64, 512, 1, 4)
+        d8 = bsgemv.upload(c8, "cuda")
+        # a zero point given to a plan without zero points is an error, not ignored
+        assert plan.run_status(d8.A, d8.W, d8.scales, d.zp, d8.y) == bsgemv.ERR_INVALID_ARG
+
+
+def test_plan_records_device_and_geometry(torch_cuda):
+    torch = torch_cuda
+    with bsgemv.Plan("int4", "bf16", 32, False, 151936, 4096, 16) as plan:
+        g = plan.describe()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert g["sm_count"] == sms
+    assert g == bsgemv.geometry_for("int4", "bf16", 32, False, 151936, 4096, 16, sms)
