@@ -1,0 +1,550 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled small-M GEMV on GB300.
+
+Metric: achieved HBM GB/s on cold weights (algorithmic bytes W + scales + zp + A + y per call,
+divided by the device time of the call), with microseconds per call and the fraction of the
+measured HBM copy bandwidth.
+
+Default workload (one "step" = one pass of the hot path over the workload): the 8-bit
+MatMulNBits configuration -- int8 weights with zero points, fp16 activations, M = 1, block
+sizes 128 and 32, shapes (K x N) 2048x5120, 4096x2048, 4096x4096, 4096x12288, 12288x4096:
+ten GEMV calls per step.  Every shape has two weight copies used on alternate steps, so each
+call reads weights last touched 19 calls (~0.5 GB of other traffic, > 4x L2) earlier: the
+weights are cold.  The timed region replays a CUDA graph of 25 steps of back-to-back launches
+(programmatic dependent launch overlaps each call's start-up with the previous call's tail);
+a separate graph with an event between every launch gives per-call durations.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
+
+With --gpus N > 1 (launched under torchrun) every rank runs the same workload on its own GPU
+(independent replicas: the GEMV has no exchange step), the time is the maximum over ranks and
+the value is the bytes of all ranks over that time.  --impl reference times the CPU oracle on
+the host cores instead.  --sweep prints one JSON line per (configuration shape, M) with
+isolated-cold and streamed-cold timings.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "achieved HBM GB/s (cold weights) and µs/call vs M=1..16, fraction of HBM roofline"
+WORKLOAD_CONFIG = 2
+GRAPH_STEPS = 25
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--config", type=int, default=WORKLOAD_CONFIG, help=argparse.SUPPRESS)
+    ap.add_argument("--M", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--no-graph", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
+    ap.add_argument("--skip-cpu", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------ environment
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a float over the ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "block_scaled_bit_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+        if rec and rec.get("kernel_hash") == kernel_source_hash():
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9 and parts[1].isdigit():
+                        rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [int(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": int(statistics.median(sm)), "sm_max_mhz": int(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------------ our arm
+class Workload:
+    """Plans, device buffers (several weight copies) and host copies for one configuration."""
+
+    def __init__(self, config: int, M: int | None, device, copies: int):
+        from block_scaled_bit_gb300 import bsgemv, synth
+        self.items = []
+        for shape in synth.config_shapes(config):
+            m = M or shape.Ms[0]
+            case = shape.case(m)
+            plan = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K, 16)
+            bufs = [bsgemv.upload(case, device) for _ in range(copies)]
+            self.items.append({"shape": shape, "case": case, "M": m, "plan": plan, "bufs": bufs,
+                               "bytes": case.algorithmic_bytes(m)})
+        self.copies = copies
+
+    @property
+    def bytes_per_step(self) -> int:
+        return sum(it["bytes"] for it in self.items)
+
+    def launch(self, it, copy, stream=None):
+        b = it["bufs"][copy % self.copies]
+        it["plan"].run(b.A, b.W, b.scales, b.zp, b.y, M=it["M"], stream=stream)
+
+
+def capture(wl, stream, steps, with_events):
+    """CUDA graph of `steps` workload steps (optionally with timing events between launches)."""
+    import torch
+    L = len(wl.items)
+    events = None
+    if with_events:
+        events = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(steps * L + 1)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        i = 0
+        for s in range(steps):
+            for it in wl.items:
+                if events:
+                    events[i].record(stream)
+                    i += 1
+                wl.launch(it, s)
+        if events:
+            events[i].record(stream)
+    return graph, events
+
+
+def time_graph(wl, steps, warmup, stream, use_graph=True):
+    """Time `steps` steps (rounded up to whole graphs of GRAPH_STEPS steps) of back-to-back
+    launches; consecutive launches overlap start-up and tail (programmatic dependent launch).
+    Then, outside the timed region, one replay of a graph with an event between every launch
+    gives per-launch durations (events serialise the launches).
+    Returns (seconds, per-launch seconds of the instrumented replay, steps, launches)."""
+    import torch
+    L = len(wl.items)
+    S = GRAPH_STEPS
+    replays = max(1, -(-steps // S))
+    with torch.cuda.stream(stream):
+        for s in range(S):                # warm every plan and weight copy outside capture
+            for it in wl.items:
+                wl.launch(it, s)
+        stream.synchronize()
+    graph = inst = events = None
+    if use_graph:
+        try:
+            graph, _ = capture(wl, stream, S, False)
+            inst, events = capture(wl, stream, S, True)
+        except Exception as e:  # older torch: no external events in graphs
+            sys.stderr.write(f"[bench] graph capture unavailable ({e}); timing eager launches\n")
+            graph = inst = None
+    if events is None or inst is None:
+        events = [torch.cuda.Event(enable_timing=True) for _ in range(S * L + 1)]
+
+    def replay():
+        if graph is not None:
+            graph.replay()
+            return
+        for s in range(S):
+            for it in wl.items:
+                wl.launch(it, s, stream)
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, -(-warmup // S))):
+            replay()
+        stream.synchronize()
+        start.record(stream)
+        for _ in range(replays):
+            replay()
+        end.record(stream)
+        end.synchronize()
+        total = start.elapsed_time(end) / 1e3
+        # per-launch durations (not part of the timed region)
+        if inst is not None:
+            inst.replay()
+        else:
+            i = 0
+            for s in range(S):
+                for it in wl.items:
+                    events[i].record(stream)
+                    i += 1
+                    wl.launch(it, s, stream)
+            events[i].record(stream)
+        stream.synchronize()
+    per_launch = [events[i].elapsed_time(events[i + 1]) / 1e3 for i in range(S * L)]
+    return total, per_launch, replays * S, replays * S * L
+
+
+def e2e_run(wl, steps, stream):
+    """Through bsgemv_run_host: A copied host->device and y device->host inside every call."""
+    import numpy as np
+    import torch
+    hosts = []
+    for it in wl.items:
+        case = it["case"]
+        A = torch.from_numpy(np.ascontiguousarray(case.A[: it["M"]]).view(np.int16)).pin_memory()
+        y = torch.empty((it["M"], case.N), dtype=torch.int16).pin_memory()
+        hosts.append((A, y))
+    h2d = sum(A.numel() * 2 for A, _ in hosts)
+    d2h = sum(y.numel() * 2 for _, y in hosts)
+
+    def step(s):
+        for it, (A, y) in zip(wl.items, hosts):
+            b = it["bufs"][s % wl.copies]
+            it["plan"].run_host(A, b.W, b.scales, b.zp, y, M=it["M"], stream=stream)
+
+    for s in range(3):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(steps):
+        step(s)
+    dt = time.perf_counter() - t0
+    return dt, h2d, d2h
+
+
+def cpu_baseline(wl, seconds: float):
+    """The oracle as it stands, on the host cores, over the same workload until `seconds` of
+    work are done (whole steps; all shapes, all output columns)."""
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    done_bytes, reps = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        for it in wl.items:
+            oracle.gemv(it["case"], M=it["M"])
+            done_bytes += it["bytes"]
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} full pass(es) over the {len(wl.items)} GEMVs of the workload "
+                      f"(all output columns, M as timed), {dt:.1f} s, OpenMP over output columns"}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    from block_scaled_bit_gb300 import bsgemv
+    bsgemv.lib()
+    wl = Workload(args.config, args.M, device, copies=2)
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind = hbm_peak()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        barrier(world)
+        total, per_launch, steps_timed, launches = time_graph(wl, args.steps, args.warmup, stream,
+                                                              not args.no_graph)
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = clk.summary()
+    total = max_over_ranks(total, world, device)
+    step_bytes = wl.bytes_per_step
+    value = world * steps_timed * step_bytes / total / 1e9
+
+    # per-launch durations of the last replayed graph: L launches per step, GRAPH_STEPS steps
+    L = len(wl.items)
+    per_shape = []
+    for j, it in enumerate(wl.items):
+        d = [per_launch[s * L + j] for s in range(GRAPH_STEPS)]
+        us = statistics.median(d) * 1e6
+        per_shape.append({"shape": it["shape"].name, "M": it["M"], "us_per_call": round(us, 3),
+                          "GBps": round(it["bytes"] / (us * 1e-6) / 1e9, 1),
+                          "frac": round(it["bytes"] / (us * 1e-6) / 1e9 / peak, 4),
+                          "bytes": it["bytes"]})
+    # the dominant (only) kernel's average launch duration over the timed region: launches run
+    # back to back with start-up overlapped, so the region divided by its launches
+    mean_launch = total / launches
+    achieved = (step_bytes / L) / mean_launch / 1e9
+    workload = f"config{args.config}"
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(workload),
+                "peak_kind": f"{peak_kind} copy bandwidth", "kernel": "bsgemv_mma_kernel"}
+
+    e2e_dt, h2d, d2h = e2e_run(wl, max(20, min(400, args.steps // 10)), stream)
+    e2e_steps = max(20, min(400, args.steps // 10))
+    e2e_dt = max_over_ranks(e2e_dt, world, device)
+    e2e = {"value": round(world * e2e_steps * step_bytes / e2e_dt / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "api": "bsgemv_run_host (host A and y, device-resident weights), synchronous per call"}
+
+    out = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.skip_cpu:
+            cpu = cpu_baseline(wl, args.cpu_seconds)
+        shapes = [it["shape"] for it in wl.items]
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": steps_timed, "warmup": args.warmup,
+            "ms_per_step": round(total / steps_timed * 1e3, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "u8 weights (int8 + zp), f16 activations, f32 accumulate",
+            "data": "synthetic (seeded), no trained weights",
+            "config": {"workload": f"int8 MatMulNBits GEMV with zero points (config {args.config}): "
+                                   + ", ".join(f"{s.K}x{s.N} bs{s.block_size}" for s in shapes)
+                                   + f" (K x N), M={wl.items[0]['M']}, fp16",
+                       "calls_per_step": L, "bytes_per_step": step_bytes,
+                       "cold": "2 weight copies per shape on alternate steps: each call's weights "
+                               "were last read 19 calls (>0.5 GB, >4x L2) earlier; inputs larger than L2",
+                       "timing": f"CUDA graph of {GRAPH_STEPS} steps replayed, CUDA events on the launch stream "
+                                 "around the timed region; per_shape from a separate graph with an "
+                                 "event between every launch (serialised)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "roofline": roofline,
+            "fraction_of_nominal_7900_GBps": round(value / world / 7900.0, 4),
+            "per_shape": per_shape,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "impl": "ours",
+        }
+    if dist is not None:
+        dist.barrier()
+    for it in wl.items:
+        it["plan"].close()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------------------ sweep
+def run_sweep(args):
+    """Every configuration shape and M: isolated-cold (L2 flushed before each call, median of
+    repeats) and streamed-cold (graph of back-to-back calls over weight copies > 3x L2)."""
+    import torch
+    from block_scaled_bit_gb300 import bsgemv, synth
+    torch.cuda.set_device(0)
+    peak, _ = hbm_peak()
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(4 * l2 // 4, dtype=torch.int32, device="cuda")
+    cfgs = [args.config] if args.config != WORKLOAD_CONFIG or "--config" in sys.argv else [1, 2, 3, 4, 5]
+    for c in cfgs:
+        for shape in synth.config_shapes(c):
+            case = shape.case(max(shape.Ms))
+            foot = case.algorithmic_bytes(1)
+            copies = max(1, min(8, -(-3 * l2 // foot)))
+            bufs = [bsgemv.upload(case, "cuda") for _ in range(copies)]
+            with bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K, 16) as plan:
+                for M in shape.Ms:
+                    # isolated cold
+                    t = []
+                    with torch.cuda.stream(stream):
+                        for r in range(25):
+                            flush.add_(1)
+                            b = bufs[r % copies]
+                            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            e0.record(stream)
+                            plan.run(b.A[:M], b.W, b.scales, b.zp, b.y[:M], M=M, stream=stream)
+                            e1.record(stream)
+                            e1.synchronize()
+                            t.append(e0.elapsed_time(e1) * 1e3)
+                    iso = statistics.median(t[5:])
+                    # streamed cold: graph of back-to-back calls cycling through the copies
+                    reps = max(copies, 40 // copies * copies)
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.stream(stream):
+                        for r in range(copies):
+                            b = bufs[r]
+                            plan.run(b.A[:M], b.W, b.scales, b.zp, b.y[:M], M=M, stream=stream)
+                        stream.synchronize()
+                        with torch.cuda.graph(g, stream=stream):
+                            for r in range(reps):
+                                b = bufs[r % copies]
+                                plan.run(b.A[:M], b.W, b.scales, b.zp, b.y[:M], M=M, stream=stream)
+                        g.replay()
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        for _ in range(5):
+                            g.replay()
+                        e1.record(stream)
+                        e1.synchronize()
+                    streamed = e0.elapsed_time(e1) * 1e3 / (5 * reps)
+                    nbytes = case.algorithmic_bytes(M)
+                    print(json.dumps({
+                        "shape": shape.name, "config": c, "M": M, "bytes": nbytes,
+                        "us_isolated_cold": round(iso, 3), "us_streamed_cold": round(streamed, 3),
+                        "GBps_isolated": round(nbytes / iso / 1e3, 1),
+                        "GBps_streamed": round(nbytes / streamed / 1e3, 1),
+                        "frac_streamed": round(nbytes / streamed / 1e3 / peak, 4),
+                        "frac_isolated": round(nbytes / iso / 1e3 / peak, 4),
+                        "weight_copies": copies}), flush=True)
+                    del g
+            del bufs
+            torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The oracle (CPU, fp64) timed on the host cores on this workload; rank 0 only."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from block_scaled_bit_gb300 import synth
+    oracle.build()
+    cores = oracle.max_threads()
+    items = []
+    for shape in synth.config_shapes(args.config):
+        m = args.M or shape.Ms[0]
+        case = shape.case(m)
+        items.append((case, m, case.algorithmic_bytes(m)))
+    # each step: 16 output columns of every shape (a bounded sample); bytes pro rata
+    cols = 16
+    step_bytes = sum(b * cols / c.N for c, _, b in items)
+
+    def step(s):
+        for c, m, _ in items:
+            n0 = (s * cols) % max(1, c.N - cols)
+            oracle.gemv(c, rows=list(range(n0, n0 + cols)), M=m)
+
+    for s in range(max(3, args.warmup)):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(s)
+    dt = time.perf_counter() - t0
+    value = args.steps * step_bytes / dt / 1e9
+    out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64 (oracle)", "data": "synthetic (seeded), no trained weights",
+           "config": {"workload": f"config {args.config} (same shapes as the GPU arm)",
+                      "sample_per_step": f"{cols} output columns of each of the {len(items)} GEMVs"},
+           "impl": "reference",
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                            "sample": f"{cols} output columns per GEMV per step, {args.steps} steps"},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

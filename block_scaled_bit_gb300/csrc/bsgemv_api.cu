@@ -1,9 +1,9 @@
 // bsgemv_api.cu -- the C ABI declared in include/bsgemv.h (host code).
 //
 // A plan holds the geometry (fixed per problem and device), the device workspace of the
-// stream-K reduction (partials, arrival counters, error word) and a one-entry cache of the TMA
-// tensor maps for the last (A, W, scales, zp, M) seen.  bsgemv_run validates, encodes tensor
-// maps when the pointers change, and launches one kernel on the caller's stream.
+// stream-K reduction (partials, arrival counters, error word) and a small cache of the weight's
+// TMA tensor maps.  bsgemv_run validates, encodes a tensor map when W changes, and launches one
+// kernel on the caller's stream.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -27,13 +27,16 @@ struct bsgemv_plan_s {
   unsigned* err = nullptr;
   void* stage = nullptr;      // bsgemv_run_host staging for A and y
   size_t stage_bytes = 0;
-  // tensor-map cache
-  bool cache_valid = false;
-  const void* c_A = nullptr;
-  const void* c_W = nullptr;
-  const void* c_S = nullptr;
-  const void* c_Z = nullptr;
-  int c_M = 0;
+  // weight tensor-map cache: the last few W pointers seen (e.g. rotating weight copies)
+  struct MapEntry {
+    bool valid = false;
+    const void* W = nullptr;
+    unsigned last_use = 0;
+    CUtensorMap tm_w;
+  };
+  static constexpr int kMapCache = 4;
+  MapEntry maps[kMapCache];
+  unsigned use_clock = 0;
   bsg::KParams params;
 };
 
@@ -110,7 +113,6 @@ int alloc_workspace(bsgemv_plan_s* p) {
   p->partials = static_cast<float*>(p->ws);
   p->counters = reinterpret_cast<unsigned*>(static_cast<char*>(p->ws) + partial_bytes);
   p->err = reinterpret_cast<unsigned*>(static_cast<char*>(p->ws) + partial_bytes + counter_bytes);
-  p->cache_valid = false;
   return BSGEMV_OK;
 }
 
@@ -124,7 +126,7 @@ int rebuild_geometry(bsgemv_plan_s* p) {
   return alloc_workspace(p);
 }
 
-// Fill p->params for this call.  Tensor maps are re-encoded only when a pointer or M changes.
+// Fill p->params for this call.  The weight tensor map is re-encoded only for a new W pointer.
 int prepare_params(bsgemv_plan_s* p, const void* A, const void* W, const void* scales,
                    const void* zp, void* y, int M) {
   const bsg::Geometry& g = p->geo;
@@ -136,34 +138,29 @@ int prepare_params(bsgemv_plan_s* p, const void* A, const void* W, const void* s
   const bool side_scale = (scale_pitch % 16 == 0) && aligned(scales, 16);
   const bool side_zp = int_fmt && g.has_zp && (zp_pitch % 16 == 0) && aligned(zp, 16);
 
-  if (!(p->cache_valid && p->c_A == A && p->c_W == W && p->c_S == scales && p->c_Z == zp &&
-        p->c_M == M)) {
-    int rc = encode_2d(&k.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, g.N, row_bytes,
-                       bsg::kStageRowBytes, bsg::kRowsPerTile, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (rc != BSGEMV_OK) return rc;
-    rc = encode_2d(&k.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, A, g.K, M, g.K * 2, 64, M,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
-    if (rc != BSGEMV_OK) return rc;
-    if (side_scale) {
-      const CUtensorMapDataType dt = g.scale_es == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                     : g.scale_es == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
-                                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-      rc = encode_2d(&k.tm_s, dt, scales, g.nb_s, g.N, scale_pitch, g.sbw, bsg::kRowsPerTile,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
-      if (rc != BSGEMV_OK) return rc;
+  bsgemv_plan_s::MapEntry* hit = nullptr;
+  for (auto& e : p->maps)
+    if (e.valid && e.W == W) hit = &e;
+  if (hit == nullptr) {
+    // an empty entry if there is one, else the least recently used
+    for (auto& e : p->maps)
+      if (!e.valid) { hit = &e; break; }
+    if (hit == nullptr) {
+      hit = &p->maps[0];
+      for (auto& e : p->maps)
+        if (e.last_use < hit->last_use) hit = &e;
     }
-    if (side_zp) {
-      rc = encode_2d(&k.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT8, zp, zp_pitch, g.N, zp_pitch,
-                     g.zbw_bytes, bsg::kRowsPerTile, CU_TENSOR_MAP_SWIZZLE_NONE);
-      if (rc != BSGEMV_OK) return rc;
-    }
-    p->cache_valid = true;
-    p->c_A = A;
-    p->c_W = W;
-    p->c_S = scales;
-    p->c_Z = zp;
-    p->c_M = M;
+    hit->valid = false;
+    const int rc = encode_2d(&hit->tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, g.N,
+                             row_bytes, bsg::kStageRowBytes, bsg::kRowsPerTile,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != BSGEMV_OK) return rc;
+    hit->valid = true;
+    hit->W = W;
   }
+  hit->last_use = ++p->use_clock;
+  k.tm_w = hit->tm_w;
+  k.A = static_cast<const uint16_t*>(A);
   k.W = static_cast<const uint8_t*>(W);
   k.scales = static_cast<const uint8_t*>(scales);
   k.zp = int_fmt ? static_cast<const uint8_t*>(zp) : nullptr;
@@ -197,11 +194,8 @@ int prepare_params(bsgemv_plan_s* p, const void* A, const void* W, const void* s
   k.zblk = g.zblk;
   k.side_scale_tma = side_scale ? 1 : 0;
   k.side_zp_tma = side_zp ? 1 : 0;
-  k.merge_pair = (g.block_size >= 2 * g.kpc) ? 1 : 0;
   k.slot_floats = g.slot_floats;
-  k.tx_bytes = bsg::kRowsPerTile * bsg::kStageRowBytes + g.nbox * M * 128 +
-               (side_scale ? bsg::kRowsPerTile * g.sbw * g.scale_es : 0) +
-               (side_zp ? bsg::kRowsPerTile * g.zbw_bytes : 0);
+  k.tx_bytes = bsg::kRowsPerTile * bsg::kStageRowBytes;
   return BSGEMV_OK;
 }
 
@@ -238,15 +232,17 @@ int launch(bsgemv_plan_s* p, cudaStream_t s) {
   const bsg::KParams& k = p->params;
   const int mt = k.M > 8 ? 2 : 1;
   const int ctas = g.pub.ctas, smem = g.pub.smem_bytes;
+  const int bm = bsg::block_mode(g.fmt, g.block_size);
   switch (g.fmt) {
     case bsg::kInt4:
-      return bsg::launch_int4(k, mt, g.bf16, g.has_zp, g.block_size == 16, ctas, smem, s);
+      return g.bf16 ? bsg::launch_int4_bf16(k, mt, g.has_zp, bm, ctas, smem, s)
+                    : bsg::launch_int4_f16(k, mt, g.has_zp, bm, ctas, smem, s);
     case bsg::kInt8:
-      return bsg::launch_int8(k, mt, g.bf16, g.has_zp, ctas, smem, s);
+      return bsg::launch_int8(k, mt, g.bf16, g.has_zp, bm, ctas, smem, s);
     case bsg::kFp8:
-      return bsg::launch_fp8(k, mt, g.bf16, ctas, smem, s);
+      return bsg::launch_fp8(k, mt, g.bf16, false, bm, ctas, smem, s);
     case bsg::kNvfp4:
-      return bsg::launch_nvfp4(k, mt, g.bf16, ctas, smem, s);
+      return bsg::launch_nvfp4(k, mt, g.bf16, false, bm, ctas, smem, s);
   }
   return BSGEMV_ERR_INVALID_ARG;
 }

@@ -5,7 +5,7 @@
 // per-row summation order (rows are bit-identical across M).
 //
 // Choices (the reasons are measurements on GB300; see the design notes):
-//   * 64 output columns per CTA tile, 4 consumer warps + 1 copy warp, 2 CTAs per SM;
+//   * 64 output columns per CTA tile, 8 consumer warps + 1 copy warp, 2 CTAs per SM;
 //   * a ring of up to 8 stages of 128 weight bytes per row, as deep as the shared-memory share
 //     of a CTA allows (2 CTAs per SM), so that every SM keeps tens of KB of weight in flight;
 //   * stream-K: the tiles x stages work is split into equal contiguous ranges over
@@ -92,7 +92,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   g->zp_off = g->sc_off + kRowsPerTile * g->sbw * g->scale_es;
   const int slot_end = g->zp_off + (has_zp ? kRowsPerTile * g->zbw_bytes : 0);
   g->slot_bytes = static_cast<int>(ceil_div(slot_end, 1024) * 1024);
-  g->red_bytes = kConsumerWarps * 4 * g->mt_max * 32 * 16;
+  g->red_bytes = kConsumerWarps * kRgPerWarp * g->mt_max * 32 * 16;
   g->slot_floats = 4 * g->mt_max * 32 * 4;
 
   auto smem_for = [&](int stages) {

@@ -1,0 +1,10 @@
+// Instantiations of the GEMV kernel for int4_f16 weights (see bsgemv_launch.cuh).
+#include "bsgemv_launch.cuh"
+
+namespace bsg {
+
+int launch_int4_f16(const KParams& p, int mt, bool zp, int bmode, int ctas, int smem, cudaStream_t s) {
+  return launch_fmt<kInt4, false>(p, mt, zp, bmode, ctas, smem, s);
+}
+
+}  // namespace bsg

@@ -2,7 +2,8 @@
 //
 // Work decomposition (one persistent kernel per call):
 //   * a CTA tile is kRowsPerTile consecutive output columns n (rows of W) over a k-range;
-//   * k is walked in "stages" of 128 weight bytes per row (one 128-byte-swizzled TMA box):
+//   * k is walked in "stages" of 128 weight bytes per row (one 128-byte-swizzled TMA box, plus
+//     the stage's activations, scales and zero points copied with cp.async):
 //     256 k for the 4-bit formats, 128 k for the 8-bit formats;
 //   * the tiles x stages grid is cut into `ctas` equal contiguous ranges (stream-K); a tile whose
 //     stages fall into several CTAs is finished by the last CTA to arrive, which adds the
@@ -20,7 +21,8 @@ namespace bsg {
 enum Fmt : int { kInt4 = 1, kInt8 = 2, kFp8 = 3, kNvfp4 = 4 };
 
 constexpr int kRowsPerTile = 64;      // output columns per CTA tile (4 mma row groups of 16)
-constexpr int kConsumerWarps = 4;     // decode + mma warps; warp 0 issues the copies
+constexpr int kConsumerWarps = 8;     // decode + mma warps; warp 0 issues the copies
+constexpr int kRgPerWarp = 2;         // 16-row mma groups per consumer warp (2 of the tile's 4)
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kChunksPerStage = 8;    // 16-byte chunks of a weight row per stage (128 B)
 constexpr int kStageRowBytes = 16 * kChunksPerStage;
@@ -34,9 +36,7 @@ constexpr unsigned kErrTimeoutEmpty = 2u;
 // aligned in parameter space).
 struct KParams {
   CUtensorMap tm_w;   // W  as uint8 [N][row_bytes], box [kRowsPerTile][128], 128B swizzle
-  CUtensorMap tm_a;   // A  as uint16 [M][K], box [M][64], 128B swizzle
-  CUtensorMap tm_s;   // scales [N][nb_s] elements, box [kRowsPerTile][sbw], no swizzle
-  CUtensorMap tm_z;   // zero points uint8 [N][zp_pitch], box [kRowsPerTile][zbw_bytes]
+  const uint16_t* A;       // activations [M][K] (fp16 / bf16 bits)
   const uint8_t* W;
   const uint8_t* scales;   // global copy, used when the scale tensor cannot be TMA-tiled
   const uint8_t* zp;       // idem for zero points
@@ -61,9 +61,8 @@ struct KParams {
   int sbw;                 // scale box width in elements (blocks)
   int zbw_bytes;           // zero-point box width in bytes
   int zblk;                // blocks covered by one zero-point box
-  int side_scale_tma;      // 1: scales arrive by TMA; 0: read from global
-  int side_zp_tma;
-  int merge_pair;          // 1: both chunks of a consumer warp share one scale block
+  int side_scale_tma;      // 1: scales are staged into the ring; 0: read from global memory
+  int side_zp_tma;         // idem for zero points
   int slot_floats;         // floats per partial slot
 };
 
@@ -88,13 +87,27 @@ struct Geometry {
 int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
                      int sm_count, int ctas_override, int stages_override, Geometry* g);
 
-// Kernel launchers (one translation unit per weight format).
-int launch_int4(const KParams& p, int mt, bool bf16, bool zp, bool sub2, int ctas, int smem,
+// Kernel launchers (one translation unit per weight format; int4 split by activation type).
+// bmode: 0 = one scale block per 16-byte chunk, 1 = a consumer warp's chunk pair in one block,
+// 2 = two blocks per chunk (int4 with 16-element blocks).
+int launch_int4_f16(const KParams& p, int mt, bool zp, int bmode, int ctas, int smem,
+                    cudaStream_t s);
+int launch_int4_bf16(const KParams& p, int mt, bool zp, int bmode, int ctas, int smem,
+                     cudaStream_t s);
+int launch_int8(const KParams& p, int mt, bool bf16, bool zp, int bmode, int ctas, int smem,
                 cudaStream_t s);
-int launch_int8(const KParams& p, int mt, bool bf16, bool zp, int ctas, int smem, cudaStream_t s);
-int launch_fp8(const KParams& p, int mt, bool bf16, int ctas, int smem, cudaStream_t s);
-int launch_nvfp4(const KParams& p, int mt, bool bf16, int ctas, int smem, cudaStream_t s);
-int prepare_kernels(int fmt, int smem);  // sets the dynamic shared memory attribute
+int launch_fp8(const KParams& p, int mt, bool bf16, bool zp, int bmode, int ctas, int smem,
+               cudaStream_t s);
+int launch_nvfp4(const KParams& p, int mt, bool bf16, bool zp, int bmode, int ctas, int smem,
+                 cudaStream_t s);
+
+// Block mode of a problem (see above).
+inline int block_mode(int fmt, int block_size) {
+  if (fmt == kInt4) return block_size == 16 ? 2 : (block_size == 32 ? 0 : 1);
+  if (fmt == kInt8) return block_size == 16 ? 0 : 1;
+  if (fmt == kFp8) return 1;
+  return 0;
+}
 
 int launch_debug_dequant(int fmt, bool bf16, bool has_zp, int bs, int64_t N, int64_t K,
                          const uint8_t* W, const uint8_t* scales, const uint8_t* zp,

@@ -41,9 +41,10 @@
 
 namespace bsg {
 
-// Polls of mbarrier.try_wait before a wait is abandoned (each poll may suspend the thread for a
-// hardware-defined interval); at least seconds, far above any legitimate stall.
-constexpr uint32_t kWaitPolls = 1u << 24;
+// Bounded waits: a waiting thread sleeps in mbarrier.try_wait (suspend-time hint, woken when the
+// phase completes) and gives up after kWaitLimitNs of wall time, far above any legitimate stall.
+constexpr uint32_t kSuspendHintNs = 1000000;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // ------------------------------------------------------------------------------ PTX wrappers
 BSG_DEV uint32_t smem_u32(const void* p) {
@@ -71,22 +72,32 @@ BSG_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait: returns false (and records `code` in the error word) if the phase never
-// completes.  Nothing in a correct launch waits anywhere near the limit.
+BSG_DEV uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: returns false (and records `code` in the error word) if the phase does not
+// complete within kWaitLimitNs.
 BSG_DEV bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, unsigned code) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, code);
+      return false;
+    }
   }
-  atomicOr(err, code);
-  return false;
 }
 
 BSG_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
@@ -96,6 +107,49 @@ BSG_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+
+// Same as tma_load_2d with an L2 eviction-priority policy (evict_first for stream-once data).
+BSG_DEV void tma_load_2d_hint(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
+                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+BSG_DEV uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte asynchronous global -> shared copy through L2; `bytes` < 16 zero-fills the rest
+// (0 copies nothing and only writes zeros).
+BSG_DEV void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+
+// Make `bar` wait for this thread's prior cp.async copies: its pending count is raised now
+// and an arrival is performed when the copies have landed.
+BSG_DEV void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Prefetch one TMA box of a 2D tensor into L2 (no shared memory, no barrier).
+BSG_DEV void tma_prefetch_l2_2d(const CUtensorMap* tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream be scheduled now, and wait
+// until the previous kernel has completed with its memory visible.  Both are no-ops for a
+// launch without the programmatic-serialization attribute.
+BSG_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+BSG_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 BSG_DEV void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
@@ -165,6 +219,35 @@ BSG_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
+}
+
+// D = A * B (the accumulator input is zero): starts a scale group without zeroing registers.
+template <bool BF16>
+BSG_DEV void mma16816_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  const float z = 0.f;
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+  }
+}
+
+// (acc0, acc1) += (x0, x1) * s, two fp32 FMAs in one packed instruction.
+BSG_DEV void ffma2(float& acc0, float& acc1, float x0, float x1, float s) {
+  uint64_t a, x, ss;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc0), "f"(acc1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x), "l"(ss));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(acc0), "=f"(acc1) : "l"(a));
 }
 
 // ------------------------------------------------------------------------------ 16-bit pairs
@@ -348,7 +431,14 @@ BSG_DEV void zp_consts(uint32_t zp, uint32_t& zl, uint32_t& zh) {
 }
 
 // ------------------------------------------------------------------------------ the kernel
-template <int FMT, bool BF16, int MT, bool ZP, bool SUB2>
+// Scale-block grouping of a consumer warp's two chunks (k = 32 per chunk for the 4-bit formats,
+// 16 for the 8-bit formats):
+//   kBlockPerChunk  block == chunk k-range: scale after every chunk       (int4 bs32, int8 bs16)
+//   kBlockPerPair   both chunks in one block: scale once per stage        (bs >= 2 chunks, fp8)
+//   kTwoPerChunk    a chunk holds two blocks, quad lanes t < 2 and t >= 2 (int4 bs16)
+enum BlockMode : int { kBlockPerChunk = 0, kBlockPerPair = 1, kTwoPerChunk = 2 };
+
+template <int FMT, bool BF16, int MT, bool ZP, int BMODE>
 struct Gemv {
   static constexpr bool kFour = (FMT == kInt4 || FMT == kNvfp4);
   static constexpr int kKpc = kFour ? 32 : 16;  // k per 16-byte chunk
@@ -356,264 +446,405 @@ struct Gemv {
   static constexpr int kKc = kChunksPerStage * kKpc;
   static constexpr int kNbox = kKc / 64;        // activation boxes per stage
   static constexpr bool kFold = (FMT == kNvfp4);
-  static constexpr int kSub = SUB2 ? 2 : 1;
+  static constexpr int kSub = (BMODE == kTwoPerChunk) ? 2 : 1;
+  static constexpr int kScaleEs = (FMT == kFp8) ? 4 : (FMT == kNvfp4 ? 1 : 2);
+  // scale box width in blocks (16 bytes, or 32 bytes when a stage holds 16 int4 blocks)
+  static constexpr int kSbw = (FMT == kFp8) ? 4 : ((FMT == kNvfp4 || BMODE == kTwoPerChunk) ? 16 : 8);
+  static constexpr int kSpitch = kSbw * kScaleEs;  // bytes per row of the scale box
+  static constexpr int kZblk = (FMT == kInt4) ? 32 : 16;  // blocks per 16-byte zero-point box row
 
-  // ---- shared-memory layout helpers
   struct Smem {
     uint8_t* base;
-    const KParams& p;
-    BSG_DEV uint32_t slot(int i) const { return smem_u32(base) + i * p.slot_bytes; }
-    BSG_DEV uint32_t full(int i) const { return smem_u32(base) + p.bar_off + 8 * i; }
-    BSG_DEV uint32_t empty(int i) const { return smem_u32(base) + p.bar_off + 8 * (p.stages + i); }
-    BSG_DEV float4* red() const { return reinterpret_cast<float4*>(base + p.red_off); }
-    BSG_DEV int* flag() const { return reinterpret_cast<int*>(base + p.bar_off + 16 * p.stages); }
+    int stages, slot_bytes, bar_off, red_off;
+    BSG_DEV uint32_t slot(int i) const { return smem_u32(base) + i * slot_bytes; }
+    BSG_DEV uint32_t full(int i) const { return smem_u32(base) + bar_off + 8 * i; }
+    BSG_DEV uint32_t empty(int i) const { return smem_u32(base) + bar_off + 8 * (stages + i); }
+    BSG_DEV float4* red() const { return reinterpret_cast<float4*>(base + red_off); }
+    BSG_DEV int* flag() const { return reinterpret_cast<int*>(base + bar_off + 16 * stages); }
   };
 
-  // ---- producer: one thread
-  static BSG_DEV void produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1) {
-    prefetch_tmap(&p.tm_w);
-    prefetch_tmap(&p.tm_a);
-    if (p.side_scale_tma) prefetch_tmap(&p.tm_s);
-    if (p.side_zp_tma) prefetch_tmap(&p.tm_z);
-    int64_t it = 0;
-    for (int64_t s = s0; s < s1; ++s, ++it) {
-      const int slot = static_cast<int>(it % p.stages);
-      const uint32_t par = static_cast<uint32_t>((it / p.stages) & 1) ^ 1u;
-      if (!mbar_wait(sm.empty(slot), par, p.err, kErrTimeoutEmpty)) return;
-      const uint32_t full = sm.full(slot);
-      mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.tx_bytes));
-      const int64_t tile = s / p.spt;
-      const int ks = static_cast<int>(s % p.spt);
-      const int row0 = static_cast<int>(tile * kRowsPerTile);
-      const uint32_t dst = sm.slot(slot);
-      tma_load_2d(dst, &p.tm_w, ks * kStageRowBytes, row0, full);
-#pragma unroll
-      for (int j = 0; j < kNbox; ++j)
-        tma_load_2d(dst + p.act_off + j * p.act_box_bytes, &p.tm_a, ks * kKc + 64 * j, 0, full);
-      const int blk0 = (ks * kKc) >> p.bs_log2;
-      if (p.side_scale_tma) {
-        const int x = (blk0 / p.sbw) * p.sbw;
-        tma_load_2d(dst + p.sc_off, &p.tm_s, x, row0, full);
-      }
-      if (ZP && p.side_zp_tma) {
-        const int xb = (blk0 / p.zblk) * p.zblk;
-        tma_load_2d(dst + p.zp_off, &p.tm_z, (FMT == kInt4) ? xb / 2 : xb, row0, full);
+  // ---- producer: warp 0.  Lane 0 copies the stage's weight box [64 rows][128 B] with one TMA
+  // (L2 evict-first: the weight is read once).  All 32 lanes copy the small pieces -- the
+  // activations [M][k of the stage] into the same 128-byte-swizzled layout TMA would write,
+  // the scale box and the zero-point box -- with 16-byte cp.async, whose completion is tracked
+  // by the same full barrier (cp.async.mbarrier.arrive).  One TMA request stream per stage
+  // keeps the TMA unit on the bulk data; rows past N and k past K are zero-filled.
+  static BSG_DEV void produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int lane) {
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_w);
+      // Before the previous kernel has finished, warm L2 with this CTA's first weight boxes: the
+      // weight is never written by a preceding GEMV.  Activations, outputs and the workspace are
+      // touched only after pdl_wait.
+      int64_t t = s0 / p.spt;
+      int k = static_cast<int>(s0 - t * p.spt);
+      for (int64_t s = s0; s < s1 && s < s0 + sm.stages; ++s) {
+        tma_prefetch_l2_2d(&p.tm_w, k * kStageRowBytes, static_cast<int>(t * kRowsPerTile));
+        if (++k == p.spt) {
+          k = 0;
+          ++t;
+        }
       }
     }
-  }
-
-  // ---- consumer helpers
-  // Activation B fragments of chunk c for n8 tile mt: b[st][0] = (k 2t, 2t+1), b[st][1] =
-  // (k 2t+8, 2t+9) of activation row mt*8 + g, permuted like the weight (phys_k).
-  static BSG_DEV void act_fragment(const KParams& p, uint32_t act_base, int c, int mt, int g, int t,
-                                   uint32_t (&b)[kSteps][2]) {
-    const int m = mt * 8 + g;
-    if constexpr (kFour) {
-      const int box = c >> 1;
-      const int q = ((c & 1) << 2) + t;  // 16-byte chunk inside the 128-byte activation row
-      const uint4 v = lds128(act_base + box * p.act_box_bytes + m * 128 + ((q ^ (m & 7)) << 4));
-      if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
-        b[0][0] = prmt(v.x, v.z, 0x5410u);
-        b[0][1] = prmt(v.x, v.z, 0x7632u);
-        b[1][0] = prmt(v.y, v.w, 0x5410u);
-        b[1][1] = prmt(v.y, v.w, 0x7632u);
-      } else {  // nvfp4: natural pairs
-        b[0][0] = v.x;
-        b[0][1] = v.y;
-        b[1][0] = v.z;
-        b[1][1] = v.w;
+    pdl_wait();
+    const uint64_t pol = policy_evict_first();
+    const int64_t spt = p.spt, N = p.N, K = p.K;
+    constexpr uint32_t kTx = kRowsPerTile * kStageRowBytes;
+    constexpr int kUpr = kKc / 8;               // 16-byte activation units per row per stage
+    constexpr int kSu = kSpitch / 16;           // 16-byte units per scale box row
+    const int act_units = p.M * kUpr;
+    const int act_off = p.act_off, abox = p.act_box_bytes, sc_off = p.sc_off, zp_off = p.zp_off;
+    const int bs_log2 = p.bs_log2, spitch_g = p.scale_pitch, zpitch_g = p.zp_pitch;
+    const bool side_s = p.side_scale_tma != 0, side_z = ZP && p.side_zp_tma != 0;
+    int slot = 0;
+    uint32_t phase = 0;
+    int64_t tile = s0 / spt;
+    int ks = static_cast<int>(s0 - tile * spt);
+    for (int64_t s = s0; s < s1; ++s) {
+      if (!mbar_wait(sm.empty(slot), phase ^ 1u, p.err, kErrTimeoutEmpty)) break;
+      const uint32_t dst = sm.slot(slot), full = sm.full(slot);
+      const int64_t k0 = static_cast<int64_t>(ks) * kKc;
+      const int64_t row0 = tile * kRowsPerTile;
+      for (int u = lane; u < act_units; u += 32) {
+        const int m = u / kUpr, qg = u % kUpr;
+        const int q = qg & 7;
+        const uint32_t d = dst + act_off + (qg >> 3) * abox + m * 128 + ((q ^ (m & 7)) << 4);
+        const int64_t k = k0 + qg * 8;
+        const bool in = k < K;
+        cp_async16(d, p.A + m * K + (in ? k : 0), in ? 16u : 0u);
       }
-    } else {
-      const int box = c >> 2;
-      const int q = ((c & 3) << 1) + (t >> 1);
-      const uint2 v = lds64(act_base + box * p.act_box_bytes + m * 128 + ((q ^ (m & 7)) << 4) +
-                            ((t & 1) << 3));
-      b[0][0] = v.x;
-      b[0][1] = v.y;
+      const int blk0 = (ks * kKc) >> bs_log2;
+      if (side_s) {
+        const int sx = (blk0 & ~(kSbw - 1)) * kScaleEs;  // byte offset of the box in a scale row
+        for (int u = lane; u < kRowsPerTile * kSu; u += 32) {
+          const int r = u / kSu, v = u % kSu;
+          const int64_t n = row0 + r;
+          const bool in = n < N && sx + v * 16 < spitch_g;
+          cp_async16(dst + sc_off + r * kSpitch + v * 16,
+                     p.scales + (in ? n * spitch_g + sx + v * 16 : 0), in ? 16u : 0u);
+        }
+      }
+      if (side_z) {
+        const int xb = blk0 & ~(kZblk - 1);
+        const int zx = (FMT == kInt4) ? xb / 2 : xb;
+        for (int r = lane; r < kRowsPerTile; r += 32) {
+          const int64_t n = row0 + r;
+          const bool in = n < N && zx < zpitch_g;
+          cp_async16(dst + zp_off + r * 16, p.zp + (in ? n * zpitch_g + zx : 0), in ? 16u : 0u);
+        }
+      }
+      cp_async_mbar_arrive(full);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, kTx);
+        tma_load_2d_hint(dst, &p.tm_w, ks * kStageRowBytes, static_cast<int>(row0), full, pol);
+      }
+      if (++slot == sm.stages) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      if (++ks == spt) {
+        ks = 0;
+        ++tile;
+      }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
-  // fp32 scale of (tile row r, block blk); blk relative to the stage's scale box when staged.
-  static BSG_DEV float scale_at(const KParams& p, uint32_t sc_base, int64_t tile, int r,
-                                int blk, int box0) {
-    if (p.side_scale_tma) {
-      const int es = (FMT == kFp8) ? 4 : 2;
-      const uint32_t a = sc_base + (r * p.sbw + (blk - box0)) * es;
-      if constexpr (FMT == kFp8) return __uint_as_float(lds32(a));
-      else return __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(a))));
-    }
-    if (blk >= p.nb_s) return 0.f;  // chunk past K in the ragged last stage: weight is zero
-    int64_t n = tile * kRowsPerTile + r;
-    if (n >= p.N) n = p.N - 1;
-    const uint8_t* src = p.scales + n * p.scale_pitch;
-    if constexpr (FMT == kFp8) return __ldg(reinterpret_cast<const float*>(src) + blk);
-    else return __half2float(__ldg(reinterpret_cast<const __half*>(src) + blk));
+  // Register copies of the launch parameters the consumer's stage loop reads (same names as
+  // in KParams, so the helpers below read them from registers instead of parameter memory).
+  struct Run {
+    int64_t N;
+    int nb_s, bs_log2, scale_pitch, zp_pitch, side_scale_tma, side_zp_tma;
+    const uint8_t* scales;
+    const uint8_t* zp;
+  };
+
+  static BSG_DEV Run make_run(const KParams& p) {
+    return Run{p.N, p.nb_s, p.bs_log2, p.scale_pitch, p.zp_pitch, p.side_scale_tma,
+               p.side_zp_tma, p.scales, p.zp};
   }
 
-  static BSG_DEV uint32_t zp_at(const KParams& p, uint32_t zp_base, int64_t tile, int r, int blk,
-                                int zbox0) {
-    uint32_t byte;
-    int rel;
-    if (p.side_zp_tma) {
-      rel = blk - zbox0;
-      byte = lds8(zp_base + r * p.zbw_bytes + ((FMT == kInt4) ? (rel >> 1) : rel));
-    } else {
-      if (blk >= p.nb_s) return 0u;  // past K: the weight and activation there are zero
-      int64_t n = tile * kRowsPerTile + r;
-      if (n >= p.N) n = p.N - 1;
-      rel = blk;
-      byte = __ldg(p.zp + n * p.zp_pitch + ((FMT == kInt4) ? (blk >> 1) : blk));
-    }
-    if constexpr (FMT == kInt4) return (rel & 1) ? (byte >> 4) : (byte & 0xFu);
-    return byte;
-  }
+  // ---- per-lane constants.  Consumer warp cw owns the chunk pair cp = cw & 3 (chunks 2cp and
+  // 2cp+1 of every stage) and the row half rh = cw >> 2 (tile rows 32 rh .. 32 rh + 31, i.e.
+  // mma row groups 2 rh and 2 rh + 1).  Lane (g, t) holds fragment rows g + 8 rr, rr = 0..3
+  // (rr = 2 * local group + upper half), of that row half.
+  struct Lane {
+    int cp, rh, lane, g, t;
+    uint32_t w[2];        // ldmatrix row address of chunk cc (rows 32 rh + lane)
+    uint32_t act[2][MT];  // activation fragment address of chunk cc, n8 tile mt
+    uint32_t srow;        // scale box row 32 rh + g; row rr adds rr * 8 * kSpitch
+    uint32_t zrow;        // zero-point box row 32 rh + g; row rr adds rr * 8 * 16
+  };
 
-  // NVFP4 E4M3 scale code of (tile row r, 16-block blk of the row) as a replicated f16 pair.
-  static BSG_DEV uint32_t fold_scale(const KParams& p, uint32_t sc_base, int64_t tile, int r,
-                                     int blk, int box0) {
-    uint32_t code;
-    if (p.side_scale_tma) {
-      code = lds8(sc_base + r * p.sbw + (blk - box0));
-    } else if (blk >= p.nb_s) {
-      code = 0;  // past K
-    } else {
-      int64_t n = tile * kRowsPerTile + r;
-      if (n >= p.N) n = p.N - 1;
-      code = __ldg(p.scales + n * p.scale_pitch + blk);
-    }
-    return e4m3x2_to_f16x2(code * 0x0101u);
-  }
-
-  // Consume one ring slot: chunks 2*cw and 2*cw+1 of stage ks of `tile`.
-  static BSG_DEV void consume_stage(const KParams& p, uint32_t slot, int64_t tile, int ks, int cw,
-                                    int lane, float (&acc)[4][MT][4]) {
-    const int g = lane >> 2, t = lane & 3;
-    const uint32_t w_base = slot, act_base = slot + p.act_off, sc_base = slot + p.sc_off,
-                   zp_base = slot + p.zp_off;
-    const int blk_stage0 = (ks * kKc) >> p.bs_log2;
-    const int sbox0 = (blk_stage0 / p.sbw) * p.sbw;
-    const int zbox0 = ZP ? (blk_stage0 / p.zblk) * p.zblk : 0;
-
-    float tmp[kSub][4][MT][4];
-    if constexpr (!kFold) {
-#pragma unroll
-      for (int u = 0; u < kSub; ++u)
-#pragma unroll
-        for (int rg = 0; rg < 4; ++rg)
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) tmp[u][rg][mt][i] = 0.f;
-    }
-
+  static BSG_DEV Lane make_lane(const KParams& p, int cw, int lane) {
+    Lane L;
+    L.cp = cw & 3;
+    L.rh = cw >> 2;
+    L.lane = lane;
+    L.g = lane >> 2;
+    L.t = lane & 3;
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * cw + cc;
-      const int kchunk = ks * kKc + c * kKpc;  // first k of the chunk
-      const int blk = kchunk >> p.bs_log2;     // scale block of the chunk (first half for SUB2)
+      const int c = 2 * L.cp + cc;
+      const int r = 32 * L.rh + lane;
+      L.w[cc] = r * kStageRowBytes + ((c ^ (r & 7)) << 4);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int m = mt * 8 + L.g;
+        if constexpr (kFour) {
+          const int q = ((c & 1) << 2) + L.t;
+          L.act[cc][mt] = p.act_off + (c >> 1) * p.act_box_bytes + m * 128 + ((q ^ (m & 7)) << 4);
+        } else {
+          const int q = ((c & 3) << 1) + (L.t >> 1);
+          L.act[cc][mt] = p.act_off + (c >> 2) * p.act_box_bytes + m * 128 +
+                          ((q ^ (m & 7)) << 4) + ((L.t & 1) << 3);
+        }
+      }
+    }
+    L.srow = p.sc_off + (32 * L.rh + L.g) * kSpitch;
+    L.zrow = p.zp_off + (32 * L.rh + L.g) * 16;
+    return L;
+  }
 
-      // activation fragments
-      uint32_t b[MT][kSteps][2];
+  static BSG_DEV int64_t row_of(const Run& p, const Lane& L, int64_t tile, int rr) {
+    const int64_t n = tile * kRowsPerTile + 32 * L.rh + L.g + 8 * rr;
+    return n < p.N ? n : p.N - 1;
+  }
+
+  // fp32 scales of the lane's 4 rows for NB consecutive blocks starting at `blk` (box-relative
+  // index `rel`); NB = 2 only for 2-byte scales at an even `rel` (one 32-bit load per row).
+  template <int NB>
+  static BSG_DEV void load_scales(const Run& p, const Lane& L, uint32_t slot, int64_t tile,
+                                  int blk, int rel, float (&s)[NB][4]) {
+    if (p.side_scale_tma) {
+      const uint32_t a = slot + L.srow + rel * kScaleEs;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) act_fragment(p, act_base, c, mt, g, t, b[mt]);
-      uint32_t bsub[kSub][MT][kSteps][2];
+      for (int rr = 0; rr < 4; ++rr) {
+        const uint32_t ar = a + rr * 8 * kSpitch;
+        if constexpr (FMT == kFp8) {
 #pragma unroll
-      for (int u = 0; u < kSub; ++u)
+          for (int u = 0; u < NB; ++u) s[u][rr] = __uint_as_float(lds32(ar + 4 * u));
+        } else if constexpr (NB == 2) {
+          const uint32_t two = lds32(ar);
+          s[0][rr] = __half2float(__ushort_as_half(static_cast<unsigned short>(two & 0xFFFFu)));
+          s[1][rr] = __half2float(__ushort_as_half(static_cast<unsigned short>(two >> 16)));
+        } else {
+          s[0][rr] = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(ar))));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const uint8_t* src = p.scales + row_of(p, L, tile, rr) * p.scale_pitch;
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          const int b = blk + u;
+          if (b >= p.nb_s) {  // chunk past K in the ragged last stage: its weight is zero
+            s[u][rr] = 0.f;
+          } else if constexpr (FMT == kFp8) {
+            s[u][rr] = __ldg(reinterpret_cast<const float*>(src) + b);
+          } else {
+            s[u][rr] = __half2float(__ldg(reinterpret_cast<const __half*>(src) + b));
+          }
+        }
+      }
+    }
+  }
+
+  // Zero-point operand constants (see zp_consts) of the lane's 4 rows for block `blk`.
+  static BSG_DEV void load_zp(const Run& p, const Lane& L, uint32_t slot, int64_t tile,
+                              int blk, int rel, uint32_t (&zl)[4], uint32_t (&zh)[4]) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      uint32_t z;
+      if constexpr (!ZP) {
+        z = (FMT == kInt4) ? 8u : 128u;
+      } else if (p.side_zp_tma) {
+        const uint32_t byte = lds8(slot + L.zrow + rr * 8 * 16 + ((FMT == kInt4) ? (rel >> 1) : rel));
+        z = (FMT == kInt4) ? ((rel & 1) ? (byte >> 4) : (byte & 0xFu)) : byte;
+      } else {
+        uint32_t byte = 0;
+        if (blk < p.nb_s)
+          byte = __ldg(p.zp + row_of(p, L, tile, rr) * p.zp_pitch + ((FMT == kInt4) ? (blk >> 1) : blk));
+        z = (FMT == kInt4) ? ((blk & 1) ? (byte >> 4) : (byte & 0xFu)) : byte;
+      }
+      zp_consts<FMT, BF16>(z, zl[rr], zh[rr]);
+    }
+  }
+
+  // NVFP4: the replicated f16 E4M3 block scale of the lane's 4 rows for 16-block `blk`.
+  static BSG_DEV void load_fold(const Run& p, const Lane& L, uint32_t slot, int64_t tile,
+                                int blk, int rel, uint32_t (&f)[4]) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      uint32_t code;
+      if (p.side_scale_tma) {
+        code = lds8(slot + L.srow + rr * 8 * kSpitch + rel);
+      } else {
+        code = (blk < p.nb_s) ? __ldg(p.scales + row_of(p, L, tile, rr) * p.scale_pitch + blk) : 0u;
+      }
+      f[rr] = e4m3x2_to_f16x2(code * 0x0101u);
+    }
+  }
+
+  // Activation B fragments of chunk cc: b[mt][st][0] = (k 2t, 2t+1), b[mt][st][1] = (k 2t+8,
+  // 2t+9) of activation row mt*8 + g, permuted like the weight (phys_k).
+  static BSG_DEV void act_fragment(const Lane& L, uint32_t slot, int cc, uint32_t (&b)[MT][kSteps][2]) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      if constexpr (kFour) {
+        const uint4 v = lds128(slot + L.act[cc][mt]);
+        if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
+          b[mt][0][0] = prmt(v.x, v.z, 0x5410u);
+          b[mt][0][1] = prmt(v.x, v.z, 0x7632u);
+          b[mt][1][0] = prmt(v.y, v.w, 0x5410u);
+          b[mt][1][1] = prmt(v.y, v.w, 0x7632u);
+        } else {  // nvfp4: natural pairs
+          b[mt][0][0] = v.x;
+          b[mt][0][1] = v.y;
+          b[mt][1][0] = v.z;
+          b[mt][1][1] = v.w;
+        }
+      } else {
+        const uint2 v = lds64(slot + L.act[cc][mt]);
+        b[mt][0][0] = v.x;
+        b[mt][0][1] = v.y;
+      }
+    }
+  }
+
+  // Decode the lane's 2 row groups of chunk cc and multiply into d[u] (u: sub-block for
+  // kTwoPerChunk).  ZC: the first k-step starts from zero instead of accumulating.
+  template <bool ZC>
+  static BSG_DEV void chunk_mma(const Lane& L, uint32_t slot, int cc, const uint32_t (&zl)[4],
+                                const uint32_t (&zh)[4], float (&d)[kSub][2][MT][4]) {
+    uint32_t b[MT][kSteps][2];
+    act_fragment(L, slot, cc, b);
+    uint32_t wv[4];
+    ldsm_x4(slot + L.w[cc], wv[0], wv[1], wv[2], wv[3]);
+#pragma unroll
+    for (int lg = 0; lg < 2; ++lg) {
+      uint32_t a[kSteps][4];
+      if constexpr (FMT == kInt4) {
+        decode_int4<BF16>(wv[2 * lg], wv[2 * lg + 1], zl[2 * lg], zh[2 * lg], zl[2 * lg + 1],
+                          zh[2 * lg + 1], a);
+      } else if constexpr (FMT == kInt8) {
+        decode_int8<BF16>(wv[2 * lg], wv[2 * lg + 1], zl[2 * lg], zl[2 * lg + 1], a);
+      } else if constexpr (FMT == kFp8) {
+        decode_fp8<BF16>(wv[2 * lg], wv[2 * lg + 1], a);
+      } else {
+        decode_nvfp4<BF16>(wv[2 * lg], wv[2 * lg + 1], zl[2 * lg], zl[2 * lg + 1], a);
+      }
+#pragma unroll
+      for (int st = 0; st < kSteps; ++st)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const bool zc = ZC && st == 0;
+#pragma unroll
+          for (int u = 0; u < kSub; ++u) {
+            uint32_t b0 = b[mt][st][0], b1 = b[mt][st][1];
+            if constexpr (kSub == 2) {
+              // quad lanes t < 2 hold the chunk's first block, t >= 2 the second
+              const bool mine = (L.t >> 1) == u;
+              b0 = mine ? b0 : 0u;
+              b1 = mine ? b1 : 0u;
+            }
+            if (zc) mma16816_zc<BF16>(d[u][lg][mt], a[st], b0, b1);
+            else mma16816<BF16>(d[u][lg][mt], a[st], b0, b1);
+          }
+        }
+    }
+  }
+
+  // acc += tmp * s (per fragment row: s[2*lg] for row g, s[2*lg+1] for row g+8).
+  static BSG_DEV void apply_scales(const float (&s)[4], const float (&tmp)[2][MT][4],
+                                   float (&acc)[2][MT][4]) {
+#pragma unroll
+    for (int lg = 0; lg < 2; ++lg)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        acc[lg][mt][0] = fmaf(tmp[lg][mt][0], s[2 * lg], acc[lg][mt][0]);
+        acc[lg][mt][1] = fmaf(tmp[lg][mt][1], s[2 * lg], acc[lg][mt][1]);
+        acc[lg][mt][2] = fmaf(tmp[lg][mt][2], s[2 * lg + 1], acc[lg][mt][2]);
+        acc[lg][mt][3] = fmaf(tmp[lg][mt][3], s[2 * lg + 1], acc[lg][mt][3]);
+      }
+  }
+
+  template <int U>
+  static BSG_DEV void zero(float (&x)[U][2][MT][4]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int lg = 0; lg < 2; ++lg)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int st = 0; st < kSteps; ++st) {
-            // SUB2: quad lanes t < 2 hold block blk, t >= 2 block blk + 1
-            const bool keep = !SUB2 || ((t >> 1) == u);
-            bsub[u][mt][st][0] = keep ? b[mt][st][0] : 0u;
-            bsub[u][mt][st][1] = keep ? b[mt][st][1] : 0u;
-          }
+          for (int i = 0; i < 4; ++i) x[u][lg][mt][i] = 0.f;
+  }
 
-      // weight words: wv[2*rg] = row 16*rg + g, wv[2*rg + 1] = row 16*rg + g + 8
-      uint32_t wv[8];
-      {
-        const int r0 = lane, r1 = 32 + lane;
-        ldsm_x4(w_base + r0 * 128 + ((c ^ (r0 & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
-        ldsm_x4(w_base + r1 * 128 + ((c ^ (r1 & 7)) << 4), wv[4], wv[5], wv[6], wv[7]);
+  // Consume one ring slot: chunks 2cp and 2cp+1, row half rh, of stage ks of `tile`.
+  static BSG_DEV void consume_stage(const Run& p, const Lane& L, uint32_t slot, int64_t tile,
+                                    int ks, float (&acc)[1][2][MT][4]) {
+    const int bs_log2 = p.bs_log2;
+    const int blk0 = (ks * kKc) >> bs_log2;  // first scale block of the stage
+    const int sbox0 = blk0 & ~(kSbw - 1);     // first block of the staged scale box
+    const int zbox0 = blk0 & ~(kZblk - 1);
+    uint32_t zl[4], zh[4];
+    if constexpr (kFold) {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        // the lane's 8 codes lie in 16-block (k of chunk + 8t) / 16
+        const int fb = ((ks * kKc + (2 * L.cp + cc) * kKpc) >> 4) + (L.t >> 1);
+        load_fold(p, L, slot, tile, fb, fb - sbox0, zl);
+        chunk_mma<false>(L, slot, cc, zl, zh, acc);
       }
-
+    } else if constexpr (BMODE == kBlockPerPair) {
+      const int blk = blk0 + ((2 * L.cp * kKpc) >> bs_log2);
+      load_zp(p, L, slot, tile, blk, blk - zbox0, zl, zh);
+      float tmp[1][2][MT][4];
+      chunk_mma<true>(L, slot, 0, zl, zh, tmp);
+      chunk_mma<false>(L, slot, 1, zl, zh, tmp);
+      float s[1][4];
+      load_scales<1>(p, L, slot, tile, blk, blk - sbox0, s);
+      apply_scales(s[0], tmp[0], acc[0]);
+    } else if constexpr (BMODE == kBlockPerChunk) {
+      const int blk = blk0 + 2 * L.cp;  // chunk cc is block blk + cc
+      float s[2][4];
+      if constexpr (kScaleEs == 2) {
+        load_scales<2>(p, L, slot, tile, blk, blk - sbox0, s);
+      } else {
+        float s1[1][4];
 #pragma unroll
-      for (int rg = 0; rg < 4; ++rg) {
-        const int rlo = 16 * rg + g, rhi = rlo + 8;
-        uint32_t a[kSteps][4];
-        if constexpr (FMT == kInt4) {
-          // zero point of the lane's own block (for SUB2: block blk + (t >> 1))
-          uint32_t zl_lo, zh_lo, zl_hi, zh_hi;
-          if constexpr (ZP) {
-            const int zb = SUB2 ? blk + (t >> 1) : blk;
-            zp_consts<FMT, BF16>(zp_at(p, zp_base, tile, rlo, zb, zbox0), zl_lo, zh_lo);
-            zp_consts<FMT, BF16>(zp_at(p, zp_base, tile, rhi, zb, zbox0), zl_hi, zh_hi);
-          } else {
-            zp_consts<FMT, BF16>(8u, zl_lo, zh_lo);
-            zl_hi = zl_lo;
-            zh_hi = zh_lo;
-          }
-          decode_int4<BF16>(wv[2 * rg], wv[2 * rg + 1], zl_lo, zh_lo, zl_hi, zh_hi, a);
-        } else if constexpr (FMT == kInt8) {
-          uint32_t z_lo, z_hi, unused;
-          if constexpr (ZP) {
-            zp_consts<FMT, BF16>(zp_at(p, zp_base, tile, rlo, blk, zbox0), z_lo, unused);
-            zp_consts<FMT, BF16>(zp_at(p, zp_base, tile, rhi, blk, zbox0), z_hi, unused);
-          } else {
-            zp_consts<FMT, BF16>(128u, z_lo, unused);
-            z_hi = z_lo;
-          }
-          decode_int8<BF16>(wv[2 * rg], wv[2 * rg + 1], z_lo, z_hi, a);
-        } else if constexpr (FMT == kFp8) {
-          decode_fp8<BF16>(wv[2 * rg], wv[2 * rg + 1], a);
-        } else {
-          // NVFP4: the lane's 8 codes lie in 16-block (k_chunk + 8t) / 16
-          const int fb = (kchunk >> 4) + (t >> 1);
-          const uint32_t s_lo = fold_scale(p, sc_base, tile, rlo, fb, sbox0);
-          const uint32_t s_hi = fold_scale(p, sc_base, tile, rhi, fb, sbox0);
-          decode_nvfp4<BF16>(wv[2 * rg], wv[2 * rg + 1], s_lo, s_hi, a);
+        for (int cc = 0; cc < 2; ++cc) {
+          load_scales<1>(p, L, slot, tile, blk + cc, blk + cc - sbox0, s1);
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) s[cc][rr] = s1[0][rr];
         }
-#pragma unroll
-        for (int st = 0; st < kSteps; ++st)
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            if constexpr (kFold) {
-              mma16816<BF16>(acc[rg][mt], a[st], b[mt][st][0], b[mt][st][1]);
-            } else {
-#pragma unroll
-              for (int u = 0; u < kSub; ++u)
-                mma16816<BF16>(tmp[u][rg][mt], a[st], bsub[u][mt][st][0], bsub[u][mt][st][1]);
-            }
-          }
       }
-
-      // per-block fp32 scale: after every chunk, or after the pair when both chunks share it
-      if constexpr (!kFold) {
-        if (cc == 1 || !p.merge_pair) {
 #pragma unroll
-          for (int u = 0; u < kSub; ++u) {
+      for (int cc = 0; cc < 2; ++cc) {
+        load_zp(p, L, slot, tile, blk + cc, blk + cc - zbox0, zl, zh);
+        float tmp[1][2][MT][4];
+        chunk_mma<true>(L, slot, cc, zl, zh, tmp);
+        apply_scales(s[cc], tmp[0], acc[0]);
+      }
+    } else {  // kTwoPerChunk: chunk cc holds blocks blk, blk + 1 (int4, 16-element blocks)
 #pragma unroll
-            for (int rg = 0; rg < 4; ++rg) {
-              const int rlo = 16 * rg + g, rhi = rlo + 8;
-              const float s_lo = scale_at(p, sc_base, tile, rlo, blk + u, sbox0);
-              const float s_hi = scale_at(p, sc_base, tile, rhi, blk + u, sbox0);
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                acc[rg][mt][0] = fmaf(tmp[u][rg][mt][0], s_lo, acc[rg][mt][0]);
-                acc[rg][mt][1] = fmaf(tmp[u][rg][mt][1], s_lo, acc[rg][mt][1]);
-                acc[rg][mt][2] = fmaf(tmp[u][rg][mt][2], s_hi, acc[rg][mt][2]);
-                acc[rg][mt][3] = fmaf(tmp[u][rg][mt][3], s_hi, acc[rg][mt][3]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) tmp[u][rg][mt][i] = 0.f;
-              }
-            }
-          }
-        }
+      for (int cc = 0; cc < 2; ++cc) {
+        const int blk = blk0 + 2 * (2 * L.cp + cc);
+        const int zb = blk + (L.t >> 1);
+        load_zp(p, L, slot, tile, zb, zb - zbox0, zl, zh);
+        float tmp[2][2][MT][4];
+        chunk_mma<true>(L, slot, cc, zl, zh, tmp);
+        float s[2][4];
+        load_scales<2>(p, L, slot, tile, blk, blk - sbox0, s);
+        apply_scales(s[0], tmp[0], acc[0]);
+        apply_scales(s[1], tmp[1], acc[0]);
       }
     }
   }
 
-  // Store 4 fp32 results of a fragment slot (rg, mt, lane) of `tile` as rounded y.
+  // Store the 4 fp32 results of fragment slot (tile row group rg, tile mt, lane ln) as y.
   static BSG_DEV void store_y(const KParams& p, int64_t tile, int rg, int mt, int ln, float4 v,
                               float gs) {
     const int g = ln >> 2, t = ln & 3;
@@ -639,132 +870,144 @@ struct Gemv {
     return ((x + 1) * G + T - 1) / T - 1;
   }
 
-  // End of a tile segment: reduce the consumer warps, then store or publish a partial.
+  // End of a tile segment: add the 4 chunk-pair warps of each row half (fixed order), then
+  // store, or publish a partial and let the last CTA of the tile add the partials in CTA order.
+  // Partial slots: CTA i writes slot 0 for the first tile of its range and slot 1 for its last
+  // tile, so among a tile's contributors only the first can hold it in slot 1 (when its range
+  // began in an earlier tile).
   static BSG_DEV void epilogue(const KParams& p, const Smem& sm, int64_t tile, bool whole,
-                               int64_t s0, int cw, int lane, float (&acc)[4][MT][4], float gs) {
-    const int tid = cw * 32 + lane;  // 0 .. 127
-    constexpr int kSlots = 4 * MT * 32;  // float4 slots per warp
+                               int64_t my_first_tile, int cw, int lane, float (&acc)[1][2][MT][4],
+                               float gs) {
+    constexpr int kNT = kConsumerWarps * 32;   // 256 consumer threads
+    constexpr int kSlots = 2 * MT * 32;        // float4 slots per warp
+    constexpr int kOut = 4 * MT * 32;          // float4 slots per tile (4 row groups)
+    const int tid = cw * 32 + lane;
     float4* red = sm.red();
 #pragma unroll
-    for (int rg = 0; rg < 4; ++rg)
+    for (int lg = 0; lg < 2; ++lg)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
-        red[cw * kSlots + (rg * MT + mt) * 32 + lane] =
-            make_float4(acc[rg][mt][0], acc[rg][mt][1], acc[rg][mt][2], acc[rg][mt][3]);
-    named_bar_sync(1, kConsumerWarps * 32);
+        red[cw * kSlots + (lg * MT + mt) * 32 + lane] =
+            make_float4(acc[0][lg][mt][0], acc[0][lg][mt][1], acc[0][lg][mt][2], acc[0][lg][mt][3]);
+    named_bar_sync(1, kNT);
 
-    const int64_t G = gridDim.x, T = p.total_stages;
-    const int64_t me = blockIdx.x;
-    float4 sum[MT];
+    // output slot tid = ((rh * 2 + lg) * MT + mt) * 32 + ln, tile row group rg = 2 rh + lg
+    const bool active = tid < kOut;
+    const int ln = tid & 31;
+    const int q = tid >> 5;
+    const int mt = q % MT, rg = q / MT;
+    const int rh = rg >> 1, lg = rg & 1;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active) {
 #pragma unroll
-    for (int j = 0; j < MT; ++j) {
-      const int slot = tid + j * kConsumerWarps * 32;
-      float4 v = red[slot];
-#pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) {
-        const float4 u = red[w * kSlots + slot];
-        v.x += u.x;
-        v.y += u.y;
-        v.z += u.z;
-        v.w += u.w;
+      for (int cp = 0; cp < 4; ++cp) {
+        const float4 u = red[(rh * 4 + cp) * kSlots + (lg * MT + mt) * 32 + ln];
+        sum.x += u.x;
+        sum.y += u.y;
+        sum.z += u.z;
+        sum.w += u.w;
       }
-      sum[j] = v;
     }
     if (whole) {
-#pragma unroll
-      for (int j = 0; j < MT; ++j) {
-        const int slot = tid + j * kConsumerWarps * 32;
-        store_y(p, tile, slot / (MT * 32), (slot / 32) % MT, slot % 32, sum[j], gs);
-      }
+      if (active) store_y(p, tile, rg, mt, ln, sum, gs);
     } else {
-      const int seg = (tile == (me * T / G) / p.spt) ? 0 : 1;
-      float4* mine = reinterpret_cast<float4*>(p.partials) + (me * 2 + seg) * (p.slot_floats / 4);
-#pragma unroll
-      for (int j = 0; j < MT; ++j) __stcg(mine + tid + j * kConsumerWarps * 32, sum[j]);
-      __threadfence();
-      named_bar_sync(1, kConsumerWarps * 32);
-      const int64_t first = cta_of_stage(tile * p.spt, T, G);
-      const int64_t last = cta_of_stage((tile + 1) * p.spt - 1, T, G);
+      const int slot_floats4 = p.slot_floats / 4;
+      const int seg = (tile == my_first_tile) ? 0 : 1;
+      float4* mine = reinterpret_cast<float4*>(p.partials) +
+                     (static_cast<int64_t>(blockIdx.x) * 2 + seg) * slot_floats4;
+      if (active) __stcg(mine + tid, sum);
+      named_bar_sync(1, kNT);
+      int* info = sm.flag();  // [0] last arriver?  [1] first CTA  [2] last CTA  [3] first's slot
       if (tid == 0) {
-        const unsigned old = atomicAdd(p.counters + tile, 1u);
-        *sm.flag() = (old == static_cast<unsigned>(last - first)) ? 1 : 0;
-      }
-      named_bar_sync(1, kConsumerWarps * 32);
-      if (*sm.flag()) {
+        const int64_t G = gridDim.x, T = p.total_stages;
+        const int64_t x0 = tile * p.spt;
+        const int64_t first = cta_of_stage(x0, T, G);
+        const int64_t last = cta_of_stage(x0 + p.spt - 1, T, G);
+        // the barrier orders every thread's partial store before this fence (fences are
+        // cumulative), which publishes them at GPU scope before the arrival count
         __threadfence();
-#pragma unroll
-        for (int j = 0; j < MT; ++j) {
-          const int slot = tid + j * kConsumerWarps * 32;
+        const unsigned old = atomicAdd(p.counters + tile, 1u);
+        info[0] = (old == static_cast<unsigned>(last - first)) ? 1 : 0;
+        info[1] = static_cast<int>(first);
+        info[2] = static_cast<int>(last);
+        info[3] = (first * T < x0 * G) ? 1 : 0;  // first CTA's range began before this tile
+      }
+      named_bar_sync(1, kNT);
+      if (info[0]) {
+        __threadfence();  // acquire side: order the partial loads after the observed count
+        const int first = info[1], last = info[2], fseg = info[3];
+        if (active) {
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int64_t i = first; i <= last; ++i) {
-            const int sg = (tile == (i * T / G) / p.spt) ? 0 : 1;
-            const float4 u =
-                __ldcg(reinterpret_cast<const float4*>(p.partials) + (i * 2 + sg) * (p.slot_floats / 4) + slot);
+          const float4* part = reinterpret_cast<const float4*>(p.partials) + tid;
+          for (int i = first; i <= last; ++i) {
+            const int sg = (i == first) ? fseg : 0;
+            const float4 u = __ldcg(part + (static_cast<int64_t>(i) * 2 + sg) * slot_floats4);
             v.x += u.x;
             v.y += u.y;
             v.z += u.z;
             v.w += u.w;
           }
-          store_y(p, tile, slot / (MT * 32), (slot / 32) % MT, slot % 32, v, gs);
+          store_y(p, tile, rg, mt, ln, v, gs);
         }
         if (tid == 0) p.counters[tile] = 0u;  // every contributor has arrived: reset for reuse
       }
     }
-    named_bar_sync(1, kConsumerWarps * 32);  // `red` and the flag are reused by the next segment
-    (void)s0;
+    named_bar_sync(1, kNT);  // `red` and the info words are reused by the next segment
   }
 
   static BSG_DEV void consume(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int cw,
                               int lane) {
-    float acc[4][MT][4];
-#pragma unroll
-    for (int rg = 0; rg < 4; ++rg)
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[rg][mt][i] = 0.f;
+    pdl_wait();  // the epilogues write y and the plan's workspace
+    const Lane L = make_lane(p, cw, lane);
+    const Run R = make_run(p);
+    float acc[1][2][MT][4];
+    zero(acc);
     const float gs = kFold ? __ldg(p.gscale) : 1.0f;
-
-    int64_t it = 0;
+    const int64_t spt = p.spt;
+    int slot = 0;
+    uint32_t phase = 0;
+    int64_t tile = s0 / spt;
+    int ks = static_cast<int>(s0 - tile * spt);
+    const int64_t first_tile = tile;
     bool ok = true;
-    for (int64_t s = s0; s < s1; ++s, ++it) {
-      const int slot = static_cast<int>(it % p.stages);
-      const uint32_t par = static_cast<uint32_t>((it / p.stages) & 1);
-      if (ok) ok = mbar_wait(sm.full(slot), par, p.err, kErrTimeoutFull);
-      const int64_t tile = s / p.spt;
-      const int ks = static_cast<int>(s % p.spt);
-      if (ok) consume_stage(p, sm.slot(slot), tile, ks, cw, lane, acc);
+    for (int64_t s = s0; s < s1; ++s) {
+      if (ok) ok = mbar_wait(sm.full(slot), phase, p.err, kErrTimeoutFull);
+      if (ok) consume_stage(R, L, sm.slot(slot), tile, ks, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.empty(slot));
-      if (ks == p.spt - 1 || s == s1 - 1) {
-        const bool whole = (s0 <= tile * p.spt) && (s1 >= (tile + 1) * p.spt);
-        epilogue(p, sm, tile, whole, s0, cw, lane, acc, gs);
-#pragma unroll
-        for (int rg = 0; rg < 4; ++rg)
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[rg][mt][i] = 0.f;
+      if (ks == spt - 1 || s == s1 - 1) {
+        const bool whole = (s0 <= tile * spt) && (s1 >= (tile + 1) * spt);
+        epilogue(p, sm, tile, whole, first_tile, cw, lane, acc, gs);
+        zero(acc);
+      }
+      if (++slot == sm.stages) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      if (++ks == spt) {
+        ks = 0;
+        ++tile;
       }
     }
   }
 };
 
-template <int FMT, bool BF16, int MT, bool ZP, bool SUB2>
+template <int FMT, bool BF16, int MT, bool ZP, int BMODE>
 __global__ void __launch_bounds__(kThreads, 2) bsgemv_mma_kernel(const __grid_constant__ KParams p) {
-  using K = Gemv<FMT, BF16, MT, ZP, SUB2>;
+  using K = Gemv<FMT, BF16, MT, ZP, BMODE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const typename K::Smem sm{base, p};
+  const typename K::Smem sm{base, p.stages, p.slot_bytes, p.bar_off, p.red_off};
 
   const int64_t G = gridDim.x, T = p.total_stages;
   const int64_t s0 = static_cast<int64_t>(blockIdx.x) * T / G;
   const int64_t s1 = (static_cast<int64_t>(blockIdx.x) + 1) * T / G;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int i = 0; i < p.stages; ++i) {
+    for (int i = 0; i < sm.stages; ++i) {
       mbar_init(sm.full(i), 1);
       mbar_init(sm.empty(i), kConsumerWarps);
     }
@@ -773,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 2) bsgemv_mma_kernel(const __grid_co
   __syncthreads();
 
   if (warp == 0) {
-    if (lane == 0) K::produce(p, sm, s0, s1);
+    K::produce(p, sm, s0, s1, lane);
   } else {
     K::consume(p, sm, s0, s1, warp - 1, lane);
   }

@@ -93,7 +93,7 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
     g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, sms)
     four = fmt in ("int4", "nvfp4")
     assert g["k_per_stage"] == (256 if four else 128)
-    assert g["rows_per_tile"] == 64 and g["consumer_warps"] == 4
+    assert g["rows_per_tile"] == 64 and g["consumer_warps"] == 8
     assert g["tiles"] == -(-N // 64)
     assert g["stages_per_tile"] == -(-K // g["k_per_stage"])
     assert g["total_stages"] == g["tiles"] * g["stages_per_tile"]
