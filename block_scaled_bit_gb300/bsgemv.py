@@ -24,12 +24,13 @@ ERR_M_TOO_LARGE = -4
 ERR_CUDA = -5
 ERR_WRONG_DEVICE = -6
 ERR_DEVICE_TIMEOUT = -7
+ERR_SCRATCH_LIMIT = -8
 
 # Every extern "C" entry point of include/bsgemv.h.
 EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_host", "bsgemv_destroy",
            "bsgemv_status_string", "bsgemv_debug_dequant", "bsgemv_plan_set_override",
            "bsgemv_plan_describe", "bsgemv_geometry_for", "bsgemv_device_status",
-           "bsgemv_version")
+           "bsgemv_run_noalloc", "bsgemv_version")
 
 
 class Geometry(ctypes.Structure):
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.bsgemv_plan_describe.argtypes = [vp, ctypes.POINTER(Geometry)]
         L.bsgemv_geometry_for.argtypes = [ci, ci, ci, i64, i64, ci, ci, ctypes.POINTER(Geometry)]
         L.bsgemv_device_status.argtypes = [vp, vp]
+        L.bsgemv_run_noalloc.argtypes = [ci, ci, ci, i64, i64, vp, vp, vp, vp, vp, ci, vp]
         for name in EXPORTS:
             if name != "bsgemv_status_string":
                 getattr(L, name).restype = ci
@@ -105,6 +107,15 @@ def geometry_for(fmt: str, act: str, block_size: int, has_zp: bool, N: int, K: i
     _check(lib().bsgemv_geometry_for(format_code(fmt, act), block_size, int(has_zp), N, K,
                                      max_M, sm_count, ctypes.byref(g)), "bsgemv_geometry_for")
     return g.as_dict()
+
+
+def run_noalloc_status(fmt: str, act: str, block_size: int, has_zp: bool, N: int, K: int, A, W,
+                       scales, zp, y, M: int | None = None, stream=None) -> int:
+    """One GEMV through bsgemv_run_noalloc (no plan, no allocation); returns the status."""
+    M = A.shape[0] if M is None else M
+    return lib().bsgemv_run_noalloc(format_code(fmt, act), block_size, int(has_zp), N, K, _ptr(A),
+                                    _ptr(W), _ptr(scales), _ptr(zp), _ptr(y), int(M),
+                                    _stream(stream))
 
 
 def _ptr(t) -> int | None:

@@ -263,6 +263,7 @@ const char* bsgemv_status_string(int status) {
     case BSGEMV_ERR_CUDA: return "CUDA error";
     case BSGEMV_ERR_WRONG_DEVICE: return "current device is not the plan's device";
     case BSGEMV_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a bounded wait";
+    case BSGEMV_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch area of bsgemv_run_noalloc";
   }
   return "unknown status";
 }

@@ -68,8 +68,10 @@ enum bsgemv_status {
   BSGEMV_ERR_M_TOO_LARGE = -4,    /* M > the plan's max_M */
   BSGEMV_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed */
   BSGEMV_ERR_WRONG_DEVICE = -6,   /* the current device is not the plan's device */
-  BSGEMV_ERR_DEVICE_TIMEOUT = -7  /* a kernel gave up a bounded wait (reported by
+  BSGEMV_ERR_DEVICE_TIMEOUT = -7, /* a kernel gave up a bounded wait (reported by
                                      bsgemv_device_status) */
+  BSGEMV_ERR_SCRATCH_LIMIT = -8   /* bsgemv_run_noalloc: the problem needs more than the fixed
+                                     scratch area holds */
 };
 
 /* Variants a plan can run (bsgemv_geometry.variant, bsgemv_plan_set_override). */
@@ -170,6 +172,28 @@ int bsgemv_geometry_for(int format, int block_size, int has_zp, int64_t N, int64
  * check, or BSGEMV_ERR_CUDA if the synchronisation failed.
  */
 int bsgemv_device_status(bsgemv_plan_t plan, void* stream);
+
+/*
+ * The GEMV without any allocation, for callers that cannot call cudaMalloc: runtimes that own
+ * all device memory up front, code running inside another framework's memory pool, paths where
+ * an allocation could fail or synchronise at the wrong moment.  (The method's pages have no
+ * counterpart; this is a property of this library's interface.)
+ *
+ * Arguments as bsgemv_plan plus bsgemv_run, with max_M = M; no plan is created.  Instead of a
+ * plan's cudaMalloc'd workspace the cross-CTA reduction uses one fixed scratch area compiled into
+ * the library (a file-scope device array of about 2.6 MiB that every GPU loading the library
+ * holds until the process exits).  Limits: N <= 524288 output columns and at most 320
+ * persistent CTAs (a 152-SM GB300 uses 304); beyond them the call returns
+ * BSGEMV_ERR_SCRATCH_LIMIT and does nothing.  The first call on a device looks up the scratch
+ * area's device address (with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one scratch area: calls that overlap on the GPU
+ * (other streams, other host threads) race on it and give wrong results, so serialise them.
+ * Each call clears the counters it uses with cudaMemsetAsync on `stream` before its kernel; it
+ * calls no cudaMalloc, cudaFree or allocating routine.  Enqueue only; no synchronisation.
+ */
+int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_t N, int64_t K,
+                       const void* A, const void* W, const void* scales, const void* zp, void* y,
+                       int M, void* stream);
 
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int bsgemv_version(void);

@@ -34,7 +34,7 @@ def test_every_declared_function_is_exported(L):
 
 
 def test_status_strings(L):
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         assert bsgemv.status_string(code) not in ("", "unknown status")
     assert bsgemv.status_string(-99) == "unknown status"
     assert L.bsgemv_version() >= 100
