@@ -188,7 +188,9 @@ class Workload:
         for shape in synth.config_shapes(config):
             m = M or shape.Ms[0]
             case = shape.case(m)
-            plan = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K, 16)
+            # plans are sized for the configuration's largest M (the M values it is quoted at)
+            plan = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K,
+                               max(max(shape.Ms), m))
             bufs = [bsgemv.upload(case, device) for _ in range(copies)]
             self.items.append({"shape": shape, "case": case, "M": m, "plan": plan, "bufs": bufs,
                                "bytes": case.algorithmic_bytes(m)})
@@ -442,7 +444,8 @@ def run_sweep(args):
             foot = case.algorithmic_bytes(1)
             copies = max(1, min(8, -(-3 * l2 // foot)))
             bufs = [bsgemv.upload(case, "cuda") for _ in range(copies)]
-            with bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K, 16) as plan:
+            with bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K,
+                             max(shape.Ms)) as plan:
                 for M in shape.Ms:
                     # isolated cold
                     t = []

@@ -6,7 +6,7 @@
 //
 // Choices (the reasons are measurements on GB300; see the design notes):
 //   * 64 output columns per CTA tile, 8 consumer warps + 1 copy warp, 2 CTAs per SM;
-//   * a ring of up to 8 stages of 128 weight bytes per row, as deep as the shared-memory share
+//   * a ring of up to 12 stages of 128 weight bytes per row, as deep as the shared-memory share
 //     of a CTA allows (2 CTAs per SM), so that every SM keeps tens of KB of weight in flight;
 //   * stream-K: the tiles x stages work is split into equal contiguous ranges over
 //     min(total stages, 2 x SMs) persistent CTAs, which balances every shape to within one

@@ -26,7 +26,7 @@ constexpr int kRgPerWarp = 2;         // 16-row mma groups per consumer warp (2 
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kChunksPerStage = 8;    // 16-byte chunks of a weight row per stage (128 B)
 constexpr int kStageRowBytes = 16 * kChunksPerStage;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 
 // Error word bits written by kernels that abandon a bounded wait.
 constexpr unsigned kErrTimeoutFull = 1u;

@@ -64,6 +64,12 @@ BSG_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
+// Raise the barrier's expected transaction bytes without arriving.
+BSG_DEV void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
 BSG_DEV void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -469,41 +475,19 @@ struct Gemv {
   // the scale box and the zero-point box -- with 16-byte cp.async, whose completion is tracked
   // by the same full barrier (cp.async.mbarrier.arrive).  One TMA request stream per stage
   // keeps the TMA unit on the bulk data; rows past N and k past K are zero-filled.
-  static BSG_DEV void produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int lane) {
-    if (lane == 0) {
-      prefetch_tmap(&p.tm_w);
-      // Before the previous kernel has finished, warm L2 with this CTA's first weight boxes: the
-      // weight is never written by a preceding GEMV.  Activations, outputs and the workspace are
-      // touched only after pdl_wait.
-      int64_t t = s0 / p.spt;
-      int k = static_cast<int>(s0 - t * p.spt);
-      for (int64_t s = s0; s < s1 && s < s0 + sm.stages; ++s) {
-        tma_prefetch_l2_2d(&p.tm_w, k * kStageRowBytes, static_cast<int>(t * kRowsPerTile));
-        if (++k == p.spt) {
-          k = 0;
-          ++t;
-        }
-      }
-    }
-    pdl_wait();
-    const uint64_t pol = policy_evict_first();
-    const int64_t spt = p.spt, N = p.N, K = p.K;
-    constexpr uint32_t kTx = kRowsPerTile * kStageRowBytes;
-    constexpr int kUpr = kKc / 8;               // 16-byte activation units per row per stage
-    constexpr int kSu = kSpitch / 16;           // 16-byte units per scale box row
-    const int act_units = p.M * kUpr;
-    const int act_off = p.act_off, abox = p.act_box_bytes, sc_off = p.sc_off, zp_off = p.zp_off;
-    const int bs_log2 = p.bs_log2, spitch_g = p.scale_pitch, zpitch_g = p.zp_pitch;
-    const bool side_s = p.side_scale_tma != 0, side_z = ZP && p.side_zp_tma != 0;
-    int slot = 0;
-    uint32_t phase = 0;
-    int64_t tile = s0 / spt;
-    int ks = static_cast<int>(s0 - tile * spt);
-    for (int64_t s = s0; s < s1; ++s) {
-      if (!mbar_wait(sm.empty(slot), phase ^ 1u, p.err, kErrTimeoutEmpty)) break;
-      const uint32_t dst = sm.slot(slot), full = sm.full(slot);
-      const int64_t k0 = static_cast<int64_t>(ks) * kKc;
-      const int64_t row0 = tile * kRowsPerTile;
+  // Copies of one stage issued by the producer warp (`dst` = the slot, `full` = its barrier).
+  struct Stager {
+    const KParams& p;
+    int lane;
+    uint64_t pol;
+    int act_units, act_off, abox, sc_off, zp_off, bs_log2, spitch_g, zpitch_g;
+    bool side_s, side_z;
+    static constexpr int kUpr = kKc / 8;      // 16-byte activation units per row per stage
+    static constexpr int kSu = kSpitch / 16;  // 16-byte units per scale box row
+
+    // activations [M][k-range of the stage], written in the 128-byte-swizzled layout
+    BSG_DEV void act(uint32_t dst, int ks) const {
+      const int64_t k0 = static_cast<int64_t>(ks) * kKc, K = p.K;
       for (int u = lane; u < act_units; u += 32) {
         const int m = u / kUpr, qg = u % kUpr;
         const int q = qg & 7;
@@ -512,6 +496,10 @@ struct Gemv {
         const bool in = k < K;
         cp_async16(d, p.A + m * K + (in ? k : 0), in ? 16u : 0u);
       }
+    }
+    // scale box and zero-point box of the stage (weights: never written by a preceding GEMV)
+    BSG_DEV void side(uint32_t dst, int64_t tile, int ks) const {
+      const int64_t row0 = tile * kRowsPerTile, N = p.N;
       const int blk0 = (ks * kKc) >> bs_log2;
       if (side_s) {
         const int sx = (blk0 & ~(kSbw - 1)) * kScaleEs;  // byte offset of the box in a scale row
@@ -532,11 +520,92 @@ struct Gemv {
           cp_async16(dst + zp_off + r * 16, p.zp + (in ? n * zpitch_g + zx : 0), in ? 16u : 0u);
         }
       }
+    }
+    // the weight box (lane 0)
+    BSG_DEV void weight(uint32_t dst, uint32_t full, int64_t tile, int ks) const {
+      tma_load_2d_hint(dst, &p.tm_w, ks * kStageRowBytes, static_cast<int>(tile * kRowsPerTile),
+                       full, pol);
+    }
+  };
+
+  // ---- producer: warp 0.  Lane 0 copies each stage's weight box [64 rows][128 B] with one TMA
+  // (L2 evict-first: the weight is read once).  All 32 lanes copy the small pieces -- the
+  // activations [M][k of the stage] into the same 128-byte-swizzled layout TMA would write, the
+  // scale box and the zero-point box -- with 16-byte cp.async, whose completion is tracked by the
+  // same full barrier (cp.async.mbarrier.arrive).  One TMA request stream per stage keeps the
+  // TMA unit on the bulk data; rows past N and k past K are zero-filled.
+  //
+  // Programmatic dependent launch: while the previous kernel in the stream is still finishing,
+  // the first ring slots are filled with everything that is weight (W box, scales, zero points);
+  // only after pdl_wait are their activations copied and the slots released to the consumers.
+  static BSG_DEV void produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int lane) {
+    if (lane == 0) prefetch_tmap(&p.tm_w);
+    constexpr uint32_t kTx = kRowsPerTile * kStageRowBytes;
+    const Stager st{p, lane, policy_evict_first(), p.M * Stager::kUpr, p.act_off,
+                    p.act_box_bytes, p.sc_off, p.zp_off, p.bs_log2, p.scale_pitch, p.zp_pitch,
+                    p.side_scale_tma != 0, ZP && p.side_zp_tma != 0};
+    const int64_t spt = p.spt;
+    int64_t tile0 = s0 / spt;
+    const int ks0 = static_cast<int>(s0 - tile0 * spt);
+
+    // phase 1: weight of the first `pre` stages (fresh slots need no empty-barrier wait); the
+    // full barrier keeps its one pending arrival (lane 0, phase 2) until the activations land
+    const int pre = static_cast<int>((s1 - s0) < sm.stages ? (s1 - s0) : sm.stages);
+    {
+      int64_t tile = tile0;
+      int ks = ks0;
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t dst = sm.slot(i), full = sm.full(i);
+        st.side(dst, tile, ks);
+        cp_async_mbar_arrive(full);
+        if (lane == 0) {
+          mbar_expect_tx(full, kTx);
+          st.weight(dst, full, tile, ks);
+        }
+        if (++ks == spt) {
+          ks = 0;
+          ++tile;
+        }
+      }
+    }
+    pdl_wait();
+    // phase 2: activations of those stages, then lane 0's arrival releases each slot
+    {
+      int64_t tile = tile0;
+      int ks = ks0;
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t dst = sm.slot(i), full = sm.full(i);
+        st.act(dst, ks);
+        cp_async_mbar_arrive(full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full);
+        if (++ks == spt) {
+          ks = 0;
+          ++tile;
+        }
+      }
+    }
+    // steady state
+    int slot = pre % sm.stages;
+    uint32_t phase = (pre == sm.stages) ? 1u : 0u;
+    int64_t tile = tile0;
+    int ks = ks0;
+    for (int i = 0; i < pre; ++i) {
+      if (++ks == spt) {
+        ks = 0;
+        ++tile;
+      }
+    }
+    for (int64_t s = s0 + pre; s < s1; ++s) {
+      if (!mbar_wait(sm.empty(slot), phase ^ 1u, p.err, kErrTimeoutEmpty)) break;
+      const uint32_t dst = sm.slot(slot), full = sm.full(slot);
+      st.act(dst, ks);
+      st.side(dst, tile, ks);
       cp_async_mbar_arrive(full);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(full, kTx);
-        tma_load_2d_hint(dst, &p.tm_w, ks * kStageRowBytes, static_cast<int>(row0), full, pol);
+        st.weight(dst, full, tile, ks);
       }
       if (++slot == sm.stages) {
         slot = 0;

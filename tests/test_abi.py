@@ -104,7 +104,7 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
     # shared memory fits the residency it was sized for
     assert g["smem_bytes"] <= 232448
     assert g["ctas_per_sm"] * (g["smem_bytes"] + 1024) <= 233472
-    assert 2 <= g["stages"] <= 8
+    assert 2 <= g["stages"] <= 12
     assert g["sm_count"] == sms
     # the same inputs give the same geometry; act dtype does not change it
     assert bsgemv.geometry_for(fmt, "bf16", bs, zp, N, K, max_M, sms) == g

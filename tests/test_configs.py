@@ -1,5 +1,5 @@
 """Every synthetic workload configuration at its full size, in the launch configuration the
-benchmark times (plan max_M = 16, default geometry), checked against the oracle on sampled
+benchmark times (plan max_M = the configuration's largest M, default geometry), checked against the oracle on sampled
 output columns: the first and last two tiles (ragged tail included) and a seeded random
 sample in between, for every M of the configuration."""
 import numpy as np
@@ -28,7 +28,8 @@ def test_full_size_config(shape):
     case = shape.case(max(shape.Ms))
     d = bsgemv.upload(case, "cuda")
     rows = sample_rows(case.N, shape.seed)
-    with bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K, 16) as plan:
+    with bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K,
+                     max(shape.Ms)) as plan:
         outs = {}
         for M in shape.Ms:
             y = torch.empty((M, case.N), dtype=torch.int16, device="cuda")
