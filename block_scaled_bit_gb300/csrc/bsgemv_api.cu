@@ -1,9 +1,9 @@
 // bsgemv_api.cu -- the C ABI declared in include/bsgemv.h (host code).
 //
 // A plan holds the geometry (fixed per problem and device), the device workspace of the
-// stream-K reduction (partials, arrival counters, error word) and a small cache of the weight's
-// TMA tensor maps.  bsgemv_run validates, encodes a tensor map when W changes, and launches one
-// kernel on the caller's stream.
+// stream-K reduction (partials, arrival counters, error word) and a small cache of the operands'
+// TMA tensor maps.  bsgemv_run validates, encodes the tensor maps when W, scales or zp change,
+// and launches one kernel on the caller's stream.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -27,12 +27,15 @@ struct bsgemv_plan_s {
   unsigned* err = nullptr;
   void* stage = nullptr;      // bsgemv_run_host staging for A and y
   size_t stage_bytes = 0;
-  // weight tensor-map cache: the last few W pointers seen (e.g. rotating weight copies)
+  // tensor-map cache: the last few (W, scales, zp) pointer triples seen (e.g. rotating weight
+  // copies)
   struct MapEntry {
     bool valid = false;
     const void* W = nullptr;
+    const void* scales = nullptr;
+    const void* zp = nullptr;
     unsigned last_use = 0;
-    CUtensorMap tm_w;
+    bsg::OperandMaps maps;
   };
   static constexpr int kMapCache = 4;
   MapEntry maps[kMapCache];
@@ -42,36 +45,7 @@ struct bsgemv_plan_s {
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-int encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t dim0,
-              uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
-              CUtensorMapSwizzle swz) {
-  auto fn = encode_fn();
-  if (!fn) return BSGEMV_ERR_CUDA;
-  const cuuint64_t dims[2] = {dim0, dim1};
-  const cuuint64_t strides[1] = {stride1_bytes};
-  const cuuint32_t box[2] = {box0, box1};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? BSGEMV_OK : BSGEMV_ERR_CUDA;
-}
 
 int query_device(int* dev, int* sms) {
   if (cudaGetDevice(dev) != cudaSuccess) {
@@ -93,8 +67,9 @@ int query_device(int* dev, int* sms) {
 // (Re)allocate the workspace for the plan's current geometry; zeroed.
 int alloc_workspace(bsgemv_plan_s* p) {
   const bsgemv_geometry& g = p->geo.pub;
-  const size_t partial_bytes = size_t(g.ctas) * 2 * p->geo.slot_floats * sizeof(float);
-  const size_t counter_bytes = size_t(g.tiles) * sizeof(unsigned);
+  const size_t partial_bytes =
+      size_t(g.ctas) * 2 * bsg::kConsumerWarps * p->geo.slot_floats * sizeof(float);
+  const size_t counter_bytes = size_t(g.tiles) * bsg::kConsumerWarps * sizeof(unsigned);
   const size_t need = partial_bytes + counter_bytes + 256;
   if (need > p->ws_bytes) {
     if (p->ws) {
@@ -126,21 +101,12 @@ int rebuild_geometry(bsgemv_plan_s* p) {
   return alloc_workspace(p);
 }
 
-// Fill p->params for this call.  The weight tensor map is re-encoded only for a new W pointer.
+// Fill p->params for this call.  The tensor maps are re-encoded only for a new (W, scales, zp).
 int prepare_params(bsgemv_plan_s* p, const void* A, const void* W, const void* scales,
                    const void* zp, void* y, int M) {
-  const bsg::Geometry& g = p->geo;
-  bsg::KParams& k = p->params;
-  const bool int_fmt = (g.fmt == bsg::kInt4 || g.fmt == bsg::kInt8);
-  const int64_t row_bytes = (g.fmt == bsg::kInt4 || g.fmt == bsg::kNvfp4) ? g.K / 2 : g.K;
-  const int scale_pitch = g.nb_s * g.scale_es;
-  const int zp_pitch = (g.fmt == bsg::kInt4) ? (g.nb_s + 1) / 2 : g.nb_s;
-  const bool side_scale = (scale_pitch % 16 == 0) && aligned(scales, 16);
-  const bool side_zp = int_fmt && g.has_zp && (zp_pitch % 16 == 0) && aligned(zp, 16);
-
   bsgemv_plan_s::MapEntry* hit = nullptr;
   for (auto& e : p->maps)
-    if (e.valid && e.W == W) hit = &e;
+    if (e.valid && e.W == W && e.scales == scales && e.zp == zp) hit = &e;
   if (hit == nullptr) {
     // an empty entry if there is one, else the least recently used
     for (auto& e : p->maps)
@@ -151,51 +117,16 @@ int prepare_params(bsgemv_plan_s* p, const void* A, const void* W, const void* s
         if (e.last_use < hit->last_use) hit = &e;
     }
     hit->valid = false;
-    const int rc = encode_2d(&hit->tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, g.N,
-                             row_bytes, bsg::kStageRowBytes, bsg::kRowsPerTile,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
+    const int rc = bsg::encode_maps(p->geo, W, scales, zp, &hit->maps);
     if (rc != BSGEMV_OK) return rc;
     hit->valid = true;
     hit->W = W;
+    hit->scales = scales;
+    hit->zp = zp;
   }
   hit->last_use = ++p->use_clock;
-  k.tm_w = hit->tm_w;
-  k.A = static_cast<const uint16_t*>(A);
-  k.W = static_cast<const uint8_t*>(W);
-  k.scales = static_cast<const uint8_t*>(scales);
-  k.zp = int_fmt ? static_cast<const uint8_t*>(zp) : nullptr;
-  k.gscale = (g.fmt == bsg::kNvfp4) ? static_cast<const float*>(zp) : nullptr;
-  k.y = y;
-  k.partials = p->partials;
-  k.counters = p->counters;
-  k.err = p->err;
-  k.N = g.N;
-  k.K = g.K;
-  k.total_stages = g.pub.total_stages;
-  k.spt = g.pub.stages_per_tile;
-  k.M = M;
-  k.nb_s = g.nb_s;
-  int l2 = 0;
-  while ((1 << l2) < g.block_size) ++l2;
-  k.bs_log2 = l2;
-  k.scale_pitch = scale_pitch;
-  k.zp_pitch = zp_pitch;
-  k.stages = g.pub.stages;
-  k.slot_bytes = g.slot_bytes;
-  k.act_off = g.act_off;
-  k.sc_off = g.sc_off;
-  k.zp_off = g.zp_off;
-  k.act_box_bytes = g.act_box_bytes;
-  k.ring_bytes = g.ring_bytes;
-  k.red_off = g.red_off;
-  k.bar_off = g.bar_off;
-  k.sbw = g.sbw;
-  k.zbw_bytes = g.zbw_bytes;
-  k.zblk = g.zblk;
-  k.side_scale_tma = side_scale ? 1 : 0;
-  k.side_zp_tma = side_zp ? 1 : 0;
-  k.slot_floats = g.slot_floats;
-  k.tx_bytes = bsg::kRowsPerTile * bsg::kStageRowBytes;
+  bsg::fill_params(p->geo, hit->maps, A, W, scales, zp, y, M, p->partials, p->counters, p->err,
+                   &p->params);
   return BSGEMV_OK;
 }
 
@@ -227,25 +158,7 @@ int validate_run(const bsgemv_plan_s* p, const void* A, const void* W, const voi
   return BSGEMV_OK;
 }
 
-int launch(bsgemv_plan_s* p, cudaStream_t s) {
-  const bsg::Geometry& g = p->geo;
-  const bsg::KParams& k = p->params;
-  const int mt = k.M > 8 ? 2 : 1;
-  const int ctas = g.pub.ctas, smem = g.pub.smem_bytes;
-  const int bm = bsg::block_mode(g.fmt, g.block_size);
-  switch (g.fmt) {
-    case bsg::kInt4:
-      return g.bf16 ? bsg::launch_int4_bf16(k, mt, g.has_zp, bm, ctas, smem, s)
-                    : bsg::launch_int4_f16(k, mt, g.has_zp, bm, ctas, smem, s);
-    case bsg::kInt8:
-      return bsg::launch_int8(k, mt, g.bf16, g.has_zp, bm, ctas, smem, s);
-    case bsg::kFp8:
-      return bsg::launch_fp8(k, mt, g.bf16, false, bm, ctas, smem, s);
-    case bsg::kNvfp4:
-      return bsg::launch_nvfp4(k, mt, g.bf16, false, bm, ctas, smem, s);
-  }
-  return BSGEMV_ERR_INVALID_ARG;
-}
+int launch(bsgemv_plan_s* p, cudaStream_t s) { return bsg::launch_gemv(p->geo, p->params, s); }
 
 }  // namespace
 

@@ -5,11 +5,15 @@
 // per-row summation order (rows are bit-identical across M).
 //
 // Choices (the reasons are measurements on GB300; see the design notes):
-//   * 64 output columns per CTA tile, 8 consumer warps + 1 copy warp, 2 CTAs per SM;
-//   * a ring of up to 12 stages of 128 weight bytes per row, as deep as the shared-memory share
-//     of a CTA allows (2 CTAs per SM), so that every SM keeps tens of KB of weight in flight;
+//   * 64 output columns per CTA tile, 4 consumer warps (one 16-row group each, over all 128
+//     bytes of a stage) + 1 copy warp, 4 CTAs per SM;
+//   * a ring of up to 12 stages of 128 weight bytes per row (plus the stage's activations), as
+//     deep as the shared-memory share of a CTA allows (4 CTAs per SM), so that every SM keeps
+//     tens of KB of weight in flight;
+//   * a side ring of scale / zero-point boxes, each covering 64 bytes of scales per row (4 to
+//     64 stages), so that side data costs one TMA per box instead of copies every stage;
 //   * stream-K: the tiles x stages work is split into equal contiguous ranges over
-//     min(total stages, 2 x SMs) persistent CTAs, which balances every shape to within one
+//     min(total stages, 4 x SMs) persistent CTAs, which balances every shape to within one
 //     stage per CTA without a wave tail.
 #include <algorithm>
 #include <cstdint>
@@ -23,7 +27,7 @@ namespace {
 constexpr int kSmemPerSm = 233472;       // 228 KB shared memory per SM on sm_100-class parts
 constexpr int kSmemPerBlockMax = 232448; // 227 KB opt-in maximum per CTA
 constexpr int kReservedPerBlock = 1024;  // reserved by the system per resident CTA
-constexpr int kCtasPerSm = 2;
+constexpr int kCtasPerSm = kMinCtasPerSm;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -71,32 +75,41 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   g->kpc = four ? 32 : 16;
   g->kc = kChunksPerStage * g->kpc;
   g->nbox = g->kc / 64;
-  g->mpad = max_M <= 8 ? 8 : 16;
-  g->mt_max = g->mpad / 8;
+  g->mt_max = max_M <= 8 ? 1 : 2;
   g->scale_es = (fmt == kFp8) ? 4 : (fmt == kNvfp4 ? 1 : 2);
   g->nb_s = static_cast<int>(K / block_size);
-  const int bps = std::max(1, g->kc / block_size);  // scale blocks per stage
-  g->sbw = std::max(16 / g->scale_es, bps);
-  if (fmt == kInt4) {
-    g->zbw_bytes = std::max(16, bps / 2);
-    g->zblk = 2 * g->zbw_bytes;
-  } else {
-    g->zbw_bytes = std::max(16, bps);
-    g->zblk = g->zbw_bytes;
-  }
+  g->scale_pitch = g->nb_s * g->scale_es;
+  g->zp_pitch = (fmt == kInt4) ? (g->nb_s + 1) / 2 : g->nb_s;
 
-  // one ring slot: [W 64 x 128 B][activation boxes][scales][zero points]
-  g->act_box_bytes = g->mpad * 128;
-  g->act_off = kRowsPerTile * kStageRowBytes;
-  g->sc_off = g->act_off + g->nbox * g->act_box_bytes;
-  g->zp_off = g->sc_off + kRowsPerTile * g->sbw * g->scale_es;
-  const int slot_end = g->zp_off + (has_zp ? kRowsPerTile * g->zbw_bytes : 0);
-  g->slot_bytes = static_cast<int>(ceil_div(slot_end, 1024) * 1024);
-  g->red_bytes = kConsumerWarps * kRgPerWarp * g->mt_max * 32 * 16;
-  g->slot_floats = 4 * g->mt_max * 32 * 4;
+  // activation ring: per stage, nbox boxes of 64 k x max_M rows (128 B per row)
+  g->act_box_bytes = max_M * 128;
+  g->act_bytes = g->nbox * g->act_box_bytes;
+  // side ring: one box holds kSideScaleBytes of scales per row (64 / es blocks), i.e.
+  // 2^rs_log2 stages, and the zero points of the same blocks
+  const int blocks_per_box = kSideScaleBytes / g->scale_es;
+  const int64_t stages_per_box = int64_t(blocks_per_box) * block_size / g->kc;
+  g->rs_log2 = 0;
+  while ((int64_t(1) << (g->rs_log2 + 1)) <= stages_per_box) ++g->rs_log2;
+  g->zbox_bytes = (fmt == kInt4) ? blocks_per_box / 2 : blocks_per_box;
+  const bool side_possible = (g->scale_pitch % 16 == 0) && (!has_zp || g->zp_pitch % 16 == 0);
+  g->side_bytes = side_possible
+                      ? static_cast<int>(ceil_div(kRowsPerTile * (kSideScaleBytes +
+                                                                  (has_zp ? g->zbox_bytes : 0)),
+                                                  128) * 128)
+                      : 0;
+  g->slot_floats = g->mt_max * 32 * 4;
 
+  const int64_t spt = ceil_div(K, g->kc);
+  // side boxes in flight over a ring of `stages`: a box spans min(2^rs, stages per tile) stages
+  auto side_slots_for = [&](int stages) {
+    if (g->side_bytes == 0) return 0;
+    const int64_t span = std::min<int64_t>(int64_t(1) << g->rs_log2, spt);
+    return static_cast<int>(std::min<int64_t>(4, std::max<int64_t>(2, ceil_div(stages, span) + 1)));
+  };
   auto smem_for = [&](int stages) {
-    return stages * g->slot_bytes + g->red_bytes + 16 * stages + 16 + 1024;
+    const int ss = side_slots_for(stages);
+    return 1024 + stages * (kStageBytes + g->act_bytes) + ss * g->side_bytes +
+           8 * (2 * stages + 8);
   };
   int ctas_per_sm = kCtasPerSm;
   const int budget = kSmemPerSm / ctas_per_sm - kReservedPerBlock;
@@ -112,9 +125,10 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
     stages = stages_override;
     if (smem_for(stages) > budget) ctas_per_sm = 1;
   }
-  g->ring_bytes = stages * g->slot_bytes;
-  g->red_off = g->ring_bytes;
-  g->bar_off = g->red_off + g->red_bytes;
+  g->side_slots = side_slots_for(stages);
+  g->act_off = stages * kStageBytes;
+  g->side_off = g->act_off + stages * g->act_bytes;
+  g->bar_off = g->side_off + g->side_slots * g->side_bytes;
 
   bsgemv_geometry& pub = g->pub;
   pub.variant = BSGEMV_VARIANT_MMA;
@@ -131,8 +145,9 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   if (ctas_override > 0) ctas = std::min<int64_t>(pub.total_stages, ctas_override);
   pub.ctas = static_cast<int>(ctas);
   pub.smem_bytes = smem_for(stages);
-  // workspace: partial slots [ctas][2], counters [tiles], error word
-  pub.workspace_bytes = int64_t(pub.ctas) * 2 * g->slot_floats * 4 + pub.tiles * 4 + 256;
+  // workspace: partial slots [ctas][2][warps], counters [tiles][warps], error word
+  pub.workspace_bytes = int64_t(pub.ctas) * 2 * kConsumerWarps * g->slot_floats * 4 +
+                        pub.tiles * kConsumerWarps * 4 + 256;
   return BSGEMV_OK;
 }
 

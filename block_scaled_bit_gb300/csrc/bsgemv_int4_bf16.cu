@@ -3,8 +3,8 @@
 
 namespace bsg {
 
-int launch_int4_bf16(const KParams& p, int mt, bool zp, int bmode, int ctas, int smem, cudaStream_t s) {
-  return launch_fmt<kInt4, true>(p, mt, zp, bmode, ctas, smem, s);
+int launch_int4_bf16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
+  return launch_fmt<kInt4, true>(p, mt, zp, cpb, ctas, smem, s);
 }
 
 }  // namespace bsg

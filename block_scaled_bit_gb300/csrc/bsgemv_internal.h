@@ -21,9 +21,9 @@ namespace bsg {
 enum Fmt : int { kInt4 = 1, kInt8 = 2, kFp8 = 3, kNvfp4 = 4 };
 
 constexpr int kRowsPerTile = 64;      // output columns per CTA tile (4 mma row groups of 16)
-constexpr int kConsumerWarps = 8;     // decode + mma warps; warp 0 issues the copies
-constexpr int kRgPerWarp = 2;         // 16-row mma groups per consumer warp (2 of the tile's 4)
+constexpr int kConsumerWarps = 4;     // decode + mma warps (one 16-row group each); warp 0 copies
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kMinCtasPerSm = 4;      // register budget: 4 CTAs of kThreads per SM
 constexpr int kChunksPerStage = 8;    // 16-byte chunks of a weight row per stage (128 B)
 constexpr int kStageRowBytes = 16 * kChunksPerStage;
 constexpr int kMaxStages = 12;
@@ -35,35 +35,39 @@ constexpr unsigned kErrTimeoutEmpty = 2u;
 // Kernel parameters (passed by value as a __grid_constant__; the tensor maps must be 64-byte
 // aligned in parameter space).
 struct KParams {
-  CUtensorMap tm_w;   // W  as uint8 [N][row_bytes], box [kRowsPerTile][128], 128B swizzle
+  CUtensorMap tm_w;   // W as uint8 [N][row_bytes], box [kRowsPerTile][128], 128B swizzle
+  CUtensorMap tm_s;   // scales as uint8 [N][scale_pitch], box [kRowsPerTile][kSideScaleBytes]
+  CUtensorMap tm_z;   // zero points as uint8 [N][zp_pitch], box [kRowsPerTile][zbox_bytes]
   const uint16_t* A;       // activations [M][K] (fp16 / bf16 bits)
   const uint8_t* W;
-  const uint8_t* scales;   // global copy, used when the scale tensor cannot be TMA-tiled
+  const uint8_t* scales;   // global copy, read directly when side_tma == 0
   const uint8_t* zp;       // idem for zero points
   const float* gscale;     // NVFP4 global scale
   void* y;
-  float* partials;         // [ctas][2][slot_floats] cross-CTA partial sums
-  unsigned* counters;      // [tiles] arrival counters, left at zero by every call
+  float* partials;         // [ctas][2][kConsumerWarps][slot_floats] cross-CTA partial sums
+  unsigned* counters;      // [tiles][kConsumerWarps] arrival counters, left at zero by every call
   unsigned* err;           // error word
   int64_t N, K;
   int64_t total_stages;    // tiles * spt
-  int64_t spt;             // stages per tile
+  int spt;                 // stages per tile
   int M;
   int nb_s;                // scale elements per row (K/bs, or K/16 for nvfp4)
   int bs_log2;
   int scale_pitch;         // bytes per scale row (global)
   int zp_pitch;            // bytes per zero-point row (global)
-  int stages;              // ring depth
-  int slot_bytes, act_off, sc_off, zp_off;  // offsets inside one ring slot
-  int act_box_bytes;       // smem bytes per activation box (MPAD * 128)
-  int ring_bytes, red_off, bar_off;
-  int tx_bytes;            // bytes landing per stage
-  int sbw;                 // scale box width in elements (blocks)
-  int zbw_bytes;           // zero-point box width in bytes
-  int zblk;                // blocks covered by one zero-point box
-  int side_scale_tma;      // 1: scales are staged into the ring; 0: read from global memory
-  int side_zp_tma;         // idem for zero points
-  int slot_floats;         // floats per partial slot
+  int stages;              // weight / activation ring depth
+  int act_off;             // activation ring: stages x act_bytes
+  int act_bytes;           // activation bytes per stage (act_box_bytes per 64 k)
+  int act_box_bytes;       // max_M * 128
+  int side_tma;            // 1: scales / zero points staged by TMA into the side ring
+  int side_off;            // side ring: side_slots x side_bytes
+  int side_bytes;          // one side box: scales [64][kSideScaleBytes], zero points after
+  int side_slots;
+  int side_tx;             // bytes one side box lands (scales + zero points)
+  int zbox_bytes;          // zero-point box width in bytes
+  int rs_log2;             // log2(stages per side box)
+  int bar_off;
+  int slot_floats;         // floats per partial slot (one warp's fragments)
 };
 
 struct Geometry {
@@ -72,42 +76,65 @@ struct Geometry {
   int64_t N, K;
   int kpc;                 // k per 16-byte chunk
   int kc;                  // k per stage
-  int nbox;                // activation boxes per stage
-  int mpad;                // activation rows reserved per box (8 or 16)
+  int nbox;                // activation boxes (64 k) per stage
   int mt_max;              // 1 or 2 n8 mma tiles
   int scale_es;            // bytes per scale element
   int nb_s;
-  int sbw, zbw_bytes, zblk;
-  int slot_bytes, act_off, sc_off, zp_off, act_box_bytes, red_bytes, ring_bytes, red_off,
-      bar_off;
+  int scale_pitch, zp_pitch;
+  int act_box_bytes, act_bytes, act_off;
+  int rs_log2, side_slots, side_bytes, zbox_bytes, side_off;
+  int bar_off;
   int slot_floats;
 };
+
+// Stage weight bytes per row, and scale bytes per row of one side box.
+constexpr int kStageBytes = kRowsPerTile * kStageRowBytes;
+constexpr int kSideScaleBytes = 64;
 
 // Validates the problem and fills the geometry for `sm_count` SMs.  Pure host code.
 int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
                      int sm_count, int ctas_override, int stages_override, Geometry* g);
 
 // Kernel launchers (one translation unit per weight format; int4 split by activation type).
-// bmode: 0 = one scale block per 16-byte chunk, 1 = a consumer warp's chunk pair in one block,
-// 2 = two blocks per chunk (int4 with 16-element blocks).
-int launch_int4_f16(const KParams& p, int mt, bool zp, int bmode, int ctas, int smem,
+// cpb: see block_mode.
+int launch_int4_f16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
                     cudaStream_t s);
-int launch_int4_bf16(const KParams& p, int mt, bool zp, int bmode, int ctas, int smem,
+int launch_int4_bf16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
                      cudaStream_t s);
-int launch_int8(const KParams& p, int mt, bool bf16, bool zp, int bmode, int ctas, int smem,
-                cudaStream_t s);
-int launch_fp8(const KParams& p, int mt, bool bf16, bool zp, int bmode, int ctas, int smem,
+int launch_int8_f16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                    cudaStream_t s);
+int launch_int8_bf16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                     cudaStream_t s);
+int launch_fp8(const KParams& p, int mt, bool bf16, bool zp, int cpb, int ctas, int smem,
                cudaStream_t s);
-int launch_nvfp4(const KParams& p, int mt, bool bf16, bool zp, int bmode, int ctas, int smem,
+int launch_nvfp4(const KParams& p, int mt, bool bf16, bool zp, int cpb, int ctas, int smem,
                  cudaStream_t s);
 
-// Block mode of a problem (see above).
+// Chunks (16 bytes of a weight row) per scale block, the kernel's CPB: 0 when a chunk holds two
+// blocks, else bs / k-per-chunk capped at 8 (a block spanning a whole stage or more).  NVFP4
+// folds its scales and uses 1.
 inline int block_mode(int fmt, int block_size) {
-  if (fmt == kInt4) return block_size == 16 ? 2 : (block_size == 32 ? 0 : 1);
-  if (fmt == kInt8) return block_size == 16 ? 0 : 1;
-  if (fmt == kFp8) return 1;
-  return 0;
+  if (fmt == kNvfp4) return 1;
+  const int k_per_chunk = (fmt == kInt4) ? 32 : 16;
+  if (block_size < k_per_chunk) return 0;
+  const int c = block_size / k_per_chunk;
+  return c >= 8 ? 8 : c;
 }
+
+// TMA tensor maps of one call's operands.  side_tma: the scales (and zero points) could be
+// tiled (16-byte aligned base and pitch), so the kernel stages them through its side ring.
+struct OperandMaps {
+  CUtensorMap tm_w, tm_s, tm_z;
+  bool side_tma;
+};
+
+// Host helpers shared by the entry points (bsgemv_host.cpp).
+int encode_maps(const Geometry& g, const void* W, const void* scales, const void* zp,
+                OperandMaps* m);
+void fill_params(const Geometry& g, const OperandMaps& m, const void* A, const void* W,
+                 const void* scales, const void* zp, void* y, int M, float* partials,
+                 unsigned* counters, unsigned* err, KParams* k);
+int launch_gemv(const Geometry& g, const KParams& k, cudaStream_t s);
 
 int launch_debug_dequant(int fmt, bool bf16, bool has_zp, int bs, int64_t N, int64_t K,
                          const uint8_t* W, const uint8_t* scales, const uint8_t* zp,

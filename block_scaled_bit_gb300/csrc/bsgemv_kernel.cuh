@@ -199,6 +199,15 @@ BSG_DEV uint32_t lds8(uint32_t addr) {
   return v;
 }
 
+// Plain shared-memory load of a T at p (p derived from the kernel's shared array).  Unlike an
+// asm statement, the compiler may reorder these among themselves and hoist them to cover
+// latency; the "memory" clobbers of the barrier waits and arrivals keep them inside the slot's
+// ownership window.
+template <typename T>
+BSG_DEV T lsh(const uint8_t* p) {
+  return *reinterpret_cast<const T*>(p);
+}
+
 BSG_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -213,13 +222,13 @@ BSG_DEV void named_bar_sync(int id, int count) {
 template <bool BF16>
 BSG_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   if constexpr (BF16) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   } else {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -232,13 +241,13 @@ template <bool BF16>
 BSG_DEV void mma16816_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   const float z = 0.f;
   if constexpr (BF16) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
   } else {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -437,273 +446,298 @@ BSG_DEV void zp_consts(uint32_t zp, uint32_t& zl, uint32_t& zh) {
 }
 
 // ------------------------------------------------------------------------------ the kernel
-// Scale-block grouping of a consumer warp's two chunks (k = 32 per chunk for the 4-bit formats,
-// 16 for the 8-bit formats):
-//   kBlockPerChunk  block == chunk k-range: scale after every chunk       (int4 bs32, int8 bs16)
-//   kBlockPerPair   both chunks in one block: scale once per stage        (bs >= 2 chunks, fp8)
-//   kTwoPerChunk    a chunk holds two blocks, quad lanes t < 2 and t >= 2 (int4 bs16)
-enum BlockMode : int { kBlockPerChunk = 0, kBlockPerPair = 1, kTwoPerChunk = 2 };
+// Scale blocks of the weight formats, per 16-byte chunk of a row (k = 32 per chunk for the 4-bit
+// formats, 16 for the 8-bit formats): the kernel's CPB template parameter is the number of
+// chunks per scale block -- 0 when a chunk holds two blocks (int4 with 16-element blocks), 1, 2,
+// 4, or 8 for a block of a whole stage or more (larger blocks, fp8).  NVFP4 folds its scales
+// into the decoded values and uses 1.
 
-template <int FMT, bool BF16, int MT, bool ZP, int BMODE>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB>
 struct Gemv {
   static constexpr bool kFour = (FMT == kInt4 || FMT == kNvfp4);
   static constexpr int kKpc = kFour ? 32 : 16;  // k per 16-byte chunk
   static constexpr int kSteps = kKpc / 16;      // mma k-steps per chunk
   static constexpr int kKc = kChunksPerStage * kKpc;
-  static constexpr int kNbox = kKc / 64;        // activation boxes per stage
+  static constexpr int kNbox = kKc / 64;        // activation boxes (64 k) per stage
   static constexpr bool kFold = (FMT == kNvfp4);
-  static constexpr int kSub = (BMODE == kTwoPerChunk) ? 2 : 1;
+  static constexpr int kSub = (CPB == 0) ? 2 : 1;  // scale blocks per chunk (int4, 16-element blocks)
   static constexpr int kScaleEs = (FMT == kFp8) ? 4 : (FMT == kNvfp4 ? 1 : 2);
-  // scale box width in blocks (16 bytes, or 32 bytes when a stage holds 16 int4 blocks)
-  static constexpr int kSbw = (FMT == kFp8) ? 4 : ((FMT == kNvfp4 || BMODE == kTwoPerChunk) ? 16 : 8);
-  static constexpr int kSpitch = kSbw * kScaleEs;  // bytes per row of the scale box
-  static constexpr int kZblk = (FMT == kInt4) ? 32 : 16;  // blocks per 16-byte zero-point box row
+  static constexpr int kZpW = (FMT == kInt4) ? 4 : 8;  // zero-point bits per block
 
+  // Shared memory: [W ring: stages x 8 KB][activation ring][side ring][barriers].
+  // The weight boxes are 1024-byte aligned (128-byte swizzle atoms).
   struct Smem {
-    uint8_t* base;
-    int stages, slot_bytes, bar_off, red_off;
-    BSG_DEV uint32_t slot(int i) const { return smem_u32(base) + i * slot_bytes; }
-    BSG_DEV uint32_t full(int i) const { return smem_u32(base) + bar_off + 8 * i; }
-    BSG_DEV uint32_t empty(int i) const { return smem_u32(base) + bar_off + 8 * (stages + i); }
-    BSG_DEV float4* red() const { return reinterpret_cast<float4*>(base + red_off); }
-    BSG_DEV int* flag() const { return reinterpret_cast<int*>(base + bar_off + 16 * stages); }
+    uint8_t* base;    // generic pointer into the kernel's shared array
+    uint32_t base_u;  // the same address in the shared window
+    int stages, act_off, act_bytes, side_off, side_bytes, side_slots, bar_off;
+    BSG_DEV uint32_t w(int i) const { return base_u + i * kStageBytes; }
+    BSG_DEV const uint8_t* act(int i) const { return base + act_off + i * act_bytes; }
+    BSG_DEV uint32_t act_u(int i) const { return base_u + act_off + i * act_bytes; }
+    BSG_DEV const uint8_t* side(int j) const { return base + side_off + j * side_bytes; }
+    BSG_DEV uint32_t side_u(int j) const { return base_u + side_off + j * side_bytes; }
+    BSG_DEV uint32_t full(int i) const { return base_u + bar_off + 8 * i; }
+    BSG_DEV uint32_t empty(int i) const { return base_u + bar_off + 8 * (stages + i); }
+    BSG_DEV uint32_t sfull(int j) const { return base_u + bar_off + 8 * (2 * stages + j); }
+    BSG_DEV uint32_t sempty(int j) const { return base_u + bar_off + 8 * (2 * stages + 4 + j); }
   };
 
-  // ---- producer: warp 0.  Lane 0 copies the stage's weight box [64 rows][128 B] with one TMA
-  // (L2 evict-first: the weight is read once).  All 32 lanes copy the small pieces -- the
-  // activations [M][k of the stage] into the same 128-byte-swizzled layout TMA would write,
-  // the scale box and the zero-point box -- with 16-byte cp.async, whose completion is tracked
-  // by the same full barrier (cp.async.mbarrier.arrive).  One TMA request stream per stage
-  // keeps the TMA unit on the bulk data; rows past N and k past K are zero-filled.
-  // Copies of one stage issued by the producer warp (`dst` = the slot, `full` = its barrier).
-  struct Stager {
-    const KParams& p;
-    int lane;
-    uint64_t pol;
-    int act_units, act_off, abox, sc_off, zp_off, bs_log2, spitch_g, zpitch_g;
-    bool side_s, side_z;
-    static constexpr int kUpr = kKc / 8;      // 16-byte activation units per row per stage
-    static constexpr int kSu = kSpitch / 16;  // 16-byte units per scale box row
+  // Position in a CTA's stream-K range: stage ks of `tile`.  The side ring holds one box of
+  // scales / zero points per 2^rs_log2 stages of a tile; a stage opens a box when it is the
+  // first of the CTA's segment on that tile or the first of its box, and closes it when it is
+  // the last of the segment or of the box.  Producer and consumers walk the same sequence.
+  struct Walk {
+    int64_t tile;
+    int ks, spt, rsm;
+    BSG_DEV bool opens(bool seg_first) const { return seg_first || (ks & rsm) == 0; }
+    BSG_DEV bool closes(bool seg_last) const { return seg_last || ((ks + 1) & rsm) == 0; }
+    BSG_DEV void next() {
+      if (++ks == spt) {
+        ks = 0;
+        ++tile;
+      }
+    }
+  };
 
-    // activations [M][k-range of the stage], written in the 128-byte-swizzled layout
-    BSG_DEV void act(uint32_t dst, int ks) const {
-      const int64_t k0 = static_cast<int64_t>(ks) * kKc, K = p.K;
-      for (int u = lane; u < act_units; u += 32) {
-        const int m = u / kUpr, qg = u % kUpr;
-        const int q = qg & 7;
-        const uint32_t d = dst + act_off + (qg >> 3) * abox + m * 128 + ((q ^ (m & 7)) << 4);
-        const int64_t k = k0 + qg * 8;
-        const bool in = k < K;
-        cp_async16(d, p.A + m * K + (in ? k : 0), in ? 16u : 0u);
+  // Ring position: slot index and the parity of its current use.
+  struct Ring {
+    int slot;
+    uint32_t phase;
+    int size;
+    BSG_DEV void next() {
+      if (++slot == size) {
+        slot = 0;
+        phase ^= 1u;
       }
-    }
-    // scale box and zero-point box of the stage (weights: never written by a preceding GEMV)
-    BSG_DEV void side(uint32_t dst, int64_t tile, int ks) const {
-      const int64_t row0 = tile * kRowsPerTile, N = p.N;
-      const int blk0 = (ks * kKc) >> bs_log2;
-      if (side_s) {
-        const int sx = (blk0 & ~(kSbw - 1)) * kScaleEs;  // byte offset of the box in a scale row
-        for (int u = lane; u < kRowsPerTile * kSu; u += 32) {
-          const int r = u / kSu, v = u % kSu;
-          const int64_t n = row0 + r;
-          const bool in = n < N && sx + v * 16 < spitch_g;
-          cp_async16(dst + sc_off + r * kSpitch + v * 16,
-                     p.scales + (in ? n * spitch_g + sx + v * 16 : 0), in ? 16u : 0u);
-        }
-      }
-      if (side_z) {
-        const int xb = blk0 & ~(kZblk - 1);
-        const int zx = (FMT == kInt4) ? xb / 2 : xb;
-        for (int r = lane; r < kRowsPerTile; r += 32) {
-          const int64_t n = row0 + r;
-          const bool in = n < N && zx < zpitch_g;
-          cp_async16(dst + zp_off + r * 16, p.zp + (in ? n * zpitch_g + zx : 0), in ? 16u : 0u);
-        }
-      }
-    }
-    // the weight box (lane 0)
-    BSG_DEV void weight(uint32_t dst, uint32_t full, int64_t tile, int ks) const {
-      tma_load_2d_hint(dst, &p.tm_w, ks * kStageRowBytes, static_cast<int>(tile * kRowsPerTile),
-                       full, pol);
     }
   };
 
   // ---- producer: warp 0.  Lane 0 copies each stage's weight box [64 rows][128 B] with one TMA
-  // (L2 evict-first: the weight is read once).  All 32 lanes copy the small pieces -- the
-  // activations [M][k of the stage] into the same 128-byte-swizzled layout TMA would write, the
-  // scale box and the zero-point box -- with 16-byte cp.async, whose completion is tracked by the
-  // same full barrier (cp.async.mbarrier.arrive).  One TMA request stream per stage keeps the
-  // TMA unit on the bulk data; rows past N and k past K are zero-filled.
+  // (L2 evict-first: the weight is read once) and, once per side box, the scale box [64][64 B]
+  // and zero-point box [64][16 or 32 B] (two more TMAs on the side ring).  All 32 lanes copy the
+  // stage's activations [M][k of the stage] with 16-byte cp.async, tracked by the stage's full
+  // barrier (cp.async.mbarrier.arrive).  Rows past N and k past K are zero-filled.
   //
   // Programmatic dependent launch: while the previous kernel in the stream is still finishing,
-  // the first ring slots are filled with everything that is weight (W box, scales, zero points);
-  // only after pdl_wait are their activations copied and the slots released to the consumers.
-  static BSG_DEV void produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int lane) {
-    if (lane == 0) prefetch_tmap(&p.tm_w);
-    constexpr uint32_t kTx = kRowsPerTile * kStageRowBytes;
-    const Stager st{p, lane, policy_evict_first(), p.M * Stager::kUpr, p.act_off,
-                    p.act_box_bytes, p.sc_off, p.zp_off, p.bs_log2, p.scale_pitch, p.zp_pitch,
-                    p.side_scale_tma != 0, ZP && p.side_zp_tma != 0};
-    const int64_t spt = p.spt;
-    int64_t tile0 = s0 / spt;
-    const int ks0 = static_cast<int>(s0 - tile0 * spt);
+  // the first ring slots are filled with everything that is weight (W boxes, side boxes); only
+  // after pdl_wait are their activations copied and the slots released to the consumers.  That
+  // prefill never waits on a consumer release (which could not come before pdl_wait).
+  static BSG_DEV void act_copy(const KParams& p, uint32_t dst, int ks, int lane) {
+    constexpr int kUpr = kKc / 8;  // 16-byte activation units per row per stage
+    const int units = p.M * kUpr;
+    const int64_t k0 = static_cast<int64_t>(ks) * kKc, K = p.K;
+    for (int u = lane; u < units; u += 32) {
+      const int m = u / kUpr, qg = u % kUpr;
+      const int q = qg & 7;
+      const uint32_t d = dst + (qg >> 3) * p.act_box_bytes + m * 128 + ((q ^ (m & 7)) << 4);
+      const int64_t k = k0 + qg * 8;
+      const bool in = k < K;
+      cp_async16(d, p.A + m * K + (in ? k : 0), in ? 16u : 0u);
+    }
+  }
 
-    // phase 1: weight of the first `pre` stages (fresh slots need no empty-barrier wait); the
-    // full barrier keeps its one pending arrival (lane 0, phase 2) until the activations land
-    const int pre = static_cast<int>((s1 - s0) < sm.stages ? (s1 - s0) : sm.stages);
+  static BSG_DEV void side_copy(const KParams& p, const Smem& sm, int j, const Walk& w,
+                                uint64_t pol) {
+    const uint32_t full = sm.sfull(j), dst = sm.side_u(j);
+    const int bx = w.ks >> p.rs_log2;
+    const int row = static_cast<int>(w.tile * kRowsPerTile);
+    mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.side_tx));
+    tma_load_2d_hint(dst, &p.tm_s, bx * kSideScaleBytes, row, full, pol);
+    if constexpr (ZP)
+      tma_load_2d_hint(dst + kRowsPerTile * kSideScaleBytes, &p.tm_z, bx * p.zbox_bytes, row, full,
+                       pol);
+  }
+
+  static BSG_DEV void produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int lane) {
+    const bool side = p.side_tma != 0;
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_w);
+      if (side) {
+        prefetch_tmap(&p.tm_s);
+        if constexpr (ZP) prefetch_tmap(&p.tm_z);
+      }
+    }
+    const uint64_t pol = policy_evict_first();
+    const int spt = p.spt;
+    const int n = static_cast<int>(s1 - s0);
+    const int64_t tile0 = s0 / spt;
+    const Walk start{tile0, static_cast<int>(s0 - tile0 * spt), spt, (1 << p.rs_log2) - 1};
+    Ring sr{sm.side_slots - 1, 1u, sm.side_slots};  // side ring: advanced before each use
+
+    // phase 1: weights (and side boxes) of the first `pre` stages; fresh slots, no waits
+    int pre = 0;
     {
-      int64_t tile = tile0;
-      int ks = ks0;
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t dst = sm.slot(i), full = sm.full(i);
-        st.side(dst, tile, ks);
-        cp_async_mbar_arrive(full);
+      Walk w = start;
+      int boxes = 0;
+      const int lim = n < sm.stages ? n : sm.stages;
+      for (int i = 0; i < lim; ++i) {
+        const bool seg_first = (i == 0) || (w.ks == 0);
+        if (side && w.opens(seg_first)) {
+          if (boxes == sm.side_slots) break;  // the next box would reuse a slot: wait for phase 3
+          ++boxes;
+          sr.next();
+          if (lane == 0) side_copy(p, sm, sr.slot, w, pol);
+        }
         if (lane == 0) {
-          mbar_expect_tx(full, kTx);
-          st.weight(dst, full, tile, ks);
+          mbar_expect_tx(sm.full(i), kStageBytes);
+          tma_load_2d_hint(sm.w(i), &p.tm_w, w.ks * kStageRowBytes,
+                           static_cast<int>(w.tile * kRowsPerTile), sm.full(i), pol);
         }
-        if (++ks == spt) {
-          ks = 0;
-          ++tile;
-        }
+        pre = i + 1;
+        w.next();
       }
     }
     pdl_wait();
-    // phase 2: activations of those stages, then lane 0's arrival releases each slot
-    {
-      int64_t tile = tile0;
-      int ks = ks0;
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t dst = sm.slot(i), full = sm.full(i);
-        st.act(dst, ks);
-        cp_async_mbar_arrive(full);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full);
-        if (++ks == spt) {
-          ks = 0;
-          ++tile;
-        }
-      }
-    }
-    // steady state
-    int slot = pre % sm.stages;
-    uint32_t phase = (pre == sm.stages) ? 1u : 0u;
-    int64_t tile = tile0;
-    int ks = ks0;
+    // phase 2: activations of those stages; lane 0's arrival then releases each slot
+    Walk w = start;
     for (int i = 0; i < pre; ++i) {
-      if (++ks == spt) {
-        ks = 0;
-        ++tile;
-      }
+      act_copy(p, sm.act_u(i), w.ks, lane);
+      cp_async_mbar_arrive(sm.full(i));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.full(i));
+      w.next();
     }
-    for (int64_t s = s0 + pre; s < s1; ++s) {
-      if (!mbar_wait(sm.empty(slot), phase ^ 1u, p.err, kErrTimeoutEmpty)) break;
-      const uint32_t dst = sm.slot(slot), full = sm.full(slot);
-      st.act(dst, ks);
-      st.side(dst, tile, ks);
+    // phase 3: steady state
+    Ring r{pre % sm.stages, pre == sm.stages ? 1u : 0u, sm.stages};
+    bool ok = true;
+    for (int i = pre; i < n && ok; ++i) {
+      const bool seg_first = (i == 0) || (w.ks == 0);
+      if (side && w.opens(seg_first)) {
+        sr.next();
+        ok = mbar_wait(sm.sempty(sr.slot), sr.phase ^ 1u, p.err, kErrTimeoutEmpty);
+        if (ok && lane == 0) side_copy(p, sm, sr.slot, w, pol);
+      }
+      if (ok) ok = mbar_wait(sm.empty(r.slot), r.phase ^ 1u, p.err, kErrTimeoutEmpty);
+      if (!ok) break;
+      const uint32_t full = sm.full(r.slot);
+      act_copy(p, sm.act_u(r.slot), w.ks, lane);
       cp_async_mbar_arrive(full);
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(full, kTx);
-        st.weight(dst, full, tile, ks);
+        mbar_arrive_expect_tx(full, kStageBytes);
+        tma_load_2d_hint(sm.w(r.slot), &p.tm_w, w.ks * kStageRowBytes,
+                         static_cast<int>(w.tile * kRowsPerTile), full, pol);
       }
-      if (++slot == sm.stages) {
-        slot = 0;
-        phase ^= 1u;
-      }
-      if (++ks == spt) {
-        ks = 0;
-        ++tile;
-      }
+      r.next();
+      w.next();
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
-  // Register copies of the launch parameters the consumer's stage loop reads (same names as
-  // in KParams, so the helpers below read them from registers instead of parameter memory).
+  // ---- per-lane constants.  Consumer warp cw owns the tile's mma row group rg = cw (tile rows
+  // 16 rg .. 16 rg + 15) over the whole stage (8 chunks of 16 bytes per row); lane (g, t) holds
+  // rows g and g + 8 of the group (rr = 0, 1).
+  static constexpr int kCpbox = kFour ? 2 : 4;  // chunks per 64-k activation box
+
+  struct Lane {
+    int rg, lane, g, t;
+    uint32_t w[4];             // ldmatrix.x4 row address of chunk pair j (chunks 2j, 2j + 1)
+    uint32_t act[kCpbox][MT];  // activation fragment offset of chunk c (c < kCpbox) in a stage's
+                               // activation slot; chunk c + kCpbox b adds b * act_box_bytes
+    uint32_t abox;             // act_box_bytes
+    uint32_t srow;             // side box: scale row 16 rg + g; row g + 8 adds 8 * kSideScaleBytes
+    uint32_t zrow;             // side box: zero-point row 16 rg + g; row g + 8 adds 8 * zbox_bytes
+  };
+
+  static BSG_DEV Lane make_lane(const KParams& p, int cw, int lane) {
+    Lane L;
+    L.rg = cw;
+    L.lane = lane;
+    L.g = lane >> 2;
+    L.t = lane & 3;
+    // ldmatrix.x4: lanes 8i .. 8i + 7 address matrix i = (rows +8 if i odd) x (chunk +1 if i >= 2)
+    const int i = lane >> 3;
+    const int r = 16 * L.rg + 8 * (i & 1) + (lane & 7);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = 2 * j + (i >> 1);
+      L.w[j] = r * kStageRowBytes + ((c ^ (r & 7)) << 4);
+    }
+#pragma unroll
+    for (int c = 0; c < kCpbox; ++c)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        // activation row of the B fragment column; columns past M read row 0 (their results
+        // are never stored), so the slot holds only the call's M rows
+        const int m0 = mt * 8 + L.g;
+        const int m = m0 < p.M ? m0 : 0;
+        if constexpr (kFour) {  // 16-byte unit (c & 1) * 4 + t of the row
+          const int q = (c << 2) + L.t;
+          L.act[c][mt] = m * 128 + ((q ^ (m & 7)) << 4);
+        } else {  // unit (c & 3) * 2 + t / 2, half t & 1
+          const int q = (c << 1) + (L.t >> 1);
+          L.act[c][mt] = m * 128 + ((q ^ (m & 7)) << 4) + ((L.t & 1) << 3);
+        }
+      }
+    L.abox = static_cast<uint32_t>(p.act_box_bytes);
+    L.srow = (16 * L.rg + L.g) * kSideScaleBytes;
+    L.zrow = kRowsPerTile * kSideScaleBytes + (16 * L.rg + L.g) * p.zbox_bytes;
+    return L;
+  }
+
+  // Offset of chunk c's activation fragment (n8 tile mt) in a stage's activation slot.
+  static BSG_DEV uint32_t act_off(const Lane& L, int c, int mt) {
+    return L.act[c % kCpbox][mt] + (c / kCpbox) * L.abox;
+  }
+
+  // Launch parameters the stage loop reads, as registers.
   struct Run {
     int64_t N;
-    int nb_s, bs_log2, scale_pitch, zp_pitch, side_scale_tma, side_zp_tma;
+    int nb_s, bs_log2, scale_pitch, zp_pitch, zbox_bytes, rs_log2;
+    bool side;
     const uint8_t* scales;
     const uint8_t* zp;
   };
 
   static BSG_DEV Run make_run(const KParams& p) {
-    return Run{p.N, p.nb_s, p.bs_log2, p.scale_pitch, p.zp_pitch, p.side_scale_tma,
-               p.side_zp_tma, p.scales, p.zp};
-  }
-
-  // ---- per-lane constants.  Consumer warp cw owns the chunk pair cp = cw & 3 (chunks 2cp and
-  // 2cp+1 of every stage) and the row half rh = cw >> 2 (tile rows 32 rh .. 32 rh + 31, i.e.
-  // mma row groups 2 rh and 2 rh + 1).  Lane (g, t) holds fragment rows g + 8 rr, rr = 0..3
-  // (rr = 2 * local group + upper half), of that row half.
-  struct Lane {
-    int cp, rh, lane, g, t;
-    uint32_t w[2];        // ldmatrix row address of chunk cc (rows 32 rh + lane)
-    uint32_t act[2][MT];  // activation fragment address of chunk cc, n8 tile mt
-    uint32_t srow;        // scale box row 32 rh + g; row rr adds rr * 8 * kSpitch
-    uint32_t zrow;        // zero-point box row 32 rh + g; row rr adds rr * 8 * 16
-  };
-
-  static BSG_DEV Lane make_lane(const KParams& p, int cw, int lane) {
-    Lane L;
-    L.cp = cw & 3;
-    L.rh = cw >> 2;
-    L.lane = lane;
-    L.g = lane >> 2;
-    L.t = lane & 3;
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * L.cp + cc;
-      const int r = 32 * L.rh + lane;
-      L.w[cc] = r * kStageRowBytes + ((c ^ (r & 7)) << 4);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const int m = mt * 8 + L.g;
-        if constexpr (kFour) {
-          const int q = ((c & 1) << 2) + L.t;
-          L.act[cc][mt] = p.act_off + (c >> 1) * p.act_box_bytes + m * 128 + ((q ^ (m & 7)) << 4);
-        } else {
-          const int q = ((c & 3) << 1) + (L.t >> 1);
-          L.act[cc][mt] = p.act_off + (c >> 2) * p.act_box_bytes + m * 128 +
-                          ((q ^ (m & 7)) << 4) + ((L.t & 1) << 3);
-        }
-      }
-    }
-    L.srow = p.sc_off + (32 * L.rh + L.g) * kSpitch;
-    L.zrow = p.zp_off + (32 * L.rh + L.g) * 16;
-    return L;
+    return Run{p.N, p.nb_s, p.bs_log2, p.scale_pitch, p.zp_pitch, p.zbox_bytes, p.rs_log2,
+               p.side_tma != 0, p.scales, p.zp};
   }
 
   static BSG_DEV int64_t row_of(const Run& p, const Lane& L, int64_t tile, int rr) {
-    const int64_t n = tile * kRowsPerTile + 32 * L.rh + L.g + 8 * rr;
+    const int64_t n = tile * kRowsPerTile + 16 * L.rg + L.g + 8 * rr;
     return n < p.N ? n : p.N - 1;
   }
 
-  // fp32 scales of the lane's 4 rows for NB consecutive blocks starting at `blk` (box-relative
-  // index `rel`); NB = 2 only for 2-byte scales at an even `rel` (one 32-bit load per row).
+  // fp32 scales of the lane's 2 rows for NB consecutive blocks: from the side box `sb` at
+  // box-relative block `rel` (a multiple of NB: one shared load of NB scales per row), or from
+  // global memory at absolute block `blk`.
   template <int NB>
-  static BSG_DEV void load_scales(const Run& p, const Lane& L, uint32_t slot, int64_t tile,
-                                  int blk, int rel, float (&s)[NB][4]) {
-    if (p.side_scale_tma) {
-      const uint32_t a = slot + L.srow + rel * kScaleEs;
+  static BSG_DEV void load_scales(const Run& p, const Lane& L, const uint8_t* sb, int64_t tile,
+                                  int blk, int rel, float (&s)[NB][2]) {
+    if (p.side) {
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const uint32_t ar = a + rr * 8 * kSpitch;
+      for (int rr = 0; rr < 2; ++rr) {
+        const uint8_t* a = sb + L.srow + rr * 8 * kSideScaleBytes + rel * kScaleEs;
         if constexpr (FMT == kFp8) {
-#pragma unroll
-          for (int u = 0; u < NB; ++u) s[u][rr] = __uint_as_float(lds32(ar + 4 * u));
-        } else if constexpr (NB == 2) {
-          const uint32_t two = lds32(ar);
-          s[0][rr] = __half2float(__ushort_as_half(static_cast<unsigned short>(two & 0xFFFFu)));
-          s[1][rr] = __half2float(__ushort_as_half(static_cast<unsigned short>(two >> 16)));
+          static_assert(NB == 1, "one fp32 scale per warp stage");
+          s[0][rr] = __uint_as_float(lsh<uint32_t>(a));
         } else {
-          s[0][rr] = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(ar))));
+          uint32_t h[4];
+          if constexpr (NB == 1) {
+            h[0] = lsh<uint16_t>(a);
+          } else if constexpr (NB == 2) {
+            h[0] = lsh<uint32_t>(a);
+          } else if constexpr (NB == 4) {
+            const uint2 v = lsh<uint2>(a);
+            h[0] = v.x;
+            h[1] = v.y;
+          } else {
+            const uint4 v = lsh<uint4>(a);
+            h[0] = v.x;
+            h[1] = v.y;
+            h[2] = v.z;
+            h[3] = v.w;
+          }
+#pragma unroll
+          for (int u = 0; u < NB; ++u) {
+            const __half2 two = *reinterpret_cast<const __half2*>(&h[u >> 1]);
+            s[u][rr] = (u & 1) ? __high2float(two) : __low2float(two);
+          }
         }
       }
     } else {
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
+      for (int rr = 0; rr < 2; ++rr) {
         const uint8_t* src = p.scales + row_of(p, L, tile, rr) * p.scale_pitch;
 #pragma unroll
         for (int u = 0; u < NB; ++u) {
@@ -720,35 +754,62 @@ struct Gemv {
     }
   }
 
-  // Zero-point operand constants (see zp_consts) of the lane's 4 rows for block `blk`.
-  static BSG_DEV void load_zp(const Run& p, const Lane& L, uint32_t slot, int64_t tile,
-                              int blk, int rel, uint32_t (&zl)[4], uint32_t (&zh)[4]) {
+  // Zero points of the lane's 2 rows for NB consecutive blocks (same addressing as
+  // load_scales), packed as loaded: block u at bit u * kZpW.  Without zero points: the
+  // implicit 2^(bits-1) of every block.
+  template <int NB>
+  static BSG_DEV void load_zp(const Run& p, const Lane& L, const uint8_t* sb, int64_t tile,
+                              int blk, int rel, uint32_t (&z)[2]) {
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      uint32_t z;
+    for (int rr = 0; rr < 2; ++rr) {
       if constexpr (!ZP) {
-        z = (FMT == kInt4) ? 8u : 128u;
-      } else if (p.side_zp_tma) {
-        const uint32_t byte = lds8(slot + L.zrow + rr * 8 * 16 + ((FMT == kInt4) ? (rel >> 1) : rel));
-        z = (FMT == kInt4) ? ((rel & 1) ? (byte >> 4) : (byte & 0xFu)) : byte;
+        z[rr] = (FMT == kInt4) ? 0x88888888u : 0x80808080u;
+      } else if (p.side) {
+        const uint8_t* a = sb + L.zrow + rr * 8 * p.zbox_bytes + ((rel * kZpW) >> 3);
+        constexpr int kBits = NB * kZpW;
+        if constexpr (kBits <= 4) {
+          z[rr] = static_cast<uint32_t>(lsh<uint8_t>(a)) >> ((rel & 1) * 4);
+        } else if constexpr (kBits == 8) {
+          z[rr] = lsh<uint8_t>(a);
+        } else if constexpr (kBits == 16) {
+          z[rr] = lsh<uint16_t>(a);
+        } else {
+          z[rr] = lsh<uint32_t>(a);
+        }
       } else {
-        uint32_t byte = 0;
-        if (blk < p.nb_s)
-          byte = __ldg(p.zp + row_of(p, L, tile, rr) * p.zp_pitch + ((FMT == kInt4) ? (blk >> 1) : blk));
-        z = (FMT == kInt4) ? ((blk & 1) ? (byte >> 4) : (byte & 0xFu)) : byte;
+        uint32_t v = 0;
+        const uint8_t* src = p.zp + row_of(p, L, tile, rr) * p.zp_pitch;
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          const int b = blk + u;
+          uint32_t q = 0;
+          if (b < p.nb_s) {
+            const uint32_t byte = __ldg(src + ((FMT == kInt4) ? (b >> 1) : b));
+            q = (FMT == kInt4) ? ((b & 1) ? (byte >> 4) : (byte & 0xFu)) : byte;
+          }
+          v |= q << (u * kZpW);
+        }
+        z[rr] = v;
       }
-      zp_consts<FMT, BF16>(z, zl[rr], zh[rr]);
     }
   }
 
-  // NVFP4: the replicated f16 E4M3 block scale of the lane's 4 rows for 16-block `blk`.
-  static BSG_DEV void load_fold(const Run& p, const Lane& L, uint32_t slot, int64_t tile,
-                                int blk, int rel, uint32_t (&f)[4]) {
+  // Zero-point operand constants (see zp_consts) of the lane's 2 rows for block u of `z`.
+  static BSG_DEV void zp_of(const uint32_t (&z)[2], int u, uint32_t (&zl)[2], uint32_t (&zh)[2]) {
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
+    for (int rr = 0; rr < 2; ++rr)
+      zp_consts<FMT, BF16>((z[rr] >> (u * kZpW)) & ((1u << kZpW) - 1u), zl[rr], zh[rr]);
+  }
+
+  // NVFP4: the replicated f16 E4M3 block scale of the lane's 2 rows for 16-block `blk` (side
+  // box block `rel`).
+  static BSG_DEV void load_fold(const Run& p, const Lane& L, const uint8_t* sb, int64_t tile,
+                                int blk, int rel, uint32_t (&f)[2]) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
       uint32_t code;
-      if (p.side_scale_tma) {
-        code = lds8(slot + L.srow + rr * 8 * kSpitch + rel);
+      if (p.side) {
+        code = lsh<uint8_t>(sb + L.srow + rr * 8 * kSideScaleBytes + rel);
       } else {
         code = (blk < p.nb_s) ? __ldg(p.scales + row_of(p, L, tile, rr) * p.scale_pitch + blk) : 0u;
       }
@@ -756,13 +817,14 @@ struct Gemv {
     }
   }
 
-  // Activation B fragments of chunk cc: b[mt][st][0] = (k 2t, 2t+1), b[mt][st][1] = (k 2t+8,
+  // Activation B fragments of chunk c: b[mt][st][0] = (k 2t, 2t+1), b[mt][st][1] = (k 2t+8,
   // 2t+9) of activation row mt*8 + g, permuted like the weight (phys_k).
-  static BSG_DEV void act_fragment(const Lane& L, uint32_t slot, int cc, uint32_t (&b)[MT][kSteps][2]) {
+  static BSG_DEV void act_fragment(const Lane& L, const uint8_t* ap, int c,
+                                   uint32_t (&b)[MT][kSteps][2]) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       if constexpr (kFour) {
-        const uint4 v = lds128(slot + L.act[cc][mt]);
+        const uint4 v = lsh<uint4>(ap + act_off(L, c, mt));
         if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
           b[mt][0][0] = prmt(v.x, v.z, 0x5410u);
           b[mt][0][1] = prmt(v.x, v.z, 0x7632u);
@@ -775,157 +837,172 @@ struct Gemv {
           b[mt][1][1] = v.w;
         }
       } else {
-        const uint2 v = lds64(slot + L.act[cc][mt]);
+        const uint2 v = lsh<uint2>(ap + act_off(L, c, mt));
         b[mt][0][0] = v.x;
         b[mt][0][1] = v.y;
       }
     }
   }
 
-  // Decode the lane's 2 row groups of chunk cc and multiply into d[u] (u: sub-block for
-  // kTwoPerChunk).  ZC: the first k-step starts from zero instead of accumulating.
+  // Decode chunk c (words lo: row g, hi: row g + 8) and multiply into d[u] (u: sub-block when a
+  // chunk holds two scale blocks).  ZC: the first k-step starts from zero instead of
+  // accumulating.  zl/zh: zero-point constants (int formats) or the fold scales (NVFP4) of rows
+  // g, g + 8.
   template <bool ZC>
-  static BSG_DEV void chunk_mma(const Lane& L, uint32_t slot, int cc, const uint32_t (&zl)[4],
-                                const uint32_t (&zh)[4], float (&d)[kSub][2][MT][4]) {
+  static BSG_DEV void chunk_mma(const Lane& L, const uint8_t* ap, int c, uint32_t lo, uint32_t hi,
+                                const uint32_t (&zl)[2], const uint32_t (&zh)[2],
+                                float (&d)[kSub][MT][4]) {
     uint32_t b[MT][kSteps][2];
-    act_fragment(L, slot, cc, b);
-    uint32_t wv[4];
-    ldsm_x4(slot + L.w[cc], wv[0], wv[1], wv[2], wv[3]);
-#pragma unroll
-    for (int lg = 0; lg < 2; ++lg) {
-      uint32_t a[kSteps][4];
-      if constexpr (FMT == kInt4) {
-        decode_int4<BF16>(wv[2 * lg], wv[2 * lg + 1], zl[2 * lg], zh[2 * lg], zl[2 * lg + 1],
-                          zh[2 * lg + 1], a);
-      } else if constexpr (FMT == kInt8) {
-        decode_int8<BF16>(wv[2 * lg], wv[2 * lg + 1], zl[2 * lg], zl[2 * lg + 1], a);
-      } else if constexpr (FMT == kFp8) {
-        decode_fp8<BF16>(wv[2 * lg], wv[2 * lg + 1], a);
-      } else {
-        decode_nvfp4<BF16>(wv[2 * lg], wv[2 * lg + 1], zl[2 * lg], zl[2 * lg + 1], a);
-      }
-#pragma unroll
-      for (int st = 0; st < kSteps; ++st)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const bool zc = ZC && st == 0;
-#pragma unroll
-          for (int u = 0; u < kSub; ++u) {
-            uint32_t b0 = b[mt][st][0], b1 = b[mt][st][1];
-            if constexpr (kSub == 2) {
-              // quad lanes t < 2 hold the chunk's first block, t >= 2 the second
-              const bool mine = (L.t >> 1) == u;
-              b0 = mine ? b0 : 0u;
-              b1 = mine ? b1 : 0u;
-            }
-            if (zc) mma16816_zc<BF16>(d[u][lg][mt], a[st], b0, b1);
-            else mma16816<BF16>(d[u][lg][mt], a[st], b0, b1);
-          }
-        }
+    act_fragment(L, ap, c, b);
+    uint32_t a[kSteps][4];
+    if constexpr (FMT == kInt4) {
+      decode_int4<BF16>(lo, hi, zl[0], zh[0], zl[1], zh[1], a);
+    } else if constexpr (FMT == kInt8) {
+      decode_int8<BF16>(lo, hi, zl[0], zl[1], a);
+    } else if constexpr (FMT == kFp8) {
+      decode_fp8<BF16>(lo, hi, a);
+    } else {
+      decode_nvfp4<BF16>(lo, hi, zl[0], zl[1], a);
     }
-  }
-
-  // acc += tmp * s (per fragment row: s[2*lg] for row g, s[2*lg+1] for row g+8).
-  static BSG_DEV void apply_scales(const float (&s)[4], const float (&tmp)[2][MT][4],
-                                   float (&acc)[2][MT][4]) {
 #pragma unroll
-    for (int lg = 0; lg < 2; ++lg)
+    for (int st = 0; st < kSteps; ++st)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        acc[lg][mt][0] = fmaf(tmp[lg][mt][0], s[2 * lg], acc[lg][mt][0]);
-        acc[lg][mt][1] = fmaf(tmp[lg][mt][1], s[2 * lg], acc[lg][mt][1]);
-        acc[lg][mt][2] = fmaf(tmp[lg][mt][2], s[2 * lg + 1], acc[lg][mt][2]);
-        acc[lg][mt][3] = fmaf(tmp[lg][mt][3], s[2 * lg + 1], acc[lg][mt][3]);
-      }
-  }
-
-  template <int U>
-  static BSG_DEV void zero(float (&x)[U][2][MT][4]) {
+        const bool zc = ZC && st == 0;
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-#pragma unroll
-      for (int lg = 0; lg < 2; ++lg)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) x[u][lg][mt][i] = 0.f;
-  }
-
-  // Consume one ring slot: chunks 2cp and 2cp+1, row half rh, of stage ks of `tile`.
-  static BSG_DEV void consume_stage(const Run& p, const Lane& L, uint32_t slot, int64_t tile,
-                                    int ks, float (&acc)[1][2][MT][4]) {
-    const int bs_log2 = p.bs_log2;
-    const int blk0 = (ks * kKc) >> bs_log2;  // first scale block of the stage
-    const int sbox0 = blk0 & ~(kSbw - 1);     // first block of the staged scale box
-    const int zbox0 = blk0 & ~(kZblk - 1);
-    uint32_t zl[4], zh[4];
-    if constexpr (kFold) {
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        // the lane's 8 codes lie in 16-block (k of chunk + 8t) / 16
-        const int fb = ((ks * kKc + (2 * L.cp + cc) * kKpc) >> 4) + (L.t >> 1);
-        load_fold(p, L, slot, tile, fb, fb - sbox0, zl);
-        chunk_mma<false>(L, slot, cc, zl, zh, acc);
-      }
-    } else if constexpr (BMODE == kBlockPerPair) {
-      const int blk = blk0 + ((2 * L.cp * kKpc) >> bs_log2);
-      load_zp(p, L, slot, tile, blk, blk - zbox0, zl, zh);
-      float tmp[1][2][MT][4];
-      chunk_mma<true>(L, slot, 0, zl, zh, tmp);
-      chunk_mma<false>(L, slot, 1, zl, zh, tmp);
-      float s[1][4];
-      load_scales<1>(p, L, slot, tile, blk, blk - sbox0, s);
-      apply_scales(s[0], tmp[0], acc[0]);
-    } else if constexpr (BMODE == kBlockPerChunk) {
-      const int blk = blk0 + 2 * L.cp;  // chunk cc is block blk + cc
-      float s[2][4];
-      if constexpr (kScaleEs == 2) {
-        load_scales<2>(p, L, slot, tile, blk, blk - sbox0, s);
-      } else {
-        float s1[1][4];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          load_scales<1>(p, L, slot, tile, blk + cc, blk + cc - sbox0, s1);
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) s[cc][rr] = s1[0][rr];
+        for (int u = 0; u < kSub; ++u) {
+          uint32_t b0 = b[mt][st][0], b1 = b[mt][st][1];
+          if constexpr (kSub == 2) {
+            // quad lanes t < 2 hold the chunk's first block, t >= 2 the second
+            const bool mine = (L.t >> 1) == u;
+            b0 = mine ? b0 : 0u;
+            b1 = mine ? b1 : 0u;
+          }
+          if (zc) mma16816_zc<BF16>(d[u][mt], a[st], b0, b1);
+          else mma16816<BF16>(d[u][mt], a[st], b0, b1);
         }
       }
+  }
+
+  // acc += tmp * s (fragment entries 0, 1: row g; 2, 3: row g + 8).
+  static BSG_DEV void apply_scales(float s0, float s1, const float (&tmp)[MT][4], float (&acc)[MT][4]) {
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        load_zp(p, L, slot, tile, blk + cc, blk + cc - zbox0, zl, zh);
-        float tmp[1][2][MT][4];
-        chunk_mma<true>(L, slot, cc, zl, zh, tmp);
-        apply_scales(s[cc], tmp[0], acc[0]);
-      }
-    } else {  // kTwoPerChunk: chunk cc holds blocks blk, blk + 1 (int4, 16-element blocks)
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int blk = blk0 + 2 * (2 * L.cp + cc);
-        const int zb = blk + (L.t >> 1);
-        load_zp(p, L, slot, tile, zb, zb - zbox0, zl, zh);
-        float tmp[2][2][MT][4];
-        chunk_mma<true>(L, slot, cc, zl, zh, tmp);
-        float s[2][4];
-        load_scales<2>(p, L, slot, tile, blk, blk - sbox0, s);
-        apply_scales(s[0], tmp[0], acc[0]);
-        apply_scales(s[1], tmp[1], acc[0]);
-      }
+    for (int mt = 0; mt < MT; ++mt) {
+      acc[mt][0] = fmaf(tmp[mt][0], s0, acc[mt][0]);
+      acc[mt][1] = fmaf(tmp[mt][1], s0, acc[mt][1]);
+      acc[mt][2] = fmaf(tmp[mt][2], s1, acc[mt][2]);
+      acc[mt][3] = fmaf(tmp[mt][3], s1, acc[mt][3]);
     }
   }
 
-  // Store the 4 fp32 results of fragment slot (tile row group rg, tile mt, lane ln) as y.
-  static BSG_DEV void store_y(const KParams& p, int64_t tile, int rg, int mt, int ln, float4 v,
+  static BSG_DEV void zero(float (&x)[MT][4]) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[mt][i] = 0.f;
+  }
+
+  // Consume one stage: the 8 chunks of row group rg, stage ks of `tile`.  `wa` is the stage's
+  // weight box (shared-window address, for ldmatrix), `ap` its activation slot, `sb` the side
+  // box holding its scales and zero points.
+  //
+  // Scale groups (CPB = chunks per scale block): the chunks are taken in groups that share one
+  // shared-memory load of scales and zero points per row -- a pair of chunks for CPB = 1 and 2,
+  // four for CPB = 4, all eight for CPB = 8 (blocks of a stage or longer), one chunk holding two
+  // blocks for CPB = 0.  Within a block the chunk products are summed on the tensor cores (two
+  // independent chains when a block has four or more chunks) and then scaled into acc.
+  static constexpr int kGC = (CPB == 0) ? 1 : (CPB <= 2 ? 2 : CPB);  // chunks per group
+  static constexpr int kGB = (CPB == 0 || CPB == 1) ? 2 : 1;          // blocks per group
+
+  static BSG_DEV void consume_stage(const Run& p, const Lane& L, uint32_t wa, const uint8_t* ap,
+                                    const uint8_t* sb, int64_t tile, int ks,
+                                    float (&acc)[1][MT][4]) {
+    uint32_t wv[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ldsm_x4(wa + L.w[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
+    // chunk c: row g in wv[c >> 1][2 (c & 1)], row g + 8 in the next word
+#define BSG_LO(c) wv[(c) >> 1][2 * ((c) & 1)]
+#define BSG_HI(c) wv[(c) >> 1][2 * ((c) & 1) + 1]
+    const int k0 = ks * kKc;                                // first k of the stage in the row
+    const int kb = (ks & ((1 << p.rs_log2) - 1)) * kKc;    // ... in the side box
+    uint32_t zl[2], zh[2];
+    if constexpr (kFold) {
+      // the lane's 8 codes of chunk c lie in 16-block (k of the chunk + 8t) / 16 = 2c + t/2
+#pragma unroll
+      for (int c = 0; c < kChunksPerStage; ++c) {
+        const int d = 2 * c + (L.t >> 1);
+        load_fold(p, L, sb, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
+        chunk_mma<false>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, acc);
+      }
+    } else {
+#pragma unroll
+      for (int grp = 0; grp < kChunksPerStage / kGC; ++grp) {
+        const int kg = grp * kGC * kKpc;  // k of the group in the stage
+        const int blk = (k0 + kg) >> p.bs_log2, rel = (kb + kg) >> p.bs_log2;
+        uint32_t z[2];
+        load_zp<kGB>(p, L, sb, tile, blk, rel, z);
+        float s[kGB][2];
+        load_scales<kGB>(p, L, sb, tile, blk, rel, s);
+        if constexpr (CPB == 0) {  // one chunk, two blocks: the lane's codes are in block t/2
+          zp_of(z, L.t >> 1, zl, zh);
+          float tmp[2][MT][4];
+          chunk_mma<true>(L, ap, grp, BSG_LO(grp), BSG_HI(grp), zl, zh, tmp);
+          apply_scales(s[0][0], s[0][1], tmp[0], acc[0]);
+          apply_scales(s[1][0], s[1][1], tmp[1], acc[0]);
+        } else if constexpr (CPB == 1) {  // two chunks, one block each
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = grp * 2 + u;
+            zp_of(z, u, zl, zh);
+            float tmp[1][MT][4];
+            chunk_mma<true>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, tmp);
+            apply_scales(s[u][0], s[u][1], tmp[0], acc[0]);
+          }
+        } else if constexpr (CPB == 2) {  // two chunks, one block
+          zp_of(z, 0, zl, zh);
+          float tmp[1][MT][4];
+          const int c = grp * 2;
+          chunk_mma<true>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, tmp);
+          chunk_mma<false>(L, ap, c + 1, BSG_LO(c + 1), BSG_HI(c + 1), zl, zh, tmp);
+          apply_scales(s[0][0], s[0][1], tmp[0], acc[0]);
+        } else {  // CPB 4 or 8: kGC chunks in one block, two independent mma chains
+          zp_of(z, 0, zl, zh);
+          float t0[1][MT][4], t1[1][MT][4];
+#pragma unroll
+          for (int u = 0; u < kGC; ++u) {
+            const int c = grp * kGC + u;
+            if (u < 2) {
+              if (u == 0) chunk_mma<true>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, t0);
+              else chunk_mma<true>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, t1);
+            } else {
+              if (u & 1) chunk_mma<false>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, t1);
+              else chunk_mma<false>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, t0);
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) t0[0][mt][e] += t1[0][mt][e];
+          apply_scales(s[0][0], s[0][1], t0[0], acc[0]);
+        }
+      }
+    }
+#undef BSG_LO
+#undef BSG_HI
+  }
+
+  // Store the 4 fp32 results of lane ln's fragment (row group rg, n8 tile mt) as y.
+  static BSG_DEV void store_y(const KParams& p, int64_t tile, int rg, int mt, int ln, const float (&v)[4],
                               float gs) {
     const int g = ln >> 2, t = ln & 3;
     const int64_t n0 = tile * kRowsPerTile + 16 * rg + g;
     const int m0 = mt * 8 + 2 * t;
-    const float vals[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t n = n0 + ((i & 2) ? 8 : 0);
       const int m = m0 + (i & 1);
       if (m < p.M && n < p.N) {
-        const float r = vals[i] * gs;
+        const float r = v[i] * gs;
         if constexpr (BF16)
           reinterpret_cast<__nv_bfloat16*>(p.y)[m * p.N + n] = __float2bfloat16_rn(r);
         else
@@ -939,135 +1016,116 @@ struct Gemv {
     return ((x + 1) * G + T - 1) / T - 1;
   }
 
-  // End of a tile segment: add the 4 chunk-pair warps of each row half (fixed order), then
-  // store, or publish a partial and let the last CTA of the tile add the partials in CTA order.
-  // Partial slots: CTA i writes slot 0 for the first tile of its range and slot 1 for its last
-  // tile, so among a tile's contributors only the first can hold it in slot 1 (when its range
-  // began in an earlier tile).
-  static BSG_DEV void epilogue(const KParams& p, const Smem& sm, int64_t tile, bool whole,
-                               int64_t my_first_tile, int cw, int lane, float (&acc)[1][2][MT][4],
-                               float gs) {
-    constexpr int kNT = kConsumerWarps * 32;   // 256 consumer threads
-    constexpr int kSlots = 2 * MT * 32;        // float4 slots per warp
-    constexpr int kOut = 4 * MT * 32;          // float4 slots per tile (4 row groups)
-    const int tid = cw * 32 + lane;
-    float4* red = sm.red();
-#pragma unroll
-    for (int lg = 0; lg < 2; ++lg)
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-        red[cw * kSlots + (lg * MT + mt) * 32 + lane] =
-            make_float4(acc[0][lg][mt][0], acc[0][lg][mt][1], acc[0][lg][mt][2], acc[0][lg][mt][3]);
-    named_bar_sync(1, kNT);
-
-    // output slot tid = ((rh * 2 + lg) * MT + mt) * 32 + ln, tile row group rg = 2 rh + lg
-    const bool active = tid < kOut;
-    const int ln = tid & 31;
-    const int q = tid >> 5;
-    const int mt = q % MT, rg = q / MT;
-    const int rh = rg >> 1, lg = rg & 1;
-    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active) {
-#pragma unroll
-      for (int cp = 0; cp < 4; ++cp) {
-        const float4 u = red[(rh * 4 + cp) * kSlots + (lg * MT + mt) * 32 + ln];
-        sum.x += u.x;
-        sum.y += u.y;
-        sum.z += u.z;
-        sum.w += u.w;
-      }
-    }
+  // End of a tile segment, per consumer warp (row group rg): store y when this CTA covered the
+  // whole tile; otherwise publish the partial sums and let the last CTA to arrive at (tile, rg)
+  // add every contributor's partial in CTA order (a fixed order: deterministic results).
+  // Partial slots [cta][seg][rg]: a CTA writes seg 0 for the first tile of its range and seg 1
+  // for its last tile, so among a tile's contributors only the first can hold it in seg 1 (when
+  // its range began in an earlier tile).
+  static BSG_DEV void epilogue(const KParams& p, int64_t tile, bool whole, int64_t my_first_tile,
+                               int rg, int lane, float (&acc)[1][MT][4], float gs) {
     if (whole) {
-      if (active) store_y(p, tile, rg, mt, ln, sum, gs);
-    } else {
-      const int slot_floats4 = p.slot_floats / 4;
-      const int seg = (tile == my_first_tile) ? 0 : 1;
-      float4* mine = reinterpret_cast<float4*>(p.partials) +
-                     (static_cast<int64_t>(blockIdx.x) * 2 + seg) * slot_floats4;
-      if (active) __stcg(mine + tid, sum);
-      named_bar_sync(1, kNT);
-      int* info = sm.flag();  // [0] last arriver?  [1] first CTA  [2] last CTA  [3] first's slot
-      if (tid == 0) {
-        const int64_t G = gridDim.x, T = p.total_stages;
-        const int64_t x0 = tile * p.spt;
-        const int64_t first = cta_of_stage(x0, T, G);
-        const int64_t last = cta_of_stage(x0 + p.spt - 1, T, G);
-        // the barrier orders every thread's partial store before this fence (fences are
-        // cumulative), which publishes them at GPU scope before the arrival count
-        __threadfence();
-        const unsigned old = atomicAdd(p.counters + tile, 1u);
-        info[0] = (old == static_cast<unsigned>(last - first)) ? 1 : 0;
-        info[1] = static_cast<int>(first);
-        info[2] = static_cast<int>(last);
-        info[3] = (first * T < x0 * G) ? 1 : 0;  // first CTA's range began before this tile
-      }
-      named_bar_sync(1, kNT);
-      if (info[0]) {
-        __threadfence();  // acquire side: order the partial loads after the observed count
-        const int first = info[1], last = info[2], fseg = info[3];
-        if (active) {
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float4* part = reinterpret_cast<const float4*>(p.partials) + tid;
-          for (int i = first; i <= last; ++i) {
-            const int sg = (i == first) ? fseg : 0;
-            const float4 u = __ldcg(part + (static_cast<int64_t>(i) * 2 + sg) * slot_floats4);
-            v.x += u.x;
-            v.y += u.y;
-            v.z += u.z;
-            v.w += u.w;
-          }
-          store_y(p, tile, rg, mt, ln, v, gs);
-        }
-        if (tid == 0) p.counters[tile] = 0u;  // every contributor has arrived: reset for reuse
-      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) store_y(p, tile, rg, mt, lane, acc[0][mt], gs);
+      return;
     }
-    named_bar_sync(1, kNT);  // `red` and the info words are reused by the next segment
+    const int slot4 = p.slot_floats / 4;  // float4 per (cta, seg, rg) slot
+    const int seg = (tile == my_first_tile) ? 0 : 1;
+    float4* mine = reinterpret_cast<float4*>(p.partials) +
+                   ((static_cast<int64_t>(blockIdx.x) * 2 + seg) * kConsumerWarps + rg) * slot4;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+      __stcg(mine + mt * 32 + lane,
+             make_float4(acc[0][mt][0], acc[0][mt][1], acc[0][mt][2], acc[0][mt][3]));
+    __syncwarp();
+    const int64_t G = gridDim.x, T = p.total_stages;
+    const int64_t x0 = tile * p.spt;
+    const int first = static_cast<int>(cta_of_stage(x0, T, G));
+    const int last = static_cast<int>(cta_of_stage(x0 + p.spt - 1, T, G));
+    unsigned is_last = 0;
+    if (lane == 0) {
+      // __syncwarp ordered the warp's partial stores before this fence (fences are
+      // cumulative), which publishes them at GPU scope before the arrival count
+      __threadfence();
+      const unsigned old = atomicAdd(p.counters + tile * kConsumerWarps + rg, 1u);
+      is_last = (old == static_cast<unsigned>(last - first)) ? 1u : 0u;
+    }
+    is_last = __shfl_sync(0xFFFFFFFFu, is_last, 0);
+    if (!is_last) return;
+    __threadfence();  // acquire side: order the partial loads after the observed count
+    const int fseg = (static_cast<int64_t>(first) * T < x0 * G) ? 1 : 0;  // first began earlier
+    const float4* part = reinterpret_cast<const float4*>(p.partials);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int i = first; i <= last; ++i) {
+        const int sg = (i == first) ? fseg : 0;
+        const float4 u =
+            __ldcg(part + ((static_cast<int64_t>(i) * 2 + sg) * kConsumerWarps + rg) * slot4 +
+                   mt * 32 + lane);
+        v[0] += u.x;
+        v[1] += u.y;
+        v[2] += u.z;
+        v[3] += u.w;
+      }
+      store_y(p, tile, rg, mt, lane, v, gs);
+    }
+    if (lane == 0) p.counters[tile * kConsumerWarps + rg] = 0u;  // all arrived: reset for reuse
   }
 
+  // ---- consumers: warps 1..4.  The CTA's range is walked tile segment by tile segment; within
+  // a segment every stage waits for its slot (and, when it opens one, its side box), is
+  // multiplied in, and is released; the segment ends with the epilogue.
   static BSG_DEV void consume(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int cw,
                               int lane) {
     pdl_wait();  // the epilogues write y and the plan's workspace
     const Lane L = make_lane(p, cw, lane);
     const Run R = make_run(p);
-    float acc[1][2][MT][4];
-    zero(acc);
+    float acc[1][MT][4];
+    zero(acc[0]);
     const float gs = kFold ? __ldg(p.gscale) : 1.0f;
-    const int64_t spt = p.spt;
-    int slot = 0;
-    uint32_t phase = 0;
-    int64_t tile = s0 / spt;
-    int ks = static_cast<int>(s0 - tile * spt);
-    const int64_t first_tile = tile;
+    const int spt = p.spt;
+    const int n = static_cast<int>(s1 - s0);
+    const int64_t first_tile = s0 / spt;
+    Walk w{first_tile, static_cast<int>(s0 - first_tile * spt), spt, (1 << p.rs_log2) - 1};
+    Ring r{0, 0u, sm.stages};
+    Ring sr{sm.side_slots - 1, 1u, sm.side_slots};
     bool ok = true;
-    for (int64_t s = s0; s < s1; ++s) {
-      if (ok) ok = mbar_wait(sm.full(slot), phase, p.err, kErrTimeoutFull);
-      if (ok) consume_stage(R, L, sm.slot(slot), tile, ks, acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.empty(slot));
-      if (ks == spt - 1 || s == s1 - 1) {
-        const bool whole = (s0 <= tile * spt) && (s1 >= (tile + 1) * spt);
-        epilogue(p, sm, tile, whole, first_tile, cw, lane, acc, gs);
-        zero(acc);
+    for (int i = 0; i < n;) {
+      const int seg = (spt - w.ks) < (n - i) ? (spt - w.ks) : (n - i);  // stages of this segment
+      const int64_t tile = w.tile;
+      for (int q = 0; q < seg; ++q) {
+        if (R.side && w.opens(q == 0)) {
+          sr.next();
+          if (ok) ok = mbar_wait(sm.sfull(sr.slot), sr.phase, p.err, kErrTimeoutFull);
+        }
+        if (ok) ok = mbar_wait(sm.full(r.slot), r.phase, p.err, kErrTimeoutFull);
+        if (ok) consume_stage(R, L, sm.w(r.slot), sm.act(r.slot), sm.side(sr.slot), tile, w.ks, acc);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(sm.empty(r.slot));
+          if (R.side && w.closes(q == seg - 1)) mbar_arrive(sm.sempty(sr.slot));
+        }
+        r.next();
+        w.next();
       }
-      if (++slot == sm.stages) {
-        slot = 0;
-        phase ^= 1u;
-      }
-      if (++ks == spt) {
-        ks = 0;
-        ++tile;
-      }
+      i += seg;
+      // whole: this CTA consumed every stage of the tile
+      epilogue(p, tile, seg == spt, first_tile, cw, lane, acc, gs);
+      zero(acc[0]);
     }
   }
 };
 
-template <int FMT, bool BF16, int MT, bool ZP, int BMODE>
-__global__ void __launch_bounds__(kThreads, 2) bsgemv_mma_kernel(const __grid_constant__ KParams p) {
-  using K = Gemv<FMT, BF16, MT, ZP, BMODE>;
+template <int FMT, bool BF16, int MT, bool ZP, int CPB>
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm) bsgemv_mma_kernel(const __grid_constant__ KParams p) {
+  using K = Gemv<FMT, BF16, MT, ZP, CPB>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const typename K::Smem sm{base, p.stages, p.slot_bytes, p.bar_off, p.red_off};
+  // 1024-byte aligned (128-byte swizzle atoms), derived from the shared array so that plain
+  // loads through it stay shared-memory loads
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const typename K::Smem sm{base, smem_u32(base), p.stages, p.act_off, p.act_bytes,
+                            p.side_off, p.side_bytes, p.side_slots, p.bar_off};
 
   const int64_t G = gridDim.x, T = p.total_stages;
   const int64_t s0 = static_cast<int64_t>(blockIdx.x) * T / G;
@@ -1079,6 +1137,10 @@ __global__ void __launch_bounds__(kThreads, 2) bsgemv_mma_kernel(const __grid_co
     for (int i = 0; i < sm.stages; ++i) {
       mbar_init(sm.full(i), 1);
       mbar_init(sm.empty(i), kConsumerWarps);
+    }
+    for (int j = 0; j < sm.side_slots; ++j) {
+      mbar_init(sm.sfull(j), 1);
+      mbar_init(sm.sempty(j), kConsumerWarps);
     }
     fence_mbar_init();
   }

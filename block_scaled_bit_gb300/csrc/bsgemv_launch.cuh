@@ -7,9 +7,9 @@
 
 namespace bsg {
 
-template <int FMT, bool BF16, int MT, bool ZP, int BMODE>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB>
 int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
-  auto k = bsgemv_mma_kernel<FMT, BF16, MT, ZP, BMODE>;
+  auto k = bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB>;
   static std::atomic<int> attr_smem{0};  // largest dynamic smem already granted to `k`
   if (smem > attr_smem.load()) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -32,36 +32,48 @@ int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
 }
 
-// Dispatch over the n8 tile count, zero points and block mode for one format / activation type.
+// Dispatch over the n8 tile count, zero points and chunks per scale block (block_mode) for one
+// format / activation type.
 template <int FMT, bool BF16>
-int launch_fmt(const KParams& p, int mt, bool zp, int bmode, int ctas, int smem, cudaStream_t s) {
-#define BSG_L(MTV, ZPV, BM) return launch_one<FMT, BF16, MTV, ZPV, BM>(p, ctas, smem, s)
-#define BSG_ZP(MTV, BM) \
-  if (zp) BSG_L(MTV, true, BM); \
-  BSG_L(MTV, false, BM)
-  if constexpr (FMT == kInt4) {
-    if (mt == 1) {
-      if (bmode == kBlockPerChunk) { BSG_ZP(1, kBlockPerChunk); }
-      if (bmode == kBlockPerPair) { BSG_ZP(1, kBlockPerPair); }
-      BSG_ZP(1, kTwoPerChunk);
-    }
-    if (bmode == kBlockPerChunk) { BSG_ZP(2, kBlockPerChunk); }
-    if (bmode == kBlockPerPair) { BSG_ZP(2, kBlockPerPair); }
-    BSG_ZP(2, kTwoPerChunk);
-  } else if constexpr (FMT == kInt8) {
-    if (mt == 1) {
-      if (bmode == kBlockPerChunk) { BSG_ZP(1, kBlockPerChunk); }
-      BSG_ZP(1, kBlockPerPair);
-    }
-    if (bmode == kBlockPerChunk) { BSG_ZP(2, kBlockPerChunk); }
-    BSG_ZP(2, kBlockPerPair);
-  } else if constexpr (FMT == kFp8) {
-    if (mt == 1) BSG_L(1, false, kBlockPerPair);
-    BSG_L(2, false, kBlockPerPair);
-  } else {
-    if (mt == 1) BSG_L(1, false, kBlockPerChunk);
-    BSG_L(2, false, kBlockPerChunk);
+int launch_fmt(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
+#define BSG_L(MTV, ZPV, C) return launch_one<FMT, BF16, MTV, ZPV, C>(p, ctas, smem, s)
+#define BSG_ZP(MTV, C) \
+  if (zp) BSG_L(MTV, true, C); \
+  BSG_L(MTV, false, C)
+#define BSG_CPB(MTV)                   \
+  switch (cpb) {                       \
+    case 0: BSG_ZP(MTV, 0);            \
+    case 1: BSG_ZP(MTV, 1);            \
+    case 2: BSG_ZP(MTV, 2);            \
+    case 4: BSG_ZP(MTV, 4);            \
+    default: BSG_ZP(MTV, 8);           \
   }
+  if constexpr (FMT == kInt4) {
+    if (mt == 1) { BSG_CPB(1); }
+    BSG_CPB(2);
+  } else if constexpr (FMT == kInt8) {  // 8-bit chunks hold 16 k: no block is smaller
+    if (mt == 1) {
+      switch (cpb) {
+        case 1: BSG_ZP(1, 1);
+        case 2: BSG_ZP(1, 2);
+        case 4: BSG_ZP(1, 4);
+        default: BSG_ZP(1, 8);
+      }
+    }
+    switch (cpb) {
+      case 1: BSG_ZP(2, 1);
+      case 2: BSG_ZP(2, 2);
+      case 4: BSG_ZP(2, 4);
+      default: BSG_ZP(2, 8);
+    }
+  } else if constexpr (FMT == kFp8) {  // one 128-k block per stage
+    if (mt == 1) BSG_L(1, false, 8);
+    BSG_L(2, false, 8);
+  } else {  // NVFP4 folds its scales
+    if (mt == 1) BSG_L(1, false, 1);
+    BSG_L(2, false, 1);
+  }
+#undef BSG_CPB
 #undef BSG_ZP
 #undef BSG_L
 }

@@ -3,9 +3,9 @@
 
 namespace bsg {
 
-int launch_nvfp4(const KParams& p, int mt, bool bf16, bool zp, int bmode, int ctas, int smem, cudaStream_t s) {
-  return bf16 ? launch_fmt<kNvfp4, true>(p, mt, zp, bmode, ctas, smem, s)
-              : launch_fmt<kNvfp4, false>(p, mt, zp, bmode, ctas, smem, s);
+int launch_nvfp4(const KParams& p, int mt, bool bf16, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
+  return bf16 ? launch_fmt<kNvfp4, true>(p, mt, zp, cpb, ctas, smem, s)
+              : launch_fmt<kNvfp4, false>(p, mt, zp, cpb, ctas, smem, s);
 }
 
 }  // namespace bsg

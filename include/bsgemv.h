@@ -181,9 +181,9 @@ int bsgemv_device_status(bsgemv_plan_t plan, void* stream);
  *
  * Arguments as bsgemv_plan plus bsgemv_run, with max_M = M; no plan is created.  Instead of a
  * plan's cudaMalloc'd workspace the cross-CTA reduction uses one fixed scratch area compiled into
- * the library (a file-scope device array of about 2.6 MiB that every GPU loading the library
- * holds until the process exits).  Limits: N <= 524288 output columns and at most 320
- * persistent CTAs (a 152-SM GB300 uses 304); beyond them the call returns
+ * the library (a file-scope device array of about 5.2 MiB that every GPU loading the library
+ * holds until the process exits).  Limits: N <= 524288 output columns and at most 640
+ * persistent CTAs (a 152-SM GB300 uses 608); beyond them the call returns
  * BSGEMV_ERR_SCRATCH_LIMIT and does nothing.  The first call on a device looks up the scratch
  * area's device address (with that device current); make that first call before any stream
  * capture.  Every call on a device shares the one scratch area: calls that overlap on the GPU
