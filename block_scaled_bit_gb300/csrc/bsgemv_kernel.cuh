@@ -157,6 +157,15 @@ BSG_DEV void tma_prefetch_l2_2d(const CUtensorMap* tm, int x, int y) {
 BSG_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 BSG_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Arrival on a global counter with release (publishes what this thread has observed, e.g. its
+// warp's stores ordered by __syncwarp) and acquire (a last arriver sees every contributor's
+// stores) semantics at GPU scope.  Returns the old value.
+BSG_DEV unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 BSG_DEV void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -206,6 +215,14 @@ BSG_DEV uint32_t lds8(uint32_t addr) {
 template <typename T>
 BSG_DEV T lsh(const uint8_t* p) {
   return *reinterpret_cast<const T*>(p);
+}
+
+// (a & b) | c in one LOP3 (b and c in registers: the compiler would otherwise split two
+// immediates into two logic instructions).
+BSG_DEV uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 BSG_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -338,22 +355,24 @@ BSG_DEV void decode_int4(uint32_t lo, uint32_t hi, uint32_t zl_lo, uint32_t zh_l
                          uint32_t zh_hi, uint32_t (&a)[2][4]) {
   if constexpr (!BF16) {
     const uint32_t k16 = 0x2C002C00u;  // 1/16 in each f16 half
+    const uint32_t m_lo = 0x000F000Fu, m_hi = 0x00F000F0u, e = 0x64006400u;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const uint32_t wl = lo >> (8 * s), wh = hi >> (8 * s);
-      a[s][0] = h2_sub((wl & 0x000F000Fu) | 0x64006400u, zl_lo);
-      a[s][1] = h2_sub((wh & 0x000F000Fu) | 0x64006400u, zl_hi);
-      a[s][2] = h2_fma((wl & 0x00F000F0u) | 0x64006400u, k16, zh_lo);
-      a[s][3] = h2_fma((wh & 0x00F000F0u) | 0x64006400u, k16, zh_hi);
+      a[s][0] = h2_sub(and_or(wl, m_lo, e), zl_lo);
+      a[s][1] = h2_sub(and_or(wh, m_lo, e), zl_hi);
+      a[s][2] = h2_fma(and_or(wl, m_hi, e), k16, zh_lo);
+      a[s][3] = h2_fma(and_or(wh, m_hi, e), k16, zh_hi);
     }
   } else {
+    const uint32_t m_lo = 0x000F000Fu, e = 0x43004300u;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const uint32_t wl = lo >> (8 * s), wh = hi >> (8 * s);
-      a[s][0] = bf2_sub((wl & 0x000F000Fu) | 0x43004300u, zl_lo);
-      a[s][1] = bf2_sub((wh & 0x000F000Fu) | 0x43004300u, zl_hi);
-      a[s][2] = bf2_sub(((wl >> 4) & 0x000F000Fu) | 0x43004300u, zl_lo);
-      a[s][3] = bf2_sub(((wh >> 4) & 0x000F000Fu) | 0x43004300u, zl_hi);
+      a[s][0] = bf2_sub(and_or(wl, m_lo, e), zl_lo);
+      a[s][1] = bf2_sub(and_or(wh, m_lo, e), zl_hi);
+      a[s][2] = bf2_sub(and_or(wl >> 4, m_lo, e), zl_lo);
+      a[s][3] = bf2_sub(and_or(wh >> 4, m_lo, e), zl_hi);
     }
   }
   (void)zh_lo;
@@ -679,21 +698,25 @@ struct Gemv {
     return L.act[c % kCpbox][mt] + (c / kCpbox) * L.abox;
   }
 
-  // Launch parameters the stage loop reads, as registers.
+  // Launch parameters the stage loop reads, as registers.  SIDE (fixed per launch, taken out of
+  // the loop): scales and zero points come from the side ring, else straight from global memory.
+  template <bool SIDE>
   struct Run {
+    static constexpr bool side = SIDE;
     int64_t N;
     int nb_s, bs_log2, scale_pitch, zp_pitch, zbox_bytes, rs_log2;
-    bool side;
     const uint8_t* scales;
     const uint8_t* zp;
   };
 
-  static BSG_DEV Run make_run(const KParams& p) {
-    return Run{p.N, p.nb_s, p.bs_log2, p.scale_pitch, p.zp_pitch, p.zbox_bytes, p.rs_log2,
-               p.side_tma != 0, p.scales, p.zp};
+  template <bool SIDE>
+  static BSG_DEV Run<SIDE> make_run(const KParams& p) {
+    return Run<SIDE>{p.N, p.nb_s, p.bs_log2, p.scale_pitch, p.zp_pitch, p.zbox_bytes, p.rs_log2,
+                     p.scales, p.zp};
   }
 
-  static BSG_DEV int64_t row_of(const Run& p, const Lane& L, int64_t tile, int rr) {
+  template <class R>
+  static BSG_DEV int64_t row_of(const R& p, const Lane& L, int64_t tile, int rr) {
     const int64_t n = tile * kRowsPerTile + 16 * L.rg + L.g + 8 * rr;
     return n < p.N ? n : p.N - 1;
   }
@@ -701,10 +724,10 @@ struct Gemv {
   // fp32 scales of the lane's 2 rows for NB consecutive blocks: from the side box `sb` at
   // box-relative block `rel` (a multiple of NB: one shared load of NB scales per row), or from
   // global memory at absolute block `blk`.
-  template <int NB>
-  static BSG_DEV void load_scales(const Run& p, const Lane& L, const uint8_t* sb, int64_t tile,
+  template <int NB, class R>
+  static BSG_DEV void load_scales(const R& p, const Lane& L, const uint8_t* sb, int64_t tile,
                                   int blk, int rel, float (&s)[NB][2]) {
-    if (p.side) {
+    if constexpr (R::side) {
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const uint8_t* a = sb + L.srow + rr * 8 * kSideScaleBytes + rel * kScaleEs;
@@ -757,14 +780,14 @@ struct Gemv {
   // Zero points of the lane's 2 rows for NB consecutive blocks (same addressing as
   // load_scales), packed as loaded: block u at bit u * kZpW.  Without zero points: the
   // implicit 2^(bits-1) of every block.
-  template <int NB>
-  static BSG_DEV void load_zp(const Run& p, const Lane& L, const uint8_t* sb, int64_t tile,
+  template <int NB, class R>
+  static BSG_DEV void load_zp(const R& p, const Lane& L, const uint8_t* sb, int64_t tile,
                               int blk, int rel, uint32_t (&z)[2]) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       if constexpr (!ZP) {
         z[rr] = (FMT == kInt4) ? 0x88888888u : 0x80808080u;
-      } else if (p.side) {
+      } else if constexpr (R::side) {
         const uint8_t* a = sb + L.zrow + rr * 8 * p.zbox_bytes + ((rel * kZpW) >> 3);
         constexpr int kBits = NB * kZpW;
         if constexpr (kBits <= 4) {
@@ -803,12 +826,13 @@ struct Gemv {
 
   // NVFP4: the replicated f16 E4M3 block scale of the lane's 2 rows for 16-block `blk` (side
   // box block `rel`).
-  static BSG_DEV void load_fold(const Run& p, const Lane& L, const uint8_t* sb, int64_t tile,
+  template <class R>
+  static BSG_DEV void load_fold(const R& p, const Lane& L, const uint8_t* sb, int64_t tile,
                                 int blk, int rel, uint32_t (&f)[2]) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       uint32_t code;
-      if (p.side) {
+      if constexpr (R::side) {
         code = lsh<uint8_t>(sb + L.srow + rr * 8 * kSideScaleBytes + rel);
       } else {
         code = (blk < p.nb_s) ? __ldg(p.scales + row_of(p, L, tile, rr) * p.scale_pitch + blk) : 0u;
@@ -914,7 +938,8 @@ struct Gemv {
   static constexpr int kGC = (CPB == 0) ? 1 : (CPB <= 2 ? 2 : CPB);  // chunks per group
   static constexpr int kGB = (CPB == 0 || CPB == 1) ? 2 : 1;          // blocks per group
 
-  static BSG_DEV void consume_stage(const Run& p, const Lane& L, uint32_t wa, const uint8_t* ap,
+  template <class R>
+  static BSG_DEV void consume_stage(const R& p, const Lane& L, uint32_t wa, const uint8_t* ap,
                                     const uint8_t* sb, int64_t tile, int ks,
                                     float (&acc)[1][MT][4]) {
     uint32_t wv[4][4];
@@ -1011,9 +1036,15 @@ struct Gemv {
     }
   }
 
-  // CTA whose stream-K range contains stage x: the largest i with floor(i*T/G) <= x.
-  static BSG_DEV int64_t cta_of_stage(int64_t x, int64_t T, int64_t G) {
-    return ((x + 1) * G + T - 1) / T - 1;
+  // CTA whose stream-K range contains stage x: the largest i with floor(i*T/G) <= x, i.e. with
+  // i*T < (x+1)*G.  A single-precision estimate (off by at most one: i <= G < 2^16) is
+  // corrected with exact 64-bit products.
+  static BSG_DEV int cta_of_stage(int64_t x, int64_t T, int G) {
+    const int64_t lim = (x + 1) * G;
+    int i = static_cast<int>(static_cast<float>(lim - 1) / static_cast<float>(T));
+    while (static_cast<int64_t>(i + 1) * T < lim) ++i;
+    while (i > 0 && static_cast<int64_t>(i) * T >= lim) --i;
+    return i;
   }
 
   // End of a tile segment, per consumer warp (row group rg): store y when this CTA covered the
@@ -1038,38 +1069,56 @@ struct Gemv {
       __stcg(mine + mt * 32 + lane,
              make_float4(acc[0][mt][0], acc[0][mt][1], acc[0][mt][2], acc[0][mt][3]));
     __syncwarp();
-    const int64_t G = gridDim.x, T = p.total_stages;
+    const int G = gridDim.x;
+    const int64_t T = p.total_stages;
     const int64_t x0 = tile * p.spt;
-    const int first = static_cast<int>(cta_of_stage(x0, T, G));
-    const int last = static_cast<int>(cta_of_stage(x0 + p.spt - 1, T, G));
+    const int first = cta_of_stage(x0, T, G);
+    const int last = cta_of_stage(x0 + p.spt - 1, T, G);
     unsigned is_last = 0;
     if (lane == 0) {
-      // __syncwarp ordered the warp's partial stores before this fence (fences are
-      // cumulative), which publishes them at GPU scope before the arrival count
-      __threadfence();
-      const unsigned old = atomicAdd(p.counters + tile * kConsumerWarps + rg, 1u);
+      // __syncwarp ordered the warp's partial stores before this arrival, whose release
+      // publishes them at GPU scope; its acquire makes a last arriver see every contributor's
+      const unsigned old = atom_add_acq_rel_gpu(p.counters + tile * kConsumerWarps + rg, 1u);
       is_last = (old == static_cast<unsigned>(last - first)) ? 1u : 0u;
     }
     is_last = __shfl_sync(0xFFFFFFFFu, is_last, 0);
     if (!is_last) return;
-    __threadfence();  // acquire side: order the partial loads after the observed count
+    __syncwarp();  // order the warp's partial loads after lane 0's acquire
     const int fseg = (static_cast<int64_t>(first) * T < x0 * G) ? 1 : 0;  // first began earlier
     const float4* part = reinterpret_cast<const float4*>(p.partials);
+    // contributors' partials in batches of kBatch independent loads, added in CTA order
+    constexpr int kBatch = 8;
+    float v[MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int i = first; i <= last; ++i) {
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[mt][e] = 0.f;
+    for (int i0 = first; i0 <= last; i0 += kBatch) {
+      float4 u[kBatch][MT];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j;
         const int sg = (i == first) ? fseg : 0;
-        const float4 u =
-            __ldcg(part + ((static_cast<int64_t>(i) * 2 + sg) * kConsumerWarps + rg) * slot4 +
-                   mt * 32 + lane);
-        v[0] += u.x;
-        v[1] += u.y;
-        v[2] += u.z;
-        v[3] += u.w;
+        const float4* src =
+            part + ((static_cast<int64_t>(i) * 2 + sg) * kConsumerWarps + rg) * slot4 + lane;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+          u[j][mt] = (i <= last) ? __ldcg(src + mt * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      store_y(p, tile, rg, mt, lane, v, gs);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (i0 + j > last) break;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          v[mt][0] += u[j][mt].x;
+          v[mt][1] += u[j][mt].y;
+          v[mt][2] += u[j][mt].z;
+          v[mt][3] += u[j][mt].w;
+        }
+      }
     }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) store_y(p, tile, rg, mt, lane, v[mt], gs);
     if (lane == 0) p.counters[tile * kConsumerWarps + rg] = 0u;  // all arrived: reset for reuse
   }
 
@@ -1079,8 +1128,15 @@ struct Gemv {
   static BSG_DEV void consume(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int cw,
                               int lane) {
     pdl_wait();  // the epilogues write y and the plan's workspace
+    if (p.side_tma) consume_range<true>(p, sm, s0, s1, cw, lane);
+    else consume_range<false>(p, sm, s0, s1, cw, lane);
+  }
+
+  template <bool SIDE>
+  static BSG_DEV void consume_range(const KParams& p, const Smem& sm, int64_t s0, int64_t s1,
+                                    int cw, int lane) {
     const Lane L = make_lane(p, cw, lane);
-    const Run R = make_run(p);
+    const Run<SIDE> R = make_run<SIDE>(p);
     float acc[1][MT][4];
     zero(acc[0]);
     const float gs = kFold ? __ldg(p.gscale) : 1.0f;
@@ -1095,7 +1151,7 @@ struct Gemv {
       const int seg = (spt - w.ks) < (n - i) ? (spt - w.ks) : (n - i);  // stages of this segment
       const int64_t tile = w.tile;
       for (int q = 0; q < seg; ++q) {
-        if (R.side && w.opens(q == 0)) {
+        if (SIDE && w.opens(q == 0)) {
           sr.next();
           if (ok) ok = mbar_wait(sm.sfull(sr.slot), sr.phase, p.err, kErrTimeoutFull);
         }
@@ -1104,7 +1160,7 @@ struct Gemv {
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(sm.empty(r.slot));
-          if (R.side && w.closes(q == seg - 1)) mbar_arrive(sm.sempty(sr.slot));
+          if (SIDE && w.closes(q == seg - 1)) mbar_arrive(sm.sempty(sr.slot));
         }
         r.next();
         w.next();

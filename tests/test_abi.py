@@ -4,6 +4,7 @@ a deterministic function of the problem and a fixed SM count."""
 import os
 import re
 
+import numpy as np
 import pytest
 
 from block_scaled_bit_gb300 import bsgemv
@@ -135,3 +136,28 @@ def test_stream_k_ranges_cover_every_stage_once():
             assert len(owner) == T
             for x in range(0, T, max(1, T // 97)):
                 assert -(-((x + 1) * G) // T) - 1 == owner[x]
+
+
+def test_owner_lookup_without_division():
+    """The kernel finds the CTA owning stage x (the largest i with i*T < (x+1)*G) from a
+    single-precision quotient corrected by exact products; it must equal the integer formula
+    for every grid size up to 640 CTAs and stage counts up to 2^31."""
+    import random
+    f32 = np.float32
+
+    def owner(x, T, G):
+        lim = (x + 1) * G
+        i = int(f32(f32(lim - 1) / f32(T)))
+        while (i + 1) * T < lim:
+            i += 1
+        while i > 0 and i * T >= lim:
+            i -= 1
+        return i
+
+    rng = random.Random(7)
+    for T in (1, 2, 3, 64, 1000, 37984, 2 ** 20 + 7, 2 ** 31 - 1):
+        for G in (1, 3, 152, 456, 608, 640):
+            if G > T:
+                continue
+            for x in [0, T - 1] + [rng.randrange(T) for _ in range(300)]:
+                assert owner(x, T, G) == ((x + 1) * G + T - 1) // T - 1
