@@ -5,15 +5,16 @@
 // per-row summation order (rows are bit-identical across M).
 //
 // Choices (the reasons are measurements on GB300; see the design notes):
-//   * 64 output columns per CTA tile, 4 consumer warps (one 16-row group each, over all 128
-//     bytes of a stage) + 1 copy warp, 4 CTAs per SM;
-//   * a ring of up to 12 stages of 128 weight bytes per row (plus the stage's activations), as
-//     deep as the shared-memory share of a CTA allows (4 CTAs per SM), so that every SM keeps
+//   * 64 output columns per CTA tile, 4 consumer warps (one 16-row group each, over a whole
+//     stage) + 1 copy warp, 4 CTAs per SM (3 when max_M > 8: more accumulator registers);
+//   * a ring of up to 12 stages of 256 k (128 or 256 weight bytes per row, plus the stage's
+//     activations), as
+//     deep as the shared-memory share of a CTA allows, so that every SM keeps
 //     tens of KB of weight in flight;
 //   * a side ring of scale / zero-point boxes, each covering 64 bytes of scales per row (4 to
 //     64 stages), so that side data costs one TMA per box instead of copies every stage;
 //   * stream-K: the tiles x stages work is split into equal contiguous ranges over
-//     min(total stages, 4 x SMs) persistent CTAs, which balances every shape to within one
+//     min(total stages, CTAs per SM x SMs) persistent CTAs, which balances every shape to within one
 //     stage per CTA without a wave tail.
 #include <algorithm>
 #include <cstdint>
@@ -27,7 +28,6 @@ namespace {
 constexpr int kSmemPerSm = 233472;       // 228 KB shared memory per SM on sm_100-class parts
 constexpr int kSmemPerBlockMax = 232448; // 227 KB opt-in maximum per CTA
 constexpr int kReservedPerBlock = 1024;  // reserved by the system per resident CTA
-constexpr int kCtasPerSm = kMinCtasPerSm;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -73,7 +73,8 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   g->N = N;
   g->K = K;
   g->kpc = four ? 32 : 16;
-  g->kc = kChunksPerStage * g->kpc;
+  g->kc = kStageK;
+  g->stage_bytes = stage_bytes(fmt);
   g->nbox = g->kc / 64;
   g->mt_max = max_M <= 8 ? 1 : 2;
   g->scale_es = (fmt == kFp8) ? 4 : (fmt == kNvfp4 ? 1 : 2);
@@ -108,10 +109,10 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   };
   auto smem_for = [&](int stages) {
     const int ss = side_slots_for(stages);
-    return 1024 + stages * (kStageBytes + g->act_bytes) + ss * g->side_bytes +
+    return 1024 + stages * (g->stage_bytes + g->act_bytes) + ss * g->side_bytes +
            8 * (2 * stages + 8);
   };
-  int ctas_per_sm = kCtasPerSm;
+  int ctas_per_sm = ctas_per_sm_for_mt(g->mt_max);
   const int budget = kSmemPerSm / ctas_per_sm - kReservedPerBlock;
   int stages = kMaxStages;
   while (stages > 2 && smem_for(stages) > budget) --stages;
@@ -126,7 +127,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
     if (smem_for(stages) > budget) ctas_per_sm = 1;
   }
   g->side_slots = side_slots_for(stages);
-  g->act_off = stages * kStageBytes;
+  g->act_off = stages * g->stage_bytes;
   g->side_off = g->act_off + stages * g->act_bytes;
   g->bar_off = g->side_off + g->side_slots * g->side_bytes;
 

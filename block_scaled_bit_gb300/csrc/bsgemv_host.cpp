@@ -50,7 +50,7 @@ int encode_maps(const Geometry& g, const void* W, const void* scales, const void
                 OperandMaps* m) {
   std::memset(m, 0, sizeof(*m));
   const int64_t row_bytes = (g.fmt == kInt4 || g.fmt == kNvfp4) ? g.K / 2 : g.K;
-  int rc = encode_u8(&m->tm_w, W, row_bytes, g.N, row_bytes, kStageRowBytes, kRowsPerTile,
+  int rc = encode_u8(&m->tm_w, W, row_bytes, g.N, row_bytes, kBoxRowBytes, kRowsPerTile,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BSGEMV_OK) return rc;
   const bool int_zp = (g.fmt == kInt4 || g.fmt == kInt8) && g.has_zp;

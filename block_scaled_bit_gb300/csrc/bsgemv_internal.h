@@ -2,9 +2,9 @@
 //
 // Work decomposition (one persistent kernel per call):
 //   * a CTA tile is kRowsPerTile consecutive output columns n (rows of W) over a k-range;
-//   * k is walked in "stages" of 128 weight bytes per row (one 128-byte-swizzled TMA box, plus
-//     the stage's activations, scales and zero points copied with cp.async):
-//     256 k for the 4-bit formats, 128 k for the 8-bit formats;
+//   * k is walked in "stages" of kStageK = 256 k: 128 weight bytes per row for the 4-bit formats
+//     (one 128-byte-swizzled TMA box), 256 for the 8-bit formats (two boxes), plus the stage's
+//     activations (cp.async) -- scales and zero points arrive per several stages on a side ring;
 //   * the tiles x stages grid is cut into `ctas` equal contiguous ranges (stream-K); a tile whose
 //     stages fall into several CTAs is finished by the last CTA to arrive, which adds the
 //     partial sums in CTA order (a fixed order, so results are deterministic).
@@ -23,9 +23,12 @@ enum Fmt : int { kInt4 = 1, kInt8 = 2, kFp8 = 3, kNvfp4 = 4 };
 constexpr int kRowsPerTile = 64;      // output columns per CTA tile (4 mma row groups of 16)
 constexpr int kConsumerWarps = 4;     // decode + mma warps (one 16-row group each); warp 0 copies
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kMinCtasPerSm = 4;      // register budget: 4 CTAs of kThreads per SM
-constexpr int kChunksPerStage = 8;    // 16-byte chunks of a weight row per stage (128 B)
-constexpr int kStageRowBytes = 16 * kChunksPerStage;
+// CTAs per SM the kernels are built for (their register budget): 4 with one n8 activation tile
+// (M <= 8), 3 with two (M <= 16, more accumulator registers).
+constexpr int ctas_per_sm_for_mt(int mt) { return mt == 1 ? 4 : 3; }
+constexpr int kBoxRowBytes = 128;     // bytes per row of one weight TMA box (128-byte swizzle)
+constexpr int kStageK = 256;          // k per stage for every format: one 128-byte box per row for
+                                      // the 4-bit formats, two for the 8-bit formats
 constexpr int kMaxStages = 12;
 
 // Error word bits written by kernels that abandon a bounded wait.
@@ -75,7 +78,8 @@ struct Geometry {
   int fmt, bf16, has_zp, block_size, max_M;
   int64_t N, K;
   int kpc;                 // k per 16-byte chunk
-  int kc;                  // k per stage
+  int kc;                  // k per stage (kStageK)
+  int stage_bytes;         // weight bytes per stage
   int nbox;                // activation boxes (64 k) per stage
   int mt_max;              // 1 or 2 n8 mma tiles
   int scale_es;            // bytes per scale element
@@ -87,8 +91,11 @@ struct Geometry {
   int slot_floats;
 };
 
-// Stage weight bytes per row, and scale bytes per row of one side box.
-constexpr int kStageBytes = kRowsPerTile * kStageRowBytes;
+// Weight bytes of one stage (kRowsPerTile rows x kStageK k), and scale bytes per row of one
+// side box.
+inline int stage_bytes(int fmt) {
+  return kRowsPerTile * ((fmt == kInt4 || fmt == kNvfp4) ? kStageK / 2 : kStageK);
+}
 constexpr int kSideScaleBytes = 64;
 
 // Validates the problem and fills the geometry for `sm_count` SMs.  Pure host code.

@@ -476,7 +476,12 @@ struct Gemv {
   static constexpr bool kFour = (FMT == kInt4 || FMT == kNvfp4);
   static constexpr int kKpc = kFour ? 32 : 16;  // k per 16-byte chunk
   static constexpr int kSteps = kKpc / 16;      // mma k-steps per chunk
-  static constexpr int kKc = kChunksPerStage * kKpc;
+  static constexpr int kKc = kStageK;            // k per stage
+  static constexpr int kCps = kKc / kKpc;         // 16-byte chunks per row per stage: 8 or 16
+  static constexpr int kSrb = 16 * kCps;          // weight bytes per row per stage: 128 or 256
+  static constexpr int kBoxes = kSrb / kBoxRowBytes;        // weight TMA boxes per stage: 1 or 2
+  static constexpr int kStageB = kRowsPerTile * kSrb;       // weight bytes per stage
+  static constexpr int kBoxB = kRowsPerTile * kBoxRowBytes;  // bytes per weight box (8 KB)
   static constexpr int kNbox = kKc / 64;        // activation boxes (64 k) per stage
   static constexpr bool kFold = (FMT == kNvfp4);
   static constexpr int kSub = (CPB == 0) ? 2 : 1;  // scale blocks per chunk (int4, 16-element blocks)
@@ -489,7 +494,7 @@ struct Gemv {
     uint8_t* base;    // generic pointer into the kernel's shared array
     uint32_t base_u;  // the same address in the shared window
     int stages, act_off, act_bytes, side_off, side_bytes, side_slots, bar_off;
-    BSG_DEV uint32_t w(int i) const { return base_u + i * kStageBytes; }
+    BSG_DEV uint32_t w(int i) const { return base_u + i * kStageB; }
     BSG_DEV const uint8_t* act(int i) const { return base + act_off + i * act_bytes; }
     BSG_DEV uint32_t act_u(int i) const { return base_u + act_off + i * act_bytes; }
     BSG_DEV const uint8_t* side(int j) const { return base + side_off + j * side_bytes; }
@@ -530,7 +535,7 @@ struct Gemv {
     }
   };
 
-  // ---- producer: warp 0.  Lane 0 copies each stage's weight box [64 rows][128 B] with one TMA
+  // ---- producer: warp 0.  Lane 0 copies each stage's weight boxes [64 rows][128 B] (one or two TMAs)
   // (L2 evict-first: the weight is read once) and, once per side box, the scale box [64][64 B]
   // and zero-point box [64][16 or 32 B] (two more TMAs on the side ring).  All 32 lanes copy the
   // stage's activations [M][k of the stage] with 16-byte cp.async, tracked by the stage's full
@@ -552,6 +557,16 @@ struct Gemv {
       const bool in = k < K;
       cp_async16(d, p.A + m * K + (in ? k : 0), in ? 16u : 0u);
     }
+  }
+
+  // The weight boxes of stage (tile, ks) into ring slot i (lane 0).
+  static BSG_DEV void weight_copy(const KParams& p, const Smem& sm, int i, const Walk& w,
+                                  uint64_t pol) {
+    const int row = static_cast<int>(w.tile * kRowsPerTile);
+#pragma unroll
+    for (int b = 0; b < kBoxes; ++b)
+      tma_load_2d_hint(sm.w(i) + b * kBoxB, &p.tm_w, w.ks * kSrb + b * kBoxRowBytes, row,
+                       sm.full(i), pol);
   }
 
   static BSG_DEV void side_copy(const KParams& p, const Smem& sm, int j, const Walk& w,
@@ -597,9 +612,8 @@ struct Gemv {
           if (lane == 0) side_copy(p, sm, sr.slot, w, pol);
         }
         if (lane == 0) {
-          mbar_expect_tx(sm.full(i), kStageBytes);
-          tma_load_2d_hint(sm.w(i), &p.tm_w, w.ks * kStageRowBytes,
-                           static_cast<int>(w.tile * kRowsPerTile), sm.full(i), pol);
+          mbar_expect_tx(sm.full(i), kStageB);
+          weight_copy(p, sm, i, w, pol);
         }
         pre = i + 1;
         w.next();
@@ -632,9 +646,8 @@ struct Gemv {
       cp_async_mbar_arrive(full);
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(full, kStageBytes);
-        tma_load_2d_hint(sm.w(r.slot), &p.tm_w, w.ks * kStageRowBytes,
-                         static_cast<int>(w.tile * kRowsPerTile), full, pol);
+        mbar_arrive_expect_tx(full, kStageB);
+        weight_copy(p, sm, r.slot, w, pol);
       }
       r.next();
       w.next();
@@ -643,13 +656,14 @@ struct Gemv {
   }
 
   // ---- per-lane constants.  Consumer warp cw owns the tile's mma row group rg = cw (tile rows
-  // 16 rg .. 16 rg + 15) over the whole stage (8 chunks of 16 bytes per row); lane (g, t) holds
-  // rows g and g + 8 of the group (rr = 0, 1).
+  // 16 rg .. 16 rg + 15) over the whole stage (kCps chunks of 16 bytes per row, in boxes of 8);
+  // lane (g, t) holds rows g and g + 8 of the group (rr = 0, 1).
   static constexpr int kCpbox = kFour ? 2 : 4;  // chunks per 64-k activation box
 
   struct Lane {
     int rg, lane, g, t;
-    uint32_t w[4];             // ldmatrix.x4 row address of chunk pair j (chunks 2j, 2j + 1)
+    uint32_t w[4];             // ldmatrix.x4 row address of chunk pair j (chunks 2j, 2j + 1) of a
+                               // weight box; box b of the stage adds b * kBoxB
     uint32_t act[kCpbox][MT];  // activation fragment offset of chunk c (c < kCpbox) in a stage's
                                // activation slot; chunk c + kCpbox b adds b * act_box_bytes
     uint32_t abox;             // act_box_bytes
@@ -669,7 +683,7 @@ struct Gemv {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int c = 2 * j + (i >> 1);
-      L.w[j] = r * kStageRowBytes + ((c ^ (r & 7)) << 4);
+      L.w[j] = r * kBoxRowBytes + ((c ^ (r & 7)) << 4);
     }
 #pragma unroll
     for (int c = 0; c < kCpbox; ++c)
@@ -703,22 +717,14 @@ struct Gemv {
   template <bool SIDE>
   struct Run {
     static constexpr bool side = SIDE;
-    int64_t N;
-    int nb_s, bs_log2, scale_pitch, zp_pitch, zbox_bytes, rs_log2;
-    const uint8_t* scales;
-    const uint8_t* zp;
+    int bs_log2, rs_log2, zbox_bytes;
+    const KParams& k;  // the rest, read where used (global-memory path)
   };
-
-  template <bool SIDE>
-  static BSG_DEV Run<SIDE> make_run(const KParams& p) {
-    return Run<SIDE>{p.N, p.nb_s, p.bs_log2, p.scale_pitch, p.zp_pitch, p.zbox_bytes, p.rs_log2,
-                     p.scales, p.zp};
-  }
 
   template <class R>
   static BSG_DEV int64_t row_of(const R& p, const Lane& L, int64_t tile, int rr) {
     const int64_t n = tile * kRowsPerTile + 16 * L.rg + L.g + 8 * rr;
-    return n < p.N ? n : p.N - 1;
+    return n < p.k.N ? n : p.k.N - 1;
   }
 
   // fp32 scales of the lane's 2 rows for NB consecutive blocks: from the side box `sb` at
@@ -761,11 +767,11 @@ struct Gemv {
     } else {
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const uint8_t* src = p.scales + row_of(p, L, tile, rr) * p.scale_pitch;
+        const uint8_t* src = p.k.scales + row_of(p, L, tile, rr) * p.k.scale_pitch;
 #pragma unroll
         for (int u = 0; u < NB; ++u) {
           const int b = blk + u;
-          if (b >= p.nb_s) {  // chunk past K in the ragged last stage: its weight is zero
+          if (b >= p.k.nb_s) {  // chunk past K in the ragged last stage: its weight is zero
             s[u][rr] = 0.f;
           } else if constexpr (FMT == kFp8) {
             s[u][rr] = __ldg(reinterpret_cast<const float*>(src) + b);
@@ -801,12 +807,12 @@ struct Gemv {
         }
       } else {
         uint32_t v = 0;
-        const uint8_t* src = p.zp + row_of(p, L, tile, rr) * p.zp_pitch;
+        const uint8_t* src = p.k.zp + row_of(p, L, tile, rr) * p.k.zp_pitch;
 #pragma unroll
         for (int u = 0; u < NB; ++u) {
           const int b = blk + u;
           uint32_t q = 0;
-          if (b < p.nb_s) {
+          if (b < p.k.nb_s) {
             const uint32_t byte = __ldg(src + ((FMT == kInt4) ? (b >> 1) : b));
             q = (FMT == kInt4) ? ((b & 1) ? (byte >> 4) : (byte & 0xFu)) : byte;
           }
@@ -835,7 +841,7 @@ struct Gemv {
       if constexpr (R::side) {
         code = lsh<uint8_t>(sb + L.srow + rr * 8 * kSideScaleBytes + rel);
       } else {
-        code = (blk < p.nb_s) ? __ldg(p.scales + row_of(p, L, tile, rr) * p.scale_pitch + blk) : 0u;
+        code = (blk < p.k.nb_s) ? __ldg(p.k.scales + row_of(p, L, tile, rr) * p.k.scale_pitch + blk) : 0u;
       }
       f[rr] = e4m3x2_to_f16x2(code * 0x0101u);
     }
@@ -926,13 +932,13 @@ struct Gemv {
       for (int i = 0; i < 4; ++i) x[mt][i] = 0.f;
   }
 
-  // Consume one stage: the 8 chunks of row group rg, stage ks of `tile`.  `wa` is the stage's
+  // Consume one stage: the kCps chunks of row group rg, stage ks of `tile`.  `wa` is the stage's
   // weight box (shared-window address, for ldmatrix), `ap` its activation slot, `sb` the side
   // box holding its scales and zero points.
   //
   // Scale groups (CPB = chunks per scale block): the chunks are taken in groups that share one
   // shared-memory load of scales and zero points per row -- a pair of chunks for CPB = 1 and 2,
-  // four for CPB = 4, all eight for CPB = 8 (blocks of a stage or longer), one chunk holding two
+  // four for CPB = 4, eight for CPB = 8 (blocks of eight chunks or longer), one chunk holding two
   // blocks for CPB = 0.  Within a block the chunk products are summed on the tensor cores (two
   // independent chains when a block has four or more chunks) and then scaled into acc.
   static constexpr int kGC = (CPB == 0) ? 1 : (CPB <= 2 ? 2 : CPB);  // chunks per group
@@ -942,27 +948,40 @@ struct Gemv {
   static BSG_DEV void consume_stage(const R& p, const Lane& L, uint32_t wa, const uint8_t* ap,
                                     const uint8_t* sb, int64_t tile, int ks,
                                     float (&acc)[1][MT][4]) {
-    uint32_t wv[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ldsm_x4(wa + L.w[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
-    // chunk c: row g in wv[c >> 1][2 (c & 1)], row g + 8 in the next word
-#define BSG_LO(c) wv[(c) >> 1][2 * ((c) & 1)]
-#define BSG_HI(c) wv[(c) >> 1][2 * ((c) & 1) + 1]
     const int k0 = ks * kKc;                                // first k of the stage in the row
     const int kb = (ks & ((1 << p.rs_log2) - 1)) * kKc;    // ... in the side box
+    // one weight box (8 chunks) at a time: 16 weight registers live
+#pragma unroll
+    for (int bx = 0; bx < kBoxes; ++bx) {
+      uint32_t wv[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ldsm_x4(wa + bx * kBoxB + L.w[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
+      consume_box(p, L, wv, ap, sb, tile, k0, kb, bx * 8, acc);
+    }
+  }
+
+  // Chunks c0 .. c0 + 7 of the stage (one weight box), from the box's ldmatrix words `wv`:
+  // chunk c0 + c has row g in wv[c >> 1][2 (c & 1)] and row g + 8 in the next word.
+  template <class R>
+  static BSG_DEV void consume_box(const R& p, const Lane& L, const uint32_t (&wv)[4][4],
+                                  const uint8_t* ap, const uint8_t* sb, int64_t tile, int k0,
+                                  int kb, int c0, float (&acc)[1][MT][4]) {
+#define BSG_LO(c) wv[(c) >> 1][2 * ((c) & 1)]
+#define BSG_HI(c) wv[(c) >> 1][2 * ((c) & 1) + 1]
     uint32_t zl[2], zh[2];
     if constexpr (kFold) {
       // the lane's 8 codes of chunk c lie in 16-block (k of the chunk + 8t) / 16 = 2c + t/2
 #pragma unroll
-      for (int c = 0; c < kChunksPerStage; ++c) {
-        const int d = 2 * c + (L.t >> 1);
+      for (int c = 0; c < 8; ++c) {
+        const int d = 2 * (c0 + c) + (L.t >> 1);
         load_fold(p, L, sb, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
-        chunk_mma<false>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, acc);
+        chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, acc);
       }
     } else {
 #pragma unroll
-      for (int grp = 0; grp < kChunksPerStage / kGC; ++grp) {
-        const int kg = grp * kGC * kKpc;  // k of the group in the stage
+      for (int grp = 0; grp < 8 / kGC; ++grp) {
+        const int kg = (c0 + grp * kGC) * kKpc;  // k of the group in the stage
         const int blk = (k0 + kg) >> p.bs_log2, rel = (kb + kg) >> p.bs_log2;
         uint32_t z[2];
         load_zp<kGB>(p, L, sb, tile, blk, rel, z);
@@ -971,7 +990,7 @@ struct Gemv {
         if constexpr (CPB == 0) {  // one chunk, two blocks: the lane's codes are in block t/2
           zp_of(z, L.t >> 1, zl, zh);
           float tmp[2][MT][4];
-          chunk_mma<true>(L, ap, grp, BSG_LO(grp), BSG_HI(grp), zl, zh, tmp);
+          chunk_mma<true>(L, ap, c0 + grp, BSG_LO(grp), BSG_HI(grp), zl, zh, tmp);
           apply_scales(s[0][0], s[0][1], tmp[0], acc[0]);
           apply_scales(s[1][0], s[1][1], tmp[1], acc[0]);
         } else if constexpr (CPB == 1) {  // two chunks, one block each
@@ -980,15 +999,15 @@ struct Gemv {
             const int c = grp * 2 + u;
             zp_of(z, u, zl, zh);
             float tmp[1][MT][4];
-            chunk_mma<true>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, tmp);
+            chunk_mma<true>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, tmp);
             apply_scales(s[u][0], s[u][1], tmp[0], acc[0]);
           }
         } else if constexpr (CPB == 2) {  // two chunks, one block
           zp_of(z, 0, zl, zh);
           float tmp[1][MT][4];
           const int c = grp * 2;
-          chunk_mma<true>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, tmp);
-          chunk_mma<false>(L, ap, c + 1, BSG_LO(c + 1), BSG_HI(c + 1), zl, zh, tmp);
+          chunk_mma<true>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, tmp);
+          chunk_mma<false>(L, ap, c0 + c + 1, BSG_LO(c + 1), BSG_HI(c + 1), zl, zh, tmp);
           apply_scales(s[0][0], s[0][1], tmp[0], acc[0]);
         } else {  // CPB 4 or 8: kGC chunks in one block, two independent mma chains
           zp_of(z, 0, zl, zh);
@@ -997,11 +1016,11 @@ struct Gemv {
           for (int u = 0; u < kGC; ++u) {
             const int c = grp * kGC + u;
             if (u < 2) {
-              if (u == 0) chunk_mma<true>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, t0);
-              else chunk_mma<true>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, t1);
+              if (u == 0) chunk_mma<true>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, t0);
+              else chunk_mma<true>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, t1);
             } else {
-              if (u & 1) chunk_mma<false>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, t1);
-              else chunk_mma<false>(L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, t0);
+              if (u & 1) chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, t1);
+              else chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, t0);
             }
           }
 #pragma unroll
@@ -1087,7 +1106,7 @@ struct Gemv {
     const int fseg = (static_cast<int64_t>(first) * T < x0 * G) ? 1 : 0;  // first began earlier
     const float4* part = reinterpret_cast<const float4*>(p.partials);
     // contributors' partials in batches of kBatch independent loads, added in CTA order
-    constexpr int kBatch = 8;
+    constexpr int kBatch = 8 / MT;
     float v[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
@@ -1136,7 +1155,7 @@ struct Gemv {
   static BSG_DEV void consume_range(const KParams& p, const Smem& sm, int64_t s0, int64_t s1,
                                     int cw, int lane) {
     const Lane L = make_lane(p, cw, lane);
-    const Run<SIDE> R = make_run<SIDE>(p);
+    const Run<SIDE> R{p.bs_log2, p.rs_log2, p.zbox_bytes, p};
     float acc[1][MT][4];
     zero(acc[0]);
     const float gs = kFold ? __ldg(p.gscale) : 1.0f;
@@ -1174,7 +1193,7 @@ struct Gemv {
 };
 
 template <int FMT, bool BF16, int MT, bool ZP, int CPB>
-__global__ void __launch_bounds__(kThreads, kMinCtasPerSm) bsgemv_mma_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT)) bsgemv_mma_kernel(const __grid_constant__ KParams p) {
   using K = Gemv<FMT, BF16, MT, ZP, CPB>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned (128-byte swizzle atoms), derived from the shared array so that plain

@@ -93,7 +93,7 @@ SHAPES = [("int4", 32, False, 151936, 4096), ("int8", 128, True, 2048, 4096),
 def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
     g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, sms)
     four = fmt in ("int4", "nvfp4")
-    assert g["k_per_stage"] == (256 if four else 128)
+    assert g["k_per_stage"] == 256
     assert g["rows_per_tile"] == 64 and g["consumer_warps"] == 4
     assert g["tiles"] == -(-N // 64)
     assert g["stages_per_tile"] == -(-K // g["k_per_stage"])
@@ -112,15 +112,19 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
 
 
 def test_summation_order_independent_of_max_M(L):
-    """The per-row summation order is fixed by the work split (CTAs, tiles, stages), which does
-    not depend on max_M; only the ring depth and shared memory do.  M of a call never enters
-    the geometry at all (it is not an argument), which gives row bit-identity across M."""
+    """The per-row summation order is fixed by the work split (CTAs, tiles, stages).  It depends
+    on max_M only through the residency class -- 4 CTAs per SM for max_M <= 8, 3 for max_M > 8
+    (more accumulator registers) -- never on M of a call (not an argument), which gives row
+    bit-identity across M within a plan."""
     keys = ("ctas", "tiles", "stages_per_tile", "k_per_stage", "rows_per_tile", "consumer_warps")
     for N, K in ((4096, 4096), (151936, 4096), (300, 2048)):
-        ref = bsgemv.geometry_for("int4", "f16", 32, False, N, K, 16, 152)
-        for max_M in (1, 2, 8, 9, 15):
-            g = bsgemv.geometry_for("int4", "f16", 32, False, N, K, max_M, 152)
-            assert {k: g[k] for k in keys} == {k: ref[k] for k in keys}
+        for group in ((1, 2, 5, 8), (9, 12, 16)):
+            ref = bsgemv.geometry_for("int4", "f16", 32, False, N, K, group[0], 152)
+            for max_M in group[1:]:
+                g = bsgemv.geometry_for("int4", "f16", 32, False, N, K, max_M, 152)
+                assert {k: g[k] for k in keys} == {k: ref[k] for k in keys}
+        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 8, 152)["ctas_per_sm"] == 4
+        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 9, 152)["ctas_per_sm"] == 3
 
 
 def test_stream_k_ranges_cover_every_stage_once():
