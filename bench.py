@@ -444,9 +444,19 @@ def run_sweep(args):
             foot = case.algorithmic_bytes(1)
             copies = max(1, min(8, -(-3 * l2 // foot)))
             bufs = [bsgemv.upload(case, "cuda") for _ in range(copies)]
-            with bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K,
-                             max(shape.Ms)) as plan:
+            # one plan per residency class: max_M <= 8 (4 CTAs per SM) and max_M > 8 (3)
+            plans = {}
+
+            def plan_for(M):
+                pm = min(max(shape.Ms), 8) if M <= 8 else max(shape.Ms)
+                if pm not in plans:
+                    plans[pm] = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp,
+                                            case.N, case.K, pm)
+                return plans[pm]
+
+            try:
                 for M in shape.Ms:
+                    plan = plan_for(M)
                     # isolated cold
                     t = []
                     with torch.cuda.stream(stream):
@@ -488,8 +498,11 @@ def run_sweep(args):
                         "GBps_streamed": round(nbytes / streamed / 1e3, 1),
                         "frac_streamed": round(nbytes / streamed / 1e3 / peak, 4),
                         "frac_isolated": round(nbytes / iso / 1e3 / peak, 4),
-                        "weight_copies": copies}), flush=True)
+                        "weight_copies": copies, "plan_max_M": plan.max_M}), flush=True)
                     del g
+            finally:
+                for pl in plans.values():
+                    pl.close()
             del bufs
             torch.cuda.empty_cache()
 

@@ -325,6 +325,41 @@ BSG_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return d;
 }
 
+// The four E2M1 code pairs of a word (byte b -> out[b], low nibble -> low half), unpacked from
+// the register's bytes inside the conversion.
+BSG_DEV void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&out)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+      : "r"(w));
+}
+
+// The E4M3 code in byte `sel & 3` of w, replicated as an exact f16 pair (sel = 0x11 * byte).
+BSG_DEV uint32_t e4m3_byte_to_f16x2(uint32_t w, uint32_t sel) {
+  uint32_t d;
+  asm("{\n\t.reg .b32 t;\n\t.reg .b16 l, h;\n\t"
+      "prmt.b32 t, %1, %1, %2;\n\t"
+      "mov.b32 {l, h}, t;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t}"
+      : "=r"(d)
+      : "r"(w), "r"(sel));
+  return d;
+}
+
+// The two E4M3 code pairs of a word (low half -> lo, high half -> hi).
+BSG_DEV void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // An f16 pair whose values are exact in bf16 and normal (or zero) in f16, re-encoded as a bf16
 // pair: keep the sign, shift exponent and top mantissa bits into bf16 position (the value is
 // then 2^-112 of the original) and scale back by 2^112, which is exact.  Used for E4M3 values
@@ -410,10 +445,8 @@ BSG_DEV void decode_int8(uint32_t lo, uint32_t hi, uint32_t z_lo, uint32_t z_hi,
 // (decode-GEMV page, FP8 tensor-core paragraph).
 template <bool BF16>
 BSG_DEV void decode_fp8(uint32_t lo, uint32_t hi, uint32_t (&a)[1][4]) {
-  a[0][0] = e4m3x2_to_f16x2(lo & 0xFFFFu);
-  a[0][1] = e4m3x2_to_f16x2(hi & 0xFFFFu);
-  a[0][2] = e4m3x2_to_f16x2(lo >> 16);
-  a[0][3] = e4m3x2_to_f16x2(hi >> 16);
+  e4m3x4_to_f16x2x2(lo, a[0][0], a[0][2]);
+  e4m3x4_to_f16x2x2(hi, a[0][1], a[0][3]);
   if constexpr (BF16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) a[0][i] = f16x2_exact_to_bf16x2(a[0][i]);
@@ -426,12 +459,15 @@ BSG_DEV void decode_fp8(uint32_t lo, uint32_t hi, uint32_t (&a)[1][4]) {
 template <bool BF16>
 BSG_DEV void decode_nvfp4(uint32_t lo, uint32_t hi, uint32_t sc_lo, uint32_t sc_hi,
                           uint32_t (&a)[2][4]) {
+  uint32_t l[4], h[4];  // byte b of the word as an f16 pair
+  e2m1x8_to_f16x2x4(lo, l);
+  e2m1x8_to_f16x2x4(hi, h);
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    a[s][0] = h2_mul(e2m1x2_to_f16x2((lo >> (16 * s)) & 0xFFu), sc_lo);
-    a[s][1] = h2_mul(e2m1x2_to_f16x2((hi >> (16 * s)) & 0xFFu), sc_hi);
-    a[s][2] = h2_mul(e2m1x2_to_f16x2((lo >> (16 * s + 8)) & 0xFFu), sc_lo);
-    a[s][3] = h2_mul(e2m1x2_to_f16x2((hi >> (16 * s + 8)) & 0xFFu), sc_hi);
+    a[s][0] = h2_mul(l[2 * s], sc_lo);
+    a[s][1] = h2_mul(h[2 * s], sc_hi);
+    a[s][2] = h2_mul(l[2 * s + 1], sc_lo);
+    a[s][3] = h2_mul(h[2 * s + 1], sc_hi);
     if constexpr (BF16) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) a[s][i] = f16x2_exact_to_bf16x2(a[s][i]);
@@ -667,6 +703,7 @@ struct Gemv {
     uint32_t act[kCpbox][MT];  // activation fragment offset of chunk c (c < kCpbox) in a stage's
                                // activation slot; chunk c + kCpbox b adds b * act_box_bytes
     uint32_t abox;             // act_box_bytes
+    uint32_t fsel[2];          // NVFP4: prmt selector of the lane's scale code, chunk parity 0/1
     uint32_t srow;             // side box: scale row 16 rg + g; row g + 8 adds 8 * kSideScaleBytes
     uint32_t zrow;             // side box: zero-point row 16 rg + g; row g + 8 adds 8 * zbox_bytes
   };
@@ -702,6 +739,9 @@ struct Gemv {
         }
       }
     L.abox = static_cast<uint32_t>(p.act_box_bytes);
+    // chunk c's codes lie in 16-block 2c + t/2 of the stage: byte 2 (c & 1) + t/2 of word c / 2
+    L.fsel[0] = 0x11u * static_cast<uint32_t>(L.t >> 1);
+    L.fsel[1] = 0x11u * static_cast<uint32_t>(2 + (L.t >> 1));
     L.srow = (16 * L.rg + L.g) * kSideScaleBytes;
     L.zrow = kRowsPerTile * kSideScaleBytes + (16 * L.rg + L.g) * p.zbox_bytes;
     return L;
@@ -972,11 +1012,31 @@ struct Gemv {
     uint32_t zl[2], zh[2];
     if constexpr (kFold) {
       // the lane's 8 codes of chunk c lie in 16-block (k of the chunk + 8t) / 16 = 2c + t/2
+      if constexpr (R::side) {
+        // the stage's 16 scale codes per row in one load; the lane's code picked by prmt
+        uint4 cv[2];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int d = 2 * (c0 + c) + (L.t >> 1);
-        load_fold(p, L, sb, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
-        chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, acc);
+        for (int rr = 0; rr < 2; ++rr)
+          cv[rr] = lsh<uint4>(sb + L.srow + rr * 8 * kSideScaleBytes + (kb >> 4));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int cc = c0 + c;
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const uint32_t wd = (cc >> 1) == 0 ? cv[rr].x
+                              : (cc >> 1) == 1 ? cv[rr].y
+                              : (cc >> 1) == 2 ? cv[rr].z : cv[rr].w;
+            zl[rr] = e4m3_byte_to_f16x2(wd, L.fsel[cc & 1]);
+          }
+          chunk_mma<false>(L, ap, cc, BSG_LO(c), BSG_HI(c), zl, zh, acc);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int d = 2 * (c0 + c) + (L.t >> 1);
+          load_fold(p, L, sb, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
+          chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, acc);
+        }
       }
     } else {
 #pragma unroll
