@@ -15,6 +15,7 @@ from . import _build
 FORMATS = {"int4": 1, "int8": 2, "fp8": 3, "nvfp4": 4}
 ACT_BF16 = 0x100
 VARIANTS = {"auto": 0, "mma": 1, "cuda_core": 2}
+SPLITS = {"auto": 0, "stream_k": 1, "cluster": 2}
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -30,7 +31,7 @@ ERR_SCRATCH_LIMIT = -8
 EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_host", "bsgemv_destroy",
            "bsgemv_status_string", "bsgemv_debug_dequant", "bsgemv_plan_set_override",
            "bsgemv_plan_describe", "bsgemv_geometry_for", "bsgemv_device_status",
-           "bsgemv_run_noalloc", "bsgemv_version")
+           "bsgemv_run_noalloc", "bsgemv_plan_set_split", "bsgemv_version")
 
 
 class Geometry(ctypes.Structure):
@@ -40,7 +41,7 @@ class Geometry(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int), ("sm_count", ctypes.c_int),
                 ("tiles", ctypes.c_int64), ("stages_per_tile", ctypes.c_int64),
                 ("total_stages", ctypes.c_int64), ("smem_bytes", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("cluster", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
         L.bsgemv_status_string.restype = ctypes.c_char_p
         L.bsgemv_debug_dequant.argtypes = [vp, vp, vp, vp, vp, vp]
         L.bsgemv_plan_set_override.argtypes = [vp, ci, ci, ci, ci]
+        L.bsgemv_plan_set_split.argtypes = [vp, ci, ci]
         L.bsgemv_plan_describe.argtypes = [vp, ctypes.POINTER(Geometry)]
         L.bsgemv_geometry_for.argtypes = [ci, ci, ci, i64, i64, ci, ci, ctypes.POINTER(Geometry)]
         L.bsgemv_device_status.argtypes = [vp, vp]
@@ -187,6 +189,10 @@ class Plan:
 
     def set_override(self, variant: int = 0, ctas: int = 0, stages: int = 0) -> int:
         return lib().bsgemv_plan_set_override(self._h, variant, ctas, 0, stages)
+
+    def set_split(self, split: str = "auto", cluster: int = 0) -> int:
+        """K split of the tiles: "auto", "stream_k" or "cluster" (cluster = CTAs per tile)."""
+        return lib().bsgemv_plan_set_split(self._h, SPLITS[split], cluster)
 
     def describe(self) -> dict:
         g = Geometry()

@@ -20,6 +20,7 @@ struct bsgemv_plan_s {
   int device = -1;
   int sm_count = 0;
   int variant_override = 0, ctas_override = 0, stages_override = 0;
+  int split = BSGEMV_SPLIT_AUTO, cluster = 0;
   void* ws = nullptr;         // one allocation: partials | counters | error word
   size_t ws_bytes = 0;
   float* partials = nullptr;
@@ -95,7 +96,7 @@ int rebuild_geometry(bsgemv_plan_s* p) {
   bsg::Geometry geo;
   const int rc = bsg::compute_geometry(p->format, p->geo.block_size, p->geo.has_zp, p->geo.N,
                                        p->geo.K, p->geo.max_M, p->sm_count, p->ctas_override,
-                                       p->stages_override, &geo);
+                                       p->stages_override, p->split, p->cluster, &geo);
   if (rc != BSGEMV_OK) return rc;
   p->geo = geo;
   return alloc_workspace(p);
@@ -186,7 +187,8 @@ int bsgemv_plan(bsgemv_plan_t* out, int format, int block_size, int has_zp, int6
   if (out == nullptr) return BSGEMV_ERR_INVALID_ARG;
   *out = nullptr;
   bsg::Geometry probe;
-  int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, max_M, 1, 0, 0, &probe);
+  int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, max_M, 1, 0, 0,
+                                 BSGEMV_SPLIT_AUTO, 0, &probe);
   if (rc != BSGEMV_OK) return rc;  // argument errors need no GPU
   int dev = -1, sms = 0;
   rc = query_device(&dev, &sms);
@@ -293,6 +295,23 @@ int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows
   if (rc != BSGEMV_OK) {
     plan->ctas_override = old_c;
     plan->stages_override = old_s;
+    rebuild_geometry(plan);
+  }
+  return rc;
+}
+
+int bsgemv_plan_set_split(bsgemv_plan_t plan, int split, int cluster_size) {
+  if (plan == nullptr || split < BSGEMV_SPLIT_AUTO || split > BSGEMV_SPLIT_CLUSTER ||
+      cluster_size < 0 || cluster_size > bsg::kMaxCluster ||
+      (cluster_size != 0 && split != BSGEMV_SPLIT_CLUSTER))
+    return BSGEMV_ERR_INVALID_ARG;
+  const int old_s = plan->split, old_c = plan->cluster;
+  plan->split = split;
+  plan->cluster = cluster_size;
+  const int rc = rebuild_geometry(plan);
+  if (rc != BSGEMV_OK) {
+    plan->split = old_s;
+    plan->cluster = old_c;
     rebuild_geometry(plan);
   }
   return rc;

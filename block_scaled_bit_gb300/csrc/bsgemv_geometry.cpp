@@ -37,7 +37,8 @@ bool is_pow2_block(int bs) {
 }  // namespace
 
 int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
-                     int sm_count, int ctas_override, int stages_override, Geometry* g) {
+                     int sm_count, int ctas_override, int stages_override, int split, int cluster,
+                     Geometry* g) {
   if (g == nullptr) return BSGEMV_ERR_INVALID_ARG;
   std::memset(g, 0, sizeof(*g));
   if ((format & ~(0xFF | BSGEMV_ACT_BF16)) != 0) return BSGEMV_ERR_INVALID_ARG;
@@ -47,6 +48,9 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   if (N < 1 || K < 1 || max_M < 1 || max_M > 16 || sm_count < 1 || block_size < 1)
     return BSGEMV_ERR_INVALID_ARG;
   if (ctas_override < 0 || stages_override < 0 || stages_override > kMaxStages)
+    return BSGEMV_ERR_INVALID_ARG;
+  if (split < BSGEMV_SPLIT_AUTO || split > BSGEMV_SPLIT_CLUSTER || cluster < 0 ||
+      cluster > kMaxCluster)
     return BSGEMV_ERR_INVALID_ARG;
   switch (fmt) {
     case kInt4:
@@ -101,21 +105,95 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   g->slot_floats = g->mt_max * 32 * 4;
 
   const int64_t spt = ceil_div(K, g->kc);
+  const int64_t tiles = ceil_div(N, kRowsPerTile);
+  const int64_t total = tiles * spt;
+
   // side boxes in flight over a ring of `stages`: a box spans min(2^rs, stages per tile) stages
   auto side_slots_for = [&](int stages) {
     if (g->side_bytes == 0) return 0;
     const int64_t span = std::min<int64_t>(int64_t(1) << g->rs_log2, spt);
     return static_cast<int>(std::min<int64_t>(4, std::max<int64_t>(2, ceil_div(stages, span) + 1)));
   };
-  auto smem_for = [&](int stages) {
+  auto smem_with = [&](int stages, int red) {
     const int ss = side_slots_for(stages);
-    return 1024 + stages * (g->stage_bytes + g->act_bytes) + ss * g->side_bytes +
+    return 1024 + stages * (g->stage_bytes + g->act_bytes) + ss * g->side_bytes + red +
            8 * (2 * stages + 8);
   };
-  int ctas_per_sm = ctas_per_sm_for_mt(g->mt_max);
-  const int budget = kSmemPerSm / ctas_per_sm - kReservedPerBlock;
-  int stages = kMaxStages;
-  while (stages > 2 && smem_for(stages) > budget) --stages;
+  const int slots_per_sm = ctas_per_sm_for_mt(g->mt_max);
+  const int64_t slots = int64_t(sm_count) * slots_per_sm;
+  const int budget_slots = kSmemPerSm / slots_per_sm - kReservedPerBlock;
+
+  // K split.  Stream-K gives every CTA ceil(T / slots) stages of the tiles x stages space T but
+  // ends every call with a global last-arriver reduction; a cluster of C CTAs per tile gives each
+  // ceil(spt / C) stages and reduces in the leader's shared memory (no atomics, no global
+  // round trips).  Automatic choice: the cluster split with the fewest stages per CTA (the
+  // smallest such C) among clusters of at most 8 CTAs that divide the tile's stages evenly,
+  // when that is within one stage of stream-K's, the tiles x C CTAs fit one wave and the
+  // leader's reduction buffer leaves room for a ring of two stages.
+  // Reduction buffer: per CTA of the cluster and consumer warp, the fragment lanes that hold
+  // output columns below max_M (quad lanes t < red_tq) of each n8 tile.
+  g->red_tq = (g->mt_max == 2) ? 4 : static_cast<int>(std::min<int64_t>(4, ceil_div(max_M, 2)));
+  const int red_warp = g->mt_max * 8 * g->red_tq * 16;
+  auto red_for = [&](int c) { return c >= 2 ? c * kConsumerWarps * red_warp : 0; };
+  // Cluster split with an even share per CTA: the ring needs no more stages than the share, and
+  // one side box when the share never crosses a box boundary (it divides the box's stages)
+  auto cluster_stages = [&](int64_t c) {
+    return static_cast<int>(std::min<int64_t>(kMaxStages, ceil_div(spt, c)));
+  };
+  auto cluster_one_box = [&](int64_t c) {
+    const int64_t share = spt / c;
+    return spt % c == 0 && ((int64_t(1) << g->rs_log2) % share == 0);
+  };
+  // (a single side slot only when that is what makes the split fit: measured on GB300, the
+  // smaller footprint was otherwise slower for back-to-back calls)
+  auto cluster_smem_ss = [&](int64_t c, int stages, bool one) {
+    const int ss = (g->side_bytes == 0) ? 0 : (one ? 1 : side_slots_for(stages));
+    return 1024 + stages * (g->stage_bytes + g->act_bytes) + ss * g->side_bytes +
+           red_for(static_cast<int>(c)) + 8 * (2 * stages + 8);
+  };
+  auto cluster_one_slot = [&](int64_t c) {
+    const int st = std::min(2, cluster_stages(c));
+    return cluster_one_box(c) && cluster_smem_ss(c, st, false) > budget_slots;
+  };
+  auto cluster_smem = [&](int64_t c, int stages) {
+    return cluster_smem_ss(c, stages, cluster_one_slot(c));
+  };
+  auto cluster_fits = [&](int64_t c) {
+    return c <= kMaxCluster && c <= spt && tiles * c <= slots &&
+           cluster_smem(c, std::min(2, cluster_stages(c))) <= budget_slots;
+  };
+  int C = 0;
+  if (split == BSGEMV_SPLIT_CLUSTER && cluster > 0) {
+    if (!cluster_fits(cluster)) return BSGEMV_ERR_UNSUPPORTED;
+    C = cluster;
+  } else if (split == BSGEMV_SPLIT_CLUSTER || (split == BSGEMV_SPLIT_AUTO && ctas_override == 0)) {
+    // (a CTA-count override describes a stream-K grid: it implies stream-K)
+    const int64_t sk = ceil_div(total, std::min<int64_t>(total, slots));  // stream-K stages/CTA
+    int64_t best = -1;
+    for (int c = 1; cluster_fits(c); ++c) {
+      // automatic: clusters of at most 8 CTAs splitting the tile evenly (measured on GB300:
+      // 16-CTA clusters and uneven shares were slower than stream-K)
+      if (split == BSGEMV_SPLIT_AUTO && (c > kMaxAutoCluster || spt % c != 0)) continue;
+      const int64_t st = ceil_div(spt, c);
+      if (best < 0 || st < best) {
+        best = st;
+        C = c;
+      }
+    }
+    if (split == BSGEMV_SPLIT_AUTO && (C == 0 || best > sk + 1)) C = 0;
+    if (split == BSGEMV_SPLIT_CLUSTER && C == 0) return BSGEMV_ERR_UNSUPPORTED;
+  }
+  g->red_bytes = red_for(C);
+  auto smem_for = [&](int stages) {
+    return C > 0 ? cluster_smem(C, stages) : smem_with(stages, g->red_bytes);
+  };
+  int ctas_per_sm = slots_per_sm;
+  const int budget = budget_slots;
+  // the ring: as deep as fits (at most the CTA's share of a tile under the cluster split)
+  const int max_stages = C > 0 ? cluster_stages(C) : kMaxStages;
+  const int min_stages = std::min(2, max_stages);
+  int stages = max_stages;
+  while (stages > min_stages && smem_for(stages) > budget) --stages;
   if (smem_for(stages) > budget) {
     ctas_per_sm = 1;
     stages = kMaxStages;
@@ -126,10 +204,11 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
     stages = stages_override;
     if (smem_for(stages) > budget) ctas_per_sm = 1;
   }
-  g->side_slots = side_slots_for(stages);
+  g->side_slots = (C > 0 && g->side_bytes != 0 && cluster_one_slot(C)) ? 1 : side_slots_for(stages);
   g->act_off = stages * g->stage_bytes;
   g->side_off = g->act_off + stages * g->act_bytes;
-  g->bar_off = g->side_off + g->side_slots * g->side_bytes;
+  g->red_off = g->side_off + g->side_slots * g->side_bytes;
+  g->bar_off = g->red_off + g->red_bytes;
 
   bsgemv_geometry& pub = g->pub;
   pub.variant = BSGEMV_VARIANT_MMA;
@@ -139,11 +218,13 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   pub.consumer_warps = kConsumerWarps;
   pub.ctas_per_sm = ctas_per_sm;
   pub.sm_count = sm_count;
-  pub.tiles = ceil_div(N, kRowsPerTile);
-  pub.stages_per_tile = ceil_div(K, g->kc);
-  pub.total_stages = pub.tiles * pub.stages_per_tile;
+  pub.tiles = tiles;
+  pub.stages_per_tile = spt;
+  pub.total_stages = total;
+  pub.cluster = C;
   int64_t ctas = std::min<int64_t>(pub.total_stages, int64_t(sm_count) * ctas_per_sm);
   if (ctas_override > 0) ctas = std::min<int64_t>(pub.total_stages, ctas_override);
+  if (C > 0) ctas = tiles * C;
   pub.ctas = static_cast<int>(ctas);
   pub.smem_bytes = smem_for(stages);
   // workspace: partial slots [ctas][2][warps], counters [tiles][warps], error word
@@ -158,7 +239,8 @@ extern "C" int bsgemv_geometry_for(int format, int block_size, int has_zp, int64
                                    int max_M, int sm_count, bsgemv_geometry* g) {
   if (g == nullptr) return BSGEMV_ERR_INVALID_ARG;
   bsg::Geometry geo;
-  const int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, max_M, sm_count, 0, 0, &geo);
+  const int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, max_M, sm_count, 0, 0,
+                                       BSGEMV_SPLIT_AUTO, 0, &geo);
   if (rc != BSGEMV_OK) return rc;
   *g = geo.pub;
   return BSGEMV_OK;

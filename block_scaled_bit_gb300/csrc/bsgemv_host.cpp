@@ -107,6 +107,9 @@ void fill_params(const Geometry& g, const OperandMaps& m, const void* A, const v
   k->rs_log2 = g.rs_log2;
   k->bar_off = g.bar_off;
   k->slot_floats = g.slot_floats;
+  k->cluster = g.pub.cluster;
+  k->red_off = g.red_off;
+  k->red_tq = g.red_tq;
 }
 
 int launch_gemv(const Geometry& g, const KParams& k, cudaStream_t s) {

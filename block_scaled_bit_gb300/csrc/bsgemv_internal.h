@@ -71,6 +71,9 @@ struct KParams {
   int rs_log2;             // log2(stages per side box)
   int bar_off;
   int slot_floats;         // floats per partial slot (one warp's fragments)
+  int cluster;             // 0: stream-K; C >= 1: C CTAs per tile in one cluster
+  int red_off;             // cluster split: [C][kConsumerWarps][MT][8 * red_tq] float4 in the
+  int red_tq;              //   leader; quad lanes t < red_tq hold output columns < max_M
 };
 
 struct Geometry {
@@ -89,6 +92,8 @@ struct Geometry {
   int rs_log2, side_slots, side_bytes, zbox_bytes, side_off;
   int bar_off;
   int slot_floats;
+  int red_off, red_bytes;  // cluster split: the leader's reduction buffer
+  int red_tq;              // cluster split: quad lanes t < red_tq hold output columns < max_M
 };
 
 // Weight bytes of one stage (kRowsPerTile rows x kStageK k), and scale bytes per row of one
@@ -99,8 +104,13 @@ inline int stage_bytes(int fmt) {
 constexpr int kSideScaleBytes = 64;
 
 // Validates the problem and fills the geometry for `sm_count` SMs.  Pure host code.
+// split = enum bsgemv_split, cluster = CTAs per tile for BSGEMV_SPLIT_CLUSTER (0 = chosen).
 int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
-                     int sm_count, int ctas_override, int stages_override, Geometry* g);
+                     int sm_count, int ctas_override, int stages_override, int split, int cluster,
+                     Geometry* g);
+
+constexpr int kMaxCluster = 16;     // CTAs per cluster (above 8: non-portable cluster size)
+constexpr int kMaxAutoCluster = 8;  // largest cluster the automatic split picks
 
 // Kernel launchers (one translation unit per weight format; int4 split by activation type).
 // cpb: see block_mode.

@@ -166,6 +166,32 @@ BSG_DEV unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
   return old;
 }
 
+// Thread-block clusters: this CTA's rank, the shared-window address of `addr` in CTA `rank` of
+// the cluster, a 16-byte store there, and a cluster-wide barrier (release / acquire: shared
+// memory written before it by any CTA of the cluster is visible after it).
+BSG_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+BSG_DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+  return d;
+}
+
+BSG_DEV void st_cluster_f32x4(uint32_t addr, float x, float y, float z, float w) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(x), "f"(y),
+               "f"(z), "f"(w)
+               : "memory");
+}
+
+BSG_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
 BSG_DEV void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -1201,6 +1227,49 @@ struct Gemv {
     if (lane == 0) p.counters[tile * kConsumerWarps + rg] = 0u;  // all arrived: reset for reuse
   }
 
+  // ---- cluster split: the CTAs of a cluster each hold a K-range of the same tile.  Every
+  // consumer warp stores the fragment lanes that hold output columns below max_M (quad lanes
+  // t < red_tq) into the leader's (rank 0) reduction buffer slot [rank][warp], through
+  // distributed shared memory; after the cluster barrier the leader's warps add the slots in rank
+  // order (fixed: deterministic) and store y.
+  static BSG_DEV uint32_t red_slot(const KParams& p, const Smem& sm, int rank, int cw, int mt,
+                                   int li) {
+    const int per_mt = 8 * p.red_tq;
+    return sm.base_u + p.red_off + ((((rank * kConsumerWarps + cw) * MT + mt) * per_mt) + li) * 16;
+  }
+
+  static BSG_DEV void cluster_publish(const KParams& p, const Smem& sm, int cw, const Lane& L,
+                                      const float (&acc)[1][MT][4]) {
+    if (L.t >= p.red_tq) return;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int li = L.g * p.red_tq + L.t;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+      st_cluster_f32x4(mapa_shared(red_slot(p, sm, rank, cw, mt, li), 0), acc[0][mt][0],
+                       acc[0][mt][1], acc[0][mt][2], acc[0][mt][3]);
+  }
+
+  static BSG_DEV void cluster_reduce(const KParams& p, const Smem& sm, int cw, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    if (t >= p.red_tq) return;
+    const int li = g * p.red_tq + t;
+    const int64_t tile = blockIdx.x / p.cluster;
+    const float gs = kFold ? __ldg(p.gscale) : 1.0f;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int r = 0; r < p.cluster; ++r) {
+        const float4 u = *reinterpret_cast<const float4*>(
+            sm.base + (red_slot(p, sm, r, cw, mt, li) - sm.base_u));
+        v[0] += u.x;
+        v[1] += u.y;
+        v[2] += u.z;
+        v[3] += u.w;
+      }
+      store_y(p, tile, cw, mt, lane, v, gs);
+    }
+  }
+
   // ---- consumers: warps 1..4.  The CTA's range is walked tile segment by tile segment; within
   // a segment every stage waits for its slot (and, when it opens one, its side box), is
   // multiplied in, and is released; the segment ends with the epilogue.
@@ -1245,8 +1314,12 @@ struct Gemv {
         w.next();
       }
       i += seg;
-      // whole: this CTA consumed every stage of the tile
-      epilogue(p, tile, seg == spt, first_tile, cw, lane, acc, gs);
+      if (p.cluster >= 2) {
+        cluster_publish(p, sm, cw, L, acc);  // the cluster's leader adds and stores
+      } else {
+        // whole: this CTA consumed every stage of the tile
+        epilogue(p, tile, seg == spt, first_tile, cw, lane, acc, gs);
+      }
       zero(acc[0]);
     }
   }
@@ -1262,9 +1335,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT)) bsgemv_mma_k
   const typename K::Smem sm{base, smem_u32(base), p.stages, p.act_off, p.act_bytes,
                             p.side_off, p.side_bytes, p.side_slots, p.bar_off};
 
-  const int64_t G = gridDim.x, T = p.total_stages;
-  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * T / G;
-  const int64_t s1 = (static_cast<int64_t>(blockIdx.x) + 1) * T / G;
+  // stream-K: an equal share of the tiles x stages space; cluster split: an equal share of the
+  // stages of tile blockIdx.x / cluster (the cluster's CTAs are consecutive in x)
+  int64_t s0, s1;
+  if (p.cluster > 0) {
+    const int64_t C = p.cluster, tile = blockIdx.x / C, r = blockIdx.x % C;
+    s0 = tile * p.spt + r * p.spt / C;
+    s1 = tile * p.spt + (r + 1) * p.spt / C;
+  } else {
+    const int64_t G = gridDim.x, T = p.total_stages;
+    s0 = static_cast<int64_t>(blockIdx.x) * T / G;
+    s1 = (static_cast<int64_t>(blockIdx.x) + 1) * T / G;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
@@ -1285,6 +1367,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT)) bsgemv_mma_k
     K::produce(p, sm, s0, s1, lane);
   } else {
     K::consume(p, sm, s0, s1, warp - 1, lane);
+  }
+  if (p.cluster >= 2) {
+    cluster_sync();  // every CTA of the cluster has stored its partials in the leader
+    if (cluster_ctarank() == 0 && warp > 0) K::cluster_reduce(p, sm, warp - 1, lane);
   }
 }
 

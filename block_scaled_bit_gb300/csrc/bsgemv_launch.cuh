@@ -11,23 +11,43 @@ template <int FMT, bool BF16, int MT, bool ZP, int CPB>
 int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
   auto k = bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB>;
   static std::atomic<int> attr_smem{0};  // largest dynamic smem already granted to `k`
+  static std::atomic<int> attr_cluster{0};  // non-portable cluster sizes allowed for `k`
   if (smem > attr_smem.load()) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    // One shared-memory carveout (the largest) for every instantiation: an SM holds CTAs of
+    // kernels with different carveouts only after draining, which would serialise consecutive
+    // calls that programmatic dependent launch otherwise overlaps.
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return BSGEMV_ERR_CUDA;
     attr_smem.store(smem);
   }
+  if (p.cluster > 8 && attr_cluster.load() == 0) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return BSGEMV_ERR_CUDA;
+    attr_cluster.store(1);
+  }
   // Programmatic dependent launch: the kernel may start while the previous kernel in the stream
   // drains; it waits (griddepcontrol.wait) before touching anything that kernel could write.
-  cudaLaunchAttribute attr[1];
+  // Cluster split: the CTAs of a tile form one cluster (consecutive in x).
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int nattr = 1;
+  if (p.cluster >= 2) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    nattr = 2;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = nattr;
   if (cudaLaunchKernelEx(&cfg, k, p) != cudaSuccess) return BSGEMV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
 }

@@ -85,7 +85,8 @@ extern "C" int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_
   }
   if (major != 10 || minor != 3) return BSGEMV_ERR_UNSUPPORTED;
   bsg::Geometry g;
-  int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, M, sms, 0, 0, &g);
+  int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, M, sms, 0, 0, BSGEMV_SPLIT_AUTO,
+                                 0, &g);
   if (rc != BSGEMV_OK) return rc;
   if (g.pub.ctas > kMaxCtas || g.pub.tiles > kMaxTiles || g.slot_floats > kMaxSlotFloats)
     return BSGEMV_ERR_SCRATCH_LIMIT;

@@ -96,7 +96,18 @@ typedef struct {
   int64_t total_stages;  /* tiles * stages_per_tile: the work split evenly over the CTAs */
   int smem_bytes;        /* dynamic shared memory per CTA */
   int64_t workspace_bytes;
+  int cluster;           /* how a tile's K is split: 0 = stream-K over all CTAs with a global
+                            last-arriver reduction; C >= 1 = C CTAs per tile in one thread-block
+                            cluster, reduced in the cluster leader's shared memory */
 } bsgemv_geometry;
+
+/* How a plan splits the K of a tile over CTAs (bsgemv_plan_set_split). */
+enum bsgemv_split {
+  BSGEMV_SPLIT_AUTO = 0,      /* cluster split where its per-CTA work is within one stage of
+                                 stream-K's, else stream-K */
+  BSGEMV_SPLIT_STREAM_K = 1,  /* the tiles x stages space cut into equal ranges over all CTAs */
+  BSGEMV_SPLIT_CLUSTER = 2    /* each tile split evenly over the CTAs of one cluster */
+};
 
 /*
  * Create a plan for one weight shape.  format = enum bsgemv_format, optionally | BSGEMV_ACT_BF16.
@@ -147,8 +158,19 @@ int bsgemv_debug_dequant(bsgemv_plan_t plan, const void* W, const void* scales, 
                          float* out, void* stream);
 
 /*
+ * Choose how the plan splits each tile's K over CTAs (no counterpart on the pages, whose kernels
+ * use a fixed split-K or none: an A/B and testing aid like bsgemv_plan_set_override).
+ * split = enum bsgemv_split; cluster_size (CLUSTER only) = CTAs per tile, 1..16, 0 = chosen by
+ * the plan from the SM count.  Returns BSGEMV_ERR_UNSUPPORTED when the tiles x cluster_size
+ * CTAs do not fit one wave of the device or cluster_size exceeds the stages of a tile; the plan
+ * is then unchanged.  Not thread-safe with bsgemv_run on the same plan.
+ */
+int bsgemv_plan_set_split(bsgemv_plan_t plan, int split, int cluster_size);
+
+/*
  * A/B override for measurements: variant (enum bsgemv_variant, 0 = keep), ctas (persistent
- * CTAs, 0 = keep), rows_per_tile (reserved, must be 0), stages (ring depth, 0 = keep).
+ * CTAs of a stream-K split, 0 = keep; under BSGEMV_SPLIT_AUTO a CTA count selects stream-K),
+ * rows_per_tile (reserved, must be 0), stages (ring depth, 0 = keep).
  * Changes the summation order, so results are bit-identical only between calls made under the
  * same settings.  Returns BSGEMV_ERR_UNSUPPORTED for a setting the plan cannot run.
  */

@@ -99,13 +99,22 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
     assert g["stages_per_tile"] == -(-K // g["k_per_stage"])
     assert g["total_stages"] == g["tiles"] * g["stages_per_tile"]
     # persistent grid: never more CTAs than stages or than the resident slots
-    assert 1 <= g["ctas"] <= min(g["total_stages"], sms * g["ctas_per_sm"])
-    if g["total_stages"] >= sms * g["ctas_per_sm"]:
-        assert g["ctas"] == sms * g["ctas_per_sm"]
+    slots = sms * g["ctas_per_sm"]
+    assert 1 <= g["ctas"] <= min(g["total_stages"], slots)
+    C, spt = g["cluster"], g["stages_per_tile"]
+    stream_k_stages = -(-g["total_stages"] // min(g["total_stages"], slots))
+    if C == 0:  # stream-K: one full wave
+        if g["total_stages"] >= slots:
+            assert g["ctas"] == slots
+    else:  # cluster split: C CTAs per tile, within one stage of stream-K's work per CTA
+        assert 1 <= C <= 8 and C <= spt and spt % C == 0
+        assert g["ctas"] == g["tiles"] * C
+        assert -(-spt // C) <= stream_k_stages + 1
     # shared memory fits the residency it was sized for
     assert g["smem_bytes"] <= 232448
     assert g["ctas_per_sm"] * (g["smem_bytes"] + 1024) <= 233472
-    assert 2 <= g["stages"] <= 12
+    # the ring: 2..12 stages, or the CTA's whole share of a tile under the cluster split
+    assert (1 if g["cluster"] else 2) <= g["stages"] <= 12
     assert g["sm_count"] == sms
     # the same inputs give the same geometry; act dtype does not change it
     assert bsgemv.geometry_for(fmt, "bf16", bs, zp, N, K, max_M, sms) == g
@@ -165,3 +174,21 @@ def test_owner_lookup_without_division():
                 continue
             for x in [0, T - 1] + [rng.randrange(T) for _ in range(300)]:
                 assert owner(x, T, G) == ((x + 1) * G + T - 1) // T - 1
+
+
+def test_split_choice_on_the_configuration_shapes(L):
+    """Automatic K split at 152 SMs (4 CTAs per SM): shapes with few tiles take a cluster of CTAs
+    per tile (reduced in shared memory), shapes with more tiles than resident CTAs stream-K."""
+    def split(fmt, bs, zp, N, K, max_M=1):
+        g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, 152)
+        return g["cluster"], -(-g["stages_per_tile"] // max(1, g["cluster"])) if g["cluster"] else None
+    assert split("int8", 32, True, 2048, 4096) == (8, 2)     # 32 tiles x 16 stages
+    assert split("int8", 128, True, 4096, 12288) == (8, 6)   # 64 tiles x 48 stages
+    assert split("fp8", 128, False, 5120, 6144) == (6, 4)    # 80 tiles x 24 stages
+    assert split("int8", 128, True, 12288, 4096)[0] == 0     # 192 tiles: no even split fits
+    assert split("fp8", 128, False, 5120, 17408)[0] == 0     # 80 tiles x 68 stages
+    assert split("int8", 128, True, 4096, 4096) == (8, 2)    # 64 tiles x 16 stages
+    assert split("int8", 128, True, 5120, 2048) == (4, 2)    # 80 tiles x 8 stages
+    assert split("fp8", 128, False, 512, 2048) == (8, 1)     # 8 tiles x 8 stages
+    assert split("int4", 32, False, 151936, 4096)[0] == 0    # 2374 tiles: stream-K
+    assert split("nvfp4", 16, False, 248320, 2048)[0] == 0   # 3880 tiles: stream-K

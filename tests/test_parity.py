@@ -120,6 +120,44 @@ def test_every_stream_k_split_is_correct(torch_cuda, ctas):
     assert_parity(case, y)
 
 
+@pytest.mark.parametrize("fmt,act,bs,zp,N,K", [
+    ("int8", "f16", 32, True, 2048, 4096), ("int4", "bf16", 32, False, 700, 2048),
+    ("nvfp4", "f16", 16, False, 300, 4096), ("fp8", "bf16", 128, False, 130, 2560),
+    ("int4", "f16", 16, True, 257, 1280)])
+@pytest.mark.parametrize("cluster,M", [(c, m) for c in (1, 2, 3, 5, 8, 16) for m in (1, 2)]
+                         + [(2, 11), (3, 11), (4, 9)])
+def test_cluster_split_is_correct(torch_cuda, fmt, act, bs, zp, N, K, cluster, M):
+    """Each tile split over a thread-block cluster of `cluster` CTAs (uneven shares when the
+    cluster size does not divide the tile's stages), reduced in the leader's shared memory."""
+    case = synth.make_case(fmt, act, bs, zp, N, K, M, 1000 + cluster + N)
+    with bsgemv.Plan(fmt, act, bs, zp, N, K, M) as plan:
+        g0 = plan.describe()
+        status = plan.set_split("cluster", cluster)
+        if cluster > g0["stages_per_tile"] or g0["tiles"] * cluster > g0["sm_count"] * g0["ctas_per_sm"]:
+            assert status == bsgemv.ERR_UNSUPPORTED  # more CTAs than stages, or than one wave
+            return
+        assert status == bsgemv.OK
+        g = plan.describe()
+        assert g["cluster"] == cluster and g["ctas"] == g["tiles"] * cluster
+        y = run(case, plan, max_M=M)
+        assert plan.device_status() == bsgemv.OK
+    assert_parity(case, y)
+
+
+def test_stream_k_and_cluster_split_agree_within_tolerance(torch_cuda):
+    """Same problem, both splits: each within the bound of the oracle, and rows bit-identical
+    across M inside each."""
+    case16 = synth.make_case("int8", "f16", 128, True, 1000, 4096, 16, 321)
+    for split in ("stream_k", "cluster"):
+        with bsgemv.Plan("int8", "f16", 128, True, case16.N, case16.K, 16) as plan:
+            assert plan.set_split(split) == bsgemv.OK
+            assert (plan.describe()["cluster"] > 0) == (split == "cluster")
+            y16 = run(case16, plan)
+            for M in (1, 3, 9):
+                assert np.array_equal(run(case16.with_M(M), plan), y16[:M])
+        assert_parity(case16, y16)
+
+
 @pytest.mark.parametrize("stages", [2, 3, 8])
 def test_ring_depths(torch_cuda, stages):
     case = synth.make_case("fp8", "bf16", 128, False, 500, 2048, 8, 93)
