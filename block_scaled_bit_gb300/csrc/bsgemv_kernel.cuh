@@ -243,11 +243,14 @@ BSG_DEV T lsh(const uint8_t* p) {
   return *reinterpret_cast<const T*>(p);
 }
 
-// (a & b) | c in one LOP3 (b and c in registers: the compiler would otherwise split two
-// immediates into two logic instructions).
-BSG_DEV uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+// Bits of a where MASK is set, bits of c elsewhere: one LOP3 with the mask as its immediate.
+// The decoders take the constant part of an operand (exponent bits) from the zero-point
+// registers they hold anyway, so no constant has to be kept in (or re-created into) a register
+// per use.
+template <uint32_t MASK>
+BSG_DEV uint32_t select_bits(uint32_t a, uint32_t c) {
   uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  asm("lop3.b32 %0, %1, %2, %3, 0xE2;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
   return d;
 }
 
@@ -311,11 +314,6 @@ BSG_DEV void ffma2(float& acc0, float& acc1, float x0, float x1, float s) {
 // ------------------------------------------------------------------------------ 16-bit pairs
 BSG_DEV uint32_t h2_sub(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-BSG_DEV uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
-                      *reinterpret_cast<__half2*>(&c));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 BSG_DEV uint32_t h2_mul(uint32_t a, uint32_t b) {
@@ -404,36 +402,33 @@ BSG_DEV uint32_t f16x2_exact_to_bf16x2(uint32_t h) {
 //   a[s][2] = (row g,   cols 2t+8, 2t+9) a[s][3] = (row g+8, cols 2t+8, 2t+9)
 // The physical k of each half is given by phys_k below; the activation fragment follows it.
 
-// int4: nibble j of the lane's word holds k = 8t + j.  (1024 + q) in f16 is the nibble OR-ed
-// under the exponent of 1024; (1024 + 16 q) for the high nibble of a byte, which an fma with
-// 1/16 brings back.  Both give the exact small integer q - zp
-// ("[CUDA] MatMulNBits 8-bit: wide fp16 M=1 kernel for decode GEMVs", Description: exact
-// (q - zp) in fp16).  zl = (1024 + zp) and zh = -(64 + zp) replicated in both halves.
-// For bf16 the exponent of 128 holds 7 mantissa bits, so each nibble is shifted to the bottom
-// first and zl = (128 + zp).
+// int4: nibble j of the lane's word holds k = 8t + j.  Put under the exponent bits of
+// zl = (1024 + zp) (zp sits in the low nibble, which the nibble replaces), the low nibble of a
+// byte gives the f16 value 1024 + q; put under the sign and exponent of zh = -(64 + zp) (zp in
+// bits 4..7, replaced), the high nibble gives -(64 + q), so that zh minus it is q - zp.  Both
+// results are the exact small integer q - zp ("[CUDA] MatMulNBits 8-bit: wide fp16 M=1 kernel
+// for decode GEMVs", Description: exact (q - zp) in fp16).  For bf16 the exponent of 128 holds
+// 7 mantissa bits, so each nibble is shifted to the bottom first and zl = (128 + zp).
 template <bool BF16>
 BSG_DEV void decode_int4(uint32_t lo, uint32_t hi, uint32_t zl_lo, uint32_t zh_lo, uint32_t zl_hi,
                          uint32_t zh_hi, uint32_t (&a)[2][4]) {
   if constexpr (!BF16) {
-    const uint32_t k16 = 0x2C002C00u;  // 1/16 in each f16 half
-    const uint32_t m_lo = 0x000F000Fu, m_hi = 0x00F000F0u, e = 0x64006400u;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const uint32_t wl = lo >> (8 * s), wh = hi >> (8 * s);
-      a[s][0] = h2_sub(and_or(wl, m_lo, e), zl_lo);
-      a[s][1] = h2_sub(and_or(wh, m_lo, e), zl_hi);
-      a[s][2] = h2_fma(and_or(wl, m_hi, e), k16, zh_lo);
-      a[s][3] = h2_fma(and_or(wh, m_hi, e), k16, zh_hi);
+      a[s][0] = h2_sub(select_bits<0x000F000Fu>(wl, zl_lo), zl_lo);
+      a[s][1] = h2_sub(select_bits<0x000F000Fu>(wh, zl_hi), zl_hi);
+      a[s][2] = h2_sub(zh_lo, select_bits<0x00F000F0u>(wl, zh_lo));
+      a[s][3] = h2_sub(zh_hi, select_bits<0x00F000F0u>(wh, zh_hi));
     }
   } else {
-    const uint32_t m_lo = 0x000F000Fu, e = 0x43004300u;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const uint32_t wl = lo >> (8 * s), wh = hi >> (8 * s);
-      a[s][0] = bf2_sub(and_or(wl, m_lo, e), zl_lo);
-      a[s][1] = bf2_sub(and_or(wh, m_lo, e), zl_hi);
-      a[s][2] = bf2_sub(and_or(wl >> 4, m_lo, e), zl_lo);
-      a[s][3] = bf2_sub(and_or(wh >> 4, m_lo, e), zl_hi);
+      a[s][0] = bf2_sub(select_bits<0x000F000Fu>(wl, zl_lo), zl_lo);
+      a[s][1] = bf2_sub(select_bits<0x000F000Fu>(wh, zl_hi), zl_hi);
+      a[s][2] = bf2_sub(select_bits<0x000F000Fu>(wl >> 4, zl_lo), zl_lo);
+      a[s][3] = bf2_sub(select_bits<0x000F000Fu>(wh >> 4, zl_hi), zl_hi);
     }
   }
   (void)zh_lo;
@@ -441,29 +436,31 @@ BSG_DEV void decode_int4(uint32_t lo, uint32_t hi, uint32_t zl_lo, uint32_t zh_l
 }
 
 // int8: byte j of the lane's word holds k = 4t + j.  f16: prmt places byte j under the
-// exponent of 1024 (exact 1024 + q), minus (1024 + zp).  bf16 (7 mantissa bits cannot hold
-// 0..255 above one exponent): 2^23 + q in fp32, minus (2^23 + zp), packed by an exact cvt.
+// exponent byte of 1024, taken from z = (1024 + zp) itself (its bytes 1 and 3), giving the
+// exact 1024 + q, minus z.  bf16 (7 mantissa bits cannot hold 0..255 above one exponent):
+// 2^23 + q in fp32 (the high bytes again from z = 2^23 + zp: bytes 1, 2 are zero, byte 3 the
+// exponent), minus z, packed by an exact cvt.
 template <bool BF16>
 BSG_DEV void decode_int8(uint32_t lo, uint32_t hi, uint32_t z_lo, uint32_t z_hi,
                          uint32_t (&a)[1][4]) {
   if constexpr (!BF16) {
-    a[0][0] = h2_sub(prmt(lo, 0x64646464u, 0x4140u), z_lo);
-    a[0][1] = h2_sub(prmt(hi, 0x64646464u, 0x4140u), z_hi);
-    a[0][2] = h2_sub(prmt(lo, 0x64646464u, 0x4342u), z_lo);
-    a[0][3] = h2_sub(prmt(hi, 0x64646464u, 0x4342u), z_hi);
+    a[0][0] = h2_sub(prmt(lo, z_lo, 0x5150u), z_lo);
+    a[0][1] = h2_sub(prmt(hi, z_hi, 0x5150u), z_hi);
+    a[0][2] = h2_sub(prmt(lo, z_lo, 0x5352u), z_lo);
+    a[0][3] = h2_sub(prmt(hi, z_hi, 0x5352u), z_hi);
   } else {
-    const float zf_lo = __uint_as_float(z_lo), zf_hi = __uint_as_float(z_hi);  // 2^23 + zp
-    auto pair = [](uint32_t w, uint32_t sel0, uint32_t sel1, float z) -> uint32_t {
-      const float x0 = __uint_as_float(prmt(w, 0x4B000000u, sel0)) - z;
-      const float x1 = __uint_as_float(prmt(w, 0x4B000000u, sel1)) - z;
+    auto pair = [](uint32_t w, uint32_t sel0, uint32_t sel1, uint32_t z) -> uint32_t {
+      const float zf = __uint_as_float(z);  // 2^23 + zp
+      const float x0 = __uint_as_float(prmt(w, z, sel0)) - zf;
+      const float x1 = __uint_as_float(prmt(w, z, sel1)) - zf;
       uint32_t d;
       asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(x1), "f"(x0));
       return d;
     };
-    a[0][0] = pair(lo, 0x7440u, 0x7441u, zf_lo);
-    a[0][1] = pair(hi, 0x7440u, 0x7441u, zf_hi);
-    a[0][2] = pair(lo, 0x7442u, 0x7443u, zf_lo);
-    a[0][3] = pair(hi, 0x7442u, 0x7443u, zf_hi);
+    a[0][0] = pair(lo, 0x7550u, 0x7551u, z_lo);
+    a[0][1] = pair(hi, 0x7550u, 0x7551u, z_hi);
+    a[0][2] = pair(lo, 0x7552u, 0x7553u, z_lo);
+    a[0][3] = pair(hi, 0x7552u, 0x7553u, z_hi);
   }
 }
 
@@ -793,84 +790,39 @@ struct Gemv {
     return n < p.k.N ? n : p.k.N - 1;
   }
 
-  // fp32 scales of the lane's 2 rows for NB consecutive blocks: from the side box `sb` at
-  // box-relative block `rel` (a multiple of NB: one shared load of NB scales per row), or from
-  // global memory at absolute block `blk`.
+  // fp32 scales of the lane's 2 rows for NB consecutive blocks from global memory, at absolute
+  // block `blk` (the path for scale arrays whose pitch a tensor map cannot describe).
   template <int NB, class R>
-  static BSG_DEV void load_scales(const R& p, const Lane& L, const uint8_t* sb, int64_t tile,
-                                  int blk, int rel, float (&s)[NB][2]) {
-    if constexpr (R::side) {
+  static BSG_DEV void load_scales(const R& p, const Lane& L, int64_t tile, int blk,
+                                  float (&s)[NB][2]) {
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const uint8_t* a = sb + L.srow + rr * 8 * kSideScaleBytes + rel * kScaleEs;
-        if constexpr (FMT == kFp8) {
-          static_assert(NB == 1, "one fp32 scale per warp stage");
-          s[0][rr] = __uint_as_float(lsh<uint32_t>(a));
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint8_t* src = p.k.scales + row_of(p, L, tile, rr) * p.k.scale_pitch;
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const int b = blk + u;
+        if (b >= p.k.nb_s) {  // chunk past K in the ragged last stage: its weight is zero
+          s[u][rr] = 0.f;
+        } else if constexpr (FMT == kFp8) {
+          s[u][rr] = __ldg(reinterpret_cast<const float*>(src) + b);
         } else {
-          uint32_t h[4];
-          if constexpr (NB == 1) {
-            h[0] = lsh<uint16_t>(a);
-          } else if constexpr (NB == 2) {
-            h[0] = lsh<uint32_t>(a);
-          } else if constexpr (NB == 4) {
-            const uint2 v = lsh<uint2>(a);
-            h[0] = v.x;
-            h[1] = v.y;
-          } else {
-            const uint4 v = lsh<uint4>(a);
-            h[0] = v.x;
-            h[1] = v.y;
-            h[2] = v.z;
-            h[3] = v.w;
-          }
-#pragma unroll
-          for (int u = 0; u < NB; ++u) {
-            const __half2 two = *reinterpret_cast<const __half2*>(&h[u >> 1]);
-            s[u][rr] = (u & 1) ? __high2float(two) : __low2float(two);
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const uint8_t* src = p.k.scales + row_of(p, L, tile, rr) * p.k.scale_pitch;
-#pragma unroll
-        for (int u = 0; u < NB; ++u) {
-          const int b = blk + u;
-          if (b >= p.k.nb_s) {  // chunk past K in the ragged last stage: its weight is zero
-            s[u][rr] = 0.f;
-          } else if constexpr (FMT == kFp8) {
-            s[u][rr] = __ldg(reinterpret_cast<const float*>(src) + b);
-          } else {
-            s[u][rr] = __half2float(__ldg(reinterpret_cast<const __half*>(src) + b));
-          }
+          s[u][rr] = __half2float(__ldg(reinterpret_cast<const __half*>(src) + b));
         }
       }
     }
   }
 
-  // Zero points of the lane's 2 rows for NB consecutive blocks (same addressing as
-  // load_scales), packed as loaded: block u at bit u * kZpW.  Without zero points: the
+  // Zero points of the lane's 2 rows for NB consecutive blocks from global memory (same
+  // addressing as load_scales), packed: block u at bit u * kZpW.  Without zero points: the
   // implicit 2^(bits-1) of every block.
+  static constexpr uint32_t kNoZp = (FMT == kInt4) ? 0x88888888u : 0x80808080u;
+
   template <int NB, class R>
-  static BSG_DEV void load_zp(const R& p, const Lane& L, const uint8_t* sb, int64_t tile,
-                              int blk, int rel, uint32_t (&z)[2]) {
+  static BSG_DEV void load_zp(const R& p, const Lane& L, int64_t tile, int blk, uint32_t (&z)[2]) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       if constexpr (!ZP) {
-        z[rr] = (FMT == kInt4) ? 0x88888888u : 0x80808080u;
-      } else if constexpr (R::side) {
-        const uint8_t* a = sb + L.zrow + rr * 8 * p.zbox_bytes + ((rel * kZpW) >> 3);
-        constexpr int kBits = NB * kZpW;
-        if constexpr (kBits <= 4) {
-          z[rr] = static_cast<uint32_t>(lsh<uint8_t>(a)) >> ((rel & 1) * 4);
-        } else if constexpr (kBits == 8) {
-          z[rr] = lsh<uint8_t>(a);
-        } else if constexpr (kBits == 16) {
-          z[rr] = lsh<uint16_t>(a);
-        } else {
-          z[rr] = lsh<uint32_t>(a);
-        }
+        z[rr] = kNoZp;
       } else {
         uint32_t v = 0;
         const uint8_t* src = p.k.zp + row_of(p, L, tile, rr) * p.k.zp_pitch;
@@ -885,6 +837,86 @@ struct Gemv {
           v |= q << (u * kZpW);
         }
         z[rr] = v;
+      }
+    }
+  }
+
+  // Scales and zero points of the lane's 2 rows for NB consecutive blocks of a side box, in one
+  // shared load per row each (NB a power of two; the first block `rel` a multiple of NB, so the
+  // loads are aligned): f16 scale pairs (or the fp32 scale of FP8, NB = 1) and zero points
+  // packed at kZpW bits per block, as stored.
+  template <int NB>
+  struct SideLoad {
+    uint32_t s[2][(NB + 1) / 2];
+    uint32_t z[2][(NB * kZpW + 31) / 32];
+  };
+
+  template <int NB, class R>
+  static BSG_DEV void load_side(const R& p, const Lane& L, const uint8_t* sb, int rel,
+                                SideLoad<NB>& v) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint8_t* a = sb + L.srow + rr * 8 * kSideScaleBytes + rel * kScaleEs;
+      if constexpr (FMT == kFp8) {
+        static_assert(NB == 1, "one fp32 scale per weight box");
+        v.s[rr][0] = lsh<uint32_t>(a);
+      } else if constexpr (NB == 1) {
+        v.s[rr][0] = lsh<uint16_t>(a);
+      } else if constexpr (NB == 2) {
+        v.s[rr][0] = lsh<uint32_t>(a);
+      } else if constexpr (NB == 4) {
+        const uint2 x = lsh<uint2>(a);
+        v.s[rr][0] = x.x;
+        v.s[rr][1] = x.y;
+      } else {
+        static_assert(NB == 8, "at most 8 blocks per side load");
+        const uint4 x = lsh<uint4>(a);
+        v.s[rr][0] = x.x;
+        v.s[rr][1] = x.y;
+        v.s[rr][2] = x.z;
+        v.s[rr][3] = x.w;
+      }
+      if constexpr (ZP) {
+        const uint8_t* za = sb + L.zrow + rr * 8 * p.zbox_bytes + ((rel * kZpW) >> 3);
+        constexpr int kBits = NB * kZpW;
+        if constexpr (kBits == 4) {
+          v.z[rr][0] = static_cast<uint32_t>(lsh<uint8_t>(za)) >> ((rel & 1) * 4);
+        } else if constexpr (kBits == 8) {
+          v.z[rr][0] = lsh<uint8_t>(za);
+        } else if constexpr (kBits == 16) {
+          v.z[rr][0] = lsh<uint16_t>(za);
+        } else if constexpr (kBits == 32) {
+          v.z[rr][0] = lsh<uint32_t>(za);
+        } else {
+          const uint2 x = lsh<uint2>(za);
+          v.z[rr][0] = x.x;
+          v.z[rr][1] = x.y;
+        }
+      }
+    }
+  }
+
+  // The scales (fp32) and packed zero points of blocks b0 .. b0 + NG - 1 of a side load.
+  template <int NG, int NB>
+  static BSG_DEV void side_group(const SideLoad<NB>& v, int b0, uint32_t (&z)[2],
+                                 float (&s)[NG][2]) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+#pragma unroll
+      for (int u = 0; u < NG; ++u) {
+        const int b = b0 + u;
+        if constexpr (FMT == kFp8) {
+          s[u][rr] = __uint_as_float(v.s[rr][0]);
+        } else {
+          const __half2 two = *reinterpret_cast<const __half2*>(&v.s[rr][b >> 1]);
+          s[u][rr] = (b & 1) ? __high2float(two) : __low2float(two);
+        }
+      }
+      if constexpr (ZP) {
+        const int bit = b0 * kZpW;  // a group's zero points never straddle a word
+        z[rr] = v.z[rr][bit >> 5] >> (bit & 31);
+      } else {
+        z[rr] = kNoZp;
       }
     }
   }
@@ -1065,14 +1097,25 @@ struct Gemv {
         }
       }
     } else {
+      // side ring: one load per row of the scales and zero points of up to 8 blocks (the whole
+      // box, or half of it for 16-element int4 blocks)
+      constexpr int kBB = (8 / kGC) * kGB;         // scale blocks per weight box
+      constexpr int kSL = kBB < 8 ? kBB : 8;       // blocks per side load
+      constexpr int kGpl = kSL / kGB;              // groups per side load
+      SideLoad<kSL> sl;
 #pragma unroll
       for (int grp = 0; grp < 8 / kGC; ++grp) {
         const int kg = (c0 + grp * kGC) * kKpc;  // k of the group in the stage
-        const int blk = (k0 + kg) >> p.bs_log2, rel = (kb + kg) >> p.bs_log2;
         uint32_t z[2];
-        load_zp<kGB>(p, L, sb, tile, blk, rel, z);
         float s[kGB][2];
-        load_scales<kGB>(p, L, sb, tile, blk, rel, s);
+        if constexpr (R::side) {
+          if (grp % kGpl == 0) load_side<kSL>(p, L, sb, (kb + kg) >> p.bs_log2, sl);
+          side_group<kGB>(sl, (grp % kGpl) * kGB, z, s);
+        } else {
+          const int blk = (k0 + kg) >> p.bs_log2;
+          load_zp<kGB>(p, L, tile, blk, z);
+          load_scales<kGB>(p, L, tile, blk, s);
+        }
         if constexpr (CPB == 0) {  // one chunk, two blocks: the lane's codes are in block t/2
           zp_of(z, L.t >> 1, zl, zh);
           float tmp[2][MT][4];
