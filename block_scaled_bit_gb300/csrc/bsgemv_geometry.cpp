@@ -79,16 +79,15 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   g->kpc = four ? 32 : 16;
   g->kc = kStageK;
   g->stage_bytes = stage_bytes(fmt);
-  g->nbox = g->kc / 64;
   g->mt_max = max_M <= 8 ? 1 : 2;
   g->scale_es = (fmt == kFp8) ? 4 : (fmt == kNvfp4 ? 1 : 2);
   g->nb_s = static_cast<int>(K / block_size);
   g->scale_pitch = g->nb_s * g->scale_es;
   g->zp_pitch = (fmt == kInt4) ? (g->nb_s + 1) / 2 : g->nb_s;
 
-  // activation ring: per stage, nbox boxes of 64 k x max_M rows (128 B per row)
-  g->act_box_bytes = max_M * 128;
-  g->act_bytes = g->nbox * g->act_box_bytes;
+  // activation ring: per stage, max_M rows of the stage's k (2 kc bytes) padded by one chunk's
+  // activation bytes (32 or 64: consecutive rows start in different banks)
+  g->act_bytes = max_M * (2 * g->kc + (four ? 64 : 32));
   // side ring: one box holds kSideScaleBytes of scales per row (64 / es blocks), i.e.
   // 2^rs_log2 stages, and the zero points of the same blocks
   const int blocks_per_box = kSideScaleBytes / g->scale_es;
@@ -108,6 +107,8 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   const int64_t tiles = ceil_div(N, kRowsPerTile);
   const int64_t total = tiles * spt;
 
+  // activation ring bytes, rounded up so that the side ring after it starts 128-byte aligned
+  auto act_ring = [&](int stages) { return (stages * g->act_bytes + 127) / 128 * 128; };
   // side boxes in flight over a ring of `stages`: a box spans min(2^rs, stages per tile) stages
   auto side_slots_for = [&](int stages) {
     if (g->side_bytes == 0) return 0;
@@ -116,7 +117,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   };
   auto smem_with = [&](int stages, int red) {
     const int ss = side_slots_for(stages);
-    return 1024 + stages * (g->stage_bytes + g->act_bytes) + ss * g->side_bytes + red +
+    return 1024 + stages * g->stage_bytes + act_ring(stages) + ss * g->side_bytes + red +
            8 * (2 * stages + 8);
   };
   const int slots_per_sm = ctas_per_sm_for_mt(g->mt_max);
@@ -148,7 +149,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   // smaller footprint was otherwise slower for back-to-back calls)
   auto cluster_smem_ss = [&](int64_t c, int stages, bool one) {
     const int ss = (g->side_bytes == 0) ? 0 : (one ? 1 : side_slots_for(stages));
-    return 1024 + stages * (g->stage_bytes + g->act_bytes) + ss * g->side_bytes +
+    return 1024 + stages * g->stage_bytes + act_ring(stages) + ss * g->side_bytes +
            red_for(static_cast<int>(c)) + 8 * (2 * stages + 8);
   };
   auto cluster_one_slot = [&](int64_t c) {
@@ -206,9 +207,15 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   }
   g->side_slots = (C > 0 && g->side_bytes != 0 && cluster_one_slot(C)) ? 1 : side_slots_for(stages);
   g->act_off = stages * g->stage_bytes;
-  g->side_off = g->act_off + stages * g->act_bytes;
+  g->side_off = g->act_off + act_ring(stages);  // side boxes are TMA destinations: 128-aligned
   g->red_off = g->side_off + g->side_slots * g->side_bytes;
   g->bar_off = g->red_off + g->red_bytes;
+  // Alignment the kernel relies on (checked here, on the host, rather than found on the device):
+  // weight boxes 1024 (128-byte swizzle atoms), activation rows 16 (cp.async, 16-byte loads),
+  // side boxes 128 (TMA destinations), the reduction buffer 16 (v4 stores), mbarriers 8.
+  if (g->act_off % 1024 != 0 || g->act_bytes % 16 != 0 || g->side_off % 128 != 0 ||
+      g->side_bytes % 128 != 0 || g->red_off % 16 != 0 || g->bar_off % 8 != 0)
+    return BSGEMV_ERR_UNSUPPORTED;
 
   bsgemv_geometry& pub = g->pub;
   pub.variant = BSGEMV_VARIANT_MMA;

@@ -97,7 +97,6 @@ void fill_params(const Geometry& g, const OperandMaps& m, const void* A, const v
   k->stages = g.pub.stages;
   k->act_off = g.act_off;
   k->act_bytes = g.act_bytes;
-  k->act_box_bytes = g.act_box_bytes;
   k->side_tma = m.side_tma ? 1 : 0;
   k->side_off = g.side_off;
   k->side_bytes = g.side_bytes;

@@ -60,8 +60,7 @@ struct KParams {
   int zp_pitch;            // bytes per zero-point row (global)
   int stages;              // weight / activation ring depth
   int act_off;             // activation ring: stages x act_bytes
-  int act_bytes;           // activation bytes per stage (act_box_bytes per 64 k)
-  int act_box_bytes;       // max_M * 128
+  int act_bytes;           // activation bytes per stage (max_M padded rows)
   int side_tma;            // 1: scales / zero points staged by TMA into the side ring
   int side_off;            // side ring: side_slots x side_bytes
   int side_bytes;          // one side box: scales [64][kSideScaleBytes], zero points after
@@ -83,12 +82,11 @@ struct Geometry {
   int kpc;                 // k per 16-byte chunk
   int kc;                  // k per stage (kStageK)
   int stage_bytes;         // weight bytes per stage
-  int nbox;                // activation boxes (64 k) per stage
   int mt_max;              // 1 or 2 n8 mma tiles
   int scale_es;            // bytes per scale element
   int nb_s;
   int scale_pitch, zp_pitch;
-  int act_box_bytes, act_bytes, act_off;
+  int act_bytes, act_off;
   int rs_log2, side_slots, side_bytes, zbox_bytes, side_off;
   int bar_off;
   int slot_floats;

@@ -74,6 +74,15 @@ BSG_DEV void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Arrive on `bar` if `pred` (a predicated instruction: no branch around it).
+BSG_DEV void mbar_arrive_if(uint32_t bar, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar),
+      "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+
 BSG_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -200,6 +209,14 @@ BSG_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, ui
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+
+// ldmatrix at addr + OFF (a compile-time offset in the instruction's immediate field).
+template <int OFF>
+BSG_DEV void ldsm_x4_at(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4+%5];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr), "n"(OFF));
 }
 
 BSG_DEV uint4 lds128(uint32_t addr) {
@@ -541,11 +558,22 @@ struct Gemv {
   static constexpr int kBoxes = kSrb / kBoxRowBytes;        // weight TMA boxes per stage: 1 or 2
   static constexpr int kStageB = kRowsPerTile * kSrb;       // weight bytes per stage
   static constexpr int kBoxB = kRowsPerTile * kBoxRowBytes;  // bytes per weight box (8 KB)
-  static constexpr int kNbox = kKc / 64;        // activation boxes (64 k) per stage
   static constexpr bool kFold = (FMT == kNvfp4);
   static constexpr int kSub = (CPB == 0) ? 2 : 1;  // scale blocks per chunk (int4, 16-element blocks)
   static constexpr int kScaleEs = (FMT == kFp8) ? 4 : (FMT == kNvfp4 ? 1 : 2);
   static constexpr int kZpW = (FMT == kInt4) ? 4 : 8;  // zero-point bits per block
+  // Activation slot of a stage: max_M rows of the stage's k, each padded by one chunk's
+  // activation bytes, so that the 8 rows a B-fragment load touches start in different banks
+  // (conflict-free without a swizzle, and every chunk's offset is a compile-time constant).
+  static constexpr int kActChunkB = 2 * kKpc;               // activation bytes of one chunk
+  static constexpr int kActPitch = 2 * kKc + kActChunkB;    // bytes per activation row
+  // zero-point bytes per side-box row: the box's 64 bytes of f16 scales are 32 blocks
+  static constexpr int kZboxB = 32 * kZpW / 8;
+  // log2 of the block size where the kernel variant fixes it (CPB < 8), else -1 (read from
+  // the launch: int8 blocks of 128 or 256, one or half a block per weight box)
+  static constexpr int kBsLog2 = (kFold || CPB == 0) ? 4
+                                : CPB == 8 ? -1
+                                           : (CPB == 1 ? 0 : CPB == 2 ? 1 : 2) + (kFour ? 5 : 4);
 
   // Shared memory: [W ring: stages x 8 KB][activation ring][side ring][barriers].
   // The weight boxes are 1024-byte aligned (128-byte swizzle atoms).
@@ -554,9 +582,7 @@ struct Gemv {
     uint32_t base_u;  // the same address in the shared window
     int stages, act_off, act_bytes, side_off, side_bytes, side_slots, bar_off;
     BSG_DEV uint32_t w(int i) const { return base_u + i * kStageB; }
-    BSG_DEV const uint8_t* act(int i) const { return base + act_off + i * act_bytes; }
     BSG_DEV uint32_t act_u(int i) const { return base_u + act_off + i * act_bytes; }
-    BSG_DEV const uint8_t* side(int j) const { return base + side_off + j * side_bytes; }
     BSG_DEV uint32_t side_u(int j) const { return base_u + side_off + j * side_bytes; }
     BSG_DEV uint32_t full(int i) const { return base_u + bar_off + 8 * i; }
     BSG_DEV uint32_t empty(int i) const { return base_u + bar_off + 8 * (stages + i); }
@@ -610,8 +636,7 @@ struct Gemv {
     const int64_t k0 = static_cast<int64_t>(ks) * kKc, K = p.K;
     for (int u = lane; u < units; u += 32) {
       const int m = u / kUpr, qg = u % kUpr;
-      const int q = qg & 7;
-      const uint32_t d = dst + (qg >> 3) * p.act_box_bytes + m * 128 + ((q ^ (m & 7)) << 4);
+      const uint32_t d = dst + m * kActPitch + qg * 16;
       const int64_t k = k0 + qg * 8;
       const bool in = k < K;
       cp_async16(d, p.A + m * K + (in ? k : 0), in ? 16u : 0u);
@@ -717,18 +742,15 @@ struct Gemv {
   // ---- per-lane constants.  Consumer warp cw owns the tile's mma row group rg = cw (tile rows
   // 16 rg .. 16 rg + 15) over the whole stage (kCps chunks of 16 bytes per row, in boxes of 8);
   // lane (g, t) holds rows g and g + 8 of the group (rr = 0, 1).
-  static constexpr int kCpbox = kFour ? 2 : 4;  // chunks per 64-k activation box
-
   struct Lane {
     int rg, lane, g, t;
     uint32_t w[4];             // ldmatrix.x4 row address of chunk pair j (chunks 2j, 2j + 1) of a
                                // weight box; box b of the stage adds b * kBoxB
-    uint32_t act[kCpbox][MT];  // activation fragment offset of chunk c (c < kCpbox) in a stage's
-                               // activation slot; chunk c + kCpbox b adds b * act_box_bytes
-    uint32_t abox;             // act_box_bytes
+    uint32_t act[MT];          // activation fragment offset of chunk 0 (n8 tile mt) in a stage's
+                               // activation slot; chunk c adds c * kActChunkB
     uint32_t fsel[2];          // NVFP4: prmt selector of the lane's scale code, chunk parity 0/1
     uint32_t srow;             // side box: scale row 16 rg + g; row g + 8 adds 8 * kSideScaleBytes
-    uint32_t zrow;             // side box: zero-point row 16 rg + g; row g + 8 adds 8 * zbox_bytes
+    uint32_t zrow;             // side box: zero-point row 16 rg + g; row g + 8 adds 8 * kZboxB
   };
 
   static BSG_DEV Lane make_lane(const KParams& p, int cw, int lane) {
@@ -746,33 +768,25 @@ struct Gemv {
       L.w[j] = r * kBoxRowBytes + ((c ^ (r & 7)) << 4);
     }
 #pragma unroll
-    for (int c = 0; c < kCpbox; ++c)
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        // activation row of the B fragment column; columns past M read row 0 (their results
-        // are never stored), so the slot holds only the call's M rows
-        const int m0 = mt * 8 + L.g;
-        const int m = m0 < p.M ? m0 : 0;
-        if constexpr (kFour) {  // 16-byte unit (c & 1) * 4 + t of the row
-          const int q = (c << 2) + L.t;
-          L.act[c][mt] = m * 128 + ((q ^ (m & 7)) << 4);
-        } else {  // unit (c & 3) * 2 + t / 2, half t & 1
-          const int q = (c << 1) + (L.t >> 1);
-          L.act[c][mt] = m * 128 + ((q ^ (m & 7)) << 4) + ((L.t & 1) << 3);
-        }
-      }
-    L.abox = static_cast<uint32_t>(p.act_box_bytes);
+    for (int mt = 0; mt < MT; ++mt) {
+      // activation row of the B fragment column; columns past M read row 0 (their results are
+      // never stored), so the slot holds only the call's M rows.  Lane t reads k 8t .. 8t + 7
+      // (4-bit formats) or 4t .. 4t + 3 (8-bit) of the chunk.
+      const int m0 = mt * 8 + L.g;
+      const int m = m0 < p.M ? m0 : 0;
+      L.act[mt] = m * kActPitch + L.t * (kActChunkB / 4);
+    }
     // chunk c's codes lie in 16-block 2c + t/2 of the stage: byte 2 (c & 1) + t/2 of word c / 2
     L.fsel[0] = 0x11u * static_cast<uint32_t>(L.t >> 1);
     L.fsel[1] = 0x11u * static_cast<uint32_t>(2 + (L.t >> 1));
     L.srow = (16 * L.rg + L.g) * kSideScaleBytes;
-    L.zrow = kRowsPerTile * kSideScaleBytes + (16 * L.rg + L.g) * p.zbox_bytes;
+    L.zrow = kRowsPerTile * kSideScaleBytes + (16 * L.rg + L.g) * kZboxB;
     return L;
   }
 
   // Offset of chunk c's activation fragment (n8 tile mt) in a stage's activation slot.
   static BSG_DEV uint32_t act_off(const Lane& L, int c, int mt) {
-    return L.act[c % kCpbox][mt] + (c / kCpbox) * L.abox;
+    return L.act[mt] + c * kActChunkB;
   }
 
   // Launch parameters the stage loop reads, as registers.  SIDE (fixed per launch, taken out of
@@ -841,6 +855,14 @@ struct Gemv {
     }
   }
 
+  // A stage's shared-memory operands: the kernel's shared array (generic pointer, so that plain
+  // loads through it stay shared-memory loads) and 32-bit offsets into it of the stage's
+  // activation slot and side box.
+  struct Sh {
+    const uint8_t* base;
+    uint32_t a, s;
+  };
+
   // Scales and zero points of the lane's 2 rows for NB consecutive blocks of a side box, in one
   // shared load per row each (NB a power of two; the first block `rel` a multiple of NB, so the
   // loads are aligned): f16 scale pairs (or the fp32 scale of FP8, NB = 1) and zero points
@@ -851,12 +873,13 @@ struct Gemv {
     uint32_t z[2][(NB * kZpW + 31) / 32];
   };
 
-  template <int NB, class R>
-  static BSG_DEV void load_side(const R& p, const Lane& L, const uint8_t* sb, int rel,
-                                SideLoad<NB>& v) {
+  template <int NB>
+  static BSG_DEV void load_side(const Lane& L, const Sh& sh, int rel, SideLoad<NB>& v) {
+    const uint32_t sa = sh.s + L.srow + rel * kScaleEs;
+    const uint32_t za0 = sh.s + L.zrow + ((rel * kZpW) >> 3);
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const uint8_t* a = sb + L.srow + rr * 8 * kSideScaleBytes + rel * kScaleEs;
+      const uint8_t* a = sh.base + (sa + rr * 8 * kSideScaleBytes);
       if constexpr (FMT == kFp8) {
         static_assert(NB == 1, "one fp32 scale per weight box");
         v.s[rr][0] = lsh<uint32_t>(a);
@@ -877,7 +900,7 @@ struct Gemv {
         v.s[rr][3] = x.w;
       }
       if constexpr (ZP) {
-        const uint8_t* za = sb + L.zrow + rr * 8 * p.zbox_bytes + ((rel * kZpW) >> 3);
+        const uint8_t* za = sh.base + (za0 + rr * 8 * kZboxB);
         constexpr int kBits = NB * kZpW;
         if constexpr (kBits == 4) {
           v.z[rr][0] = static_cast<uint32_t>(lsh<uint8_t>(za)) >> ((rel & 1) * 4);
@@ -931,13 +954,13 @@ struct Gemv {
   // NVFP4: the replicated f16 E4M3 block scale of the lane's 2 rows for 16-block `blk` (side
   // box block `rel`).
   template <class R>
-  static BSG_DEV void load_fold(const R& p, const Lane& L, const uint8_t* sb, int64_t tile,
+  static BSG_DEV void load_fold(const R& p, const Lane& L, const Sh& sh, int64_t tile,
                                 int blk, int rel, uint32_t (&f)[2]) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       uint32_t code;
       if constexpr (R::side) {
-        code = lsh<uint8_t>(sb + L.srow + rr * 8 * kSideScaleBytes + rel);
+        code = lsh<uint8_t>(sh.base + (sh.s + L.srow + rr * 8 * kSideScaleBytes + rel));
       } else {
         code = (blk < p.k.nb_s) ? __ldg(p.k.scales + row_of(p, L, tile, rr) * p.k.scale_pitch + blk) : 0u;
       }
@@ -947,12 +970,12 @@ struct Gemv {
 
   // Activation B fragments of chunk c: b[mt][st][0] = (k 2t, 2t+1), b[mt][st][1] = (k 2t+8,
   // 2t+9) of activation row mt*8 + g, permuted like the weight (phys_k).
-  static BSG_DEV void act_fragment(const Lane& L, const uint8_t* ap, int c,
+  static BSG_DEV void act_fragment(const Lane& L, const Sh& sh, int c,
                                    uint32_t (&b)[MT][kSteps][2]) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       if constexpr (kFour) {
-        const uint4 v = lsh<uint4>(ap + act_off(L, c, mt));
+        const uint4 v = lsh<uint4>(sh.base + (sh.a + act_off(L, c, mt)));
         if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
           b[mt][0][0] = prmt(v.x, v.z, 0x5410u);
           b[mt][0][1] = prmt(v.x, v.z, 0x7632u);
@@ -965,7 +988,7 @@ struct Gemv {
           b[mt][1][1] = v.w;
         }
       } else {
-        const uint2 v = lsh<uint2>(ap + act_off(L, c, mt));
+        const uint2 v = lsh<uint2>(sh.base + (sh.a + act_off(L, c, mt)));
         b[mt][0][0] = v.x;
         b[mt][0][1] = v.y;
       }
@@ -977,7 +1000,7 @@ struct Gemv {
   // accumulating.  zl/zh: zero-point constants (int formats) or the fold scales (NVFP4) of rows
   // g, g + 8.
   template <bool ZC>
-  static BSG_DEV void chunk_mma(const Lane& L, const uint8_t* ap, int c, uint32_t lo, uint32_t hi,
+  static BSG_DEV void chunk_mma(const Lane& L, const Sh& ap, int c, uint32_t lo, uint32_t hi,
                                 const uint32_t (&zl)[2], const uint32_t (&zh)[2],
                                 float (&d)[kSub][MT][4]) {
     uint32_t b[MT][kSteps][2];
@@ -1043,19 +1066,23 @@ struct Gemv {
   static constexpr int kGB = (CPB == 0 || CPB == 1) ? 2 : 1;          // blocks per group
 
   template <class R>
-  static BSG_DEV void consume_stage(const R& p, const Lane& L, uint32_t wa, const uint8_t* ap,
-                                    const uint8_t* sb, int64_t tile, int ks,
-                                    float (&acc)[1][MT][4]) {
+  static BSG_DEV void consume_stage(const R& p, const Lane& L, uint32_t wa, const Sh& ap,
+                                    int64_t tile, int ks, float (&acc)[1][MT][4]) {
     const int k0 = ks * kKc;                                // first k of the stage in the row
     const int kb = (ks & ((1 << p.rs_log2) - 1)) * kKc;    // ... in the side box
+    uint32_t wl[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wl[j] = wa + L.w[j];
     // one weight box (8 chunks) at a time: 16 weight registers live
 #pragma unroll
     for (int bx = 0; bx < kBoxes; ++bx) {
       uint32_t wv[4][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        ldsm_x4(wa + bx * kBoxB + L.w[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
-      consume_box(p, L, wv, ap, sb, tile, k0, kb, bx * 8, acc);
+      for (int j = 0; j < 4; ++j) {
+        if (bx == 0) ldsm_x4_at<0>(wl[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
+        else ldsm_x4_at<kBoxB>(wl[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
+      }
+      consume_box(p, L, wv, ap, tile, k0, kb, bx * 8, acc);
     }
   }
 
@@ -1063,7 +1090,7 @@ struct Gemv {
   // chunk c0 + c has row g in wv[c >> 1][2 (c & 1)] and row g + 8 in the next word.
   template <class R>
   static BSG_DEV void consume_box(const R& p, const Lane& L, const uint32_t (&wv)[4][4],
-                                  const uint8_t* ap, const uint8_t* sb, int64_t tile, int k0,
+                                  const Sh& ap, int64_t tile, int k0,
                                   int kb, int c0, float (&acc)[1][MT][4]) {
 #define BSG_LO(c) wv[(c) >> 1][2 * ((c) & 1)]
 #define BSG_HI(c) wv[(c) >> 1][2 * ((c) & 1) + 1]
@@ -1075,7 +1102,7 @@ struct Gemv {
         uint4 cv[2];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr)
-          cv[rr] = lsh<uint4>(sb + L.srow + rr * 8 * kSideScaleBytes + (kb >> 4));
+          cv[rr] = lsh<uint4>(ap.base + (ap.s + L.srow + rr * 8 * kSideScaleBytes + (kb >> 4)));
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int cc = c0 + c;
@@ -1092,7 +1119,7 @@ struct Gemv {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int d = 2 * (c0 + c) + (L.t >> 1);
-          load_fold(p, L, sb, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
+          load_fold(p, L, ap, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
           chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, acc);
         }
       }
@@ -1109,7 +1136,12 @@ struct Gemv {
         uint32_t z[2];
         float s[kGB][2];
         if constexpr (R::side) {
-          if (grp % kGpl == 0) load_side<kSL>(p, L, sb, (kb + kg) >> p.bs_log2, sl);
+          if (grp % kGpl == 0) {
+            int rel;
+            if constexpr (kBsLog2 >= 0) rel = (kb + kg) >> kBsLog2;
+            else rel = (kb + kg) >> p.bs_log2;
+            load_side<kSL>(L, ap, rel, sl);
+          }
           side_group<kGB>(sl, (grp % kGpl) * kGB, z, s);
         } else {
           const int blk = (k0 + kg) >> p.bs_log2;
@@ -1347,12 +1379,14 @@ struct Gemv {
           if (ok) ok = mbar_wait(sm.sfull(sr.slot), sr.phase, p.err, kErrTimeoutFull);
         }
         if (ok) ok = mbar_wait(sm.full(r.slot), r.phase, p.err, kErrTimeoutFull);
-        if (ok) consume_stage(R, L, sm.w(r.slot), sm.act(r.slot), sm.side(sr.slot), tile, w.ks, acc);
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(sm.empty(r.slot));
-          if (SIDE && w.closes(q == seg - 1)) mbar_arrive(sm.sempty(sr.slot));
+        if (ok) {
+          const Sh sh{sm.base, sm.act_off + r.slot * sm.act_bytes,
+                      sm.side_off + sr.slot * sm.side_bytes};
+          consume_stage(R, L, sm.w(r.slot), sh, tile, w.ks, acc);
         }
+        __syncwarp();
+        mbar_arrive_if(sm.empty(r.slot), lane == 0);
+        if (SIDE && w.closes(q == seg - 1)) mbar_arrive_if(sm.sempty(sr.slot), lane == 0);
         r.next();
         w.next();
       }

@@ -192,3 +192,18 @@ def test_split_choice_on_the_configuration_shapes(L):
     assert split("fp8", 128, False, 512, 2048) == (8, 1)     # 8 tiles x 8 stages
     assert split("int4", 32, False, 151936, 4096)[0] == 0    # 2374 tiles: stream-K
     assert split("nvfp4", 16, False, 248320, 2048)[0] == 0   # 3880 tiles: stream-K
+
+
+def test_shared_memory_layout_is_aligned_for_every_problem(L):
+    """The plan's shared-memory layout keeps every region at the alignment the kernel relies on
+    (weight boxes 1024, side boxes 128 as TMA destinations, activation rows and the reduction
+    buffer 16, barriers 8); the host rejects a layout that does not instead of launching it.
+    Every format, block size and max_M on a spread of shapes must therefore yield a geometry."""
+    import itertools
+    fmts = ([("int4", bs, zp) for bs in (16, 32, 64, 128, 256) for zp in (False, True)] +
+            [("int8", bs, zp) for bs in (16, 32, 64, 128, 256) for zp in (False, True)] +
+            [("fp8", 128, False), ("nvfp4", 16, False)])
+    for (fmt, bs, zp), N, K, max_M in itertools.product(
+            fmts, (1, 333, 5120, 151936), (256, 2048, 12288), (1, 2, 3, 5, 8, 9, 13, 16)):
+        g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, 152)
+        assert g["smem_bytes"] % 8 == 0
