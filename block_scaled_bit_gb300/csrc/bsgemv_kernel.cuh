@@ -41,9 +41,9 @@
 
 namespace bsg {
 
-// Bounded waits: a waiting thread sleeps in mbarrier.try_wait (suspend-time hint, woken when the
-// phase completes) and gives up after kWaitLimitNs of wall time, far above any legitimate stall.
-constexpr uint32_t kSuspendHintNs = 1000000;
+// Bounded waits: a waiting thread blocks in mbarrier.try_wait (the hardware's own time window,
+// no suspend-time hint: measured faster to wake than a hinted wait) and gives up after
+// kWaitLimitNs of wall time, far above any legitimate stall.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // ------------------------------------------------------------------------------ PTX wrappers
@@ -87,10 +87,10 @@ BSG_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -271,9 +271,11 @@ BSG_DEV uint32_t select_bits(uint32_t a, uint32_t c) {
   return d;
 }
 
-BSG_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+// prmt with a compile-time selector (the instruction's immediate field).
+template <uint32_t SEL>
+BSG_DEV uint32_t prmt(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
   return d;
 }
 
@@ -461,23 +463,25 @@ template <bool BF16>
 BSG_DEV void decode_int8(uint32_t lo, uint32_t hi, uint32_t z_lo, uint32_t z_hi,
                          uint32_t (&a)[1][4]) {
   if constexpr (!BF16) {
-    a[0][0] = h2_sub(prmt(lo, z_lo, 0x5150u), z_lo);
-    a[0][1] = h2_sub(prmt(hi, z_hi, 0x5150u), z_hi);
-    a[0][2] = h2_sub(prmt(lo, z_lo, 0x5352u), z_lo);
-    a[0][3] = h2_sub(prmt(hi, z_hi, 0x5352u), z_hi);
+    a[0][0] = h2_sub(prmt<0x5150u>(lo, z_lo), z_lo);
+    a[0][1] = h2_sub(prmt<0x5150u>(hi, z_hi), z_hi);
+    a[0][2] = h2_sub(prmt<0x5352u>(lo, z_lo), z_lo);
+    a[0][3] = h2_sub(prmt<0x5352u>(hi, z_hi), z_hi);
   } else {
-    auto pair = [](uint32_t w, uint32_t sel0, uint32_t sel1, uint32_t z) -> uint32_t {
-      const float zf = __uint_as_float(z);  // 2^23 + zp
-      const float x0 = __uint_as_float(prmt(w, z, sel0)) - zf;
-      const float x1 = __uint_as_float(prmt(w, z, sel1)) - zf;
+    auto pack = [](float x0, float x1) -> uint32_t {
       uint32_t d;
       asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(x1), "f"(x0));
       return d;
     };
-    a[0][0] = pair(lo, 0x7550u, 0x7551u, z_lo);
-    a[0][1] = pair(hi, 0x7550u, 0x7551u, z_hi);
-    a[0][2] = pair(lo, 0x7552u, 0x7553u, z_lo);
-    a[0][3] = pair(hi, 0x7552u, 0x7553u, z_hi);
+    const float zl = __uint_as_float(z_lo), zh = __uint_as_float(z_hi);  // 2^23 + zp
+    a[0][0] = pack(__uint_as_float(prmt<0x7550u>(lo, z_lo)) - zl,
+                   __uint_as_float(prmt<0x7551u>(lo, z_lo)) - zl);
+    a[0][1] = pack(__uint_as_float(prmt<0x7550u>(hi, z_hi)) - zh,
+                   __uint_as_float(prmt<0x7551u>(hi, z_hi)) - zh);
+    a[0][2] = pack(__uint_as_float(prmt<0x7552u>(lo, z_lo)) - zl,
+                   __uint_as_float(prmt<0x7553u>(lo, z_lo)) - zl);
+    a[0][3] = pack(__uint_as_float(prmt<0x7552u>(hi, z_hi)) - zh,
+                   __uint_as_float(prmt<0x7553u>(hi, z_hi)) - zh);
   }
 }
 
@@ -977,10 +981,10 @@ struct Gemv {
       if constexpr (kFour) {
         const uint4 v = lsh<uint4>(sh.base + (sh.a + act_off(L, c, mt)));
         if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
-          b[mt][0][0] = prmt(v.x, v.z, 0x5410u);
-          b[mt][0][1] = prmt(v.x, v.z, 0x7632u);
-          b[mt][1][0] = prmt(v.y, v.w, 0x5410u);
-          b[mt][1][1] = prmt(v.y, v.w, 0x7632u);
+          b[mt][0][0] = prmt<0x5410u>(v.x, v.z);
+          b[mt][0][1] = prmt<0x7632u>(v.x, v.z);
+          b[mt][1][0] = prmt<0x5410u>(v.y, v.w);
+          b[mt][1][1] = prmt<0x7632u>(v.y, v.w);
         } else {  // nvfp4: natural pairs
           b[mt][0][0] = v.x;
           b[mt][0][1] = v.y;
