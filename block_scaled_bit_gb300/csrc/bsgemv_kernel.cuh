@@ -1231,19 +1231,19 @@ struct Gemv {
     return i;
   }
 
-  // End of a tile segment, per consumer warp (row group rg): store y when this CTA covered the
-  // whole tile; otherwise publish the partial sums and let the last CTA to arrive at (tile, rg)
-  // add every contributor's partial in CTA order (a fixed order: deterministic results).
+  // ---- stream-K epilogue.  A tile the CTA consumed whole is rounded and stored at once.  For
+  // a tile shared with other CTAs the warp writes its fp32 fragments to its partial slot
+  // (st.cg) and goes on with its range; the arrivals on the tiles' (tile, row group) counters
+  // are deferred to the end of the range and made together (one lane per pending tile, one
+  // acquire-release atomic each: the release publishes all of the warp's partial stores,
+  // which __syncwarp ordered before it).  The last arriver of a tile adds the contributors'
+  // partials in CTA order and stores y -- P4's visibility protocol, without its per-call memset.
+  // Deferring keeps the mid-range tile boundary off the consumer's critical path.
   // Partial slots [cta][seg][rg]: a CTA writes seg 0 for the first tile of its range and seg 1
   // for its last tile, so among a tile's contributors only the first can hold it in seg 1 (when
   // its range began in an earlier tile).
-  static BSG_DEV void epilogue(const KParams& p, int64_t tile, bool whole, int64_t my_first_tile,
-                               int rg, int lane, float (&acc)[1][MT][4], float gs) {
-    if (whole) {
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) store_y(p, tile, rg, mt, lane, acc[0][mt], gs);
-      return;
-    }
+  static BSG_DEV void store_partial(const KParams& p, int64_t tile, int64_t my_first_tile, int rg,
+                                    int lane, const float (&acc)[1][MT][4]) {
     const int slot4 = p.slot_floats / 4;  // float4 per (cta, seg, rg) slot
     const int seg = (tile == my_first_tile) ? 0 : 1;
     float4* mine = reinterpret_cast<float4*>(p.partials) +
@@ -1252,22 +1252,43 @@ struct Gemv {
     for (int mt = 0; mt < MT; ++mt)
       __stcg(mine + mt * 32 + lane,
              make_float4(acc[0][mt][0], acc[0][mt][1], acc[0][mt][2], acc[0][mt][3]));
-    __syncwarp();
+  }
+
+  // First and last CTA holding stages of `tile`.
+  static BSG_DEV void tile_owners(const KParams& p, int64_t tile, int& first, int& last) {
     const int G = gridDim.x;
-    const int64_t T = p.total_stages;
-    const int64_t x0 = tile * p.spt;
-    const int first = cta_of_stage(x0, T, G);
-    const int last = cta_of_stage(x0 + p.spt - 1, T, G);
-    unsigned is_last = 0;
-    if (lane == 0) {
-      // __syncwarp ordered the warp's partial stores before this arrival, whose release
-      // publishes them at GPU scope; its acquire makes a last arriver see every contributor's
+    const int64_t T = p.total_stages, x0 = tile * p.spt;
+    first = cta_of_stage(x0, T, G);
+    last = cta_of_stage(x0 + p.spt - 1, T, G);
+  }
+
+  // Arrive on the np (1 or 2) pending shared tiles; reduce and store each one this warp was the
+  // last to arrive on.
+  static BSG_DEV void arrive_and_reduce(const KParams& p, const int64_t (&pend)[2], int np,
+                                        int rg, int lane, float gs) {
+    __syncwarp();  // the warp's partial stores before the arrivals' release
+    unsigned mine_last = 0;
+    if (lane < np) {
+      const int64_t tile = lane == 0 ? pend[0] : pend[1];
+      int first, last;
+      tile_owners(p, tile, first, last);
       const unsigned old = atom_add_acq_rel_gpu(p.counters + tile * kConsumerWarps + rg, 1u);
-      is_last = (old == static_cast<unsigned>(last - first)) ? 1u : 0u;
+      mine_last = (old == static_cast<unsigned>(last - first)) ? 1u : 0u;
     }
-    is_last = __shfl_sync(0xFFFFFFFFu, is_last, 0);
-    if (!is_last) return;
-    __syncwarp();  // order the warp's partial loads after lane 0's acquire
+    const unsigned last_mask = __ballot_sync(0xFFFFFFFFu, mine_last != 0);
+    if (last_mask == 0) return;
+    __syncwarp();  // order the warp's partial loads after the arriving lanes' acquire
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (j < np && ((last_mask >> j) & 1u)) reduce_tile(p, pend[j], rg, lane, gs);
+  }
+
+  static BSG_DEV void reduce_tile(const KParams& p, int64_t tile, int rg, int lane, float gs) {
+    const int slot4 = p.slot_floats / 4;
+    const int G = gridDim.x;
+    const int64_t T = p.total_stages, x0 = tile * p.spt;
+    int first, last;
+    tile_owners(p, tile, first, last);
     const int fseg = (static_cast<int64_t>(first) * T < x0 * G) ? 1 : 0;  // first began earlier
     const float4* part = reinterpret_cast<const float4*>(p.partials);
     // contributors' partials in batches of kBatch independent loads, added in CTA order
@@ -1374,6 +1395,8 @@ struct Gemv {
     Ring r{0, 0u, sm.stages};
     Ring sr{sm.side_slots - 1, 1u, sm.side_slots};
     bool ok = true;
+    int64_t pend[2] = {0, 0};  // shared tiles whose arrival is deferred to the end of the range
+    int np = 0;
     for (int i = 0; i < n;) {
       const int seg = (spt - w.ks) < (n - i) ? (spt - w.ks) : (n - i);  // stages of this segment
       const int64_t tile = w.tile;
@@ -1397,12 +1420,16 @@ struct Gemv {
       i += seg;
       if (p.cluster >= 2) {
         cluster_publish(p, sm, cw, L, acc);  // the cluster's leader adds and stores
-      } else {
-        // whole: this CTA consumed every stage of the tile
-        epilogue(p, tile, seg == spt, first_tile, cw, lane, acc, gs);
+      } else if (seg == spt) {  // whole: this CTA consumed every stage of the tile
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) store_y(p, tile, cw, mt, lane, acc[0][mt], gs);
+      } else {  // shared with other CTAs (at most the first and the last segment of the range)
+        store_partial(p, tile, first_tile, cw, lane, acc);
+        pend[np++ & 1] = tile;
       }
       zero(acc[0]);
     }
+    if (np > 0) arrive_and_reduce(p, pend, np, cw, lane, gs);
   }
 };
 
