@@ -103,8 +103,10 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
     assert 1 <= g["ctas"] <= min(g["total_stages"], slots)
     C, spt = g["cluster"], g["stages_per_tile"]
     stream_k_stages = -(-g["total_stages"] // min(g["total_stages"], slots))
-    if C == 0:  # stream-K: one full wave
-        if g["total_stages"] >= slots:
+    if C == 0:  # stream-K: one wave; a whole number of CTAs per tile when tiles are few
+        if g["total_stages"] > slots and slots // g["tiles"] >= 2:
+            assert g["ctas"] == g["tiles"] * (slots // g["tiles"])
+        elif g["total_stages"] >= slots:
             assert g["ctas"] == slots
     else:  # cluster split: C CTAs per tile, within one stage of stream-K's work per CTA
         assert 1 <= C <= 8 and C <= spt and spt % C == 0
