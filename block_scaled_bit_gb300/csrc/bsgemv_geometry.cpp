@@ -181,7 +181,9 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
         C = c;
       }
     }
-    if (split == BSGEMV_SPLIT_AUTO && (C == 0 || best > sk + 1)) C = 0;
+    // taken when a CTA's share is within one stage of stream-K's, or at most 4 stages (stream-K
+    // with a share of one or two stages has many partial sums per tile to add: measured slower)
+    if (split == BSGEMV_SPLIT_AUTO && (C == 0 || best > std::max<int64_t>(sk + 1, 4))) C = 0;
     if (split == BSGEMV_SPLIT_CLUSTER && C == 0) return BSGEMV_ERR_UNSUPPORTED;
   }
   g->red_bytes = red_for(C);

@@ -111,7 +111,7 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
     else:  # cluster split: C CTAs per tile, within one stage of stream-K's work per CTA
         assert 1 <= C <= 8 and C <= spt and spt % C == 0
         assert g["ctas"] == g["tiles"] * C
-        assert -(-spt // C) <= stream_k_stages + 1
+        assert -(-spt // C) <= max(stream_k_stages + 1, 4)
     # shared memory fits the residency it was sized for
     assert g["smem_bytes"] <= 232448
     assert g["ctas_per_sm"] * (g["smem_bytes"] + 1024) <= 233472
@@ -180,7 +180,8 @@ def test_owner_lookup_without_division():
 
 def test_split_choice_on_the_configuration_shapes(L):
     """Automatic K split at 152 SMs (4 CTAs per SM): shapes with few tiles take a cluster of CTAs
-    per tile (reduced in shared memory), shapes with more tiles than resident CTAs stream-K."""
+    per tile (reduced in shared memory), shapes with more tiles than resident CTAs stream-K, with
+    a whole number of CTAs per tile when the tiles are fewer than the resident CTAs."""
     def split(fmt, bs, zp, N, K, max_M=1):
         g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, 152)
         return g["cluster"], -(-g["stages_per_tile"] // max(1, g["cluster"])) if g["cluster"] else None
@@ -193,6 +194,10 @@ def test_split_choice_on_the_configuration_shapes(L):
     assert split("int8", 128, True, 5120, 2048) == (4, 2)    # 80 tiles x 8 stages
     assert split("fp8", 128, False, 512, 2048) == (8, 1)     # 8 tiles x 8 stages
     assert split("int4", 32, False, 151936, 4096)[0] == 0    # 2374 tiles: stream-K
+    # plans for max_M = 8: 8-CTA clusters no longer fit next to the activation ring, 4 do
+    assert split("fp8", 128, False, 2048, 4096, 8) == (4, 4)  # 32 tiles x 16 stages
+    g = bsgemv.geometry_for("int8", "f16", 128, True, 12288, 4096, 1, 152)
+    assert g["ctas"] == 576                                  # 192 tiles x 3 CTAs
     assert split("nvfp4", 16, False, 248320, 2048)[0] == 0   # 3880 tiles: stream-K
 
 
