@@ -112,7 +112,12 @@ void fill_params(const Geometry& g, const OperandMaps& m, const void* A, const v
 }
 
 int launch_gemv(const Geometry& g, const KParams& k, cudaStream_t s) {
-  const int mt = k.M > 8 ? 2 : 1;
+  // n8 activation tiles per call; 0: int4 with at most 2 rows and at least 5 stages per CTA,
+  // one tile and the activations permuted by the producer (same arithmetic; measured faster
+  // there, slower for short CTA ranges, where the producer's extra wait is on the critical path)
+  const int64_t per_cta = (g.pub.total_stages + g.pub.ctas - 1) / g.pub.ctas;
+  const bool pa = g.fmt == kInt4 && k.M <= 2 && per_cta >= 5;
+  const int mt = k.M > 8 ? 2 : pa ? 0 : 1;
   const int ctas = g.pub.ctas, smem = g.pub.smem_bytes;
   const int bm = block_mode(g.fmt, g.block_size);
   switch (g.fmt) {

@@ -227,6 +227,14 @@ BSG_DEV uint4 lds128(uint32_t addr) {
   return v;
 }
 
+BSG_DEV void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+BSG_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 BSG_DEV uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -551,7 +559,7 @@ BSG_DEV void zp_consts(uint32_t zp, uint32_t& zl, uint32_t& zh) {
 // 4, or 8 for a block of a whole stage or more (larger blocks, fp8).  NVFP4 folds its scales
 // into the decoded values and uses 1.
 
-template <int FMT, bool BF16, int MT, bool ZP, int CPB>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA>
 struct Gemv {
   static constexpr bool kFour = (FMT == kInt4 || FMT == kNvfp4);
   static constexpr int kKpc = kFour ? 32 : 16;  // k per 16-byte chunk
@@ -647,6 +655,29 @@ struct Gemv {
     }
   }
 
+  // int4: the decoder pairs k with k + 4 (the two nibbles a LOP3 select takes from one word), so
+  // the activation fragments must pair them too.  The PA kernels (int4, calls with M <= 2) store
+  // the stage's activations in that order: each 16-byte unit (k0 .. k7 of a lane's chunk
+  // segment) becomes (k0, k4), (k1, k5), (k2, k6), (k3, k7), permuted in place by the producer,
+  // once per stage, after its copies have landed -- instead of every consumer warp permuting its
+  // fragments.  Measured on GB300: int4 lm_head 0.68 -> 0.74 of the copy bandwidth at M = 1;
+  // from 4 rows on, the producer's share (it grows with M) costs more than it saves, and the
+  // other kernels let the consumers permute.  The arithmetic is the same either way.
+  static constexpr bool kPermuteAct = PA;
+  static_assert(!PA || (FMT == kInt4 && MT == 1), "permuted activations: int4, one n8 tile");
+
+  static BSG_DEV void act_permute(const KParams& p, uint32_t dst, int lane) {
+    constexpr int kUpr = kKc / 8;
+    const int units = p.M * kUpr;
+    for (int u = lane; u < units; u += 32) {
+      const int m = u / kUpr, qg = u % kUpr;
+      const uint32_t d = dst + m * kActPitch + qg * 16;
+      const uint4 v = lds128(d);
+      sts128(d, make_uint4(prmt<0x5410u>(v.x, v.z), prmt<0x7632u>(v.x, v.z), prmt<0x5410u>(v.y, v.w),
+                           prmt<0x7632u>(v.y, v.w)));
+    }
+  }
+
   // The weight boxes of stage (tile, ks) into ring slot i (lane 0).
   static BSG_DEV void weight_copy(const KParams& p, const Smem& sm, int i, const Walk& w,
                                   uint64_t pol) {
@@ -710,12 +741,24 @@ struct Gemv {
     pdl_wait();
     // phase 2: activations of those stages; lane 0's arrival then releases each slot
     Walk w = start;
-    for (int i = 0; i < pre; ++i) {
-      act_copy(p, sm.act_u(i), w.ks, lane);
-      cp_async_mbar_arrive(sm.full(i));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.full(i));
-      w.next();
+    if constexpr (kPermuteAct) {  // all copies in flight together, one wait, then permute
+      for (int i = 0; i < pre; ++i) {
+        act_copy(p, sm.act_u(i), w.ks, lane);
+        w.next();
+      }
+      cp_async_wait_all();
+      for (int i = 0; i < pre; ++i) act_permute(p, sm.act_u(i), lane);
+      __syncwarp();  // every lane's permuted units before lane 0's (release) arrivals
+      if (lane == 0)
+        for (int i = 0; i < pre; ++i) mbar_arrive(sm.full(i));
+    } else {
+      for (int i = 0; i < pre; ++i) {
+        act_copy(p, sm.act_u(i), w.ks, lane);
+        cp_async_mbar_arrive(sm.full(i));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.full(i));
+        w.next();
+      }
     }
     // phase 3: steady state
     Ring r{pre % sm.stages, pre == sm.stages ? 1u : 0u, sm.stages};
@@ -730,12 +773,24 @@ struct Gemv {
       if (ok) ok = mbar_wait(sm.empty(r.slot), r.phase ^ 1u, p.err, kErrTimeoutEmpty);
       if (!ok) break;
       const uint32_t full = sm.full(r.slot);
-      act_copy(p, sm.act_u(r.slot), w.ks, lane);
-      cp_async_mbar_arrive(full);
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, kStageB);
-        weight_copy(p, sm, r.slot, w, pol);
+      if constexpr (kPermuteAct) {  // weights first, then the activations' round trip
+        if (lane == 0) {
+          mbar_expect_tx(full, kStageB);
+          weight_copy(p, sm, r.slot, w, pol);
+        }
+        act_copy(p, sm.act_u(r.slot), w.ks, lane);
+        cp_async_wait_all();
+        act_permute(p, sm.act_u(r.slot), lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full);
+      } else {
+        act_copy(p, sm.act_u(r.slot), w.ks, lane);
+        cp_async_mbar_arrive(full);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, kStageB);
+          weight_copy(p, sm, r.slot, w, pol);
+        }
       }
       r.next();
       w.next();
@@ -980,7 +1035,12 @@ struct Gemv {
     for (int mt = 0; mt < MT; ++mt) {
       if constexpr (kFour) {
         const uint4 v = lsh<uint4>(sh.base + (sh.a + act_off(L, c, mt)));
-        if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
+        if constexpr (kPermuteAct) {  // pairs (8t+j, 8t+j+4), stored so by the producer
+          b[mt][0][0] = v.x;
+          b[mt][0][1] = v.y;
+          b[mt][1][0] = v.z;
+          b[mt][1][1] = v.w;
+        } else if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
           b[mt][0][0] = prmt<0x5410u>(v.x, v.z);
           b[mt][0][1] = prmt<0x7632u>(v.x, v.z);
           b[mt][1][0] = prmt<0x5410u>(v.y, v.w);
@@ -1433,9 +1493,9 @@ struct Gemv {
   }
 };
 
-template <int FMT, bool BF16, int MT, bool ZP, int CPB>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT)) bsgemv_mma_kernel(const __grid_constant__ KParams p) {
-  using K = Gemv<FMT, BF16, MT, ZP, CPB>;
+  using K = Gemv<FMT, BF16, MT, ZP, CPB, PA>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned (128-byte swizzle atoms), derived from the shared array so that plain
   // loads through it stay shared-memory loads

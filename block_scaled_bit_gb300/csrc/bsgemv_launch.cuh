@@ -7,9 +7,9 @@
 
 namespace bsg {
 
-template <int FMT, bool BF16, int MT, bool ZP, int CPB>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA = false>
 int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
-  auto k = bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB>;
+  auto k = bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, PA>;
   static std::atomic<int> attr_smem{0};  // largest dynamic smem already granted to `k`
   static std::atomic<int> attr_cluster{0};  // non-portable cluster sizes allowed for `k`
   if (smem > attr_smem.load()) {
@@ -69,6 +69,21 @@ int launch_fmt(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem, c
     default: BSG_ZP(MTV, 8);           \
   }
   if constexpr (FMT == kInt4) {
+    if (mt == 0) {  // one n8 tile, activations permuted by the producer (calls with M <= 2)
+#define BSG_LPA(ZPV, C) return launch_one<FMT, BF16, 1, ZPV, C, true>(p, ctas, smem, s)
+#define BSG_ZPA(C) \
+  if (zp) BSG_LPA(true, C); \
+  BSG_LPA(false, C)
+      switch (cpb) {
+        case 0: BSG_ZPA(0);
+        case 1: BSG_ZPA(1);
+        case 2: BSG_ZPA(2);
+        case 4: BSG_ZPA(4);
+        default: BSG_ZPA(8);
+      }
+#undef BSG_ZPA
+#undef BSG_LPA
+    }
     if (mt == 1) { BSG_CPB(1); }
     BSG_CPB(2);
   } else if constexpr (FMT == kInt8) {  // 8-bit chunks hold 16 k: no block is smaller
