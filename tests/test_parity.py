@@ -244,3 +244,22 @@ def test_plan_records_device_and_geometry(torch_cuda):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert g["sm_count"] == sms
     assert g == bsgemv.geometry_for("int4", "bf16", 32, False, 151936, 4096, 16, sms)
+
+
+# ---------------------------------------------------------------------------- int4 kernels
+@pytest.mark.parametrize("act,bs,zp", [("f16", 32, False), ("f16", 16, True), ("f16", 128, True),
+                                       ("bf16", 32, False), ("bf16", 64, True)])
+def test_int4_activation_permutation_paths_agree(torch_cuda, act, bs, zp):
+    """int4 calls with M <= 2 and long CTA ranges run the kernel whose producer stores the
+    activations permuted; M = 3 runs the one whose consumers permute them.  Both are checked
+    against the oracle, and their rows must be bit-identical (same arithmetic)."""
+    N, K = 40000, 2048  # 625 tiles x 8 stages over one wave of CTAs: about 8 stages per CTA
+    case = synth.make_case("int4", act, bs, zp, N, K, 3, 4242 + bs)
+    rows = np.arange(0, N, 37)
+    with bsgemv.Plan("int4", act, bs, zp, N, K, 3) as plan:
+        g = plan.describe()
+        assert -(-g["total_stages"] // g["ctas"]) >= 5
+        outs = {M: run(case, plan=plan, M=M) for M in (1, 2, 3)}
+    assert_parity(case.with_M(3), outs[3], rows=rows)
+    assert np.array_equal(outs[1], outs[3][:1])
+    assert np.array_equal(outs[2], outs[3][:2])
