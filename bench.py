@@ -56,6 +56,13 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     ap.add_argument("--skip-cpu", action="store_true", help=argparse.SUPPRESS)
+    # --sweep and --one: run the plans as this variant (cuda_core: calls with M <= 8)
+    ap.add_argument("--variant", choices=["auto", "mma", "cuda_core"], default="auto",
+                    help=argparse.SUPPRESS)
+    # one configuration shape by name (see synth.config_shapes), isolated cold calls: for
+    # capturing one launch of one kernel under a profiler
+    ap.add_argument("--one", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--calls", type=int, default=5, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -452,10 +459,14 @@ def run_sweep(args):
                 if pm not in plans:
                     plans[pm] = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp,
                                             case.N, case.K, pm)
+                    if args.variant != "auto":
+                        assert plans[pm].set_override(variant=bsgemv.VARIANTS[args.variant]) == bsgemv.OK
                 return plans[pm]
 
             try:
                 for M in shape.Ms:
+                    if args.variant == "cuda_core" and M > 8:
+                        continue
                     plan = plan_for(M)
                     # isolated cold
                     t = []
@@ -498,13 +509,52 @@ def run_sweep(args):
                         "GBps_streamed": round(nbytes / streamed / 1e3, 1),
                         "frac_streamed": round(nbytes / streamed / 1e3 / peak, 4),
                         "frac_isolated": round(nbytes / iso / 1e3 / peak, 4),
-                        "weight_copies": copies, "plan_max_M": plan.max_M}), flush=True)
+                        "weight_copies": copies, "plan_max_M": plan.max_M,
+                        "variant": "cuda_core" if plan.describe()["variant"] == 2 else "mma"}),
+                          flush=True)
                     del g
             finally:
                 for pl in plans.values():
                     pl.close()
             del bufs
             torch.cuda.empty_cache()
+
+
+def run_one(args):
+    """`--calls` isolated cold calls (L2 flushed before each) of one configuration shape."""
+    import torch
+    from block_scaled_bit_gb300 import bsgemv, synth
+    shapes = {s.name: s for s in synth.all_shapes()}
+    if args.one not in shapes:
+        raise SystemExit(f"unknown shape {args.one!r}; one of: {', '.join(sorted(shapes))}")
+    shape = shapes[args.one]
+    torch.cuda.set_device(0)
+    M = args.M or shape.Ms[0]
+    case = shape.case(M)
+    max_M = min(max(shape.Ms), 8) if M <= 8 else max(shape.Ms)   # as the sweep's plans
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(4 * l2 // 4, dtype=torch.int32, device="cuda")
+    b = bsgemv.upload(case, "cuda")
+    t = []
+    with bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K,
+                     max(max_M, M)) as plan:
+        if args.variant != "auto":
+            assert plan.set_override(variant=bsgemv.VARIANTS[args.variant]) == bsgemv.OK
+        with torch.cuda.stream(stream):
+            for _ in range(args.calls):
+                flush.add_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                plan.run(b.A, b.W, b.scales, b.zp, b.y, M=M, stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                t.append(e0.elapsed_time(e1) * 1e3)
+        variant = "cuda_core" if plan.describe()["variant"] == 2 else "mma"
+        assert plan.device_status() == bsgemv.OK
+    print(json.dumps({"shape": shape.name, "M": M, "variant": variant, "calls": args.calls,
+                      "us_isolated_cold_median": round(statistics.median(t), 3),
+                      "bytes": case.algorithmic_bytes(M)}), flush=True)
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -558,6 +608,8 @@ def main():
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.one:
+        run_one(args)
     else:
         run_ours(args)
 

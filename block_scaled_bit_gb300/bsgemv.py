@@ -28,7 +28,7 @@ ERR_DEVICE_TIMEOUT = -7
 ERR_SCRATCH_LIMIT = -8
 
 # Every extern "C" entry point of include/bsgemv.h.
-EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_host", "bsgemv_destroy",
+EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_bias", "bsgemv_run_host", "bsgemv_destroy",
            "bsgemv_status_string", "bsgemv_debug_dequant", "bsgemv_plan_set_override",
            "bsgemv_plan_describe", "bsgemv_geometry_for", "bsgemv_device_status",
            "bsgemv_run_noalloc", "bsgemv_plan_set_split", "bsgemv_version")
@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
         vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.bsgemv_plan.argtypes = [ctypes.POINTER(vp), ci, ci, ci, i64, i64, ci]
         L.bsgemv_run.argtypes = [vp, vp, vp, vp, vp, vp, ci, vp]
+        L.bsgemv_run_bias.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, vp]
         L.bsgemv_run_host.argtypes = [vp, vp, vp, vp, vp, vp, ci, vp]
         L.bsgemv_destroy.argtypes = [vp]
         L.bsgemv_status_string.argtypes = [ci]
@@ -168,14 +169,20 @@ class Plan:
     def handle(self) -> int:
         return self._h.value
 
-    def run_status(self, A, W, scales, zp, y, M: int | None = None, stream=None) -> int:
-        """Enqueue the GEMV; returns the library status instead of raising."""
+    def run_status(self, A, W, scales, zp, y, M: int | None = None, stream=None,
+                   bias=None) -> int:
+        """Enqueue the GEMV (plus `bias` [N] if given); returns the library status instead of
+        raising."""
         M = A.shape[0] if M is None and hasattr(A, "shape") else M
+        if bias is not None:
+            return lib().bsgemv_run_bias(self._h, _ptr(A), _ptr(W), _ptr(scales), _ptr(zp),
+                                         _ptr(bias), _ptr(y), int(M), _stream(stream))
         return lib().bsgemv_run(self._h, _ptr(A), _ptr(W), _ptr(scales), _ptr(zp), _ptr(y),
                                 int(M), _stream(stream))
 
-    def run(self, A, W, scales, zp, y, M: int | None = None, stream=None) -> None:
-        _check(self.run_status(A, W, scales, zp, y, M, stream), "bsgemv_run")
+    def run(self, A, W, scales, zp, y, M: int | None = None, stream=None, bias=None) -> None:
+        _check(self.run_status(A, W, scales, zp, y, M, stream, bias),
+               "bsgemv_run" if bias is None else "bsgemv_run_bias")
 
     def run_host(self, A_host, W, scales, zp, y_host, M: int | None = None, stream=None) -> None:
         """A and y in host memory (pinned for asynchronous copies); returns when y is ready."""
@@ -205,7 +212,8 @@ class Plan:
 
 def upload(case, device="cuda"):
     """Copy a host case (numpy arrays in the storage layouts) to device tensors and allocate y.
-    Returns an object with A, W, scales, zp (the NVFP4 global scale for nvfp4) and y."""
+    Returns an object with A, W, scales, zp (the NVFP4 global scale for nvfp4), bias (None
+    without one) and y."""
     import types
 
     import numpy as np
@@ -221,7 +229,8 @@ def upload(case, device="cuda"):
 
     zp = t(case.gscale) if case.fmt == "nvfp4" else t(case.zp)
     y = torch.empty((case.M, case.N), dtype=torch.int16, device=device)
-    return types.SimpleNamespace(A=t(case.A), W=t(case.W), scales=t(case.scales), zp=zp, y=y)
+    return types.SimpleNamespace(A=t(case.A), W=t(case.W), scales=t(case.scales), zp=zp,
+                                 bias=t(getattr(case, "bias", None)), y=y)
 
 
 def y_bits(y) -> "np.ndarray":

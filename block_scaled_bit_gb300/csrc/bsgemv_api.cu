@@ -98,6 +98,7 @@ int rebuild_geometry(bsgemv_plan_s* p) {
                                        p->geo.K, p->geo.max_M, p->sm_count, p->ctas_override,
                                        p->stages_override, p->split, p->cluster, &geo);
   if (rc != BSGEMV_OK) return rc;
+  if (p->variant_override == BSGEMV_VARIANT_CUDA_CORE) geo.pub.variant = BSGEMV_VARIANT_CUDA_CORE;
   p->geo = geo;
   return alloc_workspace(p);
 }
@@ -220,6 +221,20 @@ int bsgemv_run(bsgemv_plan_t plan, const void* A, const void* W, const void* sca
   return launch(plan, static_cast<cudaStream_t>(stream));
 }
 
+int bsgemv_run_bias(bsgemv_plan_t plan, const void* A, const void* W, const void* scales,
+                    const void* zp, const void* bias, void* y, int M, void* stream) {
+  int rc = validate_run(plan, A, W, scales, zp, y, M);
+  if (rc != BSGEMV_OK) return rc;
+  if (bias == nullptr) return BSGEMV_ERR_INVALID_ARG;
+  if (!aligned(bias, 2)) return BSGEMV_ERR_MISALIGNED;
+  rc = check_device(plan);
+  if (rc != BSGEMV_OK) return rc;
+  rc = prepare_params(plan, A, W, scales, zp, y, M);
+  if (rc != BSGEMV_OK) return rc;
+  plan->params.bias = static_cast<const uint16_t*>(bias);
+  return launch(plan, static_cast<cudaStream_t>(stream));
+}
+
 int bsgemv_run_host(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
                     const void* zp, void* y_host, int M, void* stream) {
   if (plan == nullptr || A_host == nullptr || y_host == nullptr) return BSGEMV_ERR_INVALID_ARG;
@@ -286,15 +301,19 @@ int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows
                              int stages) {
   if (plan == nullptr || variant < 0 || ctas < 0 || stages < 0 || rows_per_tile != 0)
     return BSGEMV_ERR_INVALID_ARG;
-  if (variant == BSGEMV_VARIANT_CUDA_CORE) return BSGEMV_ERR_UNSUPPORTED;
   if (variant > BSGEMV_VARIANT_CUDA_CORE) return BSGEMV_ERR_INVALID_ARG;
+  // the CUDA-core variant accumulates at most 8 activation rows per lane
+  if (variant == BSGEMV_VARIANT_CUDA_CORE && plan->geo.max_M > 8) return BSGEMV_ERR_UNSUPPORTED;
   const int old_c = plan->ctas_override, old_s = plan->stages_override;
+  const int old_v = plan->variant_override;
+  if (variant) plan->variant_override = variant;
   if (ctas) plan->ctas_override = ctas;
   if (stages) plan->stages_override = stages;
   const int rc = rebuild_geometry(plan);
   if (rc != BSGEMV_OK) {
     plan->ctas_override = old_c;
     plan->stages_override = old_s;
+    plan->variant_override = old_v;
     rebuild_geometry(plan);
   }
   return rc;

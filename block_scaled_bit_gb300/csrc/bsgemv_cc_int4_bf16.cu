@@ -1,0 +1,11 @@
+// Instantiations of the CUDA-core variant of the GEMV kernel for int4 weights with bf16
+// activations (see bsgemv_launch.cuh).
+#include "bsgemv_launch.cuh"
+
+namespace bsg {
+
+int launch_cc_int4_bf16(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
+  return launch_fmt_cc<kInt4, true>(p, zp, cpb, ctas, smem, s);
+}
+
+}  // namespace bsg

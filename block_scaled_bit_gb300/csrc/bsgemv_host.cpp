@@ -112,6 +112,22 @@ void fill_params(const Geometry& g, const OperandMaps& m, const void* A, const v
 }
 
 int launch_gemv(const Geometry& g, const KParams& k, cudaStream_t s) {
+  if (g.pub.variant == BSGEMV_VARIANT_CUDA_CORE) {
+    if (k.M > 8) return BSGEMV_ERR_UNSUPPORTED;
+    const int bm = block_mode(g.fmt, g.block_size);
+    const int ctas = g.pub.ctas, smem = g.pub.smem_bytes;
+    switch (g.fmt) {
+      case kInt4:
+        return g.bf16 ? launch_cc_int4_bf16(k, g.has_zp, bm, ctas, smem, s)
+                      : launch_cc_int4_f16(k, g.has_zp, bm, ctas, smem, s);
+      case kInt8:
+        return g.bf16 ? launch_cc_int8_bf16(k, g.has_zp, bm, ctas, smem, s)
+                      : launch_cc_int8_f16(k, g.has_zp, bm, ctas, smem, s);
+      case kFp8: return launch_cc_fp8(k, g.bf16, ctas, smem, s);
+      case kNvfp4: return launch_cc_nvfp4(k, g.bf16, ctas, smem, s);
+    }
+    return BSGEMV_ERR_INVALID_ARG;
+  }
   // n8 activation tiles per call; 0: int4 with at most 2 rows and at least 5 stages per CTA,
   // one tile and the activations permuted by the producer (same arithmetic; measured faster
   // there, slower for short CTA ranges, where the producer's extra wait is on the critical path)

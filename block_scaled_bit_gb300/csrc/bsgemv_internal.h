@@ -46,6 +46,7 @@ struct KParams {
   const uint8_t* scales;   // global copy, read directly when side_tma == 0
   const uint8_t* zp;       // idem for zero points
   const float* gscale;     // NVFP4 global scale
+  const uint16_t* bias;    // [N] bias in the activation dtype added before the rounding, or null
   void* y;
   float* partials;         // [ctas][2][kConsumerWarps][slot_floats] cross-CTA partial sums
   unsigned* counters;      // [tiles][kConsumerWarps] arrival counters, left at zero by every call
@@ -124,6 +125,13 @@ int launch_fp8(const KParams& p, int mt, bool bf16, bool zp, int cpb, int ctas, 
                cudaStream_t s);
 int launch_nvfp4(const KParams& p, int mt, bool bf16, bool zp, int cpb, int ctas, int smem,
                  cudaStream_t s);
+// The CUDA-core variant (BSGEMV_VARIANT_CUDA_CORE; M <= 8).
+int launch_cc_int4_f16(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s);
+int launch_cc_int4_bf16(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s);
+int launch_cc_int8_f16(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s);
+int launch_cc_int8_bf16(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s);
+int launch_cc_fp8(const KParams& p, bool bf16, int ctas, int smem, cudaStream_t s);
+int launch_cc_nvfp4(const KParams& p, bool bf16, int ctas, int smem, cudaStream_t s);
 
 // Chunks (16 bytes of a weight row) per scale block, the kernel's CPB: 0 when a chunk holds two
 // blocks, else bs / k-per-chunk capped at 8 (a block spanning a whole stage or more).  NVFP4

@@ -2,23 +2,28 @@
 //
 //     y[M, N] = A[M, K] . deq(W)[N, K]^T,  M <= 16
 //
-// Data path per CTA (one persistent CTA per ring of stages, 2 per SM):
-//   warp 0, lane 0   producer: for every stage of its stream-K range, waits for a free ring slot
-//                    and issues cp.async.bulk.tensor copies of the weight box [64 rows][128 B]
-//                    (128-byte swizzle), the activation boxes [M][64 halves] (swizzled), and the
-//                    scale / zero-point boxes, all completing on the slot's mbarrier.
-//   warps 1..4       consumers: each owns 2 of the 8 16-byte chunks of every stage.  ldmatrix
-//                    hands every lane one 32-bit word of each of the 16 rows of an mma tile;
-//                    the word is decoded in registers to exact fp16/bf16 operand pairs
-//                    ((q - zp), e4m3, or e2m1 * e4m3), fed to mma.sync.m16n8k16 with the
-//                    weight as the A operand (16 output columns) and the activations as the B
-//                    operand (8 rows of A per n8 tile), accumulating in fp32.  Int and FP8
-//                    scales multiply the fp32 partial of each scale block; NVFP4's E4M3 scale is
-//                    folded into the 16-bit operand (exact: 2 + 4 significand bits).
-//   epilogue         the 4 consumer warps' partials are added in warp order through shared
-//                    memory; a tile finished inside one CTA is rounded and stored, otherwise its
-//                    fp32 partial goes to the plan's workspace and the last CTA to arrive adds
-//                    all partials of the tile in CTA order and stores y.
+// Data path per CTA (a persistent grid, 4 CTAs of 160 threads per SM; 3 for M > 8):
+//   warp 0           producer: for every stage (256 k of a 64-row tile) of the CTA's range, lane
+//                    0 waits for a free ring slot and issues the stage's weight box(es)
+//                    [64 rows][128 B] with cp.async.bulk.tensor (128-byte swizzle, L2
+//                    evict-first); all 32 lanes copy the stage's activations [M][256 k] with
+//                    16-byte cp.async into padded rows.  Scales and zero points travel on a
+//                    side ring, one TMA box [64 rows][64 B of scales] per 2..64 stages.
+//   warps 1..4       consumers: warp w owns rows 16w .. 16w + 15 of the tile over the whole
+//                    stage.  ldmatrix hands every lane the 32-bit words of its two rows (g and
+//                    g + 8) in every 16-byte chunk; the words are decoded in registers to exact
+//                    fp16/bf16 operand pairs ((q - zp), e4m3, or e2m1 * e4m3), fed to
+//                    mma.sync.m16n8k16 with the weight as the A operand (16 output columns)
+//                    and the activations as the B operand (8 rows of A per n8 tile), summed in
+//                    fp32.  Int and FP8 scales multiply the fp32 partial of each scale block;
+//                    NVFP4's E4M3 scale is folded into the 16-bit operand (exact: 2 + 4
+//                    significand bits).  The CUDA-core variant (template parameter CC) forms
+//                    the same products with packed fp32 FMAs instead (chunk_cc).
+//   epilogue         a tile consumed whole by the CTA is rounded and stored; a tile shared with
+//                    other CTAs is finished either by the last CTA to arrive (stream-K: fp32
+//                    partials in the plan's workspace, added in CTA order) or by the leader of
+//                    the tile's thread-block cluster (partials in its shared memory, added in
+//                    rank order).  The optional bias is added in fp32 before the one rounding.
 //
 // K permutation.  K is a reduction axis, so any permutation applied to both operands gives the
 // same sum ("[CUDA] Block-scaled MatMul decode GEMV: tensor cores, packed FP4 decode and
@@ -338,7 +343,33 @@ BSG_DEV void ffma2(float& acc0, float& acc1, float x0, float x1, float s) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(acc0), "=f"(acc1) : "l"(a));
 }
 
+// Packed fp32 pairs (low word = first element) for the CUDA-core variant's FMAs.
+BSG_DEV uint64_t f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+BSG_DEV float f32x2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+BSG_DEV float f32x2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+// acc += a * b on both fp32 halves (one packed CUDA-core FMA).
+BSG_DEV void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+BSG_DEV uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // ------------------------------------------------------------------------------ 16-bit pairs
+// Half h of a 16-bit pair (f16 or bf16) as fp32 (exact).
+template <bool BF16>
+BSG_DEV float half_to_f32(uint32_t pair, int h) {
+  if constexpr (BF16) return __uint_as_float(h ? (pair & 0xFFFF0000u) : (pair << 16));
+  const __half2 v = *reinterpret_cast<const __half2*>(&pair);
+  return h ? __high2float(v) : __low2float(v);
+}
+
 BSG_DEV uint32_t h2_sub(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
@@ -559,8 +590,15 @@ BSG_DEV void zp_consts(uint32_t zp, uint32_t& zl, uint32_t& zh) {
 // 4, or 8 for a block of a whole stage or more (larger blocks, fp8).  NVFP4 folds its scales
 // into the decoded values and uses 1.
 
-template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA>
+// CC > 0 selects the CUDA-core variant: the same copies, rings, decoders and epilogues, but the
+// products are formed by fp32 FMAs on the CUDA cores (each lane over its own k positions of
+// the tile rows it holds, for CC = 1 or 8 activation rows: calls with M = 1, or M <= 8)
+// instead of mma.sync.
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA, int CC = 0>
 struct Gemv {
+  static_assert(CC == 0 || ((CC == 1 || CC == 8) && MT == 1 && !PA),
+                "CUDA-core variant: 1 or 8 activation rows, natural activation order");
+  static constexpr int kCcCols = CC > 0 ? CC : 1;  // activation rows a CUDA-core lane accumulates
   static constexpr bool kFour = (FMT == kInt4 || FMT == kNvfp4);
   static constexpr int kKpc = kFour ? 32 : 16;  // k per 16-byte chunk
   static constexpr int kSteps = kKpc / 16;      // mma k-steps per chunk
@@ -810,6 +848,8 @@ struct Gemv {
     uint32_t fsel[2];          // NVFP4: prmt selector of the lane's scale code, chunk parity 0/1
     uint32_t srow;             // side box: scale row 16 rg + g; row g + 8 adds 8 * kSideScaleBytes
     uint32_t zrow;             // side box: zero-point row 16 rg + g; row g + 8 adds 8 * kZboxB
+    uint32_t cact;             // CUDA-core variant: the lane's k positions of a chunk in an
+                               // activation row (4 or 8 halves from byte t * kActChunkB / 4)
   };
 
   static BSG_DEV Lane make_lane(const KParams& p, int cw, int lane) {
@@ -840,6 +880,7 @@ struct Gemv {
     L.fsel[1] = 0x11u * static_cast<uint32_t>(2 + (L.t >> 1));
     L.srow = (16 * L.rg + L.g) * kSideScaleBytes;
     L.zrow = kRowsPerTile * kSideScaleBytes + (16 * L.rg + L.g) * kZboxB;
+    L.cact = L.t * (kActChunkB / 4);
     return L;
   }
 
@@ -1131,7 +1172,8 @@ struct Gemv {
 
   template <class R>
   static BSG_DEV void consume_stage(const R& p, const Lane& L, uint32_t wa, const Sh& ap,
-                                    int64_t tile, int ks, float (&acc)[1][MT][4]) {
+                                    int64_t tile, int ks, float (&acc)[1][MT][4],
+                                    uint64_t (&cacc)[2][kCcCols]) {
     const int k0 = ks * kKc;                                // first k of the stage in the row
     const int kb = (ks & ((1 << p.rs_log2) - 1)) * kKc;    // ... in the side box
     uint32_t wl[4];
@@ -1146,7 +1188,8 @@ struct Gemv {
         if (bx == 0) ldsm_x4_at<0>(wl[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
         else ldsm_x4_at<kBoxB>(wl[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
       }
-      consume_box(p, L, wv, ap, tile, k0, kb, bx * 8, acc);
+      if constexpr (CC > 0) consume_box_cc(p, L, wv, ap, tile, k0, kb, bx * 8, cacc);
+      else consume_box(p, L, wv, ap, tile, k0, kb, bx * 8, acc);
     }
   }
 
@@ -1260,7 +1303,188 @@ struct Gemv {
 #undef BSG_HI
   }
 
-  // Store the 4 fp32 results of lane ln's fragment (row group rg, n8 tile mt) as y.
+  // ---- CUDA-core variant.  Lane (g, t) holds, for tile rows g and g + 8, the codes of its own k
+  // positions of every chunk (the words ldmatrix hands it), decoded by the same exact decoders
+  // as the mma path.  Each decoded 16-bit pair becomes an fp32 pair times the row's block scale
+  // (exact for the int formats: at most 9 + 11 significand bits) and is multiplied into the
+  // packed partial sums cacc[rr][m] -- one per tile row rr and activation row m, its halves the
+  // pair's two k -- with the activations of the same k of row m: one fma.rn.f32x2 per pair, tile
+  // row and activation row.  The quad's four lanes cover the chunk's k; their sums are added at
+  // the end of a tile segment (cc_fragment).
+  template <class R>
+  static BSG_DEV void chunk_cc(const R& p, const Lane& L, const Sh& ap, int c, uint32_t lo,
+                               uint32_t hi, const uint32_t (&zl)[2], const uint32_t (&zh)[2],
+                               const float (&sc)[2], uint64_t (&cacc)[2][kCcCols]) {
+    uint32_t a[kSteps][4];
+    if constexpr (FMT == kInt4) {
+      decode_int4<BF16>(lo, hi, zl[0], zh[0], zl[1], zh[1], a);
+    } else if constexpr (FMT == kInt8) {
+      decode_int8<BF16>(lo, hi, zl[0], zl[1], a);
+    } else if constexpr (FMT == kFp8) {
+      decode_fp8<BF16>(lo, hi, a);
+    } else {
+      decode_nvfp4<BF16>(lo, hi, zl[0], zl[1], a);
+    }
+    constexpr int kP = 2 * kSteps;  // k pairs of a lane per tile row and chunk
+    uint64_t w[2][kP];
+#pragma unroll
+    for (int s = 0; s < kSteps; ++s)
+#pragma unroll
+      for (int rp = 0; rp < 2; ++rp)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const uint32_t h = a[s][2 * rp + rr];
+          uint64_t v = f32x2(half_to_f32<BF16>(h, 0), half_to_f32<BF16>(h, 1));
+          if constexpr (!kFold) v = mul_f32x2(v, f32x2(sc[rr], sc[rr]));
+          w[rr][2 * s + rp] = v;
+        }
+#pragma unroll
+    for (int m = 0; m < kCcCols; ++m) {
+      if (m > 0 && m >= p.k.M) break;
+      // the lane's 8 (4-bit formats) or 4 (8-bit) activation halves of chunk c, row m
+      const uint8_t* src = ap.base + (ap.a + m * kActPitch + c * kActChunkB + L.cact);
+      uint32_t x[kFour ? 4 : 2];
+      if constexpr (kFour) {
+        const uint4 v = lsh<uint4>(src);
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
+      } else {
+        const uint2 v = lsh<uint2>(src);
+        x[0] = v.x;
+        x[1] = v.y;
+      }
+#pragma unroll
+      for (int s = 0; s < kSteps; ++s)
+#pragma unroll
+        for (int rp = 0; rp < 2; ++rp) {
+          // halves j0, j1 of x hold the pair's two k (phys_k, relative to the lane's first k)
+          const int j0 = phys_k<FMT>(s, rp, 0, 0), j1 = phys_k<FMT>(s, rp, 1, 0);
+          const uint64_t xa = f32x2(half_to_f32<BF16>(x[j0 >> 1], j0 & 1),
+                                    half_to_f32<BF16>(x[j1 >> 1], j1 & 1));
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) fma_f32x2(cacc[rr][m], w[rr][2 * s + rp], xa);
+        }
+    }
+  }
+
+  // Zero points and scales of scale group `grp` of the weight box whose first chunk is c0 (the
+  // same sources and order as consume_box).
+  template <int NS, class R>
+  static BSG_DEV void group_side(const R& p, const Lane& L, const Sh& ap, int64_t tile, int k0,
+                                 int kb, int c0, int grp, SideLoad<NS>& sl, uint32_t (&z)[2],
+                                 float (&s)[kGB][2]) {
+    const int kg = (c0 + grp * kGC) * kKpc;  // k of the group in the stage
+    if constexpr (R::side) {
+      constexpr int kGpl = NS / kGB;  // groups per side load
+      if (grp % kGpl == 0) {
+        int rel;
+        if constexpr (kBsLog2 >= 0) rel = (kb + kg) >> kBsLog2;
+        else rel = (kb + kg) >> p.bs_log2;
+        load_side<NS>(L, ap, rel, sl);
+      }
+      side_group<kGB>(sl, (grp % kGpl) * kGB, z, s);
+    } else {
+      const int blk = (k0 + kg) >> p.bs_log2;
+      load_zp<kGB>(p, L, tile, blk, z);
+      load_scales<kGB>(p, L, tile, blk, s);
+    }
+  }
+
+  // Chunks c0 .. c0 + 7 of the stage on the CUDA cores (see chunk_cc).  Every lane's codes of a
+  // chunk lie in one scale block: block t/2 of the chunk when it holds two (16-element int4
+  // blocks).
+  template <class R>
+  static BSG_DEV void consume_box_cc(const R& p, const Lane& L, const uint32_t (&wv)[4][4],
+                                     const Sh& ap, int64_t tile, int k0, int kb, int c0,
+                                     uint64_t (&cacc)[2][kCcCols]) {
+#define BSG_LO(c) wv[(c) >> 1][2 * ((c) & 1)]
+#define BSG_HI(c) wv[(c) >> 1][2 * ((c) & 1) + 1]
+    uint32_t zl[2], zh[2] = {0u, 0u};
+    if constexpr (kFold) {
+      const float one[2] = {1.f, 1.f};
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int d = 2 * (c0 + c) + (L.t >> 1);
+        load_fold(p, L, ap, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
+        chunk_cc(p, L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, one, cacc);
+      }
+    } else {
+      constexpr int kBB = (8 / kGC) * kGB;    // scale blocks per weight box
+      constexpr int kSL = kBB < 8 ? kBB : 8;  // blocks per side load
+      SideLoad<kSL> sl;
+#pragma unroll
+      for (int grp = 0; grp < 8 / kGC; ++grp) {
+        uint32_t z[2];
+        float s[kGB][2];
+        group_side<kSL>(p, L, ap, tile, k0, kb, c0, grp, sl, z, s);
+        if constexpr (CPB == 0) {  // one chunk, two blocks: the lane's codes are in block t/2
+          const int u = L.t >> 1;
+          zp_of(z, u, zl, zh);
+          const float sc[2] = {u ? s[1][0] : s[0][0], u ? s[1][1] : s[0][1]};
+          chunk_cc(p, L, ap, c0 + grp, BSG_LO(grp), BSG_HI(grp), zl, zh, sc, cacc);
+        } else if constexpr (CPB == 1) {  // two chunks, one block each
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = grp * 2 + u;
+            zp_of(z, u, zl, zh);
+            const float sc[2] = {s[u][0], s[u][1]};
+            chunk_cc(p, L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, sc, cacc);
+          }
+        } else {  // CPB 2, 4 or 8: kGC chunks in one block
+          zp_of(z, 0, zl, zh);
+          const float sc[2] = {s[0][0], s[0][1]};
+#pragma unroll
+          for (int u = 0; u < kGC; ++u) {
+            const int c = grp * kGC + u;
+            chunk_cc(p, L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, sc, cacc);
+          }
+        }
+      }
+    }
+#undef BSG_LO
+#undef BSG_HI
+  }
+
+  // End of a tile segment (CUDA-core variant): add each pair's halves, then the quad's four
+  // lanes by a butterfly (every lane of the quad gets bit-identical sums, as fp32 addition
+  // commutes), and leave in acc the mma fragment layout the epilogues take (tile rows g, g + 8;
+  // activation rows 2t, 2t + 1).  The partial sums are cleared for the next segment.
+  static BSG_DEV void cc_fragment(const Lane& L, uint64_t (&cacc)[2][kCcCols],
+                                  float (&acc)[1][MT][4]) {
+    float v[2][kCcCols];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int m = 0; m < kCcCols; ++m) {
+        float x = f32x2_lo(cacc[rr][m]) + f32x2_hi(cacc[rr][m]);
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+        v[rr][m] = x;
+        cacc[rr][m] = 0ull;
+      }
+    if constexpr (kCcCols == 8) {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          acc[0][0][2 * rr + e] = L.t == 0   ? v[rr][e]
+                                  : L.t == 1 ? v[rr][2 + e]
+                                  : L.t == 2 ? v[rr][4 + e]
+                                             : v[rr][6 + e];
+    } else {  // one activation row: column 0 is entry 0 (row g) and 2 (row g + 8) of lane t = 0
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        acc[0][0][2 * rr] = L.t == 0 ? v[rr][0] : 0.f;
+        acc[0][0][2 * rr + 1] = 0.f;
+      }
+    }
+  }
+
+  // Store the 4 fp32 results of lane ln's fragment (row group rg, n8 tile mt) as y, after
+  // adding the bias of the output column when the call has one (in fp32, before the one
+  // rounding to the activation dtype).
   static BSG_DEV void store_y(const KParams& p, int64_t tile, int rg, int mt, int ln, const float (&v)[4],
                               float gs) {
     const int g = ln >> 2, t = ln & 3;
@@ -1271,7 +1495,11 @@ struct Gemv {
       const int64_t n = n0 + ((i & 2) ? 8 : 0);
       const int m = m0 + (i & 1);
       if (m < p.M && n < p.N) {
-        const float r = v[i] * gs;
+        float r = v[i] * gs;
+        if (p.bias != nullptr) {
+          const uint32_t b = __ldg(p.bias + n);
+          r += BF16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
+        }
         if constexpr (BF16)
           reinterpret_cast<__nv_bfloat16*>(p.y)[m * p.N + n] = __float2bfloat16_rn(r);
         else
@@ -1447,6 +1675,11 @@ struct Gemv {
     const Run<SIDE> R{p.bs_log2, p.rs_log2, p.zbox_bytes, p};
     float acc[1][MT][4];
     zero(acc[0]);
+    uint64_t cacc[2][kCcCols];  // CUDA-core variant's partial sums (unused by the mma variant)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int m = 0; m < kCcCols; ++m) cacc[rr][m] = 0ull;
     const float gs = kFold ? __ldg(p.gscale) : 1.0f;
     const int spt = p.spt;
     const int n = static_cast<int>(s1 - s0);
@@ -1469,7 +1702,7 @@ struct Gemv {
         if (ok) {
           const Sh sh{sm.base, sm.act_off + r.slot * sm.act_bytes,
                       sm.side_off + sr.slot * sm.side_bytes};
-          consume_stage(R, L, sm.w(r.slot), sh, tile, w.ks, acc);
+          consume_stage(R, L, sm.w(r.slot), sh, tile, w.ks, acc, cacc);
         }
         __syncwarp();
         mbar_arrive_if(sm.empty(r.slot), lane == 0);
@@ -1478,6 +1711,7 @@ struct Gemv {
         w.next();
       }
       i += seg;
+      if constexpr (CC > 0) cc_fragment(L, cacc, acc);
       if (p.cluster >= 2) {
         cluster_publish(p, sm, cw, L, acc);  // the cluster's leader adds and stores
       } else if (seg == spt) {  // whole: this CTA consumed every stage of the tile
@@ -1493,9 +1727,9 @@ struct Gemv {
   }
 };
 
-template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT)) bsgemv_mma_kernel(const __grid_constant__ KParams p) {
-  using K = Gemv<FMT, BF16, MT, ZP, CPB, PA>;
+// The body shared by both kernels: one CTA of the persistent grid.
+template <class K>
+BSG_DEV void gemv_cta(const KParams& p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned (128-byte swizzle atoms), derived from the shared array so that plain
   // loads through it stay shared-memory loads
@@ -1540,6 +1774,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT)) bsgemv_mma_k
     cluster_sync();  // every CTA of the cluster has stored its partials in the leader
     if (cluster_ctarank() == 0 && warp > 0) K::cluster_reduce(p, sm, warp - 1, lane);
   }
+}
+
+// Tensor-core kernel (the default): products on mma.sync.m16n8k16.
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT))
+    bsgemv_mma_kernel(const __grid_constant__ KParams p) {
+  gemv_cta<Gemv<FMT, BF16, MT, ZP, CPB, PA>>(p);
+}
+
+// CUDA-core kernel (BSGEMV_VARIANT_CUDA_CORE): products on fp32 FMAs, COLS = 1 (calls with
+// M = 1) or 8 (M <= 8) activation rows per lane.
+template <int FMT, bool BF16, bool ZP, int CPB, int COLS>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(1))
+    bsgemv_fma_kernel(const __grid_constant__ KParams p) {
+  gemv_cta<Gemv<FMT, BF16, 1, ZP, CPB, false, COLS>>(p);
 }
 
 }  // namespace bsg

@@ -7,11 +7,11 @@
 
 namespace bsg {
 
-template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA = false>
-int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
-  auto k = bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, PA>;
-  static std::atomic<int> attr_smem{0};  // largest dynamic smem already granted to `k`
-  static std::atomic<int> attr_cluster{0};  // non-portable cluster sizes allowed for `k`
+// Launch kernel `k` (one instantiation; `attr_smem` / `attr_cluster` are its own records of the
+// attributes already set).
+template <class Kernel>
+int launch_kernel(Kernel k, std::atomic<int>& attr_smem, std::atomic<int>& attr_cluster,
+                  const KParams& p, int ctas, int smem, cudaStream_t s) {
   if (smem > attr_smem.load()) {
     // One shared-memory carveout (the largest) for every instantiation: an SM holds CTAs of
     // kernels with different carveouts only after draining, which would serialise consecutive
@@ -50,6 +50,60 @@ int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
   cfg.numAttrs = nattr;
   if (cudaLaunchKernelEx(&cfg, k, p) != cudaSuccess) return BSGEMV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
+}
+
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA = false>
+int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
+  static std::atomic<int> attr_smem{0};     // largest dynamic smem already granted
+  static std::atomic<int> attr_cluster{0};  // non-portable cluster sizes allowed
+  return launch_kernel(bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, PA>, attr_smem, attr_cluster, p,
+                       ctas, smem, s);
+}
+
+template <int FMT, bool BF16, bool ZP, int CPB, int COLS>
+int launch_one_cc(const KParams& p, int ctas, int smem, cudaStream_t s) {
+  static std::atomic<int> attr_smem{0};
+  static std::atomic<int> attr_cluster{0};
+  return launch_kernel(bsgemv_fma_kernel<FMT, BF16, ZP, CPB, COLS>, attr_smem, attr_cluster, p,
+                       ctas, smem, s);
+}
+
+// CUDA-core variant (M <= 8): dispatch over zero points and chunks per scale block; COLS = 1
+// for calls with M = 1, else 8 (the same arithmetic per activation row).
+template <int FMT, bool BF16, int COLS>
+int launch_fmt_cc_cols(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
+#define BSG_C(ZPV, C) return launch_one_cc<FMT, BF16, ZPV, C, COLS>(p, ctas, smem, s)
+#define BSG_CZ(C) \
+  if (zp) BSG_C(true, C); \
+  BSG_C(false, C)
+  if constexpr (FMT == kInt4) {
+    switch (cpb) {
+      case 0: BSG_CZ(0);
+      case 1: BSG_CZ(1);
+      case 2: BSG_CZ(2);
+      case 4: BSG_CZ(4);
+      default: BSG_CZ(8);
+    }
+  } else if constexpr (FMT == kInt8) {
+    switch (cpb) {
+      case 1: BSG_CZ(1);
+      case 2: BSG_CZ(2);
+      case 4: BSG_CZ(4);
+      default: BSG_CZ(8);
+    }
+  } else if constexpr (FMT == kFp8) {
+    BSG_C(false, 8);
+  } else {
+    BSG_C(false, 1);
+  }
+#undef BSG_CZ
+#undef BSG_C
+}
+
+template <int FMT, bool BF16>
+int launch_fmt_cc(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
+  if (p.M == 1) return launch_fmt_cc_cols<FMT, BF16, 1>(p, zp, cpb, ctas, smem, s);
+  return launch_fmt_cc_cols<FMT, BF16, 8>(p, zp, cpb, ctas, smem, s);
 }
 
 // Dispatch over the n8 tile count, zero points and chunks per scale block (block_mode) for one

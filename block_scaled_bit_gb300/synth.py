@@ -48,11 +48,20 @@ class Case:
     gscale: np.ndarray | None  # float32 [1] (nvfp4) or None
     seed: int = 0
     name: str = ""
+    bias: np.ndarray | None = None  # uint16 [N] activation-dtype bits, or None (no bias)
 
     def with_M(self, M: int) -> "Case":
         """The same weights with the first M rows of this case's 16-row activation draw."""
         A = activations(self.seed, M, self.K, self.act)
         return dataclasses.replace(self, M=M, A=A)
+
+    def with_bias(self, sigma: float = 1.0) -> "Case":
+        """The same case with a bias [N] ~ N(0, sigma^2) rounded to the activation dtype, drawn
+        from its own stream (the weights and activations are unchanged)."""
+        rng = np.random.Generator(np.random.PCG64([self.seed, 0xB1A5]))
+        x = rng.standard_normal(self.N) * sigma
+        bias = to_f16_bits(x) if self.act == "f16" else to_bf16_bits(x)
+        return dataclasses.replace(self, bias=bias)
 
     @property
     def nb(self) -> int:
@@ -66,6 +75,8 @@ class Case:
             b += self.zp.nbytes
         if self.gscale is not None:
             b += 4
+        if self.bias is not None:
+            b += self.bias.nbytes
         return b + 2 * M * self.K + 2 * M * self.N
 
 

@@ -78,7 +78,10 @@ enum bsgemv_status {
 enum bsgemv_variant {
   BSGEMV_VARIANT_AUTO = 0,
   BSGEMV_VARIANT_MMA = 1,        /* tensor-core mma.sync m16n8k16, fp32 accumulate */
-  BSGEMV_VARIANT_CUDA_CORE = 2   /* CUDA-core fp32 FMA, rows of A tiled in registers */
+  BSGEMV_VARIANT_CUDA_CORE = 2   /* CUDA-core packed fp32 FMA (fma.rn.f32x2) over the same
+                                    copies, decoders and reductions; plans with max_M <= 8.  A
+                                    measured alternative: the tensor-core variant is faster for
+                                    every format and M */
 };
 
 /* What a plan chose.  Filled by bsgemv_plan_describe / bsgemv_geometry_for. */
@@ -133,6 +136,17 @@ int bsgemv_run(bsgemv_plan_t plan, const void* A, const void* W, const void* sca
                const void* zp, void* y, int M, void* stream);
 
 /*
+ * y = A . deq(W)^T + bias: as bsgemv_run, plus `bias`, N values in the activation dtype (device
+ * memory, 2-byte aligned, caller-owned), added to every row's fp32 sum before the one rounding.
+ * ("[CUDA] Block-scaled MatMul decode GEMV: tensor cores, packed FP4 decode and M-tiling",
+ * Tests: the FP8 and FP4 operators take an optional bias; "[CUDA] Pin FP8 GEMV residency for
+ * grids just past two blocks per SM", Tests.)  NULL bias: BSGEMV_ERR_INVALID_ARG (call
+ * bsgemv_run instead).  Same determinism as bsgemv_run: rows are bit-identical across M.
+ */
+int bsgemv_run_bias(bsgemv_plan_t plan, const void* A, const void* W, const void* scales,
+                    const void* zp, const void* bias, void* y, int M, void* stream);
+
+/*
  * Same as bsgemv_run, but A and y are HOST memory (pinned memory gives asynchronous copies):
  * A is copied into the plan's device staging buffer, the GEMV runs, y is copied back, and the
  * call returns after the stream has finished (the host buffers are ready on return).  W,
@@ -168,7 +182,8 @@ int bsgemv_debug_dequant(bsgemv_plan_t plan, const void* W, const void* scales, 
 int bsgemv_plan_set_split(bsgemv_plan_t plan, int split, int cluster_size);
 
 /*
- * A/B override for measurements: variant (enum bsgemv_variant, 0 = keep), ctas (persistent
+ * A/B override for measurements: variant (enum bsgemv_variant, 0 = keep; CUDA_CORE needs a plan
+ * with max_M <= 8, else BSGEMV_ERR_UNSUPPORTED), ctas (persistent
  * CTAs of a stream-K split, 0 = keep; under BSGEMV_SPLIT_AUTO a CTA count selects stream-K),
  * rows_per_tile (reserved, must be 0), stages (ring depth, 0 = keep).
  * Changes the summation order, so results are bit-identical only between calls made under the

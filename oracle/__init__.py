@@ -11,7 +11,8 @@ ctypes.  It never imports ``block_scaled_bit_gb300``.
 
 Formats are named by strings ("int4", "int8", "fp8", "nvfp4"); activations by "f16" / "bf16".
 A "case" is any object with the attributes ``fmt, act, block_size, has_zp, N, K, M, A, W,
-scales, zp, gscale`` holding numpy arrays (the seeded generators produce such objects).
+scales, zp, gscale`` holding numpy arrays (the seeded generators produce such objects), and
+optionally ``bias`` (uint16 [N] activation-dtype bits, or None).
 """
 from __future__ import annotations
 
@@ -84,8 +85,8 @@ def lib() -> ctypes.CDLL:
             L.orc_gemv.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long,
                 ctypes.c_long, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_long,
-                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_long, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
             L.orc_max_threads.restype = ctypes.c_int
             L.orc_set_threads.restype = None
             L.orc_set_threads.argtypes = [ctypes.c_int]
@@ -149,9 +150,15 @@ def dequant(case, n0: int = 0, count: int | None = None) -> np.ndarray:
     return out
 
 
+def _bias_arr(case):
+    b = getattr(case, "bias", None)
+    return None if b is None else np.ascontiguousarray(np.asarray(b, dtype=np.uint16).reshape(-1))
+
+
 def gemv(case, rows=None, M: int | None = None):
     """Oracle GEMV.  Returns (ybits uint16 [M, R], exact float64 [M, R], absdot float64 [M, R])
-    for the output columns ``rows`` (all N if None); R = len(rows) or N."""
+    for the output columns ``rows`` (all N if None); R = len(rows) or N.  A case with a ``bias``
+    gets it added to every row before the rounding (and |bias| in absdot)."""
     M = case.M if M is None else M
     r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     count = case.N if r is None else r.size
@@ -162,8 +169,8 @@ def gemv(case, rows=None, M: int | None = None):
     rc = lib().orc_gemv(
         FORMAT_IDS[case.fmt], 1 if case.act == "bf16" else 0, case.block_size, int(case.has_zp),
         case.N, case.K, M, _ptr(A), _ptr(case.W), _ptr(case.scales), _ptr(case.zp),
-        _ptr(_gscale_arr(case)), _ptr(r), 0 if r is None else r.size, _ptr(ybits), _ptr(exact),
-        _ptr(absdot))
+        _ptr(_gscale_arr(case)), _ptr(_bias_arr(case)), _ptr(r), 0 if r is None else r.size,
+        _ptr(ybits), _ptr(exact), _ptr(absdot))
     if rc != 0:
         raise ValueError(f"orc_gemv failed ({rc})")
     return ybits, exact, absdot
@@ -192,7 +199,7 @@ def ulp(values: np.ndarray, act: str) -> np.ndarray:
 def tolerance_violations(case, ybits_gpu: np.ndarray, rows=None, M: int | None = None,
                          rel: float = 1e-3):
     """Compare GPU output bits [M, R] with the oracle on the same inputs.  The bar:
-        |y - y_ref| <= 1 ulp(|y_ref|) + rel * sum_k |a_k * w_k|
+        |y - y_ref| <= 1 ulp(|y_ref|) + rel * (sum_k |a_k * w_k| [+ |bias|])
     with y_ref the oracle's correctly rounded result; infinities must match exactly.
     Returns (number of violations, max |y - y_ref| / bound, oracle bits)."""
     ref_bits, _, absdot = gemv(case, rows=rows, M=M)

@@ -14,7 +14,9 @@
  *   2. the dequantised weight is formed exactly: (q - zp) * s, e4m3 * s, e2m1 * e4m3 * g -- every
  *      one of these products has at most 4 + 24 significand bits, so binary64 holds it exactly;
  *   3. the dot product over K is summed in increasing k order in binary64;
- *   4. the sum is rounded once, round-to-nearest-even, to the activation dtype.
+ *   4. an optional bias[n] (activation dtype, one value per output column) is added to the sum
+ *      in binary64;
+ *   5. the result is rounded once, round-to-nearest-even, to the activation dtype.
  *
  * Sources (web pages on the method; cited by title and section):
  *   [P1] "[CUDA] Block-scaled MatMul decode GEMV: tensor cores, packed FP4 decode and M-tiling"
@@ -36,6 +38,9 @@
  *     fp32 number.
  *   - NVFP4 codes are packed like int4 (low nibble = even k).
  *   - The output is rounded round-to-nearest-even; overflow goes to +-inf, NaN propagates.
+ *   - Bias: the FP8 / FP4 operators' tests cover an optional bias ([P1] Tests; "[CUDA] Pin FP8 GEMV
+ *     residency ...", Tests); read as y = A . deq(W)^T + bias with bias [N] in the activation
+ *     dtype, broadcast over the M rows and added before the one rounding.
  */
 #include <math.h>
 #include <stddef.h>
@@ -233,15 +238,16 @@ int orc_dequant_rows(int fmt, int block_size, int has_zp, long N, long K, const 
 /* ------------------------------------------------------------------------------------------ */
 /* The GEMV: for every requested output column n (rows[] of W, or all n if rows == NULL) and   */
 /* every activation row m < M:                                                                  */
-/*    exact[m][i]  = sum_k A[m,k] * deq(n,k)     (binary64, increasing k)                       */
-/*    absdot[m][i] = sum_k |A[m,k] * deq(n,k)|   (for the tolerance bound)                      */
+/*    exact[m][i]  = sum_k A[m,k] * deq(n,k)     (binary64, increasing k)  [+ bias[n]]          */
+/*    absdot[m][i] = sum_k |A[m,k] * deq(n,k)|   (for the tolerance bound) [+ |bias[n]|]        */
 /*    ybits[m][i]  = RNE of exact to the activation dtype                                      */
-/* A is [M, K] fp16 (act_bf16 == 0) or bf16 (act_bf16 == 1) bit patterns.                     */
+/* A is [M, K] and bias [N] (NULL: no bias) fp16 (act_bf16 == 0) or bf16 (act_bf16 == 1) bit   */
+/* patterns.                                                                                    */
 /* ------------------------------------------------------------------------------------------ */
 int orc_gemv(int fmt, int act_bf16, int block_size, int has_zp, long N, long K, int M,
              const uint16_t* A, const uint8_t* W, const void* scales, const uint8_t* zp,
-             const float* gscale, const long* rows, long nrows, uint16_t* ybits, double* exact,
-             double* absdot) {
+             const float* gscale, const uint16_t* bias, const long* rows, long nrows,
+             uint16_t* ybits, double* exact, double* absdot) {
   if (block_size <= 0 || K % block_size != 0 || M < 1) return -1;
   const long count = rows ? nrows : N;
   orc_weights w = {fmt, block_size, has_zp, N, K, W, scales, zp, gscale ? (double)*gscale : 1.0};
@@ -264,6 +270,11 @@ int orc_gemv(int fmt, int act_bf16, int block_size, int has_zp, long N, long K, 
         const double p = am[k] * orc_deq(&w, n, k);
         sum += p;
         asum += fabs(p);
+      }
+      if (bias) {
+        const double b = act_bf16 ? orc_bf16_value(bias[n]) : orc_f16_value(bias[n]);
+        sum += b;
+        asum += fabs(b);
       }
       if (exact) exact[(long)m * count + i] = sum;
       if (absdot) absdot[(long)m * count + i] = asum;

@@ -17,6 +17,8 @@ import bisect
 import os
 from fractions import Fraction
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -288,6 +290,12 @@ def brute_gemv(case, mutate=None):
     if mutate == "transpose":   # a transposed operand: rows of A against W read column-wise
         exact = [[sum((a[m][k] * deq[k % N][n % K] for k in range(K)), Fraction(0))
                   for n in range(N)] for m in range(M)]
+    bias = getattr(case, "bias", None)
+    if bias is not None and mutate != "bias_dropped":
+        # bias[n] added to every row m before the one rounding
+        col = (lambda n: (n + 1) % N) if mutate == "bias_column" else (lambda n: n)
+        exact = [[exact[m][n] + frac_act(bias[col(n)], case.act) for n in range(N)]
+                 for m in range(M)]
     bits = np.array([[table_rne(e, vals, maxc) for e in row] for row in exact], dtype=np.uint16)
     return bits, exact
 
@@ -417,3 +425,53 @@ def test_subset_rows_match_full(orc):
     ys, es, ds = orc.gemv(case, rows=rows)
     assert np.array_equal(ys, y[:, rows]) and np.array_equal(es, e[:, rows])
     assert np.array_equal(ds, d[:, rows])
+
+
+# ------------------------------------------------------------------ the optional bias
+BIAS_TINY = [("int4", "f16", 32, True), ("int8", "bf16", 16, False), ("fp8", "f16", 128, False),
+             ("nvfp4", "bf16", 16, False)]
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", BIAS_TINY)
+def test_oracle_with_bias_matches_exact_rational_brute_force(orc, fmt, act, bs, zp):
+    """y = A . deq(W)^T + bias (bias[n] broadcast over the rows, one rounding): the oracle equals
+    the exact rational result rounded by the independent table search."""
+    case = tiny_case(fmt, act, bs, zp).with_bias(sigma=4.0)
+    ybits, exact, absdot = orc.gemv(case)
+    bits, ex = brute_gemv(case)
+    assert np.array_equal(ybits, bits)
+    ex64 = np.array([[float(e) for e in row] for row in ex])
+    assert np.allclose(exact, ex64, rtol=1e-12, atol=1e-300)
+    _, _, absdot0 = orc.gemv(dataclasses.replace(case, bias=None))
+    assert np.array_equal(absdot, absdot0 + np.abs(orc.act_values(case.bias, act))[None, :])
+
+
+@pytest.mark.parametrize("mutation", ["bias_dropped", "bias_column"])
+def test_brute_force_detects_planted_bias_mistakes(orc, mutation):
+    case = tiny_case("int8", "f16", 32, True).with_bias(sigma=4.0)
+    ybits, _, _ = orc.gemv(case)
+    bad, _ = brute_gemv(case, mutate=mutation)
+    assert not np.array_equal(ybits, bad)
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", BIAS_TINY)
+def test_zero_activations_give_the_bias(orc, fmt, act, bs, zp):
+    """With A = 0 every product is zero, so y is the bias itself (it is already representable)."""
+    case = synth.make_case(fmt, act, bs, zp, 37, 256, 3, 5).with_bias()
+    case = dataclasses.replace(case, A=np.zeros_like(case.A))
+    ybits, exact, _ = orc.gemv(case)
+    b = orc.act_values(case.bias, act)
+    assert np.array_equal(orc.act_values(ybits, act), np.broadcast_to(b, ybits.shape))
+    assert np.array_equal(exact, np.broadcast_to(b, exact.shape))
+
+
+def test_bias_adds_to_the_exact_sum(orc):
+    """The bias enters after the k-sum: exact(with bias) - exact(without) = bias, when the sums are
+    small integers (s = 1, zp = 0 int8 weights, integer activations) so that nothing rounds."""
+    case = synth.make_case("int8", "f16", 32, True, 21, 128, 4, 9,
+                           scale_range=(1.0, 1.0), zp_range=(0, 0))
+    A = synth.to_f16_bits(np.random.default_rng(3).integers(-3, 4, size=case.A.shape))
+    case = dataclasses.replace(case, A=A).with_bias(sigma=8.0)
+    _, e_b, _ = orc.gemv(case)
+    _, e_0, _ = orc.gemv(dataclasses.replace(case, bias=None))
+    assert np.array_equal(e_b - e_0, np.broadcast_to(orc.act_values(case.bias, "f16"), e_b.shape))

@@ -230,6 +230,10 @@ def test_errors_on_device(torch_cuda):
         assert plan.run_status(d.A, None, d.scales, d.zp, d.y) == bsgemv.ERR_INVALID_ARG
         assert plan.set_override(variant=7) == bsgemv.ERR_INVALID_ARG
         assert plan.device_status() == bsgemv.OK
+    with bsgemv.Plan("int4", "f16", 32, True, case.N, case.K, 16) as plan:
+        # the CUDA-core variant accumulates at most 8 activation rows per lane
+        assert plan.set_override(variant=bsgemv.VARIANTS["cuda_core"]) == bsgemv.ERR_UNSUPPORTED
+        assert plan.describe()["variant"] == bsgemv.VARIANTS["mma"]
     with bsgemv.Plan("int8", "f16", 32, False, 64, 512, 1) as plan:
         c8 = synth.make_case("int8", "f16", 32, False, 64, 512, 1, 4)
         d8 = bsgemv.upload(c8, "cuda")
@@ -263,3 +267,120 @@ def test_int4_activation_permutation_paths_agree(torch_cuda, act, bs, zp):
     assert_parity(case.with_M(3), outs[3], rows=rows)
     assert np.array_equal(outs[1], outs[3][:1])
     assert np.array_equal(outs[2], outs[3][:2])
+
+
+# ---------------------------------------------------------------------------- CUDA-core variant
+CC_CASES = ([("int4", a, bs, z) for a in ("f16", "bf16") for bs in (16, 32, 64, 128, 256) for z in (True, False)]
+            + [("int8", a, bs, z) for a in ("f16", "bf16") for bs in (16, 32, 64, 128, 256) for z in (True, False)]
+            + [("fp8", a, 128, False) for a in ("f16", "bf16")]
+            + [("nvfp4", a, 16, False) for a in ("f16", "bf16")])
+
+
+def cuda_core_plan(fmt, act, bs, zp, N, K, max_M):
+    plan = bsgemv.Plan(fmt, act, bs, zp, N, K, max_M)
+    assert plan.set_override(variant=bsgemv.VARIANTS["cuda_core"]) == bsgemv.OK
+    assert plan.describe()["variant"] == bsgemv.VARIANTS["cuda_core"]
+    return plan
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", CC_CASES)
+def test_cuda_core_variant_parity_and_rows_across_M(torch_cuda, fmt, act, bs, zp):
+    """The CUDA-core variant (fp32 FMAs on the CUDA cores instead of mma.sync, same decoders and
+    pipeline): within the bound of the oracle for M = 1 and M = 8 (its two kernels) over several
+    tiles with ragged N and K tails, and every row bit-identical across M = 1..8 of one plan."""
+    K = 1536 if bs <= 128 else 1792
+    case8 = synth.make_case(fmt, act, bs, zp, 357, K, 8, 11 * bs + 5)
+    with cuda_core_plan(fmt, act, bs, zp, case8.N, case8.K, 8) as plan:
+        y8 = run(case8, plan)
+        for M in (1, 2, 7):
+            assert np.array_equal(run(case8.with_M(M), plan), y8[:M]), f"M={M}"
+    assert_parity(case8, y8)
+
+
+@pytest.mark.parametrize("split,cluster,ctas", [("stream_k", 0, 37), ("stream_k", 0, 0),
+                                                ("cluster", 3, 0), ("cluster", 8, 0)])
+@pytest.mark.parametrize("M", [1, 6])
+def test_cuda_core_variant_under_every_split(torch_cuda, split, cluster, ctas, M):
+    """Both K splits (stream-K with a last-arriver reduction, cluster split reduced in shared
+    memory) take the CUDA-core variant's partial sums in the same fragment layout."""
+    # int4: 8 KB stages, so that 3- and 8-CTA clusters fit next to the reduction buffer
+    case = synth.make_case("int4", "bf16", 64, True, 700, 4096, M, 606 + M)
+    with cuda_core_plan("int4", "bf16", 64, True, case.N, case.K, 8) as plan:
+        assert plan.set_split(split, cluster) == bsgemv.OK
+        if ctas:
+            assert plan.set_override(ctas=ctas) == bsgemv.OK
+        g = plan.describe()
+        assert g["variant"] == bsgemv.VARIANTS["cuda_core"]
+        assert (g["cluster"] == cluster) if split == "cluster" else g["cluster"] == 0
+        y = run(case, plan)
+    assert_parity(case, y)
+
+
+def test_cuda_core_and_mma_variants_agree_within_tolerance(torch_cuda):
+    """Same problem through both variants: different summation orders, each within the bound."""
+    case = synth.make_case("nvfp4", "f16", 16, False, 2048, 2048, 4, 808)
+    with bsgemv.Plan("nvfp4", "f16", 16, False, case.N, case.K, 4) as plan:
+        y_mma = run(case, plan)
+        assert plan.set_override(variant=bsgemv.VARIANTS["cuda_core"]) == bsgemv.OK
+        y_cc = run(case, plan)
+        assert plan.set_override(variant=bsgemv.VARIANTS["mma"]) == bsgemv.OK
+        assert np.array_equal(run(case, plan), y_mma)
+    assert_parity(case, y_mma)
+    assert_parity(case, y_cc)
+
+
+# ---------------------------------------------------------------------------- bias epilogue
+def run_bias(case, plan, M=None):
+    import torch
+    M = case.M if M is None else M
+    d = bsgemv.upload(case.with_M(M) if M != case.M else case, "cuda")
+    plan.run(d.A, d.W, d.scales, d.zp, d.y, M=M, bias=d.bias)
+    torch.cuda.synchronize()
+    assert plan.device_status() == bsgemv.OK
+    return bsgemv.y_bits(d.y)
+
+
+BIAS_CASES = [("int4", "f16", 32, True), ("int4", "bf16", 16, False), ("int8", "f16", 128, True),
+              ("int8", "bf16", 32, False), ("fp8", "f16", 128, False), ("fp8", "bf16", 128, False),
+              ("nvfp4", "f16", 16, False), ("nvfp4", "bf16", 16, False)]
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", BIAS_CASES)
+def test_bias_epilogue_parity_and_rows_across_M(torch_cuda, fmt, act, bs, zp):
+    """y = A . deq(W)^T + bias through bsgemv_run_bias: within the bound of the oracle (which adds
+    the bias before its one rounding) over ragged tiles and stages, rows bit-identical across M."""
+    case = synth.make_case(fmt, act, bs, zp, 357, 1536, 16, 5 * bs + 1).with_bias()
+    with bsgemv.Plan(fmt, act, bs, zp, case.N, case.K, 16) as plan:
+        y16 = run_bias(case, plan)
+        for M in (1, 8, 9):
+            assert np.array_equal(run_bias(case, plan, M), y16[:M]), f"M={M}"
+    assert_parity(case, y16)
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", BIAS_CASES[::2])
+def test_bias_with_zero_activations_is_the_bias(torch_cuda, fmt, act, bs, zp):
+    """With A = 0 every product is zero: y must equal the bias exactly."""
+    import dataclasses
+    case = synth.make_case(fmt, act, bs, zp, 200, 1024, 3, 41).with_bias()
+    case = dataclasses.replace(case, A=np.zeros_like(case.A))
+    with bsgemv.Plan(fmt, act, bs, zp, case.N, case.K, 4) as plan:
+        y = run_bias(case, plan)
+    want = oracle.act_values(case.bias, act)
+    assert np.array_equal(oracle.act_values(y, act), np.broadcast_to(want, y.shape))
+
+
+@pytest.mark.parametrize("how", ["stream_k", "cluster", "cuda_core"])
+def test_bias_under_every_split_and_variant(torch_cuda, how):
+    case = synth.make_case("int4", "f16", 32, True, 700, 4096, 5, 77).with_bias(sigma=10.0)
+    with bsgemv.Plan("int4", "f16", 32, True, case.N, case.K, 8) as plan:
+        if how == "stream_k":
+            assert plan.set_override(ctas=37) == bsgemv.OK
+        elif how == "cluster":
+            assert plan.set_split("cluster", 4) == bsgemv.OK
+        else:
+            assert plan.set_override(variant=bsgemv.VARIANTS["cuda_core"]) == bsgemv.OK
+        y = run_bias(case, plan)
+        d = bsgemv.upload(case, "cuda")
+        odd = d.bias.data_ptr() + 1  # an odd byte address: not a 16-bit element boundary
+        assert plan.run_status(d.A, d.W, d.scales, d.zp, d.y, bias=odd) == bsgemv.ERR_MISALIGNED
+    assert_parity(case, y)
