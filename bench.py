@@ -62,6 +62,10 @@ def parse_args():
     # one configuration shape by name (see synth.config_shapes), isolated cold calls: for
     # capturing one launch of one kernel under a profiler
     ap.add_argument("--one", default=None, help=argparse.SUPPRESS)
+    # --sweep: let each plan measure its candidate geometries first (bsgemv_plan_autotune)
+    ap.add_argument("--autotune", action="store_true", help=argparse.SUPPRESS)
+    # --sweep: these M values instead of the configuration's (e.g. 17,24,32)
+    ap.add_argument("--Ms", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--calls", type=int, default=5, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -447,7 +451,8 @@ def run_sweep(args):
     cfgs = [args.config] if args.config != WORKLOAD_CONFIG or "--config" in sys.argv else [1, 2, 3, 4, 5]
     for c in cfgs:
         for shape in synth.config_shapes(c):
-            case = shape.case(max(shape.Ms))
+            Ms = tuple(int(x) for x in args.Ms.split(",")) if args.Ms else shape.Ms
+            case = shape.case(max(Ms))
             foot = case.algorithmic_bytes(1)
             copies = max(1, min(8, -(-3 * l2 // foot)))
             bufs = [bsgemv.upload(case, "cuda") for _ in range(copies)]
@@ -455,16 +460,19 @@ def run_sweep(args):
             plans = {}
 
             def plan_for(M):
-                pm = min(max(shape.Ms), 8) if M <= 8 else max(shape.Ms)
+                pm = min(max(Ms), 8) if M <= 8 else max(Ms)
                 if pm not in plans:
                     plans[pm] = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp,
                                             case.N, case.K, pm)
                     if args.variant != "auto":
                         assert plans[pm].set_override(variant=bsgemv.VARIANTS[args.variant]) == bsgemv.OK
+                    if args.autotune:
+                        b = bufs[0]
+                        plans[pm].autotune(b.A[:pm], b.W, b.scales, b.zp, b.y[:pm], M=pm, reps=10)
                 return plans[pm]
 
             try:
-                for M in shape.Ms:
+                for M in Ms:
                     if args.variant == "cuda_core" and M > 8:
                         continue
                     plan = plan_for(M)
@@ -510,7 +518,9 @@ def run_sweep(args):
                         "frac_streamed": round(nbytes / streamed / 1e3 / peak, 4),
                         "frac_isolated": round(nbytes / iso / 1e3 / peak, 4),
                         "weight_copies": copies, "plan_max_M": plan.max_M,
-                        "variant": "cuda_core" if plan.describe()["variant"] == 2 else "mma"}),
+                        "variant": "cuda_core" if plan.describe()["variant"] == 2 else "mma",
+                        "autotuned": bool(args.autotune),
+                        "geometry": {k: plan.describe()[k] for k in ("ctas", "cluster", "stages")}}),
                           flush=True)
                     del g
             finally:

@@ -1,6 +1,6 @@
 """block_scaled_bit_gb300 -- fused dequantize-and-multiply small-M GEMV for one GB300 (sm_103a).
 
-    y[M, N] = A[M, K] . deq(W)[N, K]^T,   M = 1..16
+    y[M, N] = A[M, K] . deq(W)[N, K]^T,   M = 1..32
 
 The compute path is the C-ABI CUDA library ``libbsgemv.so`` (declared in ``include/bsgemv.h``);
 ``block_scaled_bit_gb300.bsgemv`` is a thin ctypes binding to it (argument marshalling only) and

@@ -31,7 +31,8 @@ ERR_SCRATCH_LIMIT = -8
 EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_bias", "bsgemv_run_host", "bsgemv_destroy",
            "bsgemv_status_string", "bsgemv_debug_dequant", "bsgemv_plan_set_override",
            "bsgemv_plan_describe", "bsgemv_geometry_for", "bsgemv_device_status",
-           "bsgemv_run_noalloc", "bsgemv_plan_set_split", "bsgemv_version")
+           "bsgemv_run_noalloc", "bsgemv_plan_set_split", "bsgemv_plan_autotune",
+           "bsgemv_version")
 
 
 class Geometry(ctypes.Structure):
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         L.bsgemv_debug_dequant.argtypes = [vp, vp, vp, vp, vp, vp]
         L.bsgemv_plan_set_override.argtypes = [vp, ci, ci, ci, ci]
         L.bsgemv_plan_set_split.argtypes = [vp, ci, ci]
+        L.bsgemv_plan_autotune.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, vp]
         L.bsgemv_plan_describe.argtypes = [vp, ctypes.POINTER(Geometry)]
         L.bsgemv_geometry_for.argtypes = [ci, ci, ci, i64, i64, ci, ci, ctypes.POINTER(Geometry)]
         L.bsgemv_device_status.argtypes = [vp, vp]
@@ -200,6 +202,19 @@ class Plan:
     def set_split(self, split: str = "auto", cluster: int = 0) -> int:
         """K split of the tiles: "auto", "stream_k" or "cluster" (cluster = CTAs per tile)."""
         return lib().bsgemv_plan_set_split(self._h, SPLITS[split], cluster)
+
+    def autotune_status(self, A, W, scales, zp, y, M: int | None = None, reps: int = 4,
+                        stream=None) -> int:
+        """Time the plan's candidate geometries on the device (back-to-back calls over weight
+        copies that keep L2 cold) and keep the fastest; returns the library status."""
+        M = A.shape[0] if M is None and hasattr(A, "shape") else M
+        return lib().bsgemv_plan_autotune(self._h, _ptr(A), _ptr(W), _ptr(scales), _ptr(zp),
+                                          _ptr(y), int(M), int(reps), _stream(stream))
+
+    def autotune(self, A, W, scales, zp, y, M: int | None = None, reps: int = 4,
+                 stream=None) -> dict:
+        _check(self.autotune_status(A, W, scales, zp, y, M, reps, stream), "bsgemv_plan_autotune")
+        return self.describe()
 
     def describe(self) -> dict:
         g = Geometry()

@@ -7,10 +7,12 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "bsgemv_internal.h"
 
@@ -334,6 +336,132 @@ int bsgemv_plan_set_split(bsgemv_plan_t plan, int split, int cluster_size) {
     rebuild_geometry(plan);
   }
   return rc;
+}
+
+int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const void* scales,
+                         const void* zp, void* y, int M, int reps, void* stream) {
+  int rc = validate_run(plan, A, W, scales, zp, y, M);
+  if (rc != BSGEMV_OK) return rc;
+  if (reps < 1 || reps > 100) return BSGEMV_ERR_INVALID_ARG;
+  rc = check_device(plan);
+  if (rc != BSGEMV_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return BSGEMV_ERR_CUDA;
+  }
+  const bsg::Geometry& g = plan->geo;
+
+  // Candidates: the plan's automatic choice first, stream-K over the default grid and over
+  // 1 .. 4 CTAs per SM, and a thread-block cluster of each size 2 .. 8 per tile.  Candidates the
+  // plan cannot run (a cluster that does not fit) are skipped, and so are repeats of a geometry
+  // already measured.
+  struct Cand {
+    int split, cluster, ctas;
+  };
+  std::vector<Cand> cands = {{BSGEMV_SPLIT_AUTO, 0, 0}, {BSGEMV_SPLIT_STREAM_K, 0, 0}};
+  for (int k = 1; k <= 4; ++k) cands.push_back({BSGEMV_SPLIT_STREAM_K, 0, k * plan->sm_count});
+  for (int c = 2; c <= bsg::kMaxAutoCluster; ++c) cands.push_back({BSGEMV_SPLIT_CLUSTER, c, 0});
+
+  // The regime the calls run in: back to back on one stream, each on weights that are not in L2.
+  // The caller's weight, scales and zero points are copied R - 1 times (R copies >= 3x the L2,
+  // at most 8); a CUDA graph of reps rounds over the R copies is timed per candidate.
+  int l2 = 0;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, plan->device) != cudaSuccess) {
+    cudaGetLastError();
+    return BSGEMV_ERR_CUDA;
+  }
+  const bool int_zp = (g.fmt == bsg::kInt4 || g.fmt == bsg::kInt8) && g.has_zp;
+  const size_t w_bytes = static_cast<size_t>(g.N) * ((g.fmt == bsg::kInt4 || g.fmt == bsg::kNvfp4) ? g.K / 2 : g.K);
+  const size_t s_bytes = static_cast<size_t>(g.N) * g.scale_pitch;
+  const size_t z_bytes = int_zp ? static_cast<size_t>(g.N) * g.zp_pitch : 0;
+  auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t copy_bytes = up(w_bytes) + up(s_bytes) + up(z_bytes);
+  const int R = static_cast<int>(std::min<size_t>(8, std::max<size_t>(1, (3 * static_cast<size_t>(l2) + copy_bytes - 1) / copy_bytes)));
+  struct Ops {
+    const void *W, *s, *z;
+  };
+  std::vector<Ops> ops(R, Ops{W, scales, zp});
+  void* pool = nullptr;
+  cudaStream_t ts = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  bool ok = cudaStreamCreateWithFlags(&ts, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess &&
+            (R == 1 || cudaMalloc(&pool, copy_bytes * (R - 1)) == cudaSuccess);
+  for (int r = 1; ok && r < R; ++r) {
+    char* base = static_cast<char*>(pool) + copy_bytes * (r - 1);
+    ops[r].W = base;
+    ops[r].s = base + up(w_bytes);
+    ops[r].z = int_zp ? base + up(w_bytes) + up(s_bytes) : zp;  // NVFP4: the global scale
+    ok = cudaMemcpyAsync(base, W, w_bytes, cudaMemcpyDeviceToDevice, ts) == cudaSuccess &&
+         cudaMemcpyAsync(base + up(w_bytes), scales, s_bytes, cudaMemcpyDeviceToDevice, ts) == cudaSuccess &&
+         (!int_zp || cudaMemcpyAsync(base + up(w_bytes) + up(s_bytes), zp, z_bytes,
+                                     cudaMemcpyDeviceToDevice, ts) == cudaSuccess);
+  }
+  if (ok) ok = cudaStreamSynchronize(ts) == cudaSuccess;
+  rc = ok ? BSGEMV_OK : BSGEMV_ERR_CUDA;
+
+  const int keep_split = plan->split, keep_cluster = plan->cluster, keep_ctas = plan->ctas_override;
+  float best_us = -1.f;
+  Cand best = {keep_split, keep_cluster, keep_ctas};
+  std::vector<std::pair<int, int>> seen;  // (cluster, ctas) of the geometries measured
+  const int calls = R * reps;
+  for (size_t ci = 0; rc == BSGEMV_OK && ci < cands.size(); ++ci) {
+    const Cand& c = cands[ci];
+    plan->split = c.split;
+    plan->cluster = c.cluster;
+    plan->ctas_override = c.ctas;
+    if (rebuild_geometry(plan) != BSGEMV_OK) continue;  // this candidate does not fit
+    const std::pair<int, int> key{plan->geo.pub.cluster, plan->geo.pub.ctas};
+    if (std::find(seen.begin(), seen.end(), key) != seen.end()) continue;
+    seen.push_back(key);
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    if (cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      rc = BSGEMV_ERR_CUDA;
+      break;
+    }
+    for (int i = 0; i < calls && rc == BSGEMV_OK; ++i) {
+      const Ops& o = ops[i % R];
+      rc = prepare_params(plan, A, o.W, o.s, o.z, y, M);
+      if (rc == BSGEMV_OK) rc = launch(plan, ts);
+    }
+    const bool captured = cudaStreamEndCapture(ts, &graph) == cudaSuccess;
+    if (rc == BSGEMV_OK && !captured) rc = BSGEMV_ERR_CUDA;
+    if (rc == BSGEMV_OK && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) rc = BSGEMV_ERR_CUDA;
+    float ms = 0.f;
+    if (rc == BSGEMV_OK &&
+        (cudaGraphLaunch(exec, ts) != cudaSuccess ||  // warm-up
+         cudaEventRecord(e0, ts) != cudaSuccess || cudaGraphLaunch(exec, ts) != cudaSuccess ||
+         cudaGraphLaunch(exec, ts) != cudaSuccess || cudaEventRecord(e1, ts) != cudaSuccess ||
+         cudaEventSynchronize(e1) != cudaSuccess || cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess))
+      rc = BSGEMV_ERR_CUDA;
+    if (exec) cudaGraphExecDestroy(exec);
+    if (graph) cudaGraphDestroy(graph);
+    if (rc != BSGEMV_OK) break;
+    const float us = ms * 1000.f / (2.f * calls);
+    // another geometry must beat the automatic choice (measured first) by more than 1 %
+    if (best_us < 0.f || us < 0.99f * best_us) {
+      best_us = us;
+      best = c;
+    }
+  }
+  if (rc != BSGEMV_OK) cudaGetLastError();
+  if (ts) {
+    cudaStreamSynchronize(ts);
+    cudaStreamDestroy(ts);
+  }
+  if (pool) cudaFree(pool);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  // the fastest candidate (or, after an error, the settings the plan had)
+  if (rc != BSGEMV_OK || best_us < 0.f) best = {keep_split, keep_cluster, keep_ctas};
+  plan->split = best.split;
+  plan->cluster = best.cluster;
+  plan->ctas_override = best.ctas;
+  const int rc2 = rebuild_geometry(plan);
+  if (rc != BSGEMV_OK) return rc;
+  if (best_us < 0.f) return BSGEMV_ERR_UNSUPPORTED;
+  return rc2;
 }
 
 int bsgemv_plan_describe(bsgemv_plan_t plan, bsgemv_geometry* g) {

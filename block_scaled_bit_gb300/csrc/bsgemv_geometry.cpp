@@ -6,7 +6,8 @@
 //
 // Choices (the reasons are measurements on GB300; see the design notes):
 //   * 64 output columns per CTA tile, 4 consumer warps (one 16-row group each, over a whole
-//     stage) + 1 copy warp, 4 CTAs per SM (3 when max_M > 8: more accumulator registers);
+//     stage) + 1 copy warp, 4 CTAs per SM (3 when max_M > 8, 2 when max_M > 16: more
+//     accumulator registers);
 //   * a ring of up to 12 stages of 256 k (128 or 256 weight bytes per row, plus the stage's
 //     activations), as
 //     deep as the shared-memory share of a CTA allows, so that every SM keeps
@@ -45,7 +46,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   const int fmt = format & 0xFF;
   if (fmt < kInt4 || fmt > kNvfp4) return BSGEMV_ERR_INVALID_ARG;
   if (has_zp != 0 && has_zp != 1) return BSGEMV_ERR_INVALID_ARG;
-  if (N < 1 || K < 1 || max_M < 1 || max_M > 16 || sm_count < 1 || block_size < 1)
+  if (N < 1 || K < 1 || max_M < 1 || max_M > kMaxM || sm_count < 1 || block_size < 1)
     return BSGEMV_ERR_INVALID_ARG;
   if (ctas_override < 0 || stages_override < 0 || stages_override > kMaxStages)
     return BSGEMV_ERR_INVALID_ARG;
@@ -79,7 +80,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   g->kpc = four ? 32 : 16;
   g->kc = kStageK;
   g->stage_bytes = stage_bytes(fmt);
-  g->mt_max = max_M <= 8 ? 1 : 2;
+  g->mt_max = mt_for_m(max_M);
   g->scale_es = (fmt == kFp8) ? 4 : (fmt == kNvfp4 ? 1 : 2);
   g->nb_s = static_cast<int>(K / block_size);
   g->scale_pitch = g->nb_s * g->scale_es;
@@ -133,7 +134,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   // leader's reduction buffer leaves room for a ring of two stages.
   // Reduction buffer: per CTA of the cluster and consumer warp, the fragment lanes that hold
   // output columns below max_M (quad lanes t < red_tq) of each n8 tile.
-  g->red_tq = (g->mt_max == 2) ? 4 : static_cast<int>(std::min<int64_t>(4, ceil_div(max_M, 2)));
+  g->red_tq = (g->mt_max >= 2) ? 4 : static_cast<int>(std::min<int64_t>(4, ceil_div(max_M, 2)));
   const int red_warp = g->mt_max * 8 * g->red_tq * 16;
   auto red_for = [&](int c) { return c >= 2 ? c * kConsumerWarps * red_warp : 0; };
   // Cluster split with an even share per CTA: the ring needs no more stages than the share, and
@@ -171,11 +172,18 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
     // (a CTA-count override describes a stream-K grid: it implies stream-K)
     const int64_t sk = ceil_div(total, std::min<int64_t>(total, slots));  // stream-K stages/CTA
     int64_t best = -1;
-    for (int c = 1; cluster_fits(c); ++c) {
+    for (int c = 1; c <= kMaxCluster; ++c) {
+      // (a size that does not fit does not end the search: a larger one can still fit, as a
+      // share that lies inside one side box needs a single side slot)
+      if (!cluster_fits(c)) continue;
       // automatic: clusters of at most 8 CTAs splitting the tile evenly (measured on GB300:
       // 16-CTA clusters and uneven shares were slower than stream-K)
       if (split == BSGEMV_SPLIT_AUTO && (c > kMaxAutoCluster || spt % c != 0)) continue;
       const int64_t st = ceil_div(spt, c);
+      // automatic: a one-stage share only while the grid stays within half the resident slots
+      // (measured on GB300: FP8 4096 x 2048, 512 CTAs of one stage each, 8-17 % slower than 256
+      // of two; FP8 512 x 2048 and NVFP4 2048 x 2048, 64 and 256 CTAs, fastest at one stage)
+      if (split == BSGEMV_SPLIT_AUTO && st == 1 && tiles * c > slots / 2) continue;
       if (best < 0 || st < best) {
         best = st;
         C = c;

@@ -106,8 +106,8 @@ int launch_fmt_cc(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaSt
   return launch_fmt_cc_cols<FMT, BF16, 8>(p, zp, cpb, ctas, smem, s);
 }
 
-// Dispatch over the n8 tile count, zero points and chunks per scale block (block_mode) for one
-// format / activation type.
+// Dispatch over the n8 tile count (1, 2 or 4; 0: int4 with permuted activations), zero points
+// and chunks per scale block (block_mode) for one format / activation type.
 template <int FMT, bool BF16>
 int launch_fmt(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
 #define BSG_L(MTV, ZPV, C) return launch_one<FMT, BF16, MTV, ZPV, C>(p, ctas, smem, s)
@@ -139,28 +139,28 @@ int launch_fmt(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem, c
 #undef BSG_LPA
     }
     if (mt == 1) { BSG_CPB(1); }
-    BSG_CPB(2);
+    if (mt == 2) { BSG_CPB(2); }
+    BSG_CPB(4);
   } else if constexpr (FMT == kInt8) {  // 8-bit chunks hold 16 k: no block is smaller
-    if (mt == 1) {
-      switch (cpb) {
-        case 1: BSG_ZP(1, 1);
-        case 2: BSG_ZP(1, 2);
-        case 4: BSG_ZP(1, 4);
-        default: BSG_ZP(1, 8);
-      }
-    }
-    switch (cpb) {
-      case 1: BSG_ZP(2, 1);
-      case 2: BSG_ZP(2, 2);
-      case 4: BSG_ZP(2, 4);
-      default: BSG_ZP(2, 8);
-    }
+#define BSG_CPB8(MTV)         \
+  switch (cpb) {              \
+    case 1: BSG_ZP(MTV, 1);   \
+    case 2: BSG_ZP(MTV, 2);   \
+    case 4: BSG_ZP(MTV, 4);   \
+    default: BSG_ZP(MTV, 8);  \
+  }
+    if (mt == 1) { BSG_CPB8(1); }
+    if (mt == 2) { BSG_CPB8(2); }
+    BSG_CPB8(4);
+#undef BSG_CPB8
   } else if constexpr (FMT == kFp8) {  // one 128-k block per stage
     if (mt == 1) BSG_L(1, false, 8);
-    BSG_L(2, false, 8);
+    if (mt == 2) BSG_L(2, false, 8);
+    BSG_L(4, false, 8);
   } else {  // NVFP4 folds its scales
     if (mt == 1) BSG_L(1, false, 1);
-    BSG_L(2, false, 1);
+    if (mt == 2) BSG_L(2, false, 1);
+    BSG_L(4, false, 1);
   }
 #undef BSG_CPB
 #undef BSG_ZP

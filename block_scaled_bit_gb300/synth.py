@@ -29,7 +29,7 @@ import dataclasses
 
 import numpy as np
 
-MAX_M = 16
+MAX_M = 32  # activation rows drawn per case; row m is the same for every M
 
 
 @dataclasses.dataclass
@@ -103,7 +103,7 @@ def to_e4m3_codes(x: np.ndarray) -> np.ndarray:
 def activations(seed: int, M: int, K: int, act: str) -> np.ndarray:
     """A ~ N(0, 1) rounded to the activation dtype; row m is independent of M."""
     if not 1 <= M <= MAX_M:
-        raise ValueError("M must be in 1..16")
+        raise ValueError(f"M must be in 1..{MAX_M}")
     rng = np.random.Generator(np.random.PCG64([seed, 0xA11CE]))
     x = rng.standard_normal((MAX_M, K))[:M]
     return to_f16_bits(x) if act == "f16" else to_bf16_bits(x)

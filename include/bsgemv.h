@@ -2,7 +2,7 @@
  * bsgemv.h -- C ABI of the fused dequantize-and-multiply small-M GEMV for one NVIDIA GB300
  * (sm_103a):
  *
- *     y[M, N] = A[M, K] . deq(W)[N, K]^T,        1 <= M <= 16
+ *     y[M, N] = A[M, K] . deq(W)[N, K]^T,        1 <= M <= 32
  *
  * A is fp16 or bf16.  W is block-quantised along K and stored in the [N, blocks, blob] layout
  * ("[CUDA] Batched small-M GEMV for MatMulNBits (4-bit/8-bit)", Description), in one of:
@@ -116,7 +116,9 @@ enum bsgemv_split {
  * Create a plan for one weight shape.  format = enum bsgemv_format, optionally | BSGEMV_ACT_BF16.
  * block_size: int4/int8 one of 16, 32, 64, 128, 256; fp8 128; nvfp4 16.
  * has_zp: 0 or 1 (int formats only; must be 0 for fp8 and nvfp4).
- * N >= 1 (any tail); K >= 64 with K % 64 == 0 and K % block_size == 0; 1 <= max_M <= 16.
+ * N >= 1 (any tail); K >= 64 with K % 64 == 0 and K % block_size == 0; 1 <= max_M <= 32 (the
+ * pages' decode GEMVs take M <= 16; plans with max_M > 16 run four n8 activation tiles at 2 CTAs
+ * per SM).
  * Uses the current CUDA device, which must be sm_103 (GB300).  Allocates the plan's own device
  * workspace (cross-CTA partial sums, arrival counters and an error word, all zeroed here) with
  * cudaMalloc; every call reuses it and the kernels leave the counters at zero.
@@ -192,6 +194,24 @@ int bsgemv_plan_set_split(bsgemv_plan_t plan, int split, int cluster_size);
 int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows_per_tile,
                              int stages);
 
+/*
+ * Measure this plan's candidate geometries on the device and keep the fastest (the "online
+ * profiler" that "[CUDA] Batched small-M GEMV for MatMulNBits (4-bit/8-bit)", review, proposes
+ * instead of thresholds tuned on one GPU).  Candidates: the automatic choice, stream-K over the
+ * default grid and over 1 .. 4 CTAs per SM, and thread-block clusters of 2 .. 8 CTAs per tile
+ * (those that fit).  They are timed in the regime the calls run in: back to back on one stream
+ * (a CUDA graph of `reps` (1 .. 100) rounds over R copies of W, scales and zp, R copies >= 3x
+ * the L2, at most 8, so that no call finds its weights in L2), with the caller's A and y (y is
+ * overwritten).  The copies, a private stream and the graphs are made and freed here.  Another
+ * geometry replaces the automatic choice only if it is more than 1 % faster.
+ * Synchronises `stream` first and returns when done; not for use inside stream capture.
+ * Afterwards every call of the plan runs the chosen geometry, so rows stay bit-identical across
+ * M from then on (results may differ in the last bits from calls made before, as the
+ * summation order can change).  On an error the plan keeps its previous settings.
+ */
+int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const void* scales,
+                         const void* zp, void* y, int M, int reps, void* stream);
+
 /* Copy the plan's current geometry into *g. */
 int bsgemv_plan_describe(bsgemv_plan_t plan, bsgemv_geometry* g);
 
@@ -219,7 +239,8 @@ int bsgemv_device_status(bsgemv_plan_t plan, void* stream);
  * Arguments as bsgemv_plan plus bsgemv_run, with max_M = M; no plan is created.  Instead of a
  * plan's cudaMalloc'd workspace the cross-CTA reduction uses one fixed scratch area compiled into
  * the library (a file-scope device array of about 5.2 MiB that every GPU loading the library
- * holds until the process exits).  Limits: N <= 524288 output columns and at most 640
+ * holds until the process exits).  Limits: M <= 16 (BSGEMV_ERR_INVALID_ARG beyond), N <= 524288
+ * output columns and at most 640
  * persistent CTAs (a 152-SM GB300 uses 608); beyond them the call returns
  * BSGEMV_ERR_SCRATCH_LIMIT and does nothing.  The first call on a device looks up the scratch
  * area's device address (with that device current); make that first call before any stream

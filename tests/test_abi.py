@@ -44,7 +44,7 @@ def test_status_strings(L):
 @pytest.mark.parametrize("args,code", [
     (("int4", "f16", 32, True, 0, 512, 1), bsgemv.ERR_INVALID_ARG),      # N = 0
     (("int4", "f16", 32, True, 64, 512, 0), bsgemv.ERR_INVALID_ARG),     # max_M = 0
-    (("int4", "f16", 32, True, 64, 512, 17), bsgemv.ERR_INVALID_ARG),    # max_M > 16
+    (("int4", "f16", 32, True, 64, 512, 33), bsgemv.ERR_INVALID_ARG),    # max_M > 32
     (("int4", "f16", 48, True, 64, 512, 1), bsgemv.ERR_UNSUPPORTED),     # block size
     (("int4", "f16", 32, True, 64, 544, 1), bsgemv.ERR_UNSUPPORTED),     # K % 64
     (("fp8", "f16", 64, False, 64, 512, 1), bsgemv.ERR_UNSUPPORTED),     # fp8 needs 128
@@ -89,7 +89,7 @@ SHAPES = [("int4", 32, False, 151936, 4096), ("int8", 128, True, 2048, 4096),
 
 @pytest.mark.parametrize("fmt,bs,zp,N,K", SHAPES)
 @pytest.mark.parametrize("sms", [132, 148, 152])
-@pytest.mark.parametrize("max_M", [1, 8, 16])
+@pytest.mark.parametrize("max_M", [1, 8, 16, 17, 32])
 def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
     g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, sms)
     four = fmt in ("int4", "nvfp4")
@@ -124,11 +124,13 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
 
 def test_summation_order_independent_of_max_M(L):
     """The per-row summation order is fixed by the work split (CTAs, tiles, stages).  It depends
-    on max_M only through the residency class -- 4 CTAs per SM for max_M <= 8, 3 for max_M > 8
-    (more accumulator registers) -- never on M of a call (not an argument), which gives row
-    bit-identity across M within a plan."""
+    on max_M through the residency class -- 4 CTAs per SM for max_M <= 8, 3 for max_M <= 16,
+    2 for max_M <= 32 (more accumulator registers) -- never on M of a call (not an argument),
+    which gives row bit-identity across M within a plan."""
     keys = ("ctas", "tiles", "stages_per_tile", "k_per_stage", "rows_per_tile", "consumer_warps")
     for N, K in ((4096, 4096), (151936, 4096), (300, 2048)):
+        # (plans with max_M > 16 also differ by their activation ring, 32 rows per stage, which
+        # can change the cluster size that fits: the geometry is the plan's, never the call's)
         for group in ((1, 2, 5, 8), (9, 12, 16)):
             ref = bsgemv.geometry_for("int4", "f16", 32, False, N, K, group[0], 152)
             for max_M in group[1:]:
@@ -136,6 +138,7 @@ def test_summation_order_independent_of_max_M(L):
                 assert {k: g[k] for k in keys} == {k: ref[k] for k in keys}
         assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 8, 152)["ctas_per_sm"] == 4
         assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 9, 152)["ctas_per_sm"] == 3
+        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 17, 152)["ctas_per_sm"] == 2
 
 
 def test_stream_k_ranges_cover_every_stage_once():
@@ -211,6 +214,7 @@ def test_shared_memory_layout_is_aligned_for_every_problem(L):
             [("int8", bs, zp) for bs in (16, 32, 64, 128, 256) for zp in (False, True)] +
             [("fp8", 128, False), ("nvfp4", 16, False)])
     for (fmt, bs, zp), N, K, max_M in itertools.product(
-            fmts, (1, 333, 5120, 151936), (256, 2048, 12288), (1, 2, 3, 5, 8, 9, 13, 16)):
+            fmts, (1, 333, 5120, 151936), (256, 2048, 12288),
+            (1, 2, 3, 5, 8, 9, 13, 16, 17, 23, 32)):
         g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, 152)
         assert g["smem_bytes"] % 8 == 0

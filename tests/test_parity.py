@@ -384,3 +384,83 @@ def test_bias_under_every_split_and_variant(torch_cuda, how):
         odd = d.bias.data_ptr() + 1  # an odd byte address: not a 16-bit element boundary
         assert plan.run_status(d.A, d.W, d.scales, d.zp, d.y, bias=odd) == bsgemv.ERR_MISALIGNED
     assert_parity(case, y)
+
+
+# ---------------------------------------------------------------------------- autotune
+@pytest.mark.parametrize("fmt,act,bs,zp,N,K", [("int8", "f16", 128, True, 4096, 4096),
+                                               ("nvfp4", "bf16", 16, False, 2048, 2048),
+                                               ("int4", "f16", 32, False, 12288, 4096),
+                                               ("fp8", "f16", 128, False, 512, 2048)])
+def test_autotune_keeps_a_candidate_and_stays_deterministic(torch_cuda, fmt, act, bs, zp, N, K):
+    """bsgemv_plan_autotune times the candidate geometries and keeps one; the plan then gives
+    results within the bound of the oracle with rows bit-identical across M."""
+    case = synth.make_case(fmt, act, bs, zp, N, K, 8, 99)
+    d = bsgemv.upload(case, "cuda")
+    with bsgemv.Plan(fmt, act, bs, zp, N, K, 8) as plan:
+        sms, per_sm = plan.describe()["sm_count"], plan.describe()["ctas_per_sm"]
+        g = plan.autotune(d.A, d.W, d.scales, d.zp, d.y, M=8, reps=5)
+        assert g["variant"] == bsgemv.VARIANTS["mma"]
+        if g["cluster"] > 0:
+            assert 1 <= g["cluster"] <= 8 and g["ctas"] == g["tiles"] * g["cluster"]
+        else:
+            assert g["ctas"] <= min(g["total_stages"], sms * per_sm)
+        y8 = run(case, plan)
+        for M in (1, 3):
+            assert np.array_equal(run(case.with_M(M), plan), y8[:M]), f"M={M}"
+        assert plan.describe() == g  # running does not change the geometry
+    assert_parity(case, y8)
+
+
+def test_autotune_argument_errors_leave_the_plan_unchanged(torch_cuda):
+    case = synth.make_case("int8", "f16", 32, True, 1000, 2048, 2, 5)
+    d = bsgemv.upload(case, "cuda")
+    with bsgemv.Plan("int8", "f16", 32, True, case.N, case.K, 2) as plan:
+        g0 = plan.describe()
+        assert plan.autotune_status(d.A, d.W, d.scales, d.zp, d.y, M=2, reps=0) == bsgemv.ERR_INVALID_ARG
+        assert plan.autotune_status(d.A, d.W, d.scales, d.zp, d.y, M=3) == bsgemv.ERR_M_TOO_LARGE
+        assert plan.autotune_status(d.A, d.W, d.scales, None, d.y, M=2) == bsgemv.ERR_INVALID_ARG
+        assert plan.describe() == g0
+
+
+# ---------------------------------------------------------------------------- M = 17 .. 32
+WIDE_CASES = [("int4", "f16", 32, True), ("int4", "bf16", 16, False), ("int4", "f16", 128, False),
+              ("int8", "f16", 128, True), ("int8", "bf16", 16, True), ("int8", "f16", 256, False),
+              ("fp8", "f16", 128, False), ("fp8", "bf16", 128, False),
+              ("nvfp4", "f16", 16, False), ("nvfp4", "bf16", 16, False)]
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", WIDE_CASES)
+@pytest.mark.parametrize("M", [17, 24, 32])
+def test_gemv_parity_up_to_32_rows(torch_cuda, fmt, act, bs, zp, M):
+    """Plans with max_M > 16 run four n8 activation tiles (2 CTAs per SM): within the bound over
+    ragged tiles and stages."""
+    K = 1536 if bs <= 128 else 1792
+    case = synth.make_case(fmt, act, bs, zp, 357, K, M, 3 * bs + M)
+    assert_parity(case, run(case, max_M=32))
+
+
+@pytest.mark.parametrize("fmt,act,bs,zp", WIDE_CASES[::3])
+def test_rows_bit_identical_across_M_up_to_32(torch_cuda, fmt, act, bs, zp):
+    case32 = synth.make_case(fmt, act, bs, zp, 300, 2048, 32, 56)
+    with bsgemv.Plan(fmt, act, bs, zp, case32.N, case32.K, 32) as plan:
+        assert plan.describe()["ctas_per_sm"] == 2
+        y32 = run(case32, plan)
+        for M in (1, 2, 3, 8, 9, 16, 17, 31):
+            assert np.array_equal(run(case32.with_M(M), plan), y32[:M]), f"M={M}"
+    assert_parity(case32, y32)
+
+
+@pytest.mark.parametrize("how", ["stream_k", "cluster", "bias"])
+def test_32_rows_under_every_split_and_with_bias(torch_cuda, how):
+    case = synth.make_case("int4", "bf16", 32, True, 700, 4096, 29, 2929)
+    with bsgemv.Plan("int4", "bf16", 32, True, case.N, case.K, 32) as plan:
+        if how == "stream_k":
+            assert plan.set_override(ctas=37) == bsgemv.OK
+            y = run(case, plan)
+        elif how == "cluster":
+            assert plan.set_split("cluster", 4) == bsgemv.OK
+            y = run(case, plan)
+        else:
+            case = case.with_bias()
+            y = run_bias(case, plan)
+    assert_parity(case, y)
