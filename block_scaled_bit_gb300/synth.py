@@ -164,6 +164,18 @@ def make_case(fmt: str, act: str, block_size: int, has_zp: bool, N: int, K: int,
     return Case(fmt, act, block_size, bool(has_zp), N, K, M, A, W, scales, zp, g, seed, name)
 
 
+def dense_operands(act: str, M: int, N: int, K: int, seed: int):
+    """Dense small-N GEMV inputs ("[CUDA] MatMul: add an opt-in split-K GEMV for small-N fp16
+    shapes"): A [M, K] ~ N(0, 1) and B [K, N] ~ N(0, 1/K) (unit-variance outputs), row-major,
+    rounded to the activation dtype; returned as uint16 bit patterns.  Row m of A is the same
+    for every M."""
+    A = activations(seed, M, K, act)
+    rng = np.random.Generator(np.random.PCG64([seed, 0xDE45E]))
+    x = rng.standard_normal((K, N)) / np.sqrt(K)
+    B = to_f16_bits(x) if act == "f16" else to_bf16_bits(x)
+    return A, B
+
+
 # ------------------------------------------------------------------------------------ configs
 @dataclasses.dataclass(frozen=True)
 class Shape:

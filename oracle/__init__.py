@@ -87,6 +87,10 @@ def lib() -> ctypes.CDLL:
                 ctypes.c_long, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_long, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            L.orc_dense_gemv.restype = ctypes.c_int
+            L.orc_dense_gemv.argtypes = [ctypes.c_int, ctypes.c_long, ctypes.c_long, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p]
             L.orc_max_threads.restype = ctypes.c_int
             L.orc_set_threads.restype = None
             L.orc_set_threads.argtypes = [ctypes.c_int]
@@ -174,6 +178,39 @@ def gemv(case, rows=None, M: int | None = None):
     if rc != 0:
         raise ValueError(f"orc_gemv failed ({rc})")
     return ybits, exact, absdot
+
+
+def dense_gemv(A_bits, B_bits, act: str):
+    """Dense oracle GEMV y[M, N] = A[M, K] . B[K, N] (fp16 / bf16 bit patterns, B row-major).
+    Returns (ybits uint16 [M, N], exact float64 [M, N], absdot float64 [M, N])."""
+    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    B = np.ascontiguousarray(B_bits, dtype=np.uint16)
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("A is [M, K] and B is [K, N]")
+    ybits = np.empty((M, N), dtype=np.uint16)
+    exact = np.empty((M, N), dtype=np.float64)
+    absdot = np.empty((M, N), dtype=np.float64)
+    rc = lib().orc_dense_gemv(1 if act == "bf16" else 0, N, K, M, _ptr(A), _ptr(B), _ptr(ybits),
+                              _ptr(exact), _ptr(absdot))
+    if rc != 0:
+        raise ValueError(f"orc_dense_gemv failed ({rc})")
+    return ybits, exact, absdot
+
+
+def dense_tolerance_violations(A_bits, B_bits, act: str, ybits_gpu, rel: float = 1e-3):
+    """The parity bar of tolerance_violations for the dense GEMV."""
+    ref_bits, _, absdot = dense_gemv(A_bits, B_bits, act)
+    y = act_values(np.asarray(ybits_gpu), act)
+    r = act_values(ref_bits, act)
+    bound = ulp(r, act) + rel * absdot
+    finite = np.isfinite(r)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(y - r)
+    bad = np.where(finite, ~(err <= bound), ~((y == r) | (np.isnan(y) & np.isnan(r))))
+    worst = float(np.max(np.where(finite, err / bound, 0.0))) if r.size else 0.0
+    return int(bad.sum()), worst, ref_bits
 
 
 def max_threads() -> int:

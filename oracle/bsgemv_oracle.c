@@ -286,6 +286,35 @@ int orc_gemv(int fmt, int act_bf16, int block_size, int has_zp, long N, long K, 
   return bad ? -1 : 0;
 }
 
+/* ------------------------------------------------------------------------------------------ */
+/* Dense GEMV ("[CUDA] MatMul: add an opt-in split-K GEMV for small-N fp16 shapes",          */
+/* Description): y[m][n] = sum_k A[m,k] * B[k,n] with A [M, K] and B [K, N] row-major fp16     */
+/* (act_bf16 == 0) or bf16 bit patterns; every product is exact in binary64, the sum runs in   */
+/* increasing k, the result is rounded once (RNE) to the same dtype.  absdot as orc_gemv.      */
+/* ------------------------------------------------------------------------------------------ */
+int orc_dense_gemv(int act_bf16, long N, long K, int M, const uint16_t* A, const uint16_t* B,
+                   uint16_t* ybits, double* exact, double* absdot) {
+  if (N < 1 || K < 1 || M < 1) return -1;
+#pragma omp parallel for schedule(static)
+  for (long n = 0; n < N; ++n) {
+    for (int m = 0; m < M; ++m) {
+      double sum = 0.0, asum = 0.0;
+      for (long k = 0; k < K; ++k) {
+        const uint16_t a = A[(long)m * K + k], b = B[k * N + n];
+        const double p = act_bf16 ? orc_bf16_value(a) * orc_bf16_value(b)
+                                  : orc_f16_value(a) * orc_f16_value(b);
+        sum += p;
+        asum += fabs(p);
+      }
+      if (exact) exact[(long)m * N + n] = sum;
+      if (absdot) absdot[(long)m * N + n] = asum;
+      if (ybits) ybits[(long)m * N + n] = (uint16_t)(act_bf16 ? orc_round_bf16(sum)
+                                                              : orc_round_f16(sum));
+    }
+  }
+  return 0;
+}
+
 int orc_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

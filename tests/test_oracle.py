@@ -475,3 +475,65 @@ def test_bias_adds_to_the_exact_sum(orc):
     _, e_b, _ = orc.gemv(case)
     _, e_0, _ = orc.gemv(dataclasses.replace(case, bias=None))
     assert np.array_equal(e_b - e_0, np.broadcast_to(orc.act_values(case.bias, "f16"), e_b.shape))
+
+
+# ------------------------------------------------------------------ the dense small-N GEMV
+def brute_dense(A, B, act, mutate=None):
+    """Exact rational y = A . B ([M, K] x [K, N], row-major bit patterns), rounded by the table
+    search.  `mutate` plants one mistake."""
+    vals, maxc = act_table(act)
+    M, K = A.shape
+    N = B.shape[1]
+    a = [[frac_act(A[m, k], act) for k in range(K)] for m in range(M)]
+    if mutate == "transposed_B":   # B read as if it were stored [N, K]
+        flat = B.reshape(-1)
+        b = [[frac_act(flat[n * K + k], act) for n in range(N)] for k in range(K)]
+    else:
+        b = [[frac_act(B[k, n], act) for n in range(N)] for k in range(K)]
+    row = (lambda m: (m + 1) % M) if mutate == "row_of_A" else (lambda m: m)
+    exact = [[sum((a[row(m)][k] * b[k][n] for k in range(K)), Fraction(0)) for n in range(N)]
+             for m in range(M)]
+    bits = np.array([[table_rne(e, vals, maxc) for e in r] for r in exact], dtype=np.uint16)
+    return bits, exact
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(1, 8, 64), (3, 5, 40), (2, 16, 33)])
+def test_dense_oracle_matches_exact_rational_brute_force(orc, act, M, N, K):
+    A, B = synth.dense_operands(act, M, N, K, seed=M * 100 + N + K)
+    ybits, exact, absdot = orc.dense_gemv(A, B, act)
+    bits, ex = brute_dense(A, B, act)
+    assert np.array_equal(ybits, bits)
+    assert np.allclose(exact, np.array([[float(e) for e in r] for r in ex]), rtol=1e-12, atol=1e-300)
+    assert np.all(absdot >= np.abs(exact))
+
+
+@pytest.mark.parametrize("mutation", ["transposed_B", "row_of_A"])
+def test_dense_brute_force_detects_planted_mistakes(orc, mutation):
+    A, B = synth.dense_operands("f16", 3, 6, 48, seed=5)
+    ybits, _, _ = orc.dense_gemv(A, B, "f16")
+    bad, _ = brute_dense(A, B, "f16", mutate=mutation)
+    assert not np.array_equal(ybits, bad)
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_dense_one_hot_activations_select_a_row_of_B(orc, act):
+    """A = e_k picks row k of B: y[m, :] = B[k_m, :] exactly."""
+    K, N = 96, 24
+    _, B = synth.dense_operands(act, 1, N, K, seed=9)
+    ks = [0, 17, 95]
+    one = synth.to_f16_bits(np.ones(1))[0] if act == "f16" else synth.to_bf16_bits(np.ones(1))[0]
+    A = np.zeros((len(ks), K), dtype=np.uint16)
+    for m, k in enumerate(ks):
+        A[m, k] = one
+    ybits, _, _ = orc.dense_gemv(A, B, act)
+    assert np.array_equal(orc.act_values(ybits, act), orc.act_values(B[ks, :], act))
+
+
+def test_dense_small_integers_are_an_integer_matmul(orc):
+    rng = np.random.default_rng(11)
+    a = rng.integers(-4, 5, size=(4, 64))
+    b = rng.integers(-4, 5, size=(64, 9))
+    ybits, exact, _ = orc.dense_gemv(synth.to_f16_bits(a), synth.to_f16_bits(b), "f16")
+    assert np.array_equal(exact, (a @ b).astype(np.float64))
+    assert np.array_equal(orc.act_values(ybits, "f16"), (a @ b).astype(np.float64))
