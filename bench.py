@@ -34,6 +34,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -66,6 +68,8 @@ def parse_args():
     ap.add_argument("--autotune", action="store_true", help=argparse.SUPPRESS)
     # --sweep: these M values instead of the configuration's (e.g. 17,24,32)
     ap.add_argument("--Ms", default=None, help=argparse.SUPPRESS)
+    # the dense small-N split-K GEMV against cuBLAS (torch.mm), streamed cold
+    ap.add_argument("--dense", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--calls", type=int, default=5, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -567,6 +571,64 @@ def run_one(args):
                       "bytes": case.algorithmic_bytes(M)}), flush=True)
 
 
+DENSE_SHAPES = [(32, 2048), (256, 2048), (512, 2048), (1024, 2048), (1024, 4096), (4096, 4096)]
+
+
+def run_dense_sweep(args):
+    """Dense y[M, N] = A[M, K] . B[K, N] (fp16, B row-major; the split-K GEMV page's shape corner
+    M <= 8, N <= 1024 and one larger N): this library's split-K kernel and cuBLAS (torch.mm), each
+    as a CUDA graph of back-to-back calls over copies of B totalling >= 3x L2 (cold weights)."""
+    import torch
+    from block_scaled_bit_gb300 import bsgemv, synth
+    torch.cuda.set_device(0)
+    peak, _ = hbm_peak()
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    for N, K in DENSE_SHAPES:
+        A_bits, B_bits = synth.dense_operands("f16", 8, N, K, seed=N + K)
+        copies = max(2, min(256, -(-3 * l2 // (2 * N * K))))
+        B0 = torch.from_numpy(B_bits.view(np.int16)).cuda().view(torch.float16)
+        Bs = [B0.clone() for _ in range(copies)]
+        for M in (1, 4, 8):
+            A = torch.from_numpy(np.ascontiguousarray(A_bits[:M]).view(np.int16)).cuda().view(torch.float16)
+            y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+            nbytes = 2 * (N * K + M * K + M * N)
+            res = {}
+            with bsgemv.DensePlan("f16", N, K, 8) as plan:
+                geo = plan.describe()
+                for impl in ("ours", "cublas"):
+                    def call(b):
+                        if impl == "ours":
+                            plan.run(A, b, y, M=M, stream=stream)
+                        else:
+                            torch.mm(A, b, out=y)
+                    with torch.cuda.stream(stream):
+                        for b in Bs[:2]:
+                            call(b)
+                        stream.synchronize()
+                        g = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(g, stream=stream):
+                            for b in Bs:
+                                call(b)
+                        g.replay()
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        for _ in range(5):
+                            g.replay()
+                        e1.record(stream)
+                        e1.synchronize()
+                    res[impl] = e0.elapsed_time(e1) * 1e3 / (5 * copies)
+                    del g
+            print(json.dumps({"dense": True, "N": N, "K": K, "M": M, "bytes": nbytes,
+                              "us_ours": round(res["ours"], 3), "us_cublas": round(res["cublas"], 3),
+                              "frac_ours": round(nbytes / res["ours"] / 1e3 / peak, 4),
+                              "frac_cublas": round(nbytes / res["cublas"] / 1e3 / peak, 4),
+                              "B_copies": copies, "geometry": {k: geo[k] for k in ("ctas", "cluster", "stages")}}),
+                  flush=True)
+        del Bs
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------------------ reference arm
 def run_reference(args):
     """The oracle (CPU, fp64) timed on the host cores on this workload; rank 0 only."""
@@ -620,6 +682,8 @@ def main():
         run_sweep(args)
     elif args.one:
         run_one(args)
+    elif args.dense:
+        run_dense_sweep(args)
     else:
         run_ours(args)
 

@@ -32,6 +32,8 @@ EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_bias", "bsgemv_run_host", "b
            "bsgemv_status_string", "bsgemv_debug_dequant", "bsgemv_plan_set_override",
            "bsgemv_plan_describe", "bsgemv_geometry_for", "bsgemv_device_status",
            "bsgemv_run_noalloc", "bsgemv_plan_set_split", "bsgemv_plan_autotune",
+           "bsgemv_dense_plan", "bsgemv_dense_run", "bsgemv_dense_describe",
+           "bsgemv_dense_geometry_for", "bsgemv_dense_device_status", "bsgemv_dense_destroy",
            "bsgemv_version")
 
 
@@ -81,6 +83,12 @@ def lib() -> ctypes.CDLL:
         L.bsgemv_plan_set_override.argtypes = [vp, ci, ci, ci, ci]
         L.bsgemv_plan_set_split.argtypes = [vp, ci, ci]
         L.bsgemv_plan_autotune.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, vp]
+        L.bsgemv_dense_plan.argtypes = [ctypes.POINTER(vp), ci, i64, i64, ci]
+        L.bsgemv_dense_run.argtypes = [vp, vp, vp, vp, ci, vp]
+        L.bsgemv_dense_describe.argtypes = [vp, ctypes.POINTER(Geometry)]
+        L.bsgemv_dense_geometry_for.argtypes = [ci, i64, i64, ci, ci, ctypes.POINTER(Geometry)]
+        L.bsgemv_dense_device_status.argtypes = [vp, vp]
+        L.bsgemv_dense_destroy.argtypes = [vp]
         L.bsgemv_plan_describe.argtypes = [vp, ctypes.POINTER(Geometry)]
         L.bsgemv_geometry_for.argtypes = [ci, ci, ci, i64, i64, ci, ci, ctypes.POINTER(Geometry)]
         L.bsgemv_device_status.argtypes = [vp, vp]
@@ -223,6 +231,57 @@ class Plan:
 
     def device_status(self, stream=None) -> int:
         return lib().bsgemv_device_status(self._h, _stream(stream))
+
+
+def dense_geometry_for(act: str, N: int, K: int, max_M: int, sm_count: int) -> dict:
+    """The geometry a dense plan would take on a device with `sm_count` SMs (no GPU needed)."""
+    g = Geometry()
+    _check(lib().bsgemv_dense_geometry_for(1 if act == "bf16" else 0, N, K, max_M, sm_count,
+                                           ctypes.byref(g)), "bsgemv_dense_geometry_for")
+    return g.as_dict()
+
+
+class DensePlan:
+    """The dense small-N GEMV y[M, N] = A[M, K] . B[K, N] (B row-major) for M <= max_M <= 8."""
+
+    def __init__(self, act: str, N: int, K: int, max_M: int = 8):
+        self.act, self.N, self.K, self.max_M = act, N, K, max_M
+        h = ctypes.c_void_p()
+        _check(lib().bsgemv_dense_plan(ctypes.byref(h), 1 if act == "bf16" else 0, N, K, max_M),
+               "bsgemv_dense_plan")
+        self._h = h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().bsgemv_dense_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def run_status(self, A, B, y, M: int | None = None, stream=None) -> int:
+        M = A.shape[0] if M is None and hasattr(A, "shape") else M
+        return lib().bsgemv_dense_run(self._h, _ptr(A), _ptr(B), _ptr(y), int(M), _stream(stream))
+
+    def run(self, A, B, y, M: int | None = None, stream=None) -> None:
+        _check(self.run_status(A, B, y, M, stream), "bsgemv_dense_run")
+
+    def describe(self) -> dict:
+        g = Geometry()
+        _check(lib().bsgemv_dense_describe(self._h, ctypes.byref(g)), "bsgemv_dense_describe")
+        return g.as_dict()
+
+    def device_status(self, stream=None) -> int:
+        return lib().bsgemv_dense_device_status(self._h, _stream(stream))
 
 
 def upload(case, device="cuda"):

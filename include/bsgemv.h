@@ -253,6 +253,37 @@ int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_t N, int64_
                        const void* A, const void* W, const void* scales, const void* zp, void* y,
                        int M, void* stream);
 
+/*
+ * Dense small-N GEMV ("[CUDA] MatMul: add an opt-in split-K GEMV for small-N fp16 shapes",
+ * Description): y[M, N] = A[M, K] . B[K, N] with A, B and y fp16 (act_bf16 = 0) or bf16
+ * (act_bf16 = 1), B row-major [K, N] (the MatMul right-hand side), 1 <= M <= max_M <= 8.
+ * K is split over the CTAs of a thread-block cluster per 64-column tile and the partial sums
+ * are added in a fixed order (results are deterministic and rows bit-identical across M).
+ * Requirements: N % 8 == 0 and K % 8 == 0, K >= 16 (TMA row pitches of 16 bytes; the page's
+ * kernel also takes N = 1, here such a B must be padded to 8 columns), A, B, y device memory,
+ * 16-byte aligned.  The plan allocates only an error word.  Same status conventions as above.
+ */
+typedef struct bsgemv_dense_plan_s* bsgemv_dense_plan_t;
+
+int bsgemv_dense_plan(bsgemv_dense_plan_t* out, int act_bf16, int64_t N, int64_t K, int max_M);
+
+/* Enqueue y = A . B for the first M rows of A on `stream` (one kernel; no synchronisation). */
+int bsgemv_dense_run(bsgemv_dense_plan_t plan, const void* A, const void* B, void* y, int M,
+                     void* stream);
+
+/* The plan's geometry: rows_per_tile = 64 columns, k_per_stage = 64, cluster = CTAs per tile. */
+int bsgemv_dense_describe(bsgemv_dense_plan_t plan, bsgemv_geometry* g);
+
+/* Pure host function: the geometry bsgemv_dense_plan would choose with `sm_count` SMs. */
+int bsgemv_dense_geometry_for(int act_bf16, int64_t N, int64_t K, int max_M, int sm_count,
+                              bsgemv_geometry* g);
+
+/* Synchronise `stream`, then read and clear the plan's error word (as bsgemv_device_status). */
+int bsgemv_dense_device_status(bsgemv_dense_plan_t plan, void* stream);
+
+/* Free the plan (synchronises the device first).  NULL is a no-op. */
+int bsgemv_dense_destroy(bsgemv_dense_plan_t plan);
+
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int bsgemv_version(void);
 

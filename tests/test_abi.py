@@ -218,3 +218,38 @@ def test_shared_memory_layout_is_aligned_for_every_problem(L):
             (1, 2, 3, 5, 8, 9, 13, 16, 17, 23, 32)):
         g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, 152)
         assert g["smem_bytes"] % 8 == 0
+
+
+# ---------------------------------------------------------------------------- dense GEMV
+@pytest.mark.parametrize("args,code", [
+    (("f16", 0, 2048, 1), bsgemv.ERR_INVALID_ARG),        # N = 0
+    (("f16", 64, 2048, 9), bsgemv.ERR_INVALID_ARG),       # max_M > 8
+    (("f16", 64, 2048, 0), bsgemv.ERR_INVALID_ARG),       # max_M = 0
+    (("f16", 1, 2048, 1), bsgemv.ERR_UNSUPPORTED),        # N % 8 (TMA pitch of B)
+    (("f16", 64, 2044, 1), bsgemv.ERR_UNSUPPORTED),       # K % 8 (TMA pitch of A)
+    (("bf16", 64, 8, 1), bsgemv.ERR_UNSUPPORTED),         # K < 16
+])
+def test_dense_invalid_problems_rejected_on_host(L, args, code):
+    act, N, K, mm = args
+    with pytest.raises(bsgemv.BsgemvError) as e:
+        bsgemv.dense_geometry_for(act, N, K, mm, 152)
+    assert e.value.status == code
+    with pytest.raises(bsgemv.BsgemvError) as e:
+        bsgemv.DensePlan(act, N, K, mm)
+    assert e.value.status == code
+
+
+@pytest.mark.parametrize("N,K", [(8, 16), (32, 2048), (256, 2048), (1024, 2048), (1000, 4096),
+                                 (4096, 4096), (65536, 512)])
+@pytest.mark.parametrize("sms", [132, 152])
+def test_dense_geometry(L, N, K, sms):
+    g = bsgemv.dense_geometry_for("f16", N, K, 8, sms)
+    assert g["rows_per_tile"] == 64 and g["k_per_stage"] == 64 and g["consumer_warps"] == 4
+    assert g["tiles"] == -(-N // 64) and g["stages_per_tile"] == -(-K // 64)
+    S = g["cluster"]
+    assert 1 <= S <= 8 and S <= g["stages_per_tile"]           # every CTA holds a stage
+    assert g["ctas"] == g["tiles"] * S
+    assert S == 1 or g["ctas"] <= 2 * sms                       # split only to fill the SMs
+    assert 1 <= g["stages"] <= 8 and g["stages"] <= -(-g["stages_per_tile"] // S)
+    assert g["smem_bytes"] <= 232448
+    assert bsgemv.dense_geometry_for("bf16", N, K, 8, sms) == g

@@ -464,3 +464,47 @@ def test_32_rows_under_every_split_and_with_bias(torch_cuda, how):
             case = case.with_bias()
             y = run_bias(case, plan)
     assert_parity(case, y)
+
+
+# ---------------------------------------------------------------------------- dense GEMV
+def run_dense(act, A_bits, B_bits, plan, M=None):
+    import torch
+    M = A_bits.shape[0] if M is None else M
+    dA = torch.from_numpy(np.ascontiguousarray(A_bits[:M]).view(np.int16)).cuda()
+    dB = torch.from_numpy(np.ascontiguousarray(B_bits).view(np.int16)).cuda()
+    y = torch.empty((M, B_bits.shape[1]), dtype=torch.int16, device="cuda")
+    plan.run(dA, dB, y, M=M)
+    torch.cuda.synchronize()
+    assert plan.device_status() == bsgemv.OK
+    return bsgemv.y_bits(y)
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("N,K", [(8, 16), (32, 2048), (1024, 2048), (1000, 1000), (72, 4104),
+                                 (256, 128), (4096, 512)])
+def test_dense_gemv_parity_and_rows_across_M(torch_cuda, act, N, K):
+    """The dense small-N split-K GEMV: within the bound of the oracle for M = 8 (ragged N and K
+    tails, every split the plan chooses), and every row bit-identical for M = 1 .. 7."""
+    A, B = synth.dense_operands(act, 8, N, K, seed=N + K)
+    with bsgemv.DensePlan(act, N, K, 8) as plan:
+        y8 = run_dense(act, A, B, plan)
+        for M in (1, 2, 5, 7):
+            assert np.array_equal(run_dense(act, A, B, plan, M), y8[:M]), f"M={M}"
+        for _ in range(2):  # repeated calls: nothing to reset, same bits
+            assert np.array_equal(run_dense(act, A, B, plan), y8)
+    bad, worst, _ = oracle.dense_tolerance_violations(A, B, act, y8)
+    assert bad == 0, f"{bad} outputs outside the bound (worst {worst:.3g})"
+
+
+def test_dense_errors_on_device(torch_cuda):
+    torch = torch_cuda
+    A, B = synth.dense_operands("f16", 4, 64, 256, seed=3)
+    with bsgemv.DensePlan("f16", 64, 256, 4) as plan:
+        dA = torch.from_numpy(A.view(np.int16)).cuda()
+        dB = torch.from_numpy(B.view(np.int16)).cuda()
+        y = torch.empty((4, 64), dtype=torch.int16, device="cuda")
+        assert plan.run_status(dA, dB, y, M=5) == bsgemv.ERR_M_TOO_LARGE
+        assert plan.run_status(dA, dB, y, M=0) == bsgemv.ERR_INVALID_ARG
+        assert plan.run_status(dA.data_ptr() + 2, dB, y, M=4) == bsgemv.ERR_MISALIGNED
+        assert plan.run_status(dA, None, y, M=4) == bsgemv.ERR_INVALID_ARG
+        assert plan.device_status() == bsgemv.OK
