@@ -70,6 +70,7 @@ def parse_args():
     ap.add_argument("--Ms", default=None, help=argparse.SUPPRESS)
     # the dense small-N split-K GEMV against cuBLAS (torch.mm), streamed cold
     ap.add_argument("--dense", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--dense-shape", default=None, help=argparse.SUPPRESS)  # "N,K": one shape
     ap.add_argument("--calls", type=int, default=5, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -303,7 +304,9 @@ def time_graph(wl, steps, warmup, stream, use_graph=True):
 
 
 def e2e_run(wl, steps, stream):
-    """Through bsgemv_run_host: A copied host->device and y device->host inside every call."""
+    """Through bsgemv_run_host_async: every call copies its A host->device and its y
+    device->host (pinned memory) around the GEMV; a step enqueues its calls and waits for the
+    stream once, when all its results are on the host."""
     import numpy as np
     import torch
     hosts = []
@@ -318,7 +321,8 @@ def e2e_run(wl, steps, stream):
     def step(s):
         for it, (A, y) in zip(wl.items, hosts):
             b = it["bufs"][s % wl.copies]
-            it["plan"].run_host(A, b.W, b.scales, b.zp, y, M=it["M"], stream=stream)
+            it["plan"].run_host_async(A, b.W, b.scales, b.zp, y, M=it["M"], stream=stream)
+        stream.synchronize()
 
     for s in range(3):
         step(s)
@@ -399,7 +403,7 @@ def run_ours(args):
     e2e_dt = max_over_ranks(e2e_dt, world, device)
     e2e = {"value": round(world * e2e_steps * step_bytes / e2e_dt / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "api": "bsgemv_run_host (host A and y, device-resident weights), synchronous per call"}
+           "api": "bsgemv_run_host_async (pinned host A and y copied in and out by every call, device-resident weights), one stream synchronisation per step"}
 
     out = None
     if rank == 0:
@@ -584,12 +588,15 @@ def run_dense_sweep(args):
     peak, _ = hbm_peak()
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    for N, K in DENSE_SHAPES:
+    shapes = DENSE_SHAPES
+    if args.dense_shape:
+        shapes = [tuple(int(x) for x in args.dense_shape.split(","))]
+    for N, K in shapes:
         A_bits, B_bits = synth.dense_operands("f16", 8, N, K, seed=N + K)
         copies = max(2, min(256, -(-3 * l2 // (2 * N * K))))
         B0 = torch.from_numpy(B_bits.view(np.int16)).cuda().view(torch.float16)
         Bs = [B0.clone() for _ in range(copies)]
-        for M in (1, 4, 8):
+        for M in ((args.M,) if args.M else (1, 4, 8)):
             A = torch.from_numpy(np.ascontiguousarray(A_bits[:M]).view(np.int16)).cuda().view(torch.float16)
             y = torch.empty((M, N), dtype=torch.float16, device="cuda")
             nbytes = 2 * (N * K + M * K + M * N)

@@ -28,7 +28,8 @@ ERR_DEVICE_TIMEOUT = -7
 ERR_SCRATCH_LIMIT = -8
 
 # Every extern "C" entry point of include/bsgemv.h.
-EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_bias", "bsgemv_run_host", "bsgemv_destroy",
+EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_bias", "bsgemv_run_host",
+           "bsgemv_run_host_async", "bsgemv_destroy",
            "bsgemv_status_string", "bsgemv_debug_dequant", "bsgemv_plan_set_override",
            "bsgemv_plan_describe", "bsgemv_geometry_for", "bsgemv_device_status",
            "bsgemv_run_noalloc", "bsgemv_plan_set_split", "bsgemv_plan_autotune",
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
         L.bsgemv_run.argtypes = [vp, vp, vp, vp, vp, vp, ci, vp]
         L.bsgemv_run_bias.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, vp]
         L.bsgemv_run_host.argtypes = [vp, vp, vp, vp, vp, vp, ci, vp]
+        L.bsgemv_run_host_async.argtypes = [vp, vp, vp, vp, vp, vp, ci, vp]
         L.bsgemv_destroy.argtypes = [vp]
         L.bsgemv_status_string.argtypes = [ci]
         L.bsgemv_status_string.restype = ctypes.c_char_p
@@ -199,6 +201,14 @@ class Plan:
         M = A_host.shape[0] if M is None else M
         _check(lib().bsgemv_run_host(self._h, _ptr(A_host), _ptr(W), _ptr(scales), _ptr(zp),
                                      _ptr(y_host), int(M), _stream(stream)), "bsgemv_run_host")
+
+    def run_host_async(self, A_host, W, scales, zp, y_host, M: int | None = None,
+                       stream=None) -> None:
+        """As run_host, but only enqueued: y_host is ready after the stream is synchronised."""
+        M = A_host.shape[0] if M is None else M
+        _check(lib().bsgemv_run_host_async(self._h, _ptr(A_host), _ptr(W), _ptr(scales), _ptr(zp),
+                                           _ptr(y_host), int(M), _stream(stream)),
+               "bsgemv_run_host_async")
 
     def debug_dequant(self, W, scales, zp, out, stream=None) -> None:
         _check(lib().bsgemv_debug_dequant(self._h, _ptr(W), _ptr(scales), _ptr(zp), _ptr(out),

@@ -168,7 +168,7 @@ int launch(bsgemv_plan_s* p, cudaStream_t s) { return bsg::launch_gemv(p->geo, p
 
 extern "C" {
 
-int bsgemv_version(void) { return 100; }
+int bsgemv_version(void) { return 200; }
 
 const char* bsgemv_status_string(int status) {
   switch (status) {
@@ -237,8 +237,12 @@ int bsgemv_run_bias(bsgemv_plan_t plan, const void* A, const void* W, const void
   return launch(plan, static_cast<cudaStream_t>(stream));
 }
 
-int bsgemv_run_host(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
-                    const void* zp, void* y_host, int M, void* stream) {
+namespace {
+
+// A host -> device into the plan's staging buffer, the GEMV, y device -> host, all on `stream`;
+// waits for the stream when `sync`.
+int run_host_impl(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
+                  const void* zp, void* y_host, int M, void* stream, bool sync) {
   if (plan == nullptr || A_host == nullptr || y_host == nullptr) return BSGEMV_ERR_INVALID_ARG;
   const bsg::Geometry& g = plan->geo;
   if (M < 1) return BSGEMV_ERR_INVALID_ARG;
@@ -267,7 +271,20 @@ int bsgemv_run_host(bsgemv_plan_t plan, const void* A_host, const void* W, const
   if (rc != BSGEMV_OK) return rc;
   if (cudaMemcpyAsync(y_host, dy, size_t(M) * g.N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return BSGEMV_ERR_CUDA;
+  if (!sync) return BSGEMV_OK;
   return cudaStreamSynchronize(s) == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
+}
+
+}  // namespace
+
+int bsgemv_run_host(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
+                    const void* zp, void* y_host, int M, void* stream) {
+  return run_host_impl(plan, A_host, W, scales, zp, y_host, M, stream, true);
+}
+
+int bsgemv_run_host_async(bsgemv_plan_t plan, const void* A_host, const void* W,
+                          const void* scales, const void* zp, void* y_host, int M, void* stream) {
+  return run_host_impl(plan, A_host, W, scales, zp, y_host, M, stream, false);
 }
 
 int bsgemv_destroy(bsgemv_plan_t plan) {

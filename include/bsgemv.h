@@ -158,6 +158,17 @@ int bsgemv_run_bias(bsgemv_plan_t plan, const void* A, const void* W, const void
 int bsgemv_run_host(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
                     const void* zp, void* y_host, int M, void* stream);
 
+/*
+ * bsgemv_run_host without the final wait: the copy of A in, the GEMV and the copy of y out are
+ * enqueued on `stream` and the call returns.  y_host holds the result once the stream has been
+ * synchronised, and A_host must not change before then.  With pinned host memory the copies are
+ * asynchronous, so a step of several GEMVs costs one synchronisation, not one per GEMV.  Calls
+ * on one plan share its staging buffer: issue them on one stream (stream order keeps each
+ * call's copy of A after the previous call's copy of y).
+ */
+int bsgemv_run_host_async(bsgemv_plan_t plan, const void* A_host, const void* W,
+                          const void* scales, const void* zp, void* y_host, int M, void* stream);
+
 /* Free the plan and its device memory (synchronises the device first).  NULL is a no-op. */
 int bsgemv_destroy(bsgemv_plan_t plan);
 

@@ -216,6 +216,28 @@ def test_run_host_matches_device_run(torch_cuda):
     assert_parity(case, bsgemv.y_bits(d.y))
 
 
+def test_run_host_async_steps_match_device_runs(torch_cuda):
+    """Several calls enqueued through bsgemv_run_host_async on one stream and one plan (sharing
+    its staging buffer), one synchronisation: every host output equals the device run's."""
+    torch = torch_cuda
+    case = synth.make_case("int8", "f16", 32, True, 3000, 2048, 4, 19)
+    d = bsgemv.upload(case, "cuda")
+    stream = torch.cuda.Stream()
+    with bsgemv.Plan("int8", "f16", 32, True, case.N, case.K, 4) as plan:
+        plan.run(d.A, d.W, d.scales, d.zp, d.y)
+        torch.cuda.synchronize()
+        ref = bsgemv.y_bits(d.y)
+        outs = []
+        for M in (4, 1, 3, 4):
+            A_host = torch.from_numpy(np.ascontiguousarray(case.A[:M]).view(np.int16)).pin_memory()
+            y_host = torch.full((M, case.N), -1, dtype=torch.int16).pin_memory()
+            plan.run_host_async(A_host, d.W, d.scales, d.zp, y_host, M=M, stream=stream)
+            outs.append((M, A_host, y_host))
+        stream.synchronize()
+    for M, _, y_host in outs:
+        assert np.array_equal(y_host.numpy().view(np.uint16), ref[:M]), f"M={M}"
+
+
 def test_errors_on_device(torch_cuda):
     torch = torch_cuda
     case = synth.make_case("int4", "f16", 32, True, 128, 512, 4, 3)
