@@ -431,6 +431,9 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
     const std::pair<int, int> key{plan->geo.pub.cluster, plan->geo.pub.ctas};
     if (std::find(seen.begin(), seen.end(), key) != seen.end()) continue;
     seen.push_back(key);
+    // one eager call first: kernel attributes (shared-memory size) are set outside the capture
+    if ((rc = prepare_params(plan, A, W, scales, zp, y, M)) != BSGEMV_OK) break;
+    if ((rc = launch(plan, ts)) != BSGEMV_OK) break;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     if (cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {

@@ -5,9 +5,11 @@
 //   * k is walked in "stages" of kStageK = 256 k: 128 weight bytes per row for the 4-bit formats
 //     (one 128-byte-swizzled TMA box), 256 for the 8-bit formats (two boxes), plus the stage's
 //     activations (cp.async) -- scales and zero points arrive per several stages on a side ring;
-//   * the tiles x stages grid is cut into `ctas` equal contiguous ranges (stream-K); a tile whose
-//     stages fall into several CTAs is finished by the last CTA to arrive, which adds the
-//     partial sums in CTA order (a fixed order, so results are deterministic).
+//   * the tiles x stages grid is cut into `ctas` equal contiguous ranges (stream-K), and a tile
+//     whose stages fall into several CTAs is finished by the last CTA to arrive, which adds the
+//     partial sums in CTA order; or, for shapes with few tiles, each tile's stages are split
+//     evenly over the CTAs of one thread-block cluster and added in rank order in the leader's
+//     shared memory.  Either way the order is fixed, so results are deterministic.
 #pragma once
 
 #include <cuda.h>

@@ -158,14 +158,6 @@ BSG_DEV void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Prefetch one TMA box of a 2D tensor into L2 (no shared memory, no barrier).
-BSG_DEV void tma_prefetch_l2_2d(const CUtensorMap* tm, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tm)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // Programmatic dependent launch: let the next kernel in the stream be scheduled now, and wait
 // until the previous kernel has completed with its memory visible.  Both are no-ops for a
 // launch without the programmatic-serialization attribute.
@@ -211,12 +203,6 @@ BSG_DEV void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
 
-BSG_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
 // ldmatrix at addr + OFF (a compile-time offset in the instruction's immediate field).
 template <int OFF>
 BSG_DEV void ldsm_x4_at(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -241,27 +227,9 @@ BSG_DEV void sts128(uint32_t addr, uint4 v) {
 
 BSG_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-BSG_DEV uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
 BSG_DEV uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-BSG_DEV uint32_t lds16(uint32_t addr) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
-
-BSG_DEV uint32_t lds8(uint32_t addr) {
-  unsigned short v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
   return v;
 }
 
@@ -291,10 +259,6 @@ BSG_DEV uint32_t prmt(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
   return d;
-}
-
-BSG_DEV void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // D += A * B on the tensor cores: m16n8k16, fp16 or bf16 operands, fp32 accumulate.
@@ -332,16 +296,6 @@ BSG_DEV void mma16816_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uin
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
   }
-}
-
-// (acc0, acc1) += (x0, x1) * s, two fp32 FMAs in one packed instruction.
-BSG_DEV void ffma2(float& acc0, float& acc1, float x0, float x1, float s) {
-  uint64_t a, x, ss;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc0), "f"(acc1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x), "l"(ss));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(acc0), "=f"(acc1) : "l"(a));
 }
 
 // Packed fp32 pairs (low word = first element) for the CUDA-core variant's FMAs.
@@ -395,16 +349,6 @@ BSG_DEV uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t d;
   const unsigned short v = static_cast<unsigned short>(two_codes);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
-  return d;
-}
-
-// Two E2M1 codes in one byte (low nibble -> low half) to an exact f16 pair.
-BSG_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t d;
-  const unsigned short v = static_cast<unsigned short>(byte);
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(d)
-      : "h"(v));
   return d;
 }
 
