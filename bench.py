@@ -71,6 +71,8 @@ def parse_args():
     # the dense small-N split-K GEMV against cuBLAS (torch.mm), streamed cold
     ap.add_argument("--dense", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--dense-shape", default=None, help=argparse.SUPPRESS)  # "N,K": one shape
+    # the fused GEMV against cuBLAS on the already dequantised fp16 weight, M = 1 .. 32
+    ap.add_argument("--crossover", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--calls", type=int, default=5, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -696,6 +698,80 @@ def run_dense_sweep(args):
         torch.cuda.empty_cache()
 
 
+CROSSOVER_SHAPES = ["c3_int4_f16_bs32_nozp_N151936_K4096", "c3_int4_f16_bs32_nozp_N12288_K4096",
+                    "c2_int8_f16_bs128_zp_N12288_K4096", "c4_fp8_f16_bs128_nozp_N5120_K17408",
+                    "c5_nvfp4_f16_bs16_nozp_N248320_K2048"]
+
+
+def run_crossover(args):
+    """Where the fused GEMV stops paying: for M = 1 .. 32, the fused dequantise-and-multiply call
+    against a tensor-core GEMM (cuBLAS, torch.mm) on the same weight already dequantised to fp16
+    [N, K] (its dequantisation not counted, which favours cuBLAS).  Both as CUDA graphs of
+    back-to-back calls over weight copies totalling >= 3x L2 (cold weights), same run."""
+    import torch
+    from block_scaled_bit_gb300 import bsgemv, synth
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    shapes = {s.name: s for s in synth.all_shapes()}
+    Ms = tuple(int(x) for x in args.Ms.split(",")) if args.Ms else (1, 4, 8, 16, 24, 32)
+
+    def graph_time(call, copies):
+        with torch.cuda.stream(stream):
+            for c in range(min(2, copies)):
+                call(c)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            reps = max(copies, 8 // copies * copies)
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(reps):
+                    call(r % copies)
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(3):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (3 * reps)
+
+    for name in CROSSOVER_SHAPES:
+        shape = shapes[name]
+        case = shape.case(1)
+        fused_copies = max(1, min(8, -(-3 * l2 // case.algorithmic_bytes(1))))
+        dense_copies = max(1, min(8, -(-3 * l2 // (2 * case.N * case.K))))
+        bufs = [bsgemv.upload(case, "cuda") for _ in range(fused_copies)]
+        with bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K, 1) as p1:
+            deq = torch.empty((case.N, case.K), dtype=torch.float32, device="cuda")
+            p1.debug_dequant(bufs[0].W, bufs[0].scales, bufs[0].zp, deq)
+            torch.cuda.synchronize()
+            w16 = deq.to(torch.float16)
+            del deq
+        Ws = [w16] + [w16.clone() for _ in range(dense_copies - 1)]
+        A32 = torch.randn((32, case.K), generator=torch.Generator().manual_seed(7)).to("cuda", torch.float16)
+        plans = {}
+        for M in Ms:
+            pm = 8 if M <= 8 else 16 if M <= 16 else 32
+            if pm not in plans:
+                plans[pm] = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N,
+                                        case.K, pm)
+            plan = plans[pm]
+            A = A32[:M].contiguous()
+            y = torch.empty((M, case.N), dtype=torch.float16, device="cuda")
+            yt = torch.empty((M, case.N), dtype=torch.float16, device="cuda")
+            t_fused = graph_time(lambda c: plan.run(A, bufs[c].W, bufs[c].scales, bufs[c].zp, y,
+                                                    M=M, stream=stream), fused_copies)
+            t_cublas = graph_time(lambda c: torch.mm(A, Ws[c].t(), out=yt), dense_copies)
+            print(json.dumps({"crossover": True, "shape": name, "M": M,
+                              "us_fused": round(t_fused, 2), "us_cublas_fp16": round(t_cublas, 2),
+                              "fused_over_cublas": round(t_fused / t_cublas, 3),
+                              "plan_max_M": pm}), flush=True)
+        for pl in plans.values():
+            pl.close()
+        del bufs, Ws, w16
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------------------ reference arm
 def run_reference(args):
     """The oracle (CPU, fp64) timed on the host cores on this workload; rank 0 only."""
@@ -751,6 +827,8 @@ def main():
         run_one(args)
     elif args.dense:
         run_dense_sweep(args)
+    elif args.crossover:
+        run_crossover(args)
     else:
         run_ours(args)
 
