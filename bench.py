@@ -751,7 +751,7 @@ def run_crossover(args):
         A32 = torch.randn((32, case.K), generator=torch.Generator().manual_seed(7)).to("cuda", torch.float16)
         plans = {}
         for M in Ms:
-            pm = 8 if M <= 8 else 16 if M <= 16 else 32
+            pm = 8 if M <= 8 else 16 if M <= 16 else 24 if M <= 24 else 32
             if pm not in plans:
                 plans[pm] = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N,
                                         case.K, pm)

@@ -6,7 +6,7 @@
 //
 // Choices (the reasons are measurements on GB300; see the design notes):
 //   * 64 output columns per CTA tile, 4 consumer warps (one 16-row group each, over a whole
-//     stage) + 1 copy warp, 4 CTAs per SM (3 when max_M > 8, 2 when max_M > 16: more
+//     stage) + 1 copy warp, 4 CTAs per SM (3 when max_M > 8, 2 when max_M > 24: more
 //     accumulator registers);
 //   * a ring of up to 12 stages of 256 k (128 or 256 weight bytes per row, plus the stage's
 //     activations), as
@@ -37,9 +37,12 @@ bool is_pow2_block(int bs) {
 }
 }  // namespace
 
-int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
-                     int sm_count, int ctas_override, int stages_override, int split, int cluster,
-                     Geometry* g) {
+namespace {
+
+// The geometry for a kernel of `mt` n8 activation tiles (mt >= mt_for_m(max_M)).
+int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
+                       int sm_count, int ctas_override, int stages_override, int split,
+                       int cluster, int mt, Geometry* g) {
   if (g == nullptr) return BSGEMV_ERR_INVALID_ARG;
   std::memset(g, 0, sizeof(*g));
   if ((format & ~(0xFF | BSGEMV_ACT_BF16)) != 0) return BSGEMV_ERR_INVALID_ARG;
@@ -80,7 +83,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   g->kpc = four ? 32 : 16;
   g->kc = kStageK;
   g->stage_bytes = stage_bytes(fmt);
-  g->mt_max = mt_for_m(max_M);
+  g->mt_max = mt;
   g->scale_es = (fmt == kFp8) ? 4 : (fmt == kNvfp4 ? 1 : 2);
   g->nb_s = static_cast<int>(K / block_size);
   g->scale_pitch = g->nb_s * g->scale_es;
@@ -253,6 +256,30 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   // workspace: partial slots [ctas][2][warps], counters [tiles][warps], error word
   pub.workspace_bytes = int64_t(pub.ctas) * 2 * kConsumerWarps * g->slot_floats * 4 +
                         pub.tiles * kConsumerWarps * 4 + 256;
+  return BSGEMV_OK;
+}
+
+}  // namespace
+
+int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
+                     int sm_count, int ctas_override, int stages_override, int split, int cluster,
+                     Geometry* g) {
+  const int mt = (max_M >= 1 && max_M <= kMaxM) ? mt_for_m(max_M) : 1;
+  int rc = geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, ctas_override,
+                              stages_override, split, cluster, mt, g);
+  if (rc != BSGEMV_OK || mt != 3 || split != BSGEMV_SPLIT_AUTO || ctas_override != 0 ||
+      stages_override != 0)
+    return rc;
+  // Plans for 17..24 rows: three n8 tiles at 3 CTAs per SM, unless that residency's shared
+  // memory (activation ring of 24 rows, reduction buffer) costs the cluster split that four
+  // tiles at 2 CTAs per SM keep, with shares of at most 4 stages (measured on GB300: such small
+  // shapes ran 15-25 % faster at 2 CTAs per SM; larger shapes 13-22 % faster at 3).
+  Geometry four;
+  if (geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, 0, 0, split, 0, 4,
+                         &four) != BSGEMV_OK)
+    return rc;
+  const int C4 = four.pub.cluster, C3 = g->pub.cluster;
+  if (C4 >= 2 && C3 < C4 && (four.pub.stages_per_tile + C4 - 1) / C4 <= 4) *g = four;
   return BSGEMV_OK;
 }
 

@@ -1,11 +1,15 @@
-// Instantiations of the GEMV kernel for int8 weights with fp16 activations (see
-// bsgemv_launch.cuh).
+// Instantiations of the GEMV kernel for int8 weights with fp16 activations, calls with up to 16
+// rows (one or two n8 tiles; see bsgemv_launch.cuh).  Wider calls: bsgemv_int8_f16_wide.cu.
 #include "bsgemv_launch.cuh"
 
 namespace bsg {
 
 int launch_int8_f16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
-  return launch_fmt<kInt8, false>(p, mt, zp, cpb, ctas, smem, s);
+  switch (mt) {
+    case 1: return launch_fmt_mt<kInt8, false, 1>(p, zp, cpb, ctas, smem, s);
+    case 2: return launch_fmt_mt<kInt8, false, 2>(p, zp, cpb, ctas, smem, s);
+    default: return launch_int8_f16_wide(p, mt, zp, cpb, ctas, smem, s);
+  }
 }
 
 }  // namespace bsg

@@ -27,12 +27,12 @@ constexpr int kConsumerWarps = 4;     // decode + mma warps (one 16-row group ea
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxM = 32;             // activation rows per call: up to four n8 mma tiles
 // CTAs per SM the kernels are built for (their register budget): 4 with one n8 activation tile
-// (M <= 8), 3 with two (M <= 16), 2 with four (M <= 32: more accumulator and fragment
-// registers).
-constexpr int ctas_per_sm_for_mt(int mt) { return mt == 1 ? 4 : mt == 2 ? 3 : 2; }
+// (M <= 8), 3 with two or three (M <= 24; 128 registers, no spills), 2 with four (M <= 32: at
+// 128 registers some of them spill).
+constexpr int ctas_per_sm_for_mt(int mt) { return mt == 1 ? 4 : mt <= 3 ? 3 : 2; }
 // n8 activation tiles of the kernel a plan is sized for (and of the kernel a call with M rows
 // runs, apart from the int4 variant with permuted activations).
-constexpr int mt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : 4; }
+constexpr int mt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 24 ? 3 : 4; }
 constexpr int kBoxRowBytes = 128;     // bytes per row of one weight TMA box (128-byte swizzle)
 constexpr int kStageK = 256;          // k per stage for every format: one 128-byte box per row for
                                       // the 4-bit formats, two for the 8-bit formats
@@ -122,6 +122,14 @@ constexpr int kMaxAutoCluster = 8;  // largest cluster the automatic split picks
 // cpb: see block_mode.
 int launch_int4_f16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
                     cudaStream_t s);
+int launch_int4_f16_wide(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                         cudaStream_t s);
+int launch_int4_bf16_wide(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                          cudaStream_t s);
+int launch_int8_f16_wide(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                         cudaStream_t s);
+int launch_int8_bf16_wide(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                          cudaStream_t s);
 int launch_int4_bf16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
                      cudaStream_t s);
 int launch_int8_f16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,

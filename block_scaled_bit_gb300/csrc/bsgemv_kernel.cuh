@@ -3,7 +3,7 @@
 //     y[M, N] = A[M, K] . deq(W)[N, K]^T,  M <= 32
 //
 // Data path per CTA (a persistent grid, 4 CTAs of 160 threads per SM; 3 for plans with M up to
-// 16, 2 for M up to 32):
+// 24, 2 for M up to 32):
 //   warp 0           producer: for every stage (256 k of a 64-row tile) of the CTA's range, lane
 //                    0 waits for a free ring slot and issues the stage's weight box(es)
 //                    [64 rows][128 B] with cp.async.bulk.tensor (128-byte swizzle, L2

@@ -106,63 +106,36 @@ int launch_fmt_cc(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaSt
   return launch_fmt_cc_cols<FMT, BF16, 8>(p, zp, cpb, ctas, smem, s);
 }
 
-// Dispatch over the n8 tile count (1, 2 or 4; 0: int4 with permuted activations), zero points
-// and chunks per scale block (block_mode) for one format / activation type.
-template <int FMT, bool BF16>
-int launch_fmt(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
-#define BSG_L(MTV, ZPV, C) return launch_one<FMT, BF16, MTV, ZPV, C>(p, ctas, smem, s)
-#define BSG_ZP(MTV, C) \
-  if (zp) BSG_L(MTV, true, C); \
-  BSG_L(MTV, false, C)
-#define BSG_CPB(MTV)                   \
-  switch (cpb) {                       \
-    case 0: BSG_ZP(MTV, 0);            \
-    case 1: BSG_ZP(MTV, 1);            \
-    case 2: BSG_ZP(MTV, 2);            \
-    case 4: BSG_ZP(MTV, 4);            \
-    default: BSG_ZP(MTV, 8);           \
-  }
+// Dispatch over zero points and chunks per scale block (block_mode) for one format, activation
+// type and n8 tile count MT (1 .. 4; 0: int4, one tile, activations permuted by the producer).
+template <int FMT, bool BF16, int MT>
+int launch_fmt_mt(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
+  constexpr int kTiles = MT == 0 ? 1 : MT;
+  constexpr bool kPa = MT == 0;
+#define BSG_L(ZPV, C) return launch_one<FMT, BF16, kTiles, ZPV, C, kPa>(p, ctas, smem, s)
+#define BSG_ZP(C) \
+  if (zp) BSG_L(true, C); \
+  BSG_L(false, C)
   if constexpr (FMT == kInt4) {
-    if (mt == 0) {  // one n8 tile, activations permuted by the producer (calls with M <= 2)
-#define BSG_LPA(ZPV, C) return launch_one<FMT, BF16, 1, ZPV, C, true>(p, ctas, smem, s)
-#define BSG_ZPA(C) \
-  if (zp) BSG_LPA(true, C); \
-  BSG_LPA(false, C)
-      switch (cpb) {
-        case 0: BSG_ZPA(0);
-        case 1: BSG_ZPA(1);
-        case 2: BSG_ZPA(2);
-        case 4: BSG_ZPA(4);
-        default: BSG_ZPA(8);
-      }
-#undef BSG_ZPA
-#undef BSG_LPA
+    switch (cpb) {
+      case 0: BSG_ZP(0);
+      case 1: BSG_ZP(1);
+      case 2: BSG_ZP(2);
+      case 4: BSG_ZP(4);
+      default: BSG_ZP(8);
     }
-    if (mt == 1) { BSG_CPB(1); }
-    if (mt == 2) { BSG_CPB(2); }
-    BSG_CPB(4);
   } else if constexpr (FMT == kInt8) {  // 8-bit chunks hold 16 k: no block is smaller
-#define BSG_CPB8(MTV)         \
-  switch (cpb) {              \
-    case 1: BSG_ZP(MTV, 1);   \
-    case 2: BSG_ZP(MTV, 2);   \
-    case 4: BSG_ZP(MTV, 4);   \
-    default: BSG_ZP(MTV, 8);  \
-  }
-    if (mt == 1) { BSG_CPB8(1); }
-    if (mt == 2) { BSG_CPB8(2); }
-    BSG_CPB8(4);
-#undef BSG_CPB8
+    switch (cpb) {
+      case 1: BSG_ZP(1);
+      case 2: BSG_ZP(2);
+      case 4: BSG_ZP(4);
+      default: BSG_ZP(8);
+    }
   } else if constexpr (FMT == kFp8) {  // one 128-k block per stage
-    if (mt == 1) BSG_L(1, false, 8);
-    if (mt == 2) BSG_L(2, false, 8);
-    BSG_L(4, false, 8);
+    BSG_L(false, 8);
   } else {  // NVFP4 folds its scales
-    if (mt == 1) BSG_L(1, false, 1);
-    if (mt == 2) BSG_L(2, false, 1);
-    BSG_L(4, false, 1);
+    BSG_L(false, 1);
   }
-#undef BSG_CPB
 #undef BSG_ZP
 #undef BSG_L
 }

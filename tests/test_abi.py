@@ -124,7 +124,7 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
 
 def test_summation_order_independent_of_max_M(L):
     """The per-row summation order is fixed by the work split (CTAs, tiles, stages).  It depends
-    on max_M through the residency class -- 4 CTAs per SM for max_M <= 8, 3 for max_M <= 16,
+    on max_M through the residency class -- 4 CTAs per SM for max_M <= 8, 3 for max_M <= 24,
     2 for max_M <= 32 (more accumulator registers) -- never on M of a call (not an argument),
     which gives row bit-identity across M within a plan."""
     keys = ("ctas", "tiles", "stages_per_tile", "k_per_stage", "rows_per_tile", "consumer_warps")
@@ -138,7 +138,9 @@ def test_summation_order_independent_of_max_M(L):
                 assert {k: g[k] for k in keys} == {k: ref[k] for k in keys}
         assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 8, 152)["ctas_per_sm"] == 4
         assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 9, 152)["ctas_per_sm"] == 3
-        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 17, 152)["ctas_per_sm"] == 2
+        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 17, 152)["ctas_per_sm"] == 3
+        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 24, 152)["ctas_per_sm"] == 3
+        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 25, 152)["ctas_per_sm"] == 2
 
 
 def test_stream_k_ranges_cover_every_stage_once():
@@ -253,3 +255,18 @@ def test_dense_geometry(L, N, K, sms):
     assert 1 <= g["stages"] <= 8 and g["stages"] <= -(-g["stages_per_tile"] // S)
     assert g["smem_bytes"] <= 232448
     assert bsgemv.dense_geometry_for("bf16", N, K, 8, sms) == g
+
+
+def test_residency_of_plans_for_17_to_24_rows(L):
+    """Plans for 17..24 rows take three n8 tiles at 3 CTAs per SM, unless that residency loses the
+    cluster split (shares of at most 4 stages) that four tiles at 2 CTAs per SM keep."""
+    def geo(fmt, bs, zp, N, K, mm):
+        g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, mm, 152)
+        return g["ctas_per_sm"], g["cluster"]
+    assert geo("fp8", 128, False, 4096, 2048, 24) == (2, 4)       # small: the split wins
+    assert geo("int8", 128, True, 2048, 4096, 20) == (2, 4)
+    assert geo("int4", 32, False, 12288, 4096, 24)[0] == 3        # larger: three tiles win
+    assert geo("int4", 32, False, 4096, 12288, 17)[0] == 3        # long shares (12 stages)
+    assert geo("nvfp4", 16, False, 248320, 2048, 24) == (3, 0)
+    for mm in (17, 20, 24):   # the same plan geometry for every max_M of the range
+        assert geo("fp8", 128, False, 4096, 2048, mm) == (2, 4)

@@ -472,6 +472,34 @@ def test_rows_bit_identical_across_M_up_to_32(torch_cuda, fmt, act, bs, zp):
     assert_parity(case32, y32)
 
 
+@pytest.mark.parametrize("fmt,act,bs,zp", WIDE_CASES)
+def test_plans_for_24_rows_run_three_tiles(torch_cuda, fmt, act, bs, zp):
+    """Plans with 17 <= max_M <= 24 are sized for three n8 tiles at 3 CTAs per SM: parity at
+    M = 17 and 24, and rows bit-identical across M (one, two and three tiles)."""
+    K = 1536 if bs <= 128 else 1792
+    case24 = synth.make_case(fmt, act, bs, zp, 357, K, 24, 5 * bs + 24)
+    with bsgemv.Plan(fmt, act, bs, zp, case24.N, case24.K, 24) as plan:
+        assert plan.describe()["ctas_per_sm"] == 3
+        y24 = run(case24, plan)
+        for M in (1, 9, 17, 23):
+            assert np.array_equal(run(case24.with_M(M), plan), y24[:M]), f"M={M}"
+    assert_parity(case24, y24)
+    assert_parity(case24.with_M(17), y24[:17])
+
+
+def test_plans_for_24_rows_that_keep_four_tiles(torch_cuda):
+    """A small shape whose 24-row plan keeps four n8 tiles at 2 CTAs per SM (for the cluster
+    split): calls with 17..24 rows run four tiles, fewer rows one or two; rows bit-identical."""
+    case = synth.make_case("fp8", "f16", 128, False, 4096, 2048, 24, 2424)
+    with bsgemv.Plan("fp8", "f16", 128, False, case.N, case.K, 24) as plan:
+        g = plan.describe()
+        assert (g["ctas_per_sm"], g["cluster"]) == (2, 4)
+        y24 = run(case, plan)
+        for M in (1, 8, 9, 17, 20):
+            assert np.array_equal(run(case.with_M(M), plan), y24[:M]), f"M={M}"
+    assert_parity(case, y24)
+
+
 @pytest.mark.parametrize("how", ["stream_k", "cluster", "bias"])
 def test_32_rows_under_every_split_and_with_bias(torch_cuda, how):
     case = synth.make_case("int4", "bf16", 32, True, 700, 4096, 29, 2929)
