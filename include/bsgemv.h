@@ -117,8 +117,9 @@ enum bsgemv_split {
  * block_size: int4/int8 one of 16, 32, 64, 128, 256; fp8 128; nvfp4 16.
  * has_zp: 0 or 1 (int formats only; must be 0 for fp8 and nvfp4).
  * N >= 1 (any tail); K >= 64 with K % 64 == 0 and K % block_size == 0; 1 <= max_M <= 32 (the
- * pages' decode GEMVs take M <= 16; calls with 17 to 24 rows run three n8 activation tiles at
- * 3 CTAs per SM, with 25 to 32 four at 2 CTAs per SM).
+ * pages' decode GEMVs take M <= 16; a plan for up to 24 rows runs three n8 activation tiles at
+ * 3 CTAs per SM, or four at 2 CTAs per SM where that keeps a cluster split of its tiles; a plan
+ * for up to 32 rows runs four at 2 CTAs per SM.  Size a plan for the largest M it serves).
  * Uses the current CUDA device, which must be sm_103 (GB300).  Allocates the plan's own device
  * workspace (cross-CTA partial sums, arrival counters and an error word, all zeroed here) with
  * cudaMalloc; every call reuses it and the kernels leave the counters at zero.
