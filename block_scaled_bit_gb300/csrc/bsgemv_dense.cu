@@ -173,13 +173,113 @@ __global__ void __launch_bounds__(32 * 5, 1) bsgemv_dense_kernel(const __grid_co
   }
 }
 
+// ---- N not a multiple of 8 (B's rows are not 16-byte aligned, so no TMA): CUDA-core kernel.
+// A CTA owns kNarrowN columns and a K-slice; its 256 threads stride over k (thread t takes
+// k = k0 + t, k0 + t + 256, ...), each keeping fp32 sums for the 8 columns and up to 8 rows.
+// Then, in a fixed order: a butterfly over the warp's lanes, the 8 warps in order, and (K
+// split over a cluster) the CTAs of the cluster in rank order in the leader's shared memory.
+constexpr int kNarrowN = 8;
+constexpr int kNarrowThreads = 256;
+
+struct NParams {
+  const uint16_t* A;
+  const uint16_t* B;
+  void* y;
+  int64_t N, K;
+  int M, splits;
+};
+
+template <bool BF16>
+BSG_DEV float bits_to_f32(uint16_t b) {
+  if constexpr (BF16) return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  return __half2float(__ushort_as_half(b));
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kNarrowThreads, 1)
+    bsgemv_dense_narrow_kernel(const __grid_constant__ NParams p) {
+  __shared__ float part[kNarrowThreads / 32][kDenseMaxM * kNarrowN];  // per warp
+  __shared__ __align__(16) float red[kDenseMaxSplit][kDenseMaxM * kNarrowN];  // leader: per rank
+  const int S = p.splits;
+  const int64_t tile = blockIdx.x / S;
+  const int rank = static_cast<int>(blockIdx.x % S);
+  const int64_t n0 = tile * kNarrowN;
+  const int nn = static_cast<int>(p.N - n0 < kNarrowN ? p.N - n0 : kNarrowN);
+  const int64_t k0 = rank * p.K / S, k1 = (rank + 1) * p.K / S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait();  // A may be the previous kernel's output
+  float acc[kDenseMaxM][kNarrowN];
+#pragma unroll
+  for (int m = 0; m < kDenseMaxM; ++m)
+#pragma unroll
+    for (int n = 0; n < kNarrowN; ++n) acc[m][n] = 0.f;
+  for (int64_t k = k0 + threadIdx.x; k < k1; k += kNarrowThreads) {
+    float b[kNarrowN];
+    const uint16_t* row = p.B + k * p.N + n0;
+#pragma unroll
+    for (int n = 0; n < kNarrowN; ++n) b[n] = n < nn ? bits_to_f32<BF16>(__ldg(row + n)) : 0.f;
+#pragma unroll
+    for (int m = 0; m < kDenseMaxM; ++m) {
+      if (m < p.M) {
+        const float a = bits_to_f32<BF16>(__ldg(p.A + m * p.K + k));
+#pragma unroll
+        for (int n = 0; n < kNarrowN; ++n) acc[m][n] = fmaf(a, b[n], acc[m][n]);
+      }
+    }
+  }
+  // lanes: butterfly (every lane ends with the same sum: fp32 addition commutes)
+#pragma unroll
+  for (int m = 0; m < kDenseMaxM; ++m)
+#pragma unroll
+    for (int n = 0; n < kNarrowN; ++n) {
+      float v = acc[m][n];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      acc[m][n] = v;
+    }
+  if (lane == 0) {
+#pragma unroll
+    for (int m = 0; m < kDenseMaxM; ++m)
+#pragma unroll
+      for (int n = 0; n < kNarrowN; ++n) part[warp][m * kNarrowN + n] = acc[m][n];
+  }
+  __syncthreads();
+  // warps in order; then the cluster's CTAs in rank order
+  const int e = threadIdx.x;  // one (m, n) per thread for e < 64
+  float v = 0.f;
+  if (e < kDenseMaxM * kNarrowN) {
+    for (int w = 0; w < kNarrowThreads / 32; ++w) v += part[w][e];
+  }
+  if (S >= 2) {
+    if (e < kDenseMaxM * kNarrowN) {
+      const uint32_t dst = smem_u32(&red[rank][e]);
+      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(mapa_shared(dst, 0)), "f"(v) : "memory");
+    }
+    cluster_sync();
+    if (rank != 0) return;
+    v = 0.f;
+    if (e < kDenseMaxM * kNarrowN)
+      for (int r = 0; r < S; ++r) v += red[r][e];
+  }
+  if (e < kDenseMaxM * kNarrowN) {
+    const int m = e / kNarrowN, n = e % kNarrowN;
+    if (m < p.M && n < nn) {
+      if constexpr (BF16)
+        reinterpret_cast<__nv_bfloat16*>(p.y)[m * p.N + n0 + n] = __float2bfloat16_rn(v);
+      else
+        reinterpret_cast<__half*>(p.y)[m * p.N + n0 + n] = __float2half_rn(v);
+    }
+  }
+}
+
 namespace {
 
 constexpr int kDenseThreads = 32 * 5;
 
 struct DenseGeo {
   bsgemv_geometry pub;
-  int bf16, max_M;
+  int bf16, max_M, narrow;
   int64_t N, K;
   int red_off, bar_off;
 };
@@ -192,13 +292,36 @@ int dense_geometry(int act_bf16, int64_t N, int64_t K, int max_M, int sm_count, 
   if ((act_bf16 != 0 && act_bf16 != 1) || N < 1 || K < 1 || max_M < 1 || max_M > kDenseMaxM ||
       sm_count < 1)
     return BSGEMV_ERR_INVALID_ARG;
-  // TMA: row pitches of B (N) and A (K) must be multiples of 16 bytes
-  if (N % 8 != 0 || K % 8 != 0 || K < 16) return BSGEMV_ERR_UNSUPPORTED;
   if (N > (int64_t(1) << 31) - kDenseTileN || K > (int64_t(1) << 30)) return BSGEMV_ERR_UNSUPPORTED;
   g->bf16 = act_bf16;
   g->max_M = max_M;
   g->N = N;
   g->K = K;
+  // TMA needs row pitches of B (N) and A (K) in multiples of 16 bytes; otherwise the CUDA-core
+  // kernel (8 columns per CTA, 256 threads striding over k, K split over a cluster)
+  g->narrow = (N % 8 != 0 || K % 8 != 0 || K < 16) ? 1 : 0;
+  if (g->narrow) {
+    const int64_t tiles = (N + kNarrowN - 1) / kNarrowN;
+    const int64_t kslices = (K + kNarrowThreads - 1) / kNarrowThreads;
+    const int64_t cap = std::max<int64_t>(1, (2 * int64_t(sm_count)) / tiles);
+    const int S = static_cast<int>(std::min<int64_t>({kDenseMaxSplit, kslices, cap}));
+    bsgemv_geometry& q = g->pub;
+    q.variant = BSGEMV_VARIANT_CUDA_CORE;
+    q.rows_per_tile = kNarrowN;
+    q.k_per_stage = kNarrowThreads;
+    q.stages = 1;
+    q.consumer_warps = kNarrowThreads / 32;
+    q.ctas = static_cast<int>(tiles * S);
+    q.ctas_per_sm = 2;
+    q.sm_count = sm_count;
+    q.tiles = tiles;
+    q.stages_per_tile = kslices;
+    q.total_stages = tiles * kslices;
+    q.smem_bytes = 0;
+    q.workspace_bytes = 256;
+    q.cluster = S;
+    return BSGEMV_OK;
+  }
   const int64_t tiles = (N + kDenseTileN - 1) / kDenseTileN;
   const int64_t spt = (K + kDenseStageK - 1) / kDenseStageK;
   const int64_t cap = std::max<int64_t>(1, (2 * int64_t(sm_count)) / tiles);
@@ -257,6 +380,43 @@ int encode_u16(CUtensorMap* tm, const void* ptr, uint64_t cols, uint64_t rows, u
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) % 2) == 0; }
+
+int launch_dense_narrow(const DenseGeo& g, const void* A, const void* B, void* y, int M,
+                        cudaStream_t s) {
+  NParams k;
+  k.A = static_cast<const uint16_t*>(A);
+  k.B = static_cast<const uint16_t*>(B);
+  k.y = y;
+  k.N = g.N;
+  k.K = g.K;
+  k.M = M;
+  k.splits = g.pub.cluster;
+  auto kern = g.bf16 ? bsgemv_dense_narrow_kernel<true> : bsgemv_dense_narrow_kernel<false>;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 1;
+  if (g.pub.cluster >= 2) {
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = static_cast<unsigned>(g.pub.cluster);
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    na = 2;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(g.pub.ctas));
+  cfg.blockDim = dim3(kNarrowThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, kern, k) != cudaSuccess) {
+    cudaGetLastError();
+    return BSGEMV_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
+}
 
 }  // namespace
 }  // namespace bsg
@@ -325,13 +485,17 @@ int bsgemv_dense_run(bsgemv_dense_plan_t plan, const void* A, const void* B, voi
     return BSGEMV_ERR_INVALID_ARG;
   const bsg::DenseGeo& g = plan->geo;
   if (M > g.max_M) return BSGEMV_ERR_M_TOO_LARGE;
-  if (!bsg::aligned16(A) || !bsg::aligned16(B) || !bsg::aligned16(y)) return BSGEMV_ERR_MISALIGNED;
+  const bool narrow = g.narrow != 0;
+  if (narrow ? (!bsg::aligned2(A) || !bsg::aligned2(B) || !bsg::aligned2(y))
+             : (!bsg::aligned16(A) || !bsg::aligned16(B) || !bsg::aligned16(y)))
+    return BSGEMV_ERR_MISALIGNED;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) {
     cudaGetLastError();
     return BSGEMV_ERR_CUDA;
   }
   if (cur != plan->device) return BSGEMV_ERR_WRONG_DEVICE;
+  if (narrow) return bsg::launch_dense_narrow(g, A, B, y, M, static_cast<cudaStream_t>(stream));
   if (B != plan->b_ptr) {
     plan->b_ptr = nullptr;
     if (bsg::encode_u16(&plan->tm_b, B, g.N, g.K, bsg::kDenseTileN, bsg::kDenseStageK) != BSGEMV_OK)

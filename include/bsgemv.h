@@ -271,9 +271,11 @@ int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_t N, int64_
  * (act_bf16 = 1), B row-major [K, N] (the MatMul right-hand side), 1 <= M <= max_M <= 8.
  * K is split over the CTAs of a thread-block cluster per 64-column tile and the partial sums
  * are added in a fixed order (results are deterministic and rows bit-identical across M).
- * Requirements: N % 8 == 0 and K % 8 == 0, K >= 16 (TMA row pitches of 16 bytes; the page's
- * kernel also takes N = 1, here such a B must be padded to 8 columns), A, B, y device memory,
- * 16-byte aligned.  The plan allocates only an error word.  Same status conventions as above.
+ * N % 8 == 0, K % 8 == 0 and K >= 16 (16-byte row pitches) run the TMA / tensor-core kernel, with
+ * A, B and y 16-byte aligned; any other N >= 1, K >= 1 (the page's tests include N = 1) runs a
+ * CUDA-core kernel (8 columns per CTA, K split over a cluster, the same fixed-order reduction),
+ * with A, B and y 2-byte aligned.  Device memory.  The plan allocates only an error word.  Same
+ * status conventions as above.
  */
 typedef struct bsgemv_dense_plan_s* bsgemv_dense_plan_t;
 

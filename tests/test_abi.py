@@ -227,9 +227,7 @@ def test_shared_memory_layout_is_aligned_for_every_problem(L):
     (("f16", 0, 2048, 1), bsgemv.ERR_INVALID_ARG),        # N = 0
     (("f16", 64, 2048, 9), bsgemv.ERR_INVALID_ARG),       # max_M > 8
     (("f16", 64, 2048, 0), bsgemv.ERR_INVALID_ARG),       # max_M = 0
-    (("f16", 1, 2048, 1), bsgemv.ERR_UNSUPPORTED),        # N % 8 (TMA pitch of B)
-    (("f16", 64, 2044, 1), bsgemv.ERR_UNSUPPORTED),       # K % 8 (TMA pitch of A)
-    (("bf16", 64, 8, 1), bsgemv.ERR_UNSUPPORTED),         # K < 16
+    (("f16", 64, 0, 1), bsgemv.ERR_INVALID_ARG),          # K = 0
 ])
 def test_dense_invalid_problems_rejected_on_host(L, args, code):
     act, N, K, mm = args
@@ -239,6 +237,16 @@ def test_dense_invalid_problems_rejected_on_host(L, args, code):
     with pytest.raises(bsgemv.BsgemvError) as e:
         bsgemv.DensePlan(act, N, K, mm)
     assert e.value.status == code
+
+
+@pytest.mark.parametrize("N,K", [(1, 2048), (7, 100), (1001, 4096), (64, 2044), (64, 8)])
+def test_dense_geometry_without_tma_pitches(L, N, K):
+    """N or K not a multiple of 8 (or K < 16): the CUDA-core kernel, 8 columns per CTA."""
+    g = bsgemv.dense_geometry_for("f16", N, K, 8, 152)
+    assert g["variant"] == bsgemv.VARIANTS["cuda_core"] and g["rows_per_tile"] == 8
+    assert g["tiles"] == -(-N // 8) and g["stages_per_tile"] == -(-K // 256)
+    S = g["cluster"]
+    assert 1 <= S <= min(8, g["stages_per_tile"]) and g["ctas"] == g["tiles"] * S
 
 
 @pytest.mark.parametrize("N,K", [(8, 16), (32, 2048), (256, 2048), (1024, 2048), (1000, 4096),

@@ -546,6 +546,23 @@ def test_dense_gemv_parity_and_rows_across_M(torch_cuda, act, N, K):
     assert bad == 0, f"{bad} outputs outside the bound (worst {worst:.3g})"
 
 
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("N,K", [(1, 2048), (3, 100), (7, 5000), (9, 1), (33, 777), (1001, 2048),
+                                 (64, 2044), (16, 8)])
+def test_dense_gemv_without_tma_pitches(torch_cuda, act, N, K):
+    """N or K not a multiple of 8 (the split-K page's tests include N = 1): the CUDA-core kernel,
+    within the bound of the oracle, rows bit-identical across M, repeated calls identical."""
+    A, B = synth.dense_operands(act, 8, N, K, seed=3 * N + K)
+    with bsgemv.DensePlan(act, N, K, 8) as plan:
+        assert plan.describe()["variant"] == bsgemv.VARIANTS["cuda_core"]
+        y8 = run_dense(act, A, B, plan)
+        for M in (1, 3, 6):
+            assert np.array_equal(run_dense(act, A, B, plan, M), y8[:M]), f"M={M}"
+        assert np.array_equal(run_dense(act, A, B, plan), y8)
+    bad, worst, _ = oracle.dense_tolerance_violations(A, B, act, y8)
+    assert bad == 0, f"{bad} outputs outside the bound (worst {worst:.3g})"
+
+
 def test_dense_errors_on_device(torch_cuda):
     torch = torch_cuda
     A, B = synth.dense_operands("f16", 4, 64, 256, seed=3)
