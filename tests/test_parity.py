@@ -575,3 +575,80 @@ def test_dense_errors_on_device(torch_cuda):
         assert plan.run_status(dA.data_ptr() + 2, dB, y, M=4) == bsgemv.ERR_MISALIGNED
         assert plan.run_status(dA, None, y, M=4) == bsgemv.ERR_INVALID_ARG
         assert plan.device_status() == bsgemv.OK
+
+
+# ---------------------------------------------------------------------------- ordering
+@pytest.mark.parametrize("fmt,act,bs,zp,N,K", [("int8", "f16", 128, True, 4096, 4096),
+                                               ("int4", "bf16", 32, False, 12288, 4096),
+                                               ("nvfp4", "f16", 16, False, 2048, 2048)])
+def test_activations_written_by_the_previous_kernel_are_seen(torch_cuda, fmt, act, bs, zp, N, K):
+    """Each GEMV starts while the previous kernel drains (programmatic dependent launch) and
+    prefetches weights before the dependency wait, activations only after it: a kernel that
+    rewrites A right before the call must be seen.  Five rounds of (overwrite A, GEMV) on one
+    stream, each output equal to the same GEMV run alone on that round's activations."""
+    torch = torch_cuda
+    case = synth.make_case(fmt, act, bs, zp, N, K, 4, 4711)
+    d = bsgemv.upload(case, "cuda")
+    rounds = [torch.randn((4, K), generator=torch.Generator().manual_seed(r)).to(
+        torch.float16 if act == "f16" else torch.bfloat16).view(torch.int16).cuda() for r in range(5)]
+    stream = torch.cuda.Stream()
+    ys = [torch.empty((4, N), dtype=torch.int16, device="cuda") for _ in rounds]
+    with bsgemv.Plan(fmt, act, bs, zp, N, K, 4) as plan:
+        with torch.cuda.stream(stream):
+            for a, y in zip(rounds, ys):
+                d.A.copy_(a)                     # a torch kernel writes A ...
+                plan.run(d.A, d.W, d.scales, d.zp, y, stream=stream)   # ... the GEMV reads it
+        stream.synchronize()
+        for a, y in zip(rounds, ys):
+            ref = torch.empty_like(y)
+            plan.run(a, d.W, d.scales, d.zp, ref)
+            torch.cuda.synchronize()
+            assert torch.equal(ref, y)
+
+
+def test_dense_activations_written_by_the_previous_kernel_are_seen(torch_cuda):
+    torch = torch_cuda
+    N, K = 1024, 2048
+    A, B = synth.dense_operands("f16", 8, N, K, seed=9)
+    dB = torch.from_numpy(B.view(np.int16)).cuda()
+    dA = torch.empty((8, K), dtype=torch.int16, device="cuda")
+    rounds = [torch.randn((8, K), generator=torch.Generator().manual_seed(r)).half().view(torch.int16).cuda()
+              for r in range(5)]
+    ys = [torch.empty((8, N), dtype=torch.int16, device="cuda") for _ in rounds]
+    stream = torch.cuda.Stream()
+    with bsgemv.DensePlan("f16", N, K, 8) as plan:
+        with torch.cuda.stream(stream):
+            for a, y in zip(rounds, ys):
+                dA.copy_(a)
+                plan.run(dA, dB, y, stream=stream)
+        stream.synchronize()
+        for a, y in zip(rounds, ys):
+            ref = torch.empty_like(y)
+            plan.run(a, dB, ref)
+            torch.cuda.synchronize()
+            assert torch.equal(ref, y)
+
+
+def test_two_plans_on_two_streams_concurrently(torch_cuda):
+    """Plans own separate workspaces: two of them driven from two streams at once give the same
+    bits as when run alone."""
+    torch = torch_cuda
+    c1 = synth.make_case("int8", "f16", 32, True, 12288, 4096, 2, 71)
+    c2 = synth.make_case("int4", "f16", 32, True, 4096, 12288, 3, 72)
+    d1, d2 = bsgemv.upload(c1, "cuda"), bsgemv.upload(c2, "cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    with bsgemv.Plan("int8", "f16", 32, True, c1.N, c1.K, 2) as p1, \
+            bsgemv.Plan("int4", "f16", 32, True, c2.N, c2.K, 3) as p2:
+        p1.run(d1.A, d1.W, d1.scales, d1.zp, d1.y)
+        p2.run(d2.A, d2.W, d2.scales, d2.zp, d2.y)
+        torch.cuda.synchronize()
+        r1, r2 = d1.y.clone(), d2.y.clone()
+        outs1 = [torch.empty_like(d1.y) for _ in range(10)]
+        outs2 = [torch.empty_like(d2.y) for _ in range(10)]
+        for o1, o2 in zip(outs1, outs2):
+            p1.run(d1.A, d1.W, d1.scales, d1.zp, o1, stream=s1)
+            p2.run(d2.A, d2.W, d2.scales, d2.zp, o2, stream=s2)
+        torch.cuda.synchronize()
+        assert p1.device_status() == bsgemv.OK and p2.device_status() == bsgemv.OK
+    assert all(torch.equal(o, r1) for o in outs1)
+    assert all(torch.equal(o, r2) for o in outs2)
