@@ -102,6 +102,16 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def workload_name(config: int, shapes, M: int) -> str:
+    """The workload of a configuration named by what it is, with its sizes (both arms)."""
+    s0 = shapes[0]
+    fmt = {"int4": "int4", "int8": "int8", "fp8": "FP8 E4M3", "nvfp4": "NVFP4"}[s0.fmt]
+    zp = " with zero points" if s0.has_zp else ""
+    return (f"{fmt} MatMulNBits GEMV{zp} (config {config}): "
+            + ", ".join(f"{s.K}x{s.N} bs{s.block_size}" for s in shapes)
+            + f" (K x N), M={M}, {'bf16' if s0.act == 'bf16' else 'fp16'}")
+
+
 def job_throughput_gbps(world: int, steps: int, step_bytes: int, seconds: float) -> float:
     """Whole-job GB/s: every rank moves `step_bytes` per step (replicas, weak scaling) and the
     job takes the slowest rank's time."""
@@ -480,9 +490,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u8 weights (int8 + zp), f16 activations, f32 accumulate",
             "data": "synthetic (seeded), no trained weights",
-            "config": {"workload": f"int8 MatMulNBits GEMV with zero points (config {args.config}): "
-                                   + ", ".join(f"{s.K}x{s.N} bs{s.block_size}" for s in shapes)
-                                   + f" (K x N), M={wl.items[0]['M']}, fp16",
+            "config": {"workload": workload_name(args.config, shapes, wl.items[0]["M"]),
                        "calls_per_step": L, "bytes_per_step": step_bytes,
                        "cold": "2 weight copies per shape on alternate steps: each call's weights "
                                "were last read 19 calls (>0.5 GB, >4x L2) earlier; inputs larger than L2",
@@ -787,14 +795,16 @@ def run_reference(args):
         m = args.M or shape.Ms[0]
         case = shape.case(m)
         items.append((case, m, case.algorithmic_bytes(m)))
-    # each step: 16 output columns of every shape (a bounded sample); bytes pro rata
-    cols = 16
-    step_bytes = sum(b * cols / c.N for c, _, b in items)
+    # each step: a bounded sample of output columns of every shape, 8 per host thread (the
+    # oracle hands its OpenMP threads columns in chunks of 8); bytes pro rata
+    cols = 8 * cores
+    step_bytes = sum(b * min(cols, c.N) / c.N for c, _, b in items)
 
     def step(s):
         for c, m, _ in items:
-            n0 = (s * cols) % max(1, c.N - cols)
-            oracle.gemv(c, rows=list(range(n0, n0 + cols)), M=m)
+            n = min(cols, c.N)
+            n0 = (s * n) % max(1, c.N - n + 1)
+            oracle.gemv(c, rows=list(range(n0, n0 + n)), M=m)
 
     for s in range(max(3, args.warmup)):
         step(s)
@@ -807,7 +817,9 @@ def run_reference(args):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "f64 (oracle)", "data": "synthetic (seeded), no trained weights",
-           "config": {"workload": f"config {args.config} (same shapes as the GPU arm)",
+           "config": {"workload": workload_name(args.config, [synth_shape for synth_shape in
+                                                             synth.config_shapes(args.config)],
+                                                items[0][1]),
                       "sample_per_step": f"{cols} output columns of each of the {len(items)} GEMVs"},
            "impl": "reference",
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
