@@ -107,7 +107,7 @@ def workload_name(config: int, shapes, M: int) -> str:
     s0 = shapes[0]
     fmt = {"int4": "int4", "int8": "int8", "fp8": "FP8 E4M3", "nvfp4": "NVFP4"}[s0.fmt]
     zp = " with zero points" if s0.has_zp else ""
-    return (f"{fmt} MatMulNBits GEMV{zp} (config {config}): "
+    return (f"{fmt} MatMulNBits GEMV{zp}: "
             + ", ".join(f"{s.K}x{s.N} bs{s.block_size}" for s in shapes)
             + f" (K x N), M={M}, {'bf16' if s0.act == 'bf16' else 'fp16'}")
 
