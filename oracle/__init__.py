@@ -209,7 +209,8 @@ def dense_tolerance_violations(A_bits, B_bits, act: str, ybits_gpu, rel: float =
     with np.errstate(invalid="ignore"):
         err = np.abs(y - r)
     bad = np.where(finite, ~(err <= bound), ~((y == r) | (np.isnan(y) & np.isnan(r))))
-    worst = float(np.max(np.where(finite, err / bound, 0.0))) if r.size else 0.0
+    with np.errstate(invalid="ignore", divide="ignore"):  # inf / inf where the oracle overflows
+        worst = float(np.max(np.where(finite, err / bound, 0.0))) if r.size else 0.0
     return int(bad.sum()), worst, ref_bits
 
 
@@ -247,5 +248,6 @@ def tolerance_violations(case, ybits_gpu: np.ndarray, rows=None, M: int | None =
     with np.errstate(invalid="ignore"):
         err = np.abs(y - r)
     bad = np.where(finite, ~(err <= bound), ~((y == r) | (np.isnan(y) & np.isnan(r))))
-    worst = float(np.max(np.where(finite, err / bound, 0.0))) if r.size else 0.0
+    with np.errstate(invalid="ignore", divide="ignore"):  # inf / inf where the oracle overflows
+        worst = float(np.max(np.where(finite, err / bound, 0.0))) if r.size else 0.0
     return int(bad.sum()), worst, ref_bits

@@ -537,3 +537,48 @@ def test_dense_small_integers_are_an_integer_matmul(orc):
     ybits, exact, _ = orc.dense_gemv(synth.to_f16_bits(a), synth.to_f16_bits(b), "f16")
     assert np.array_equal(exact, (a @ b).astype(np.float64))
     assert np.array_equal(orc.act_values(ybits, "f16"), (a @ b).astype(np.float64))
+
+
+# ------------------------------------------------------------------ the parity bar itself
+def test_ulp_matches_the_formats_spacing(orc):
+    """ulp(|v|) is the distance from v to the next larger value of the dtype, subnormals
+    included: numpy's float16 spacing, and for bf16 the difference of neighbouring codes."""
+    codes = np.arange(1, 0x7BFF, 37, dtype=np.uint16)  # positive finite fp16, subnormals first
+    v16 = codes.view(np.float16).astype(np.float64)
+    assert np.array_equal(orc.ulp(v16, "f16"), np.spacing(codes.view(np.float16)).astype(np.float64))
+    bcodes = np.arange(1, 0x7F7F, 41, dtype=np.uint16)  # positive finite bf16
+    vb = orc.act_values(bcodes, "bf16")
+    nxt = orc.act_values(bcodes + 1, "bf16")
+    assert np.array_equal(orc.ulp(vb, "bf16"), nxt - vb)
+
+
+def test_tolerance_check_accepts_the_oracle_and_flags_a_planted_error(orc):
+    case = synth.make_case("int8", "f16", 32, True, 40, 256, 3, 12)
+    ref_bits, _, absdot = orc.gemv(case)
+    bad, worst, _ = orc.tolerance_violations(case, ref_bits)
+    assert bad == 0 and worst == 0.0
+    # one output off by twice its bound
+    y = orc.act_values(ref_bits, "f16")
+    bound = orc.ulp(y, "f16") + 1e-3 * absdot
+    planted = y.copy()
+    planted[1, 7] += 2 * bound[1, 7]
+    bad, worst, _ = orc.tolerance_violations(case, synth.to_f16_bits(planted))
+    assert bad == 1 and worst > 1.0
+    # within the bound: accepted
+    near = y.copy()
+    near[2, 3] += 0.5 * bound[2, 3]
+    bits = synth.to_f16_bits(near)
+    ok, _, _ = orc.tolerance_violations(case, bits)
+    assert ok == 0
+
+
+def test_tolerance_check_requires_infinities_to_match(orc):
+    """Where the oracle's result overflows, the GPU value must be the same infinity."""
+    case = synth.make_case("int8", "f16", 32, False, 8, 256, 1, 3, scale_range=(60000.0, 60000.0))
+    case = dataclasses.replace(case, A=synth.to_f16_bits(np.full((1, 256), 60000.0)))
+    ref_bits, _, _ = orc.gemv(case)
+    vals = orc.act_values(ref_bits, "f16")
+    assert np.all(np.isinf(vals))
+    assert orc.tolerance_violations(case, ref_bits)[0] == 0
+    finite = synth.to_f16_bits(np.full(vals.shape, 65504.0) * np.sign(vals))
+    assert orc.tolerance_violations(case, finite)[0] == vals.size
