@@ -278,3 +278,21 @@ def test_residency_of_plans_for_17_to_24_rows(L):
     assert geo("nvfp4", 16, False, 248320, 2048, 24) == (3, 0)
     for mm in (17, 20, 24):   # the same plan geometry for every max_M of the range
         assert geo("fp8", 128, False, 4096, 2048, mm) == (2, 4)
+
+
+def test_header_is_c_and_the_library_links_from_c(L, tmp_path):
+    """include/bsgemv.h compiles as C11 and a C program links against the library and runs its
+    host-only entry points."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib = bsgemv.lib_path()
+    exe = tmp_path / "c_abi_check"
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c_abi_check.c"), lib, "-o", str(exe),
+                        f"-Wl,-rpath,{os.path.dirname(lib)}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr
