@@ -37,3 +37,27 @@ def test_config_enumeration():
     assert len({s.seed for s in shapes}) == len({(s.config, s.shape_index, s.block_size) for s in shapes})
     c1 = synth.config_shapes(1)[0]
     assert (c1.N, c1.K, c1.block_size, c1.has_zp) == (1024, 512, 32, True)
+
+
+def test_rows_up_to_32_and_bias_draws():
+    a32 = synth.make_case("int4", "f16", 32, False, 16, 256, 32, 5)
+    a16 = synth.make_case("int4", "f16", 32, False, 16, 256, 16, 5)
+    assert a32.A.shape == (32, 256) and np.array_equal(a32.A[:16], a16.A)
+    b = a32.with_bias()
+    assert b.bias.shape == (16,) and b.bias.dtype == np.uint16
+    assert np.array_equal(b.with_M(3).bias, b.bias)            # the bias does not depend on M
+    assert np.array_equal(b.W, a32.W) and np.array_equal(b.A, a32.A)
+    assert np.array_equal(synth.make_case("int4", "f16", 32, False, 16, 256, 32, 5).with_bias().bias,
+                          b.bias)                              # seeded
+    assert b.algorithmic_bytes() == a32.algorithmic_bytes() + 2 * 16
+
+
+def test_dense_operands():
+    A, B = synth.dense_operands("f16", 8, 300, 1024, seed=1)
+    assert A.shape == (8, 1024) and B.shape == (1024, 300) and A.dtype == B.dtype == np.uint16
+    A2, B2 = synth.dense_operands("f16", 3, 300, 1024, seed=1)
+    assert np.array_equal(A2, A[:3]) and np.array_equal(B2, B)
+    var = B.view(np.float16).astype(np.float64).var()
+    assert abs(var * 1024 - 1.0) < 0.05                        # B ~ N(0, 1/K)
+    Ab, Bb = synth.dense_operands("bf16", 2, 8, 64, seed=2)
+    assert Ab.dtype == Bb.dtype == np.uint16 and Bb.shape == (64, 8)
