@@ -3,24 +3,27 @@
 
 Metric: achieved HBM GB/s on cold weights (algorithmic bytes W + scales + zp + A + y per call,
 divided by the device time of the call), with microseconds per call and the fraction of the
-measured HBM copy bandwidth.
+measured HBM copy bandwidth, against M.
 
-Default workload (one "step" = one pass of the hot path over the workload): the 8-bit
-MatMulNBits configuration -- int8 weights with zero points, fp16 activations, M = 1, block
-sizes 128 and 32, shapes (K x N) 2048x5120, 4096x2048, 4096x4096, 4096x12288, 12288x4096:
-ten GEMV calls per step.  Every shape has two weight copies used on alternate steps, so each
-call reads weights last touched 19 calls (~0.5 GB of other traffic, > 4x L2) earlier: the
-weights are cold.  The timed region replays a CUDA graph of 25 steps of back-to-back launches
-(programmatic dependent launch overlaps each call's start-up with the previous call's tail);
-a separate graph with an event between every launch gives per-call durations.
+Default workload (one "step" = one pass of the hot path over the workload): the int4
+MatMulNBits small-M sweep -- int4 weights, block size 32, zero point fixed at 8, fp16 and bf16
+activations, shapes (K x N) 4096x4096, 4096x12288, 12288x4096, 4096x151936, at M = 1, 2, 4, 8
+and 16: forty GEMV calls per step, one plan per shape sized for 16 rows.  Calls run M by M over
+all shapes, so two calls on one weight are separated by the other shapes' calls (> 3x L2), and
+each shape's two weight copies alternate between steps: the weights are cold.  The timed region
+replays CUDA graphs holding exactly --steps steps of back-to-back launches (programmatic
+dependent launch overlaps each call's start-up with the previous call's tail); separate replays
+of a graph with an event between every launch give per-call durations (per_shape, by_M).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
+                    [--config C]
 
-With --gpus N > 1 (launched under torchrun) every rank runs the same workload on its own GPU
-(independent replicas: the GEMV has no exchange step), the time is the maximum over ranks and
-the value is the bytes of all ranks over that time.  --impl reference times the CPU oracle on
-the host cores instead.  --sweep prints one JSON line per (configuration shape, M) with
-isolated-cold and streamed-cold timings.
+--config 2 times the int8-with-zero-points workload (M = 1) instead.  With --gpus N > 1
+(launched under torchrun) every rank runs the same workload on its own GPU (independent
+replicas: the GEMV has no exchange step), the time is the maximum over ranks and the value is
+the bytes of all ranks over that time.  --impl reference times the CPU oracle on the host cores
+instead.  --sweep prints one JSON line per (configuration shape, M) with isolated-cold and
+streamed-cold timings.
 """
 from __future__ import annotations
 
@@ -42,20 +45,19 @@ if ROOT not in sys.path:
 
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "achieved HBM GB/s (cold weights) and µs/call vs M=1..16, fraction of HBM roofline"
-WORKLOAD_CONFIG = 2
-GRAPH_STEPS = 25
+WORKLOAD_CONFIG = 3
+GRAPH_STEPS = 24  # steps per captured graph: even, so that weight copies alternate across replays
 
 
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=24)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--config", type=int, default=WORKLOAD_CONFIG, help=argparse.SUPPRESS)
     ap.add_argument("--M", type=int, default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--no-graph", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     ap.add_argument("--skip-cpu", action="store_true", help=argparse.SUPPRESS)
     # --sweep and --one: run the plans as this variant (cuda_core: calls with M <= 8)
@@ -102,14 +104,35 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def workload_name(config: int, shapes, M: int) -> str:
+def workload_name(config: int, shapes, Ms) -> str:
     """The workload of a configuration named by what it is, with its sizes (both arms)."""
+    Ms = [Ms] if isinstance(Ms, int) else list(Ms)
     s0 = shapes[0]
-    fmt = {"int4": "int4", "int8": "int8", "fp8": "FP8 E4M3", "nvfp4": "NVFP4"}[s0.fmt]
-    zp = " with zero points" if s0.has_zp else ""
-    return (f"{fmt} MatMulNBits GEMV{zp}: "
-            + ", ".join(f"{s.K}x{s.N} bs{s.block_size}" for s in shapes)
-            + f" (K x N), M={M}, {'bf16' if s0.act == 'bf16' else 'fp16'}")
+    kind = {"int4": "int4 MatMulNBits GEMV", "int8": "int8 MatMulNBits GEMV",
+            "fp8": "FP8 E4M3 block-scaled GEMV", "nvfp4": "NVFP4 GEMV"}[s0.fmt]
+    if s0.has_zp:
+        kind += " with zero points"
+    elif s0.fmt in ("int4", "int8"):
+        kind += f" (zero point fixed at {8 if s0.fmt == 'int4' else 128})"
+    dims, acts = [], []
+    for s in shapes:
+        d = f"{s.K}x{s.N} bs{s.block_size}"
+        if d not in dims:
+            dims.append(d)
+        a = "bf16" if s.act == "bf16" else "fp16"
+        if a not in acts:
+            acts.append(a)
+    return (f"{kind}: " + ", ".join(dims) + f" (K x N), M={','.join(str(m) for m in Ms)}, "
+            + " and ".join(acts))
+
+
+def workload_dtype(shapes) -> str:
+    """The arithmetic types of the path: stored weight codes, activation type(s), accumulation."""
+    s0 = shapes[0]
+    w = {"int4": "u4 weights", "int8": "u8 weights", "fp8": "e4m3 weights",
+         "nvfp4": "e2m1 weights + e4m3 block scales"}[s0.fmt]
+    acts = sorted({"bf16" if s.act == "bf16" else "f16" for s in shapes})
+    return f"{w}, {' and '.join(acts)} activations, f32 accumulate"
 
 
 def job_throughput_gbps(world: int, steps: int, step_bytes: int, seconds: float) -> float:
@@ -214,20 +237,34 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------ our arm
 class Workload:
-    """Plans, device buffers (several weight copies) and host copies for one configuration."""
+    """Plans, device buffers (weight copies) and the call list of one configuration.
+
+    One plan per shape, sized for the largest M the configuration is quoted at (so that every M
+    of a shape sums each row in the same order).  One step calls every shape at every M, M in the
+    outer loop: two calls on one weight copy are separated by the calls on every other shape
+    (with the lm_head shapes among them, hundreds of MB > 3x L2), and a shape's copies alternate
+    from step to step, so the weights come from HBM."""
 
     def __init__(self, config: int, M: int | None, device, copies: int):
         from block_scaled_bit_gb300 import bsgemv, synth
-        self.items = []
-        for shape in synth.config_shapes(config):
-            m = M or shape.Ms[0]
-            case = shape.case(m)
-            # plans are sized for the configuration's largest M (the M values it is quoted at)
+        self.config = config
+        self.shapes = synth.config_shapes(config)
+        per_shape = []
+        for shape in self.shapes:
+            Ms = (M,) if M else tuple(shape.Ms)
+            case = shape.case(max(Ms))
             plan = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp, case.N, case.K,
-                               max(max(shape.Ms), m))
+                               max(Ms))
             bufs = [bsgemv.upload(case, device) for _ in range(copies)]
-            self.items.append({"shape": shape, "case": case, "M": m, "plan": plan, "bufs": bufs,
-                               "bytes": case.algorithmic_bytes(m)})
+            per_shape.append((shape, case, plan, bufs, Ms))
+        self.plans = [ps[2] for ps in per_shape]
+        self.Ms = sorted({m for ps in per_shape for m in ps[4]})
+        self.items = []
+        for m in self.Ms:
+            for shape, case, plan, bufs, Ms in per_shape:
+                if m in Ms:
+                    self.items.append({"shape": shape, "case": case, "M": m, "plan": plan,
+                                       "bufs": bufs, "bytes": case.algorithmic_bytes(m)})
         self.copies = copies
 
     @property
@@ -236,11 +273,17 @@ class Workload:
 
     def launch(self, it, copy, stream=None):
         b = it["bufs"][copy % self.copies]
-        it["plan"].run(b.A, b.W, b.scales, b.zp, b.y, M=it["M"], stream=stream)
+        M = it["M"]
+        it["plan"].run(b.A[:M], b.W, b.scales, b.zp, b.y[:M], M=M, stream=stream)
+
+    def close(self):
+        for p in self.plans:
+            p.close()
 
 
 def capture(wl, stream, steps, with_events):
-    """CUDA graph of `steps` workload steps (optionally with timing events between launches)."""
+    """CUDA graph of `steps` workload steps (optionally with timing events between launches);
+    step s uses weight copy s."""
     import torch
     L = len(wl.items)
     events = None
@@ -260,168 +303,150 @@ def capture(wl, stream, steps, with_events):
     return graph, events
 
 
-def time_graph(wl, steps, warmup, stream, use_graph=True):
-    """Time `steps` steps (rounded up to whole graphs of GRAPH_STEPS steps) of back-to-back
-    launches; consecutive launches overlap start-up and tail (programmatic dependent launch).
-    Then, outside the timed region, one replay of a graph with an event between every launch
-    gives per-launch durations (events serialise the launches).
-    Returns (seconds, per-launch seconds of the instrumented replay, steps, launches)."""
+def graph_plan(steps: int, chunk: int = GRAPH_STEPS):
+    """Graph sizes covering exactly `steps` steps: (steps per graph, full replays, remainder)."""
+    S = max(1, min(steps, chunk))
+    full, rem = divmod(steps, S)
+    return S, full, rem
+
+
+def time_graph(wl, steps, warmup, stream):
+    """Time exactly `steps` steps of back-to-back launches, replayed from CUDA graphs (consecutive
+    launches overlap start-up and tail through programmatic dependent launch).  Then, outside the
+    timed region, replays of a graph with an event between every launch give per-launch
+    durations (events serialise the launches).
+    Returns (seconds, {item index: [per-launch seconds]}, launches)."""
     import torch
     L = len(wl.items)
-    S = GRAPH_STEPS
-    replays = max(1, -(-steps // S))
+    S, full, rem = graph_plan(steps)
     with torch.cuda.stream(stream):
-        for s in range(S):                # warm every plan and weight copy outside capture
+        for s in range(2):                # warm every plan and weight copy outside capture
             for it in wl.items:
                 wl.launch(it, s)
         stream.synchronize()
-    graph = inst = events = None
-    if use_graph:
-        try:
-            graph, _ = capture(wl, stream, S, False)
-            inst, events = capture(wl, stream, S, True)
-        except Exception as e:  # older torch: no external events in graphs
-            sys.stderr.write(f"[bench] graph capture unavailable ({e}); timing eager launches\n")
-            graph = inst = None
-    if events is None or inst is None:
-        events = [torch.cuda.Event(enable_timing=True) for _ in range(S * L + 1)]
-
-    def replay():
-        if graph is not None:
-            graph.replay()
-            return
-        for s in range(S):
-            for it in wl.items:
-                wl.launch(it, s, stream)
-
+    g_full, _ = capture(wl, stream, S, False)
+    g_rem = capture(wl, stream, rem, False)[0] if rem else None
+    isteps = 2
+    inst, events = capture(wl, stream, isteps, True)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for _ in range(max(1, -(-warmup // S))):
-            replay()
+            g_full.replay()
         stream.synchronize()
         start.record(stream)
-        for _ in range(replays):
-            replay()
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
         end.record(stream)
         end.synchronize()
         total = start.elapsed_time(end) / 1e3
-        # per-launch durations (not part of the timed region)
-        if inst is not None:
+        per = {j: [] for j in range(L)}
+        for _ in range(5):                # per-launch durations (not part of the timed region)
             inst.replay()
-        else:
-            i = 0
-            for s in range(S):
-                for it in wl.items:
-                    events[i].record(stream)
-                    i += 1
-                    wl.launch(it, s, stream)
-            events[i].record(stream)
-        stream.synchronize()
-    per_launch = [events[i].elapsed_time(events[i + 1]) / 1e3 for i in range(S * L)]
-    return total, per_launch, replays * S, replays * S * L
+            stream.synchronize()
+            for s in range(isteps):
+                for j in range(L):
+                    i = s * L + j
+                    per[j].append(events[i].elapsed_time(events[i + 1]) / 1e3)
+    return total, per, steps * L
 
 
 def e2e_run(wl, steps, stream):
-    """End to end through the public API: every step copies the activations of its ten GEMVs from
-    pinned host memory to the device (one copy), runs the ten bsgemv_run calls on them and copies
-    the ten outputs back to pinned host memory (one copy), and waits for the stream once, when
-    all results are on the host.  The step is captured once per weight copy into a CUDA graph
-    (the library's calls only enqueue work) and replayed; without graph support the step is
-    issued directly."""
-    import numpy as np
+    """End to end through the library's host-buffer entry point: every call of a step goes
+    through bsgemv_run_host_async (its activations copied from pinned host memory into the plan's
+    staging buffer, the GEMV, its output copied back to pinned host memory, all enqueued on the
+    stream), and the step waits for the stream once, when all results are on the host.  The step
+    is captured once per weight copy into a CUDA graph (the calls only enqueue work) and
+    replayed.  Weights stay device-resident, as model weights do."""
     import torch
     dev = stream.device
-
-    def pad8(n):  # keep every slice 16-byte aligned
-        return (n + 7) // 8 * 8
-    a_off, y_off, na, ny = [], [], 0, 0
+    A_host, y_host = [], []
     for it in wl.items:
-        a_off.append(na)
-        y_off.append(ny)
-        na += pad8(it["M"] * it["case"].K)
-        ny += pad8(it["M"] * it["case"].N)
-    A_host = torch.zeros(na, dtype=torch.int16).pin_memory()
-    y_host = torch.empty(ny, dtype=torch.int16).pin_memory()
-    for it, o in zip(wl.items, a_off):
-        a = np.ascontiguousarray(it["case"].A[: it["M"]]).view(np.int16).reshape(-1)
-        A_host[o:o + a.size] = torch.from_numpy(a)
-    A_dev = torch.empty(na, dtype=torch.int16, device=dev)
-    y_dev = torch.empty(ny, dtype=torch.int16, device=dev)
+        M, case = it["M"], it["case"]
+        a = np.ascontiguousarray(case.A[:M]).view(np.int16)
+        A_host.append(torch.from_numpy(a).pin_memory())
+        y_host.append(torch.empty((M, case.N), dtype=torch.int16).pin_memory())
     h2d = sum(it["M"] * it["case"].K * 2 for it in wl.items)
     d2h = sum(it["M"] * it["case"].N * 2 for it in wl.items)
 
     def enqueue(s):
-        with torch.cuda.stream(stream):
-            A_dev.copy_(A_host, non_blocking=True)
-            for it, ao, yo in zip(wl.items, a_off, y_off):
-                b = it["bufs"][s % wl.copies]
-                M, case = it["M"], it["case"]
-                it["plan"].run(A_dev[ao:ao + M * case.K], b.W, b.scales, b.zp,
-                               y_dev[yo:yo + M * case.N], M=M, stream=stream)
-            y_host.copy_(y_dev, non_blocking=True)
+        for it, ah, yh in zip(wl.items, A_host, y_host):
+            b = it["bufs"][s % wl.copies]
+            it["plan"].run_host_async(ah, b.W, b.scales, b.zp, yh, M=it["M"], stream=stream)
 
-    for s in range(3):
-        enqueue(s)
-        stream.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(2):                # staging buffers are allocated outside capture
+            enqueue(s)
+            stream.synchronize()
     graphs = []
-    try:
-        for c in range(wl.copies):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                enqueue(c)
-            graphs.append(g)
-        with torch.cuda.stream(stream):  # (a graph replays on the current stream)
-            for g in graphs:
-                g.replay()
+    for c in range(wl.copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            enqueue(c)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
         stream.synchronize()
-    except Exception as e:  # no graph capture: issue the step directly
-        sys.stderr.write(f"[bench] e2e graph capture unavailable ({e}); direct calls\n")
-        graphs = []
-    y_host.fill_(-1)  # every output must come back from the timed steps
-    y_dev.fill_(-1)
+    for yh in y_host:                     # every output must come back from the timed steps
+        yh.fill_(-1)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for s in range(steps):
-            if graphs:
-                graphs[s % len(graphs)].replay()
-            else:
-                enqueue(s)
+            graphs[s % len(graphs)].replay()
             stream.synchronize()
     dt = time.perf_counter() - t0
-    # the step's outputs made the round trip: check them against the device run of each plan
-    ref = torch.empty_like(y_dev)
+    # the outputs made the round trip: each equals the device run of its call
     with torch.cuda.stream(stream):
-        for it, ao, yo in zip(wl.items, a_off, y_off):
+        for it, yh in zip(wl.items, y_host):
             b = it["bufs"][(steps - 1) % wl.copies]
-            M, case = it["M"], it["case"]
-            it["plan"].run(A_dev[ao:ao + M * case.K], b.W, b.scales, b.zp, ref[yo:yo + M * case.N],
-                           M=M, stream=stream)
-    stream.synchronize()
-    if not torch.equal(ref.cpu(), y_host):
-        raise RuntimeError("e2e: host outputs differ from the device run")
-    return dt, h2d, d2h, bool(graphs)
+            M = it["M"]
+            ref = torch.empty_like(b.y[:M])
+            it["plan"].run(b.A[:M], b.W, b.scales, b.zp, ref, M=M, stream=stream)
+            stream.synchronize()
+            if not torch.equal(ref.cpu(), yh):
+                raise RuntimeError(f"e2e: host output of {it['shape'].name} M={M} differs from the device run")
+    return dt, h2d, d2h
+
+
+def oracle_sample(items, cols_per_item: int):
+    """One bounded oracle pass: `cols_per_item` output columns (a window moving with `s`) of
+    every call; returns (step function, algorithmic bytes per step pro rata)."""
+    import oracle
+    step_bytes = sum(it["bytes"] * min(cols_per_item, it["case"].N) / it["case"].N for it in items)
+
+    def step(s):
+        for it in items:
+            c = it["case"]
+            n = min(cols_per_item, c.N)
+            n0 = (s * n) % max(1, c.N - n + 1)
+            oracle.gemv(c, rows=list(range(n0, n0 + n)), M=it["M"])
+    return step, step_bytes
 
 
 def cpu_baseline(wl, seconds: float):
-    """The oracle as it stands, on the host cores, over the same workload until `seconds` of
-    work are done (whole steps; all shapes, all output columns)."""
+    """The oracle as it stands, on the host cores, over a bounded sample of the same workload:
+    64 output columns per host thread of every call, repeated until `seconds` of work are done;
+    GB/s counts the sampled columns' share of each call's algorithmic bytes."""
     import oracle
     oracle.build()
     cores = oracle.max_threads()
-    done_bytes, reps = 0, 0
+    cols = 64 * cores
+    step, step_bytes = oracle_sample(wl.items, cols)
+    done, reps = 0.0, 0
     t0 = time.perf_counter()
     while True:
-        for it in wl.items:
-            oracle.gemv(it["case"], M=it["M"])
-            done_bytes += it["bytes"]
+        step(reps)
+        done += step_bytes
         reps += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} full pass(es) over the {len(wl.items)} GEMVs of the workload "
-                      f"(all output columns, M as timed), {dt:.1f} s, OpenMP over output columns"}
+    return {"value": done / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} pass(es) of {cols} output columns of each of the {len(wl.items)} calls "
+                      f"(M as timed), {dt:.1f} s, OpenMP over output columns"}
 
 
 def run_ours(args):
@@ -440,63 +465,66 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         barrier(world)
-        total, per_launch, steps_timed, launches = time_graph(wl, args.steps, args.warmup, stream,
-                                                              not args.no_graph)
+        total, per, launches = time_graph(wl, args.steps, args.warmup, stream)
         torch.cuda.synchronize()
         barrier(world)
     clocks = clk.summary()
     total = max_over_ranks(total, world, device)
     step_bytes = wl.bytes_per_step
-    value = job_throughput_gbps(world, steps_timed, step_bytes, total)
+    value = job_throughput_gbps(world, args.steps, step_bytes, total)
 
-    # per-launch durations of the last replayed graph: L launches per step, GRAPH_STEPS steps
-    L = len(wl.items)
     per_shape = []
     for j, it in enumerate(wl.items):
-        d = [per_launch[s * L + j] for s in range(GRAPH_STEPS)]
-        us = statistics.median(d) * 1e6
+        us = statistics.median(per[j]) * 1e6
         per_shape.append({"shape": it["shape"].name, "M": it["M"], "us_per_call": round(us, 3),
                           "GBps": round(it["bytes"] / (us * 1e-6) / 1e9, 1),
                           "frac": round(it["bytes"] / (us * 1e-6) / 1e9 / peak, 4),
                           "bytes": it["bytes"]})
     # the dominant (only) kernel's average launch duration over the timed region: launches run
     # back to back with start-up overlapped, so the region divided by its launches
+    L = len(wl.items)
     mean_launch = total / launches
     achieved = (step_bytes / L) / mean_launch / 1e9
     workload = f"config{args.config}"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(workload),
-                "peak_kind": f"{peak_kind} copy bandwidth", "kernel": "bsgemv_mma_kernel"}
+                "peak_kind": f"{peak_kind} copy bandwidth (of {peak_kind})",
+                "kernel": "bsgemv_mma_kernel"}
 
-    e2e_dt, h2d, d2h, e2e_graph = e2e_run(wl, max(20, min(400, args.steps // 10)), stream)
-    e2e_steps = max(20, min(400, args.steps // 10))
+    e2e_steps = max(10, min(200, args.steps))
+    e2e_dt, h2d, d2h = e2e_run(wl, e2e_steps, stream)
     e2e_dt = max_over_ranks(e2e_dt, world, device)
-    e2e = {"value": round(job_throughput_gbps(world, e2e_steps, step_bytes, e2e_dt), 1), "unit": "GB/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "api": "bsgemv_run on the step's activations copied host->device (pinned, one copy per step) "
-                  "with the ten outputs copied device->host (one copy per step), device-resident weights, "
-                  + ("the step replayed from a CUDA graph, " if e2e_graph else "") + "one stream synchronisation per step"}
+    e2e = {"value": round(job_throughput_gbps(world, e2e_steps, step_bytes, e2e_dt), 1),
+           "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": e2e_steps,
+           "api": f"bsgemv_run_host_async for each of the {L} calls of a step (pinned host A in, "
+                  "pinned host y out, through the plan's staging buffers), device-resident weights, "
+                  "the step replayed from a CUDA graph, one stream synchronisation per step"}
 
     out = None
     if rank == 0:
         cpu = None
         if world == 1 and not args.skip_cpu:
             cpu = cpu_baseline(wl, args.cpu_seconds)
-        shapes = [it["shape"] for it in wl.items]
+        S, full, rem = graph_plan(args.steps)
+        s0 = wl.shapes[0]
         out = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
-            "steps": steps_timed, "warmup": args.warmup,
-            "ms_per_step": round(total / steps_timed * 1e3, 5),
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "u8 weights (int8 + zp), f16 activations, f32 accumulate",
+            "dtype": workload_dtype(wl.shapes),
             "data": "synthetic (seeded), no trained weights",
-            "config": {"workload": workload_name(args.config, shapes, wl.items[0]["M"]),
+            "config": {"workload": workload_name(args.config, wl.shapes, wl.Ms),
                        "calls_per_step": L, "bytes_per_step": step_bytes,
-                       "cold": "2 weight copies per shape on alternate steps: each call's weights "
-                               "were last read 19 calls (>0.5 GB, >4x L2) earlier; inputs larger than L2",
-                       "timing": f"CUDA graph of {GRAPH_STEPS} steps replayed, CUDA events on the launch stream "
-                                 "around the timed region; per_shape from a separate graph with an "
-                                 "event between every launch (serialised)",
+                       "plan_max_M": {s.name: max((args.M,) if args.M else s.Ms) for s in wl.shapes},
+                       "cold": "M in the outer loop: two calls on one weight copy are separated by the "
+                               "calls on every other shape of the step (> 3x L2), and each shape's 2 "
+                               "weight copies alternate between steps; inputs larger than L2",
+                       "timing": f"exactly {args.steps} steps replayed from CUDA graphs ({full} x {S} steps"
+                                 + (f" + {rem}" if rem else "") + "), CUDA events on the launch stream "
+                                 "around the timed region; per_shape from separate replays of a graph "
+                                 "with an event between every launch (serialised)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "roofline": roofline,
             "fraction_of_nominal_7900_GBps": round(value / world / 7900.0, 4),
@@ -507,12 +535,26 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "impl": "ours",
         }
+        if s0.fmt == "int4" and len(wl.Ms) > 1:
+            out["by_M"] = by_M_summary(per_shape, peak)
     if dist is not None:
         dist.barrier()
-    for it in wl.items:
-        it["plan"].close()
+    wl.close()
     if out is not None:
         print(json.dumps(out), flush=True)
+
+
+def by_M_summary(per_shape, peak):
+    """Per M: total bytes and serialised time of that M's calls, and the fraction of the peak."""
+    out = {}
+    for e in per_shape:
+        d = out.setdefault(str(e["M"]), {"bytes": 0, "us": 0.0})
+        d["bytes"] += e["bytes"]
+        d["us"] += e["us_per_call"]
+    for d in out.values():
+        d["frac"] = round(d["bytes"] / (d["us"] * 1e-6) / 1e9 / peak, 4)
+        d["us"] = round(d["us"], 2)
+    return out
 
 
 # ------------------------------------------------------------------------------ sweep
@@ -782,7 +824,9 @@ def run_crossover(args):
 
 # ------------------------------------------------------------------------------ reference arm
 def run_reference(args):
-    """The oracle (CPU, fp64) timed on the host cores on this workload; rank 0 only."""
+    """The oracle (CPU, fp64) timed on the host cores on this workload; rank 0 only.  Each step
+    is a bounded sample: 8 output columns per host thread of every call of the workload's step
+    (every shape at every M), bytes pro rata."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -790,22 +834,17 @@ def run_reference(args):
     from block_scaled_bit_gb300 import synth
     oracle.build()
     cores = oracle.max_threads()
+    shapes = synth.config_shapes(args.config)
     items = []
-    for shape in synth.config_shapes(args.config):
-        m = args.M or shape.Ms[0]
-        case = shape.case(m)
-        items.append((case, m, case.algorithmic_bytes(m)))
-    # each step: a bounded sample of output columns of every shape, 8 per host thread (the
-    # oracle hands its OpenMP threads columns in chunks of 8); bytes pro rata
+    Ms = sorted({m for s in shapes for m in ((args.M,) if args.M else s.Ms)})
+    cases = {s.name: s.case(max((args.M,) if args.M else s.Ms)) for s in shapes}
+    for m in Ms:
+        for s in shapes:
+            if m in ((args.M,) if args.M else s.Ms):
+                c = cases[s.name]
+                items.append({"case": c, "M": m, "bytes": c.algorithmic_bytes(m)})
     cols = 8 * cores
-    step_bytes = sum(b * min(cols, c.N) / c.N for c, _, b in items)
-
-    def step(s):
-        for c, m, _ in items:
-            n = min(cols, c.N)
-            n0 = (s * n) % max(1, c.N - n + 1)
-            oracle.gemv(c, rows=list(range(n0, n0 + n)), M=m)
-
+    step, step_bytes = oracle_sample(items, cols)
     for s in range(max(3, args.warmup)):
         step(s)
     t0 = time.perf_counter()
@@ -817,13 +856,11 @@ def run_reference(args):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "f64 (oracle)", "data": "synthetic (seeded), no trained weights",
-           "config": {"workload": workload_name(args.config, [synth_shape for synth_shape in
-                                                             synth.config_shapes(args.config)],
-                                                items[0][1]),
-                      "sample_per_step": f"{cols} output columns of each of the {len(items)} GEMVs"},
+           "config": {"workload": workload_name(args.config, shapes, Ms),
+                      "sample_per_step": f"{cols} output columns of each of the {len(items)} calls"},
            "impl": "reference",
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                            "sample": f"{cols} output columns per GEMV per step, {args.steps} steps"},
+                            "sample": f"{cols} output columns per call per step, {args.steps} steps"},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)

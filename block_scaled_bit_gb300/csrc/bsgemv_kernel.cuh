@@ -387,15 +387,21 @@ BSG_DEV void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
       : "r"(w));
 }
 
-// An f16 pair whose values are exact in bf16 and normal (or zero) in f16, re-encoded as a bf16
-// pair: keep the sign, shift exponent and top mantissa bits into bf16 position (the value is
-// then 2^-112 of the original) and scale back by 2^112, which is exact.  Used for E4M3 values
-// and E2M1 x E4M3 products, which have at most 6 significand bits, so the 3 bits shifted out of
-// each half are zero.
-BSG_DEV uint32_t f16x2_exact_to_bf16x2(uint32_t h) {
-  const uint32_t mag = ((h & 0x7FFF7FFFu) >> 3);
-  const uint32_t bits = (mag & 0x0FFF0FFFu) | (h & 0x80008000u);
-  return bf2_mul(bits, 0x77807780u);  // 2^112 in each bf16 half
+// An f16 pair as a bf16 pair: each half widened to fp32 (exact) and the two packed by one
+// round-to-nearest-even conversion, which is exact for values bf16 holds -- E4M3 values and
+// E2M1 x E4M3 products have at most 6 significand bits and lie in [2^-10, 2688] -- and keeps a
+// NaN a NaN (E4M3 codes 0x7F / 0xFF decode to an f16 NaN; as a weight, or as an NVFP4 block
+// scale, the product must stay NaN, as the format's definition and the oracle have it).
+BSG_DEV uint32_t f16x2_to_bf16x2(uint32_t h) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 l, u;\n\t.reg .f32 fl, fu;\n\t"
+      "mov.b32 {l, u}, %1;\n\t"
+      "cvt.f32.f16 fl, l;\n\t"
+      "cvt.f32.f16 fu, u;\n\t"
+      "cvt.rn.bf16x2.f32 %0, fu, fl;\n\t}"
+      : "=r"(d)
+      : "r"(h));
+  return d;
 }
 
 // ------------------------------------------------------------------------------ decoders
@@ -477,7 +483,7 @@ BSG_DEV void decode_fp8(uint32_t lo, uint32_t hi, uint32_t (&a)[1][4]) {
   e4m3x4_to_f16x2x2(hi, a[0][1], a[0][3]);
   if constexpr (BF16) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[0][i] = f16x2_exact_to_bf16x2(a[0][i]);
+    for (int i = 0; i < 4; ++i) a[0][i] = f16x2_to_bf16x2(a[0][i]);
   }
 }
 
@@ -498,7 +504,7 @@ BSG_DEV void decode_nvfp4(uint32_t lo, uint32_t hi, uint32_t sc_lo, uint32_t sc_
     a[s][3] = h2_mul(h[2 * s + 1], sc_hi);
     if constexpr (BF16) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[s][i] = f16x2_exact_to_bf16x2(a[s][i]);
+      for (int i = 0; i < 4; ++i) a[s][i] = f16x2_to_bf16x2(a[s][i]);
     }
   }
 }

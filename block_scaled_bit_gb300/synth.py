@@ -164,6 +164,153 @@ def make_case(fmt: str, act: str, block_size: int, has_zp: bool, N: int, K: int,
     return Case(fmt, act, block_size, bool(has_zp), N, K, M, A, W, scales, zp, g, seed, name)
 
 
+# ------------------------------------------------------------------------------------ pin inputs
+# Inputs built to pin the GPU path to the oracle bit for bit (not draws of a workload).  They
+# hold codes and values only; what they make exact or special is stated per function.
+
+def _act_bits(x, act: str) -> np.ndarray:
+    return to_f16_bits(x) if act == "f16" else to_bf16_bits(x)
+
+
+def _pack_nibbles(codes: np.ndarray) -> np.ndarray:
+    """[R, 2n] codes 0..15 -> [R, n] bytes, the even position in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _row_perms(rng, rows: int, n: int) -> np.ndarray:
+    """`rows` independent permutations of 0 .. n-1."""
+    return np.argsort(rng.random((rows, n)), axis=1)
+
+
+ALL_CODES_K = {"int4": 16 * 16 * 16, "int8": 256 * 256, "fp8": 4 * 256, "nvfp4": 16 * 256}
+
+
+def all_codes_case(fmt: str, act: str, block_size: int, has_zp: bool, N: int, M: int,
+                   seed: int) -> Case:
+    """Every code of the format in every row, K fixed per format (ALL_CODES_K):
+    int4 / int8: the codes of each row are consecutive random permutations of 0..15 / 0..255.
+      With zero points, K is cut into spans of max(levels, block_size) k; every block of span j
+      has the zero point j mod levels, every span holds whole permutations, and there are at
+      least `levels` spans -- so every (q, zp) pair occurs in every row.  Without zero points
+      every code meets the implicit zero point;
+    fp8: all 256 E4M3 codes (NaN 0x7F / 0xFF, subnormals, +-0, +-448) four times per row;
+    nvfp4: all 256 E4M3 codes as block scales (one per 16-block, a random order per row), and
+      every E2M1 code once in every block.
+    Scales of the int formats and FP8 come from the format's usual draw; A ~ N(0, 1)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 0xC0DE5]))
+    K = ALL_CODES_K[fmt]
+    base = make_case(fmt, act, block_size, has_zp, N, K, M, seed)
+    if fmt in ("int4", "int8"):
+        levels = 16 if fmt == "int4" else 256
+        q = np.concatenate([_row_perms(rng, N, levels) for _ in range(K // levels)], axis=1)
+        W = _pack_nibbles(q) if fmt == "int4" else q.astype(np.uint8)
+        zp = base.zp
+        if has_zp:
+            nb = K // block_size
+            span = max(levels, block_size)
+            zb = ((np.arange(nb) * block_size // span) % levels)[None, :].repeat(N, axis=0)
+            if fmt == "int4":
+                z = np.zeros((N, 2 * ((nb + 1) // 2)), dtype=np.int64)
+                z[:, :nb] = zb
+                zp = _pack_nibbles(z)
+            else:
+                zp = zb.astype(np.uint8)
+        return dataclasses.replace(base, W=W, zp=zp, name=f"allcodes_{fmt}")
+    if fmt == "fp8":
+        W = np.concatenate([_row_perms(rng, N, 256) for _ in range(K // 256)], axis=1).astype(np.uint8)
+        return dataclasses.replace(base, W=W, name="allcodes_fp8")
+    # nvfp4
+    e2m1 = np.concatenate([_row_perms(rng, N, 16) for _ in range(K // 16)], axis=1)
+    scales = _row_perms(rng, N, 256).astype(np.uint8)
+    return dataclasses.replace(base, W=_pack_nibbles(e2m1), scales=scales, name="allcodes_nvfp4")
+
+
+def nan_rows_case(fmt: str, act: str, N: int, K: int, M: int, seed: int, nan_rows) -> Case:
+    """FP8 or NVFP4 weights whose only NaN codes (E4M3 0x7F / 0xFF: FP8 weight codes, NVFP4
+    block scales) sit in the rows `nan_rows`, one or a few per row at random k; every other
+    E4M3 code is drawn uniformly from the 254 finite codes (subnormals, +-0, +-448 included)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 0x4A4E]))
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    if fmt == "fp8":
+        base = make_case("fp8", act, 128, False, N, K, M, seed)
+        W = finite[rng.integers(0, finite.size, size=(N, K))]
+        for n in nan_rows:
+            for _ in range(int(rng.integers(1, 4))):
+                W[n, rng.integers(0, K)] = rng.choice([0x7F, 0xFF])
+        return dataclasses.replace(base, W=W, name="nanrows_fp8")
+    if fmt != "nvfp4":
+        raise ValueError("NaN codes exist in the E4M3-coded formats only")
+    base = make_case("nvfp4", act, 16, False, N, K, M, seed)
+    S = finite[rng.integers(0, finite.size, size=(N, K // 16))]
+    for n in nan_rows:
+        for _ in range(int(rng.integers(1, 4))):
+            S[n, rng.integers(0, K // 16)] = rng.choice([0x7F, 0xFF])
+    return dataclasses.replace(base, scales=S, name="nanrows_nvfp4")
+
+
+def exact_case(fmt: str, act: str, block_size: int, has_zp: bool, N: int, K: int, M: int,
+               seed: int) -> Case:
+    """Inputs whose every partial sum, in any order, is exact in fp32, so that an fp32
+    accumulation reaches the exact dot product and the output rounds as the oracle's does:
+    small-integer activations in [-3, 3], power-of-two block scales, weight values on a coarse
+    grid, K small enough that sum_k |a_k w_k| stays below 2^24 grid steps:
+      int4  scales 2^-2 .. 2^2 (fp16), q and zp uniform nibbles;
+      int8  scales 2^-2 .. 2^0 (fp16), q and zp uniform bytes;
+      fp8   E4M3 codes of exponent field 5..9 (|w| in [0.25, 7.5]), either sign, scales
+            2^-1 .. 2^0 (fp32);
+      nvfp4 E2M1 codes uniform, E4M3 block scales 2^-2 .. 2^2 (codes 0x28 .. 0x48, mantissa 0),
+            global scale 2^-6.
+    Row m of A is the same for every M."""
+    base = make_case(fmt, act, block_size, has_zp, N, K, M, seed)
+    rng = np.random.Generator(np.random.PCG64([seed, 0xE4AC7]))
+    nb = K // block_size
+    arng = np.random.Generator(np.random.PCG64([seed, 0xA11CE, 3]))   # row m independent of M
+    A = _act_bits(arng.integers(-3, 4, size=(MAX_M, K))[:M].astype(np.float64), act)
+    if fmt == "int4":
+        scales = to_f16_bits(np.exp2(rng.integers(-2, 3, size=(N, nb))))
+        return dataclasses.replace(base, A=A, scales=scales, name="exact_int4")
+    if fmt == "int8":
+        scales = to_f16_bits(np.exp2(rng.integers(-2, 1, size=(N, nb))))
+        zp = rng.integers(0, 256, size=(N, nb), dtype=np.uint8) if has_zp else None
+        return dataclasses.replace(base, A=A, scales=scales, zp=zp, name="exact_int8")
+    if fmt == "fp8":
+        e = rng.integers(5, 10, size=(N, K))
+        m = rng.integers(0, 8, size=(N, K))
+        s = rng.integers(0, 2, size=(N, K))
+        W = ((s << 7) | (e << 3) | m).astype(np.uint8)
+        scales = np.exp2(rng.integers(-1, 1, size=(N, nb))).astype(np.float32)
+        return dataclasses.replace(base, A=A, W=W, scales=scales, name="exact_fp8")
+    if fmt == "nvfp4":
+        scales = (rng.integers(5, 10, size=(N, nb)) << 3).astype(np.uint8)
+        return dataclasses.replace(base, A=A, scales=scales,
+                                   gscale=np.array([2.0 ** -6], dtype=np.float32), name="exact_nvfp4")
+    raise ValueError(f"unknown format {fmt!r}")
+
+
+def one_hot_rows(M: int, K: int, act: str) -> tuple:
+    """Activations whose row m is 1.0 at k_m and 0 elsewhere (the k_m distinct, spread over the
+    blocks of K); returns (A bits [M, K], k_m [M])."""
+    ks = (np.arange(M) * 613 + 17) % K
+    x = np.zeros((M, K))
+    x[np.arange(M), ks] = 1.0
+    return _act_bits(x, act), ks
+
+
+def one_hot_case(fmt: str, act: str, block_size: int, has_zp: bool, N: int, K: int, M: int,
+                 seed: int) -> tuple:
+    """A one-hot activation case (see one_hot_rows) over the format's usual weight draw, with
+    FP8 scales drawn on the fp16 grid (U[0.5, 2] / 448 rounded to fp16, stored as fp32) so that
+    every dequantised weight is exact in fp32.  Returns (case, k_m)."""
+    base = make_case(fmt, act, block_size, has_zp, N, K, M, seed)
+    A, ks = one_hot_rows(M, K, act)
+    case = dataclasses.replace(base, A=A, name=f"onehot_{fmt}")
+    if fmt == "fp8":
+        s16 = np.asarray(base.scales, dtype=np.float64).astype(np.float16).astype(np.float32)
+        case = dataclasses.replace(case, scales=s16)
+    return case, ks
+
+
 def dense_operands(act: str, M: int, N: int, K: int, seed: int):
     """Dense small-N GEMV inputs ("[CUDA] MatMul: add an opt-in split-K GEMV for small-N fp16
     shapes"): A [M, K] ~ N(0, 1) and B [K, N] ~ N(0, 1/K) (unit-variance outputs), row-major,

@@ -39,3 +39,20 @@ def test_workload_name_and_job_throughput():
     # replicas: every rank's bytes over the slowest rank's time
     assert bench.job_throughput_gbps(4, 100, 10 ** 9, 2.0) == 200.0
     assert bench.job_throughput_gbps(1, 100, 10 ** 9, 2.0) == 50.0
+
+
+def test_default_workload_is_the_int4_M_sweep():
+    shapes = synth.config_shapes(bench.WORKLOAD_CONFIG)
+    name = bench.workload_name(bench.WORKLOAD_CONFIG, shapes, [1, 2, 4, 8, 16])
+    assert name.startswith("int4 MatMulNBits GEMV (zero point fixed at 8)")
+    for kn in ("4096x4096", "4096x12288", "12288x4096", "4096x151936"):
+        assert f"{kn} bs32" in name and name.count(kn + " ") == 1
+    assert "M=1,2,4,8,16" in name and name.endswith("fp16 and bf16")
+    assert bench.workload_dtype(shapes) == "u4 weights, bf16 and f16 activations, f32 accumulate"
+
+
+def test_graphs_cover_exactly_the_requested_steps():
+    for steps in (1, 3, 20, 23, 24, 25, 48, 100, 1000):
+        S, full, rem = bench.graph_plan(steps)
+        assert S * full + rem == steps and 0 <= rem < S and S <= bench.GRAPH_STEPS
+    assert bench.GRAPH_STEPS % 2 == 0  # weight copies alternate across graph replays

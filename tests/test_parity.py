@@ -6,9 +6,12 @@ register decoders); the GEMV output satisfies |y - y_ref| <= 1 ulp(|y_ref|) + 1e
 every element; every row is bit-identical for every M of a plan; repeated calls are
 bit-identical.
 """
+import os
+
 import numpy as np
 import pytest
 
+import conftest
 import oracle
 from block_scaled_bit_gb300 import bsgemv, synth
 
@@ -49,8 +52,13 @@ def run(case, plan=None, M=None, max_M=16, stream=None):
 
 def assert_parity(case, ybits, rows=None):
     bad, worst, ref = oracle.tolerance_violations(case, ybits if rows is None else ybits[:, rows], rows=rows)
+    conftest.record_worst(current_test(), worst)
     assert bad == 0, f"{bad} outputs outside the bound (worst error/bound {worst:.3g})"
     return worst
+
+
+def current_test() -> str:
+    return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
 
 
 # ---------------------------------------------------------------------------- decode stage
@@ -543,6 +551,7 @@ def test_dense_gemv_parity_and_rows_across_M(torch_cuda, act, N, K):
         for _ in range(2):  # repeated calls: nothing to reset, same bits
             assert np.array_equal(run_dense(act, A, B, plan), y8)
     bad, worst, _ = oracle.dense_tolerance_violations(A, B, act, y8)
+    conftest.record_worst(current_test(), worst)
     assert bad == 0, f"{bad} outputs outside the bound (worst {worst:.3g})"
 
 
@@ -560,6 +569,7 @@ def test_dense_gemv_without_tma_pitches(torch_cuda, act, N, K):
             assert np.array_equal(run_dense(act, A, B, plan, M), y8[:M]), f"M={M}"
         assert np.array_equal(run_dense(act, A, B, plan), y8)
     bad, worst, _ = oracle.dense_tolerance_violations(A, B, act, y8)
+    conftest.record_worst(current_test(), worst)
     assert bad == 0, f"{bad} outputs outside the bound (worst {worst:.3g})"
 
 
