@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--autotune", action="store_true", help=argparse.SUPPRESS)
     # --sweep: these M values instead of the configuration's (e.g. 17,24,32)
     ap.add_argument("--Ms", default=None, help=argparse.SUPPRESS)
+    # --sweep / --one: plans sized for this many rows (default: the configuration's largest M up
+    # to 8 for calls with M <= 8, else its largest M)
+    ap.add_argument("--plan-max-M", type=int, default=0, help=argparse.SUPPRESS)
     # the dense small-N split-K GEMV against cuBLAS (torch.mm), streamed cold
     ap.add_argument("--dense", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--dense-shape", default=None, help=argparse.SUPPRESS)  # "N,K": one shape
@@ -581,6 +584,8 @@ def run_sweep(args):
 
             def plan_for(M):
                 pm = min(max(Ms), 8) if M <= 8 else max(Ms)
+                if args.plan_max_M:
+                    pm = max(args.plan_max_M, M)
                 if pm not in plans:
                     plans[pm] = bsgemv.Plan(case.fmt, case.act, case.block_size, case.has_zp,
                                             case.N, case.K, pm)
@@ -662,6 +667,8 @@ def run_one(args):
     M = args.M or shape.Ms[0]
     case = shape.case(M)
     max_M = min(max(shape.Ms), 8) if M <= 8 else max(shape.Ms)   # as the sweep's plans
+    if args.plan_max_M:
+        max_M = args.plan_max_M
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     flush = torch.empty(4 * l2 // 4, dtype=torch.int32, device="cuda")

@@ -33,6 +33,7 @@ EXPORTS = ("bsgemv_plan", "bsgemv_run", "bsgemv_run_bias", "bsgemv_run_host",
            "bsgemv_status_string", "bsgemv_debug_dequant", "bsgemv_plan_set_override",
            "bsgemv_plan_describe", "bsgemv_geometry_for", "bsgemv_device_status",
            "bsgemv_run_noalloc", "bsgemv_plan_set_split", "bsgemv_plan_autotune",
+           "bsgemv_plan_set_test_fault",
            "bsgemv_dense_plan", "bsgemv_dense_run", "bsgemv_dense_describe",
            "bsgemv_dense_geometry_for", "bsgemv_dense_device_status", "bsgemv_dense_destroy",
            "bsgemv_version")
@@ -95,6 +96,7 @@ def lib() -> ctypes.CDLL:
         L.bsgemv_geometry_for.argtypes = [ci, ci, ci, i64, i64, ci, ci, ctypes.POINTER(Geometry)]
         L.bsgemv_device_status.argtypes = [vp, vp]
         L.bsgemv_run_noalloc.argtypes = [ci, ci, ci, i64, i64, vp, vp, vp, vp, vp, ci, vp]
+        L.bsgemv_plan_set_test_fault.argtypes = [vp, ci, i64]
         for name in EXPORTS:
             if name != "bsgemv_status_string":
                 getattr(L, name).restype = ci
@@ -131,6 +133,12 @@ def run_noalloc_status(fmt: str, act: str, block_size: int, has_zp: bool, N: int
     return lib().bsgemv_run_noalloc(format_code(fmt, act), block_size, int(has_zp), N, K, _ptr(A),
                                     _ptr(W), _ptr(scales), _ptr(zp), _ptr(y), int(M),
                                     _stream(stream))
+
+
+def noalloc_device_status(stream=None) -> int:
+    """Read and clear bsgemv_run_noalloc's error word on the current device (after a stream
+    synchronisation): bsgemv_device_status(NULL, stream)."""
+    return lib().bsgemv_device_status(None, _stream(stream))
 
 
 def _ptr(t) -> int | None:
@@ -241,6 +249,11 @@ class Plan:
 
     def device_status(self, stream=None) -> int:
         return lib().bsgemv_device_status(self._h, _stream(stream))
+
+    def set_test_fault(self, skip_stage: int = -1, wait_ns: int = 0) -> int:
+        """Test hook of the bounded waits (bsgemv_plan_set_test_fault): CTA 0's copy warp leaves
+        out stage `skip_stage` of its range, the waits give up after `wait_ns`; (-1, 0) undoes it."""
+        return lib().bsgemv_plan_set_test_fault(self._h, int(skip_stage), int(wait_ns))
 
 
 def dense_geometry_for(act: str, N: int, K: int, max_M: int, sm_count: int) -> dict:

@@ -23,6 +23,8 @@ struct bsgemv_plan_s {
   int sm_count = 0;
   int variant_override = 0, ctas_override = 0, stages_override = 0;
   int split = BSGEMV_SPLIT_AUTO, cluster = 0;
+  int fault_skip = -1;            // bsgemv_plan_set_test_fault
+  uint64_t fault_wait_ns = 0;
   void* ws = nullptr;         // one allocation: partials | counters | error word
   size_t ws_bytes = 0;
   float* partials = nullptr;
@@ -131,6 +133,8 @@ int prepare_params(bsgemv_plan_s* p, const void* A, const void* W, const void* s
   hit->last_use = ++p->use_clock;
   bsg::fill_params(p->geo, hit->maps, A, W, scales, zp, y, M, p->partials, p->counters, p->err,
                    &p->params);
+  p->params.skip_stage = p->fault_skip;
+  if (p->fault_wait_ns > 0) p->params.wait_ns = p->fault_wait_ns;
   return BSGEMV_OK;
 }
 
@@ -490,16 +494,33 @@ int bsgemv_plan_describe(bsgemv_plan_t plan, bsgemv_geometry* g) {
   return BSGEMV_OK;
 }
 
+int bsgemv_plan_set_test_fault(bsgemv_plan_t plan, int skip_stage, int64_t wait_ns) {
+  if (plan == nullptr || skip_stage < -1 || wait_ns < 0) return BSGEMV_ERR_INVALID_ARG;
+  plan->fault_skip = skip_stage;
+  plan->fault_wait_ns = static_cast<uint64_t>(wait_ns);
+  return BSGEMV_OK;
+}
+
 int bsgemv_device_status(bsgemv_plan_t plan, void* stream) {
-  if (plan == nullptr) return BSGEMV_ERR_INVALID_ARG;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  unsigned* err = nullptr;
+  if (plan != nullptr) {
+    err = plan->err;
+  } else {
+    const int rc = bsg::noalloc_error_word(&err);  // bsgemv_run_noalloc's, current device
+    if (rc != BSGEMV_OK) return rc;
+  }
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
     return BSGEMV_ERR_CUDA;
+  }
   unsigned word = 0;
-  if (cudaMemcpy(&word, plan->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(&word, err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
     return BSGEMV_ERR_CUDA;
+  }
   if (word != 0) {
     const unsigned zero = 0;
-    cudaMemcpy(plan->err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     return BSGEMV_ERR_DEVICE_TIMEOUT;
   }
   return BSGEMV_OK;

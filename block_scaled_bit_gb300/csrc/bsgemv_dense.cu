@@ -524,13 +524,17 @@ int bsgemv_dense_run(bsgemv_dense_plan_t plan, const void* A, const void* B, voi
   k.red_off = g.red_off;
   k.bar_off = g.bar_off;
   auto kern = g.bf16 ? bsg::bsgemv_dense_kernel<true> : bsg::bsgemv_dense_kernel<false>;
-  static std::atomic<int> attr_bf16{0}, attr_f16{0};
-  std::atomic<int>& attr = g.bf16 ? attr_bf16 : attr_f16;
-  if (g.pub.smem_bytes > attr.load()) {
+  static bsg::AttrRecord rec_bf16, rec_f16;  // per device and context
+  bsg::AttrRecord& rec = g.bf16 ? rec_bf16 : rec_f16;
+  int dev = -1;
+  uint64_t ctx = 0;
+  if (!bsg::current_device_context(&dev, &ctx)) return BSGEMV_ERR_CUDA;
+  const int d = rec.slot(dev, ctx);
+  if (g.pub.smem_bytes > rec.smem[d].load()) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              g.pub.smem_bytes) != cudaSuccess)
       return BSGEMV_ERR_CUDA;
-    attr.store(g.pub.smem_bytes);
+    rec.smem[d].store(g.pub.smem_bytes);
   }
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -122,7 +122,7 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   auto smem_with = [&](int stages, int red) {
     const int ss = side_slots_for(stages);
     return 1024 + stages * g->stage_bytes + act_ring(stages) + ss * g->side_bytes + red +
-           8 * (2 * stages + 8);
+           8 * (2 * stages + 9);
   };
   const int slots_per_sm = ctas_per_sm_for_mt(g->mt_max);
   const int64_t slots = int64_t(sm_count) * slots_per_sm;
@@ -154,7 +154,7 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   auto cluster_smem_ss = [&](int64_t c, int stages, bool one) {
     const int ss = (g->side_bytes == 0) ? 0 : (one ? 1 : side_slots_for(stages));
     return 1024 + stages * g->stage_bytes + act_ring(stages) + ss * g->side_bytes +
-           red_for(static_cast<int>(c)) + 8 * (2 * stages + 8);
+           red_for(static_cast<int>(c)) + 8 * (2 * stages + 9);
   };
   auto cluster_one_slot = [&](int64_t c) {
     const int st = std::min(2, cluster_stages(c));

@@ -27,6 +27,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+const CtxFns& ctx_fns() {
+  static CtxFns f;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return f;
+}
+
 // 2D uint8 tensor [rows][row_bytes] with row pitch `pitch`, box [box_rows][box_bytes].
 int encode_u8(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows,
               uint64_t pitch, uint32_t box_bytes, uint32_t box_rows, CUtensorMapSwizzle swz) {
@@ -45,6 +66,31 @@ int encode_u8(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t ro
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
 
 }  // namespace
+
+bool current_device_context(int* dev, uint64_t* ctx_id) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (*dev < 0 || *dev >= kMaxDevices) return false;
+  const CtxFns& f = ctx_fns();
+  if (!f.get_current || !f.get_id) return false;
+  CUcontext ctx = nullptr;
+  if (f.get_current(&ctx) != CUDA_SUCCESS) return false;
+  if (ctx == nullptr) {
+    // a thread that has not used the device yet: the runtime binds its primary context on the
+    // first call that needs one
+    if (cudaFree(nullptr) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  }
+  unsigned long long id = 0;
+  if (f.get_id(ctx, &id) != CUDA_SUCCESS) return false;
+  *ctx_id = id;
+  return true;
+}
 
 int encode_maps(const Geometry& g, const void* W, const void* scales, const void* zp,
                 OperandMaps* m) {
@@ -109,6 +155,8 @@ void fill_params(const Geometry& g, const OperandMaps& m, const void* A, const v
   k->cluster = g.pub.cluster;
   k->red_off = g.red_off;
   k->red_tq = g.red_tq;
+  k->wait_ns = kDefaultWaitNs;
+  k->skip_stage = -1;
 }
 
 int launch_gemv(const Geometry& g, const KParams& k, cudaStream_t s) {

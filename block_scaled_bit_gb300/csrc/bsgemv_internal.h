@@ -16,6 +16,8 @@
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "bsgemv.h"
 
 namespace bsg {
@@ -41,6 +43,7 @@ constexpr int kMaxStages = 12;
 // Error word bits written by kernels that abandon a bounded wait.
 constexpr unsigned kErrTimeoutFull = 1u;
 constexpr unsigned kErrTimeoutEmpty = 2u;
+constexpr uint64_t kDefaultWaitNs = 4000000000ull;  // 4 s: far above any legitimate stall
 
 // Kernel parameters (passed by value as a __grid_constant__; the tensor maps must be 64-byte
 // aligned in parameter space).
@@ -60,6 +63,7 @@ struct KParams {
   unsigned* err;           // error word
   int64_t N, K;
   int64_t total_stages;    // tiles * spt
+  uint64_t wait_ns;        // limit of every bounded wait (kWaitLimitNs unless a test lowers it)
   int spt;                 // stages per tile
   int M;
   int nb_s;                // scale elements per row (K/bs, or K/16 for nvfp4)
@@ -81,6 +85,8 @@ struct KParams {
   int cluster;             // 0: stream-K; C >= 1: C CTAs per tile in one cluster
   int red_off;             // cluster split: [C][kConsumerWarps][MT][8 * red_tq] float4 in the
   int red_tq;              //   leader; quad lanes t < red_tq hold output columns < max_M
+  int skip_stage;          // test hook: CTA 0's producer leaves out this stage of its range
+                           // (its consumers' wait then runs out); -1 = none
 };
 
 struct Geometry {
@@ -173,6 +179,33 @@ void fill_params(const Geometry& g, const OperandMaps& m, const void* A, const v
                  const void* scales, const void* zp, void* y, int M, float* partials,
                  unsigned* counters, unsigned* err, KParams* k);
 int launch_gemv(const Geometry& g, const KParams& k, cudaStream_t s);
+
+// The current device and the id of its current context (unique for the life of the process,
+// never reused, unlike a context's handle); false if either cannot be read.  Function
+// attributes (dynamic shared-memory size, carveout, non-portable cluster sizes) and symbol
+// addresses belong to a context, so every record of them is keyed by both.
+bool current_device_context(int* dev, uint64_t* ctx_id);
+constexpr int kMaxDevices = 64;
+
+// The launch attributes already set for one kernel, per device: a record made under another
+// context (another device's, or one destroyed by a device reset) counts as nothing set.
+struct AttrRecord {
+  std::atomic<uint64_t> ctx[kMaxDevices];
+  std::atomic<int> smem[kMaxDevices];     // largest dynamic shared memory granted
+  std::atomic<int> cluster[kMaxDevices];  // non-portable cluster sizes allowed
+  // Slot of device `dev` under context `ctx`, cleared when the context changed.
+  int slot(int dev, uint64_t ctx_id) {
+    if (ctx[dev].load() != ctx_id) {
+      smem[dev].store(0);
+      cluster[dev].store(0);
+      ctx[dev].store(ctx_id);
+    }
+    return dev;
+  }
+};
+
+// The error word of bsgemv_run_noalloc's scratch area on the current device.
+int noalloc_error_word(unsigned** out);
 
 int launch_debug_dequant(int fmt, bool bf16, bool has_zp, int bs, int64_t N, int64_t K,
                          const uint8_t* W, const uint8_t* scales, const uint8_t* zp,

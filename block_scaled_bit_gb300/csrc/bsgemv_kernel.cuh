@@ -48,9 +48,10 @@
 namespace bsg {
 
 // Bounded waits: a waiting thread blocks in mbarrier.try_wait (the hardware's own time window,
-// no suspend-time hint: measured faster to wake than a hinted wait) and gives up after
-// kWaitLimitNs of wall time, far above any legitimate stall.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
+// no suspend-time hint: measured faster to wake than a hinted wait) and gives up after a limit
+// of wall time -- kWaitLimitNs unless the launch sets another (KParams::wait_ns), far above any
+// legitimate stall.
+constexpr uint64_t kWaitLimitNs = kDefaultWaitNs;
 
 // ------------------------------------------------------------------------------ PTX wrappers
 BSG_DEV uint32_t smem_u32(const void* p) {
@@ -108,13 +109,14 @@ BSG_DEV uint64_t globaltimer_ns() {
 }
 
 // Bounded wait: returns false (and records `code` in the error word) if the phase does not
-// complete within kWaitLimitNs.
-BSG_DEV bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, unsigned code) {
+// complete within limit_ns.
+BSG_DEV bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, unsigned code,
+                       uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, code);
       return false;
     }
@@ -589,6 +591,11 @@ struct Gemv {
     BSG_DEV uint32_t empty(int i) const { return base_u + bar_off + 8 * (stages + i); }
     BSG_DEV uint32_t sfull(int j) const { return base_u + bar_off + 8 * (2 * stages + j); }
     BSG_DEV uint32_t sempty(int j) const { return base_u + bar_off + 8 * (2 * stages + 4 + j); }
+    // abort word: set by a consumer warp that gave up a wait, before it releases any further
+    // slot; the producer stops issuing copies once it sees it
+    BSG_DEV volatile uint32_t* abort_word() const {
+      return reinterpret_cast<volatile uint32_t*>(base + bar_off + 8 * (2 * stages + 8));
+    }
   };
 
   // Position in a CTA's stream-K range: stage ks of `tile`.  The side ring holds one box of
@@ -689,6 +696,34 @@ struct Gemv {
                        pol);
   }
 
+  // Failure handling.  Every wait is bounded (KParams::wait_ns).  A consumer warp that gives up
+  // sets the CTA's abort word and from then on releases its slots without reading them; the
+  // producer, which learns of it with its next slot (the release orders the word before the
+  // arrival), issues nothing more.  Before the producer warp returns it waits -- bounded again --
+  // until every copy it issued has landed (pending weight and side boxes are tracked per ring
+  // slot with the parity of their use), so that no asynchronous copy outlives the CTA.  A test
+  // hook (KParams::skip_stage) makes CTA 0's producer leave out one stage of its range entirely,
+  // so that the consumers' wait on it runs out.
+  struct Pending {
+    uint32_t mask = 0, parity = 0;
+    BSG_DEV void issued(int slot, uint32_t phase) {
+      mask |= 1u << slot;
+      parity = (parity & ~(1u << slot)) | (phase << slot);
+    }
+  };
+
+  // Lane 0 (which issued them) waits until the tracked weight and side copies have landed.
+  static BSG_DEV void drain(const KParams& p, const Smem& sm, const Pending& wpend,
+                            const Pending& spend, int lane) {
+    if (lane != 0) return;
+    for (int s = 0; s < sm.stages; ++s)
+      if ((wpend.mask >> s) & 1u)
+        mbar_wait(sm.full(s), (wpend.parity >> s) & 1u, p.err, kErrTimeoutFull, p.wait_ns);
+    for (int j = 0; j < sm.side_slots; ++j)
+      if ((spend.mask >> j) & 1u)
+        mbar_wait(sm.sfull(j), (spend.parity >> j) & 1u, p.err, kErrTimeoutFull, p.wait_ns);
+  }
+
   static BSG_DEV void produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int lane) {
     const bool side = p.side_tma != 0;
     if (lane == 0) {
@@ -704,6 +739,8 @@ struct Gemv {
     const int64_t tile0 = s0 / spt;
     const Walk start{tile0, static_cast<int>(s0 - tile0 * spt), spt, (1 << p.rs_log2) - 1};
     Ring sr{sm.side_slots - 1, 1u, sm.side_slots};  // side ring: advanced before each use
+    const int skip = blockIdx.x == 0 ? p.skip_stage : -1;  // test hook (-1: none)
+    Pending wpend, spend;
 
     // phase 1: weights (and side boxes) of the first `pre` stages; fresh slots, no waits
     int pre = 0;
@@ -718,10 +755,14 @@ struct Gemv {
           ++boxes;
           sr.next();
           if (lane == 0) side_copy(p, sm, sr.slot, w, pol);
+          spend.issued(sr.slot, sr.phase);
         }
-        if (lane == 0) {
-          mbar_expect_tx(sm.full(i), kStageB);
-          weight_copy(p, sm, i, w, pol);
+        if (i != skip) {
+          if (lane == 0) {
+            mbar_expect_tx(sm.full(i), kStageB);
+            weight_copy(p, sm, i, w, pol);
+          }
+          wpend.issued(i, 0u);
         }
         pre = i + 1;
         w.next();
@@ -732,59 +773,71 @@ struct Gemv {
     Walk w = start;
     if constexpr (kPermuteAct) {  // all copies in flight together, one wait, then permute
       for (int i = 0; i < pre; ++i) {
-        act_copy(p, sm.act_u(i), w.ks, lane);
+        if (i != skip) act_copy(p, sm.act_u(i), w.ks, lane);
         w.next();
       }
       cp_async_wait_all();
-      for (int i = 0; i < pre; ++i) act_permute(p, sm.act_u(i), lane);
+      for (int i = 0; i < pre; ++i)
+        if (i != skip) act_permute(p, sm.act_u(i), lane);
       __syncwarp();  // every lane's permuted units before lane 0's (release) arrivals
       if (lane == 0)
-        for (int i = 0; i < pre; ++i) mbar_arrive(sm.full(i));
+        for (int i = 0; i < pre; ++i)
+          if (i != skip) mbar_arrive(sm.full(i));
     } else {
       for (int i = 0; i < pre; ++i) {
-        act_copy(p, sm.act_u(i), w.ks, lane);
-        cp_async_mbar_arrive(sm.full(i));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.full(i));
+        if (i != skip) {
+          act_copy(p, sm.act_u(i), w.ks, lane);
+          cp_async_mbar_arrive(sm.full(i));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sm.full(i));
+        }
         w.next();
       }
     }
     // phase 3: steady state
     Ring r{pre % sm.stages, pre == sm.stages ? 1u : 0u, sm.stages};
-    bool ok = true;
-    for (int i = pre; i < n && ok; ++i) {
+    for (int i = pre; i < n; ++i) {
       const bool seg_first = (i == 0) || (w.ks == 0);
+      bool ok = true;
       if (side && w.opens(seg_first)) {
         sr.next();
-        ok = mbar_wait(sm.sempty(sr.slot), sr.phase ^ 1u, p.err, kErrTimeoutEmpty);
-        if (ok && lane == 0) side_copy(p, sm, sr.slot, w, pol);
+        ok = mbar_wait(sm.sempty(sr.slot), sr.phase ^ 1u, p.err, kErrTimeoutEmpty, p.wait_ns);
+        ok = __all_sync(0xFFFFFFFFu, ok && *sm.abort_word() == 0u);
+        if (!ok) break;
+        if (lane == 0) side_copy(p, sm, sr.slot, w, pol);
+        spend.issued(sr.slot, sr.phase);
       }
-      if (ok) ok = mbar_wait(sm.empty(r.slot), r.phase ^ 1u, p.err, kErrTimeoutEmpty);
+      ok = mbar_wait(sm.empty(r.slot), r.phase ^ 1u, p.err, kErrTimeoutEmpty, p.wait_ns);
+      ok = __all_sync(0xFFFFFFFFu, ok && *sm.abort_word() == 0u);
       if (!ok) break;
-      const uint32_t full = sm.full(r.slot);
-      if constexpr (kPermuteAct) {  // weights first, then the activations' round trip
-        if (lane == 0) {
-          mbar_expect_tx(full, kStageB);
-          weight_copy(p, sm, r.slot, w, pol);
+      if (i != skip) {
+        const uint32_t full = sm.full(r.slot);
+        if constexpr (kPermuteAct) {  // weights first, then the activations' round trip
+          if (lane == 0) {
+            mbar_expect_tx(full, kStageB);
+            weight_copy(p, sm, r.slot, w, pol);
+          }
+          act_copy(p, sm.act_u(r.slot), w.ks, lane);
+          cp_async_wait_all();
+          act_permute(p, sm.act_u(r.slot), lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full);
+        } else {
+          act_copy(p, sm.act_u(r.slot), w.ks, lane);
+          cp_async_mbar_arrive(full);
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full, kStageB);
+            weight_copy(p, sm, r.slot, w, pol);
+          }
         }
-        act_copy(p, sm.act_u(r.slot), w.ks, lane);
-        cp_async_wait_all();
-        act_permute(p, sm.act_u(r.slot), lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full);
-      } else {
-        act_copy(p, sm.act_u(r.slot), w.ks, lane);
-        cp_async_mbar_arrive(full);
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full, kStageB);
-          weight_copy(p, sm, r.slot, w, pol);
-        }
+        wpend.issued(r.slot, r.phase);
       }
       r.next();
       w.next();
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+    drain(p, sm, wpend, spend, lane);
   }
 
   // ---- per-lane constants.  Consumer warp cw owns the tile's mma row group rg = cw (tile rows
@@ -1638,22 +1691,30 @@ struct Gemv {
     Walk w{first_tile, static_cast<int>(s0 - first_tile * spt), spt, (1 << p.rs_log2) - 1};
     Ring r{0, 0u, sm.stages};
     Ring sr{sm.side_slots - 1, 1u, sm.side_slots};
-    bool ok = true;
+    bool ok = true;  // false once a wait of this warp has run out (see produce)
     int64_t pend[2] = {0, 0};  // shared tiles whose arrival is deferred to the end of the range
     int np = 0;
     for (int i = 0; i < n;) {
       const int seg = (spt - w.ks) < (n - i) ? (spt - w.ks) : (n - i);  // stages of this segment
       const int64_t tile = w.tile;
       for (int q = 0; q < seg; ++q) {
-        if (SIDE && w.opens(q == 0)) {
-          sr.next();
-          if (ok) ok = mbar_wait(sm.sfull(sr.slot), sr.phase, p.err, kErrTimeoutFull);
-        }
-        if (ok) ok = mbar_wait(sm.full(r.slot), r.phase, p.err, kErrTimeoutFull);
         if (ok) {
-          const Sh sh{sm.base, sm.act_off + r.slot * sm.act_bytes,
-                      sm.side_off + sr.slot * sm.side_bytes};
-          consume_stage(R, L, sm.w(r.slot), sh, tile, w.ks, acc, cacc);
+          bool got = true;
+          if (SIDE && w.opens(q == 0)) {
+            sr.next();
+            got = mbar_wait(sm.sfull(sr.slot), sr.phase, p.err, kErrTimeoutFull, p.wait_ns);
+          }
+          if (got) got = mbar_wait(sm.full(r.slot), r.phase, p.err, kErrTimeoutFull, p.wait_ns);
+          ok = __all_sync(0xFFFFFFFFu, got);
+          if (ok) {
+            const Sh sh{sm.base, sm.act_off + r.slot * sm.act_bytes,
+                        sm.side_off + sr.slot * sm.side_bytes};
+            consume_stage(R, L, sm.w(r.slot), sh, tile, w.ks, acc, cacc);
+          } else if (lane == 0) {
+            *sm.abort_word() = 1u;  // before this warp's next (release) arrival
+          }
+        } else if (SIDE && w.opens(q == 0)) {
+          sr.next();
         }
         __syncwarp();
         mbar_arrive_if(sm.empty(r.slot), lane == 0);
@@ -1712,6 +1773,7 @@ BSG_DEV void gemv_cta(const KParams& p) {
       mbar_init(sm.sfull(j), 1);
       mbar_init(sm.sempty(j), kConsumerWarps);
     }
+    *sm.abort_word() = 0u;
     fence_mbar_init();
   }
   __syncthreads();

@@ -7,12 +7,15 @@
 
 namespace bsg {
 
-// Launch kernel `k` (one instantiation; `attr_smem` / `attr_cluster` are its own records of the
-// attributes already set).
+// Launch kernel `k` (one instantiation; `rec` is its own record of the attributes already set,
+// per device and context).
 template <class Kernel>
-int launch_kernel(Kernel k, std::atomic<int>& attr_smem, std::atomic<int>& attr_cluster,
-                  const KParams& p, int ctas, int smem, cudaStream_t s) {
-  if (smem > attr_smem.load()) {
+int launch_kernel(Kernel k, AttrRecord& rec, const KParams& p, int ctas, int smem, cudaStream_t s) {
+  int dev = -1;
+  uint64_t ctx = 0;
+  if (!current_device_context(&dev, &ctx)) return BSGEMV_ERR_CUDA;
+  const int d = rec.slot(dev, ctx);
+  if (smem > rec.smem[d].load()) {
     // One shared-memory carveout (the largest) for every instantiation: an SM holds CTAs of
     // kernels with different carveouts only after draining, which would serialise consecutive
     // calls that programmatic dependent launch otherwise overlaps.
@@ -20,12 +23,12 @@ int launch_kernel(Kernel k, std::atomic<int>& attr_smem, std::atomic<int>& attr_
         cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return BSGEMV_ERR_CUDA;
-    attr_smem.store(smem);
+    rec.smem[d].store(smem);
   }
-  if (p.cluster > 8 && attr_cluster.load() == 0) {
+  if (p.cluster > 8 && rec.cluster[d].load() == 0) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return BSGEMV_ERR_CUDA;
-    attr_cluster.store(1);
+    rec.cluster[d].store(1);
   }
   // Programmatic dependent launch: the kernel may start while the previous kernel in the stream
   // drains; it waits (griddepcontrol.wait) before touching anything that kernel could write.
@@ -54,18 +57,14 @@ int launch_kernel(Kernel k, std::atomic<int>& attr_smem, std::atomic<int>& attr_
 
 template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA = false>
 int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
-  static std::atomic<int> attr_smem{0};     // largest dynamic smem already granted
-  static std::atomic<int> attr_cluster{0};  // non-portable cluster sizes allowed
-  return launch_kernel(bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, PA>, attr_smem, attr_cluster, p,
-                       ctas, smem, s);
+  static AttrRecord rec;
+  return launch_kernel(bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, PA>, rec, p, ctas, smem, s);
 }
 
 template <int FMT, bool BF16, bool ZP, int CPB, int COLS>
 int launch_one_cc(const KParams& p, int ctas, int smem, cudaStream_t s) {
-  static std::atomic<int> attr_smem{0};
-  static std::atomic<int> attr_cluster{0};
-  return launch_kernel(bsgemv_fma_kernel<FMT, BF16, ZP, CPB, COLS>, attr_smem, attr_cluster, p,
-                       ctas, smem, s);
+  static AttrRecord rec;
+  return launch_kernel(bsgemv_fma_kernel<FMT, BF16, ZP, CPB, COLS>, rec, p, ctas, smem, s);
 }
 
 // CUDA-core variant (M <= 8): dispatch over zero points and chunks per scale block; COLS = 1

@@ -8,12 +8,19 @@
 // fixed scratch area that is part of the library's device image.
 //
 // The scratch area is the file-scope array below.  Every GPU that loads the library holds it
-// (kScratchBytes, about 5.2 MiB) until the process exits.  Its device address is looked up once
-// per device, on the first call made with that device current; that first call should happen
-// before any stream capture.  All calls on a device share the one array: two calls that overlap
-// on the GPU (different streams, or different host threads) race on it and give wrong results,
-// so callers serialise them.  Each call clears the arrival counters and the error word it uses
-// before its kernel runs; the partial sums need no clearing (each is written before it is read).
+// (kScratchBytes, about 5.2 MiB) until the process exits.  Its device address is looked up on
+// the first call made with a device current, and again on the first call after that device's
+// context changed (a device reset ends the context the address belonged to); such a first call
+// should happen before any stream capture.  All calls on a device share the one array: two calls
+// that overlap on the GPU (different streams, or different host threads) race on it and give
+// wrong results, so callers serialise them.  Each call clears the arrival counters it uses
+// before its kernel runs; the partial sums need no clearing (each is written before it is
+// read).  The error word is not cleared by a call: a bounded wait that ran out stays recorded
+// until bsgemv_device_status(NULL, stream) reads and clears it.
+//
+// Every call runs the geometry of a plan sized for 16 rows, whatever its M, so that a row comes
+// out bit-identical for every M (the summation order of a row is fixed by the geometry), and
+// equal to what bsgemv_plan(..., max_M = 16) + bsgemv_run gives.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -40,23 +47,36 @@ constexpr size_t kScratchBytes = kHeaderBytes + kCounterBytes + kPartialBytes;
 // [error word][arrival counters][partial sums]
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+constexpr int kRows = 16;  // the geometry's max_M, for every call
+
+// Per device: the context the scratch address was looked up under, and the address.
+struct ScratchRecord {
+  std::atomic<uint64_t> ctx{0};
+  std::atomic<void*> addr{nullptr};
+};
+ScratchRecord g_scratch[bsg::kMaxDevices];
 std::mutex g_setup_mutex;
 
-// Device address of the scratch array on the current device `dev` (looked up on first use).
-int scratch_address(int dev, unsigned char** out) {
-  if (dev < 0 || dev >= kMaxDevices) return BSGEMV_ERR_UNSUPPORTED;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
+// Device address of the scratch array for the current device and context (looked up once per
+// device and context, with that device current).
+int scratch_address(unsigned char** out) {
+  int dev = -1;
+  uint64_t ctx = 0;
+  if (!bsg::current_device_context(&dev, &ctx)) return BSGEMV_ERR_CUDA;
+  ScratchRecord& r = g_scratch[dev];
+  void* p = r.addr.load(std::memory_order_acquire);
+  if (p == nullptr || r.ctx.load(std::memory_order_acquire) != ctx) {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
+    p = r.addr.load(std::memory_order_acquire);
+    if (p == nullptr || r.ctx.load(std::memory_order_acquire) != ctx) {
+      p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return BSGEMV_ERR_CUDA;
       }
-      g_scratch_addr[dev].store(p, std::memory_order_release);
+      r.addr.store(nullptr, std::memory_order_release);
+      r.ctx.store(ctx, std::memory_order_release);
+      r.addr.store(p, std::memory_order_release);
     }
   }
   *out = static_cast<unsigned char*>(p);
@@ -67,11 +87,24 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 }  // namespace
 
+namespace bsg {
+
+// The no-allocation path's error word on the current device (bsgemv_device_status(NULL, ...)).
+int noalloc_error_word(unsigned** out) {
+  unsigned char* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != BSGEMV_OK) return rc;
+  *out = reinterpret_cast<unsigned*>(scratch);
+  return BSGEMV_OK;
+}
+
+}  // namespace bsg
+
 extern "C" int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_t N, int64_t K,
                                   const void* A, const void* W, const void* scales,
                                   const void* zp, void* y, int M, void* stream) {
-  // The problem: same rules as bsgemv_plan, with max_M = M.
-  if (M < 1 || M > 16) return BSGEMV_ERR_INVALID_ARG;
+  // The problem: same rules as bsgemv_plan with max_M = 16.
+  if (M < 1 || M > kRows) return BSGEMV_ERR_INVALID_ARG;
   int dev = -1, sms = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -85,8 +118,8 @@ extern "C" int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_
   }
   if (major != 10 || minor != 3) return BSGEMV_ERR_UNSUPPORTED;
   bsg::Geometry g;
-  int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, M, sms, 0, 0, BSGEMV_SPLIT_AUTO,
-                                 0, &g);
+  int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, kRows, sms, 0, 0,
+                                 BSGEMV_SPLIT_AUTO, 0, &g);
   if (rc != BSGEMV_OK) return rc;
   if (g.pub.ctas > kMaxCtas || g.pub.tiles > kMaxTiles || g.slot_floats > kMaxSlotFloats)
     return BSGEMV_ERR_SCRATCH_LIMIT;
@@ -102,7 +135,7 @@ extern "C" int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_
   if (g.fmt == bsg::kNvfp4 && !aligned(zp, 4)) return BSGEMV_ERR_MISALIGNED;
 
   unsigned char* scratch = nullptr;
-  rc = scratch_address(dev, &scratch);
+  rc = scratch_address(&scratch);
   if (rc != BSGEMV_OK) return rc;
   unsigned* err = reinterpret_cast<unsigned*>(scratch);
   unsigned* counters = reinterpret_cast<unsigned*>(scratch + kHeaderBytes);
@@ -115,9 +148,9 @@ extern "C" int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_
   bsg::fill_params(g, maps, A, W, scales, zp, y, M, partials, counters, err, &k);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // clear the error word and the arrival counters this call uses (stream-ordered, no allocation)
-  if (cudaMemsetAsync(scratch, 0,
-                      kHeaderBytes + size_t(g.pub.tiles) * bsg::kConsumerWarps * sizeof(unsigned),
+  // clear the arrival counters this call uses (stream-ordered, no allocation); the error word
+  // keeps what earlier calls recorded until it is read
+  if (cudaMemsetAsync(counters, 0, size_t(g.pub.tiles) * bsg::kConsumerWarps * sizeof(unsigned),
                       s) != cudaSuccess)
     return BSGEMV_ERR_CUDA;
   return bsg::launch_gemv(g, k, s);

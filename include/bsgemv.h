@@ -238,9 +238,24 @@ int bsgemv_geometry_for(int format, int block_size, int has_zp, int64_t N, int64
 /*
  * Synchronise `stream`, then read and clear the plan's device error word.  Returns BSGEMV_OK,
  * BSGEMV_ERR_DEVICE_TIMEOUT if a kernel of this plan abandoned a bounded wait since the last
- * check, or BSGEMV_ERR_CUDA if the synchronisation failed.
+ * check, or BSGEMV_ERR_CUDA if the synchronisation failed.  plan = NULL reads and clears the
+ * error word of bsgemv_run_noalloc on the current device instead (kept across its calls until
+ * read here).  Every wait of the kernels is bounded (4 s): a kernel that gives one up stops
+ * reading its copies, waits (bounded again) for the copies it issued to land, completes its
+ * partial sums so that the plan stays usable, and returns; its output is not valid.
  */
 int bsgemv_device_status(bsgemv_plan_t plan, void* stream);
+
+/*
+ * Test hook of the failure path above (the method's pages have no counterpart; it exercises this
+ * library's bounded waits without faulting the GPU).  skip_stage >= 0: in the plan's next calls
+ * the copy warp of CTA 0 leaves out stage `skip_stage` of that CTA's range (nothing is copied
+ * for it, so its consumer warps' wait on it runs out); -1: none.  wait_ns > 0: the calls' waits
+ * give up after wait_ns nanoseconds instead of 4 s; 0: the default.  Host only, no CUDA call;
+ * returns BSGEMV_ERR_INVALID_ARG for NULL, skip_stage < -1 or wait_ns < 0.
+ * bsgemv_plan_set_test_fault(plan, -1, 0) restores normal calls.
+ */
+int bsgemv_plan_set_test_fault(bsgemv_plan_t plan, int skip_stage, int64_t wait_ns);
 
 /*
  * The GEMV without any allocation, for callers that cannot call cudaMalloc: runtimes that own
@@ -248,18 +263,22 @@ int bsgemv_device_status(bsgemv_plan_t plan, void* stream);
  * an allocation could fail or synchronise at the wrong moment.  (The method's pages have no
  * counterpart; this is a property of this library's interface.)
  *
- * Arguments as bsgemv_plan plus bsgemv_run, with max_M = M; no plan is created.  Instead of a
- * plan's cudaMalloc'd workspace the cross-CTA reduction uses one fixed scratch area compiled into
- * the library (a file-scope device array of about 5.2 MiB that every GPU loading the library
- * holds until the process exits).  Limits: M <= 16 (BSGEMV_ERR_INVALID_ARG beyond), N <= 524288
- * output columns and at most 640
- * persistent CTAs (a 152-SM GB300 uses 608); beyond them the call returns
+ * Arguments as bsgemv_plan plus bsgemv_run; no plan is created.  Every call runs the geometry of
+ * a plan sized for 16 rows, whatever its M: a row's result is bit-identical for every M and
+ * equal to bsgemv_plan(..., max_M = 16) + bsgemv_run.  Instead of a plan's cudaMalloc'd
+ * workspace the cross-CTA reduction uses one fixed scratch area compiled into the library (a
+ * file-scope device array of about 5.2 MiB that every GPU loading the library holds until the
+ * process exits).  Limits: M <= 16 (BSGEMV_ERR_INVALID_ARG beyond), N <= 524288 output columns
+ * and at most 640 persistent CTAs (a 152-SM GB300 uses 456); beyond them the call returns
  * BSGEMV_ERR_SCRATCH_LIMIT and does nothing.  The first call on a device looks up the scratch
- * area's device address (with that device current); make that first call before any stream
- * capture.  Every call on a device shares the one scratch area: calls that overlap on the GPU
- * (other streams, other host threads) race on it and give wrong results, so serialise them.
- * Each call clears the counters it uses with cudaMemsetAsync on `stream` before its kernel; it
- * calls no cudaMalloc, cudaFree or allocating routine.  Enqueue only; no synchronisation.
+ * area's device address (with that device current), and so does the first call after the
+ * device's context changed (e.g. after cudaDeviceReset); make such a first call before any
+ * stream capture.  Every call on a device shares the one scratch area: calls that overlap on
+ * the GPU (other streams, other host threads) race on it and give wrong results, so serialise
+ * them.  Each call clears the counters it uses with cudaMemsetAsync on `stream` before its
+ * kernel; it calls no cudaMalloc, cudaFree or allocating routine.  A bounded wait that ran out
+ * in one of these calls is reported by bsgemv_device_status(NULL, stream).  Enqueue only; no
+ * synchronisation.
  */
 int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_t N, int64_t K,
                        const void* A, const void* W, const void* scales, const void* zp, void* y,

@@ -30,6 +30,7 @@ int main(void) {
   CHECK(bsgemv_destroy(NULL) == BSGEMV_OK && bsgemv_dense_destroy(NULL) == BSGEMV_OK);
   bsgemv_plan_t plan = NULL;
   CHECK(bsgemv_plan(&plan, BSGEMV_INT8, 48, 1, 64, 512, 1) == BSGEMV_ERR_UNSUPPORTED && !plan);
+  CHECK(bsgemv_plan_set_test_fault(NULL, -1, 0) == BSGEMV_ERR_INVALID_ARG);
   CHECK(bsgemv_version() >= 100);
   printf("ok\n");
   return 0;
