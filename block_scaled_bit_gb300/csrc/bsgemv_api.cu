@@ -17,7 +17,8 @@
 #include "bsgemv_internal.h"
 
 struct bsgemv_plan_s {
-  bsg::Geometry geo;
+  bsg::Geometry geo;                 // the plan's geometry (ring laid out for max_M rows)
+  std::vector<bsg::Geometry> rows;   // [M - 1]: the same split, the ring laid out for M rows
   int format = 0;
   int device = -1;
   int sm_count = 0;
@@ -98,12 +99,23 @@ int alloc_workspace(bsgemv_plan_s* p) {
 
 int rebuild_geometry(bsgemv_plan_s* p) {
   bsg::Geometry geo;
-  const int rc = bsg::compute_geometry(p->format, p->geo.block_size, p->geo.has_zp, p->geo.N,
-                                       p->geo.K, p->geo.max_M, p->sm_count, p->ctas_override,
-                                       p->stages_override, p->split, p->cluster, &geo);
+  const int max_M = p->geo.max_M;
+  int rc = bsg::compute_geometry(p->format, p->geo.block_size, p->geo.has_zp, p->geo.N, p->geo.K,
+                                 max_M, p->sm_count, p->ctas_override, p->stages_override,
+                                 p->split, p->cluster, &geo);
   if (rc != BSGEMV_OK) return rc;
-  if (p->variant_override == BSGEMV_VARIANT_CUDA_CORE) geo.pub.variant = BSGEMV_VARIANT_CUDA_CORE;
+  std::vector<bsg::Geometry> rows(max_M);
+  for (int m = 1; m <= max_M && rc == BSGEMV_OK; ++m)
+    rc = bsg::compute_geometry(p->format, p->geo.block_size, p->geo.has_zp, p->geo.N, p->geo.K,
+                               max_M, p->sm_count, p->ctas_override, p->stages_override, p->split,
+                               p->cluster, &rows[m - 1], m);
+  if (rc != BSGEMV_OK) return rc;
+  if (p->variant_override == BSGEMV_VARIANT_CUDA_CORE) {
+    geo.pub.variant = BSGEMV_VARIANT_CUDA_CORE;
+    for (auto& r : rows) r.pub.variant = BSGEMV_VARIANT_CUDA_CORE;
+  }
   p->geo = geo;
+  p->rows.swap(rows);
   return alloc_workspace(p);
 }
 
@@ -131,8 +143,8 @@ int prepare_params(bsgemv_plan_s* p, const void* A, const void* W, const void* s
     hit->zp = zp;
   }
   hit->last_use = ++p->use_clock;
-  bsg::fill_params(p->geo, hit->maps, A, W, scales, zp, y, M, p->partials, p->counters, p->err,
-                   &p->params);
+  bsg::fill_params(p->rows[M - 1], hit->maps, A, W, scales, zp, y, M, p->partials, p->counters,
+                   p->err, &p->params);
   p->params.skip_stage = p->fault_skip;
   if (p->fault_wait_ns > 0) p->params.wait_ns = p->fault_wait_ns;
   return BSGEMV_OK;
@@ -166,7 +178,10 @@ int validate_run(const bsgemv_plan_s* p, const void* A, const void* W, const voi
   return BSGEMV_OK;
 }
 
-int launch(bsgemv_plan_s* p, cudaStream_t s) { return bsg::launch_gemv(p->geo, p->params, s); }
+// The geometry of the prepared call (its ring laid out for the call's M).
+int launch(bsgemv_plan_s* p, cudaStream_t s) {
+  return bsg::launch_gemv(p->rows[p->params.M - 1], p->params, s);
+}
 
 }  // namespace
 

@@ -42,7 +42,7 @@ namespace {
 // The geometry for a kernel of `mt` n8 activation tiles (mt >= mt_for_m(max_M)).
 int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
                        int sm_count, int ctas_override, int stages_override, int split,
-                       int cluster, int mt, Geometry* g) {
+                       int cluster, int mt, int rows, Geometry* g) {
   if (g == nullptr) return BSGEMV_ERR_INVALID_ARG;
   std::memset(g, 0, sizeof(*g));
   if ((format & ~(0xFF | BSGEMV_ACT_BF16)) != 0) return BSGEMV_ERR_INVALID_ARG;
@@ -51,6 +51,7 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   if (has_zp != 0 && has_zp != 1) return BSGEMV_ERR_INVALID_ARG;
   if (N < 1 || K < 1 || max_M < 1 || max_M > kMaxM || sm_count < 1 || block_size < 1)
     return BSGEMV_ERR_INVALID_ARG;
+  if (rows < 1 || rows > max_M) return BSGEMV_ERR_INVALID_ARG;
   if (ctas_override < 0 || stages_override < 0 || stages_override > kMaxStages)
     return BSGEMV_ERR_INVALID_ARG;
   if (split < BSGEMV_SPLIT_AUTO || split > BSGEMV_SPLIT_CLUSTER || cluster < 0 ||
@@ -91,7 +92,8 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
 
   // activation ring: per stage, max_M rows of the stage's k (2 kc bytes) padded by one chunk's
   // activation bytes (32 or 64: consecutive rows start in different banks)
-  g->act_bytes = max_M * (2 * g->kc + (four ? 64 : 32));
+  const int act_pitch = 2 * g->kc + (four ? 64 : 32);
+  g->act_bytes = max_M * act_pitch;
   // side ring: one box holds kSideScaleBytes of scales per row (64 / es blocks), i.e.
   // 2^rs_log2 stages, and the zero points of the same blocks
   const int blocks_per_box = kSideScaleBytes / g->scale_es;
@@ -218,6 +220,19 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
     stages = stages_override;
     if (smem_for(stages) > budget) ctas_per_sm = 1;
   }
+  // Everything above is decided for max_M rows (and so is the same for every call of a plan).
+  // The ring of a call with fewer rows holds fewer activation bytes per stage, so the same
+  // per-CTA budget takes more stages: the ring depth changes nothing that a row's summation
+  // order depends on (which CTA sums which stages, and in what order), only how many stages
+  // are in flight.
+  if (rows < max_M) {
+    g->act_bytes = rows * act_pitch;
+    if (stages_override == 0) {
+      const int b = ctas_per_sm == 1 ? kSmemPerBlockMax : budget;
+      stages = max_stages;
+      while (stages > min_stages && smem_for(stages) > b) --stages;
+    }
+  }
   g->side_slots = (C > 0 && g->side_bytes != 0 && cluster_one_slot(C)) ? 1 : side_slots_for(stages);
   g->act_off = stages * g->stage_bytes;
   g->side_off = g->act_off + act_ring(stages);  // side boxes are TMA destinations: 128-aligned
@@ -263,10 +278,11 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
 
 int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
                      int sm_count, int ctas_override, int stages_override, int split, int cluster,
-                     Geometry* g) {
+                     Geometry* g, int rows) {
   const int mt = (max_M >= 1 && max_M <= kMaxM) ? mt_for_m(max_M) : 1;
+  if (rows == 0) rows = max_M;
   int rc = geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, ctas_override,
-                              stages_override, split, cluster, mt, g);
+                              stages_override, split, cluster, mt, rows, g);
   if (rc != BSGEMV_OK || mt != 3 || split != BSGEMV_SPLIT_AUTO || ctas_override != 0 ||
       stages_override != 0)
     return rc;
@@ -276,7 +292,7 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
   // shapes ran 15-25 % faster at 2 CTAs per SM; larger shapes 13-22 % faster at 3).
   Geometry four;
   if (geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, 0, 0, split, 0, 4,
-                         &four) != BSGEMV_OK)
+                         rows, &four) != BSGEMV_OK)
     return rc;
   const int C4 = four.pub.cluster, C3 = g->pub.cluster;
   if (C4 >= 2 && C3 < C4 && (four.pub.stages_per_tile + C4 - 1) / C4 <= 4) *g = four;

@@ -176,13 +176,9 @@ int launch_gemv(const Geometry& g, const KParams& k, cudaStream_t s) {
     }
     return BSGEMV_ERR_INVALID_ARG;
   }
-  // n8 activation tiles per call; 0: int4 with at most 2 rows and at least 5 stages per CTA,
-  // one tile and the activations permuted by the producer (same arithmetic; measured faster
-  // there, slower for short CTA ranges, where the producer's extra wait is on the critical path)
-  const int64_t per_cta = (g.pub.total_stages + g.pub.ctas - 1) / g.pub.ctas;
-  const bool pa = g.fmt == kInt4 && k.M <= 2 && per_cta >= 5;
-  // calls with more than 16 rows run the tile count their plan was sized for (3 or 4)
-  const int mt = k.M > 16 ? g.mt_max : k.M > 8 ? 2 : pa ? 0 : 1;
+  // n8 activation tiles per call: calls with more than 16 rows run the tile count their plan
+  // was sized for (3 or 4)
+  const int mt = k.M > 16 ? g.mt_max : k.M > 8 ? 2 : 1;
   const int ctas = g.pub.ctas, smem = g.pub.smem_bytes;
   const int bm = block_mode(g.fmt, g.block_size);
   switch (g.fmt) {

@@ -33,7 +33,7 @@ constexpr int kMaxM = 32;             // activation rows per call: up to four n8
 // 128 registers some of them spill).
 constexpr int ctas_per_sm_for_mt(int mt) { return mt == 1 ? 4 : mt <= 3 ? 3 : 2; }
 // n8 activation tiles of the kernel a plan is sized for (and of the kernel a call with M rows
-// runs, apart from the int4 variant with permuted activations).
+// runs).
 constexpr int mt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 24 ? 3 : 4; }
 constexpr int kBoxRowBytes = 128;     // bytes per row of one weight TMA box (128-byte swizzle)
 constexpr int kStageK = 256;          // k per stage for every format: one 128-byte box per row for
@@ -117,9 +117,11 @@ constexpr int kSideScaleBytes = 64;
 
 // Validates the problem and fills the geometry for `sm_count` SMs.  Pure host code.
 // split = enum bsgemv_split, cluster = CTAs per tile for BSGEMV_SPLIT_CLUSTER (0 = chosen).
+// rows (1 .. max_M, 0 = max_M): the layout of the shared-memory ring for a call with that many
+// activation rows; the split, CTA count and residency are those of max_M whatever `rows` is.
 int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
                      int sm_count, int ctas_override, int stages_override, int split, int cluster,
-                     Geometry* g);
+                     Geometry* g, int rows = 0);
 
 constexpr int kMaxCluster = 16;     // CTAs per cluster (above 8: non-portable cluster size)
 constexpr int kMaxAutoCluster = 8;  // largest cluster the automatic split picks

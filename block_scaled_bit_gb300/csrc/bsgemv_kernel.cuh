@@ -213,22 +213,6 @@ BSG_DEV void ldsm_x4_at(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                : "r"(addr), "n"(OFF));
 }
 
-BSG_DEV uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-BSG_DEV void sts128(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-
-BSG_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 BSG_DEV uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -547,9 +531,9 @@ BSG_DEV void zp_consts(uint32_t zp, uint32_t& zl, uint32_t& zh) {
 // products are formed by fp32 FMAs on the CUDA cores (each lane over its own k positions of
 // the tile rows it holds, for CC = 1 or 8 activation rows: calls with M = 1, or M <= 8)
 // instead of mma.sync.
-template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA, int CC = 0>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, int CC = 0>
 struct Gemv {
-  static_assert(CC == 0 || ((CC == 1 || CC == 8) && MT == 1 && !PA),
+  static_assert(CC == 0 || ((CC == 1 || CC == 8) && MT == 1),
                 "CUDA-core variant: 1 or 8 activation rows, natural activation order");
   static constexpr int kCcCols = CC > 0 ? CC : 1;  // activation rows a CUDA-core lane accumulates
   static constexpr bool kFour = (FMT == kInt4 || FMT == kNvfp4);
@@ -591,8 +575,7 @@ struct Gemv {
     BSG_DEV uint32_t empty(int i) const { return base_u + bar_off + 8 * (stages + i); }
     BSG_DEV uint32_t sfull(int j) const { return base_u + bar_off + 8 * (2 * stages + j); }
     BSG_DEV uint32_t sempty(int j) const { return base_u + bar_off + 8 * (2 * stages + 4 + j); }
-    // abort word: set by a consumer warp that gave up a wait, before it releases any further
-    // slot; the producer stops issuing copies once it sees it
+    // failure word: set by a warp whose bounded wait ran out (read once, at the CTA's end)
     BSG_DEV volatile uint32_t* abort_word() const {
       return reinterpret_cast<volatile uint32_t*>(base + bar_off + 8 * (2 * stages + 8));
     }
@@ -651,29 +634,6 @@ struct Gemv {
     }
   }
 
-  // int4: the decoder pairs k with k + 4 (the two nibbles a LOP3 select takes from one word), so
-  // the activation fragments must pair them too.  The PA kernels (int4, calls with M <= 2) store
-  // the stage's activations in that order: each 16-byte unit (k0 .. k7 of a lane's chunk
-  // segment) becomes (k0, k4), (k1, k5), (k2, k6), (k3, k7), permuted in place by the producer,
-  // once per stage, after its copies have landed -- instead of every consumer warp permuting its
-  // fragments.  Measured on GB300: int4 lm_head 0.68 -> 0.74 of the copy bandwidth at M = 1;
-  // from 4 rows on, the producer's share (it grows with M) costs more than it saves, and the
-  // other kernels let the consumers permute.  The arithmetic is the same either way.
-  static constexpr bool kPermuteAct = PA;
-  static_assert(!PA || (FMT == kInt4 && MT == 1), "permuted activations: int4, one n8 tile");
-
-  static BSG_DEV void act_permute(const KParams& p, uint32_t dst, int lane) {
-    constexpr int kUpr = kKc / 8;
-    const int units = p.M * kUpr;
-    for (int u = lane; u < units; u += 32) {
-      const int m = u / kUpr, qg = u % kUpr;
-      const uint32_t d = dst + m * kActPitch + qg * 16;
-      const uint4 v = lds128(d);
-      sts128(d, make_uint4(prmt<0x5410u>(v.x, v.z), prmt<0x7632u>(v.x, v.z), prmt<0x5410u>(v.y, v.w),
-                           prmt<0x7632u>(v.y, v.w)));
-    }
-  }
-
   // The weight boxes of stage (tile, ks) into ring slot i (lane 0).
   static BSG_DEV void weight_copy(const KParams& p, const Smem& sm, int i, const Walk& w,
                                   uint64_t pol) {
@@ -697,34 +657,41 @@ struct Gemv {
   }
 
   // Failure handling.  Every wait is bounded (KParams::wait_ns).  A consumer warp that gives up
-  // sets the CTA's abort word and from then on releases its slots without reading them; the
-  // producer, which learns of it with its next slot (the release orders the word before the
-  // arrival), issues nothing more.  Before the producer warp returns it waits -- bounded again --
+  // records it in the CTA's failure word and from then on neither reads nor releases its ring
+  // slots, so the copy warp's own wait for a free slot runs out in turn and it stops issuing
+  // (a slot is never refilled while a copy into it may be in flight).  After both roles have
+  // returned, the CTA's copy warp -- only when the failure word is set -- waits, bounded again,
   // until every copy it issued has landed (pending weight and side boxes are tracked per ring
-  // slot with the parity of their use), so that no asynchronous copy outlives the CTA.  A test
-  // hook (KParams::skip_stage) makes CTA 0's producer leave out one stage of its range entirely,
-  // so that the consumers' wait on it runs out.
+  // slot with the parity of their use), so that no asynchronous copy outlives the CTA; on the
+  // normal path the consumers have waited for every copy already.  A test hook
+  // (KParams::skip_stage) makes CTA 0's copy warp leave out one stage of its range entirely, so
+  // that the consumers' wait on it runs out.
   struct Pending {
-    uint32_t mask = 0, parity = 0;
-    BSG_DEV void issued(int slot, uint32_t phase) {
-      mask |= 1u << slot;
-      parity = (parity & ~(1u << slot)) | (phase << slot);
+    uint32_t wmask = 0, wpar = 0, smask = 0, spar = 0;  // weight / side slots, parity of the use
+    BSG_DEV void weight(int slot, uint32_t phase) {
+      wmask |= 1u << slot;
+      wpar = (wpar & ~(1u << slot)) | (phase << slot);
+    }
+    BSG_DEV void side(int slot, uint32_t phase) {
+      smask |= 1u << slot;
+      spar = (spar & ~(1u << slot)) | (phase << slot);
     }
   };
 
   // Lane 0 (which issued them) waits until the tracked weight and side copies have landed.
-  static BSG_DEV void drain(const KParams& p, const Smem& sm, const Pending& wpend,
-                            const Pending& spend, int lane) {
+  static BSG_DEV void drain(const KParams& p, const Smem& sm, const Pending& pd, int lane) {
     if (lane != 0) return;
     for (int s = 0; s < sm.stages; ++s)
-      if ((wpend.mask >> s) & 1u)
-        mbar_wait(sm.full(s), (wpend.parity >> s) & 1u, p.err, kErrTimeoutFull, p.wait_ns);
+      if ((pd.wmask >> s) & 1u)
+        mbar_wait(sm.full(s), (pd.wpar >> s) & 1u, p.err, kErrTimeoutFull, p.wait_ns);
     for (int j = 0; j < sm.side_slots; ++j)
-      if ((spend.mask >> j) & 1u)
-        mbar_wait(sm.sfull(j), (spend.parity >> j) & 1u, p.err, kErrTimeoutFull, p.wait_ns);
+      if ((pd.smask >> j) & 1u)
+        mbar_wait(sm.sfull(j), (pd.spar >> j) & 1u, p.err, kErrTimeoutFull, p.wait_ns);
   }
 
-  static BSG_DEV void produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int lane) {
+  // Returns with the copy warp's record of what it issued (for the end-of-CTA drain).
+  static BSG_DEV Pending produce(const KParams& p, const Smem& sm, int64_t s0, int64_t s1,
+                                 int lane) {
     const bool side = p.side_tma != 0;
     if (lane == 0) {
       prefetch_tmap(&p.tm_w);
@@ -740,7 +707,7 @@ struct Gemv {
     const Walk start{tile0, static_cast<int>(s0 - tile0 * spt), spt, (1 << p.rs_log2) - 1};
     Ring sr{sm.side_slots - 1, 1u, sm.side_slots};  // side ring: advanced before each use
     const int skip = blockIdx.x == 0 ? p.skip_stage : -1;  // test hook (-1: none)
-    Pending wpend, spend;
+    Pending pd;
 
     // phase 1: weights (and side boxes) of the first `pre` stages; fresh slots, no waits
     int pre = 0;
@@ -755,14 +722,14 @@ struct Gemv {
           ++boxes;
           sr.next();
           if (lane == 0) side_copy(p, sm, sr.slot, w, pol);
-          spend.issued(sr.slot, sr.phase);
+          pd.side(sr.slot, sr.phase);
         }
         if (i != skip) {
           if (lane == 0) {
             mbar_expect_tx(sm.full(i), kStageB);
             weight_copy(p, sm, i, w, pol);
           }
-          wpend.issued(i, 0u);
+          pd.weight(i, 0u);
         }
         pre = i + 1;
         w.next();
@@ -771,73 +738,46 @@ struct Gemv {
     pdl_wait();
     // phase 2: activations of those stages; lane 0's arrival then releases each slot
     Walk w = start;
-    if constexpr (kPermuteAct) {  // all copies in flight together, one wait, then permute
-      for (int i = 0; i < pre; ++i) {
-        if (i != skip) act_copy(p, sm.act_u(i), w.ks, lane);
-        w.next();
+    for (int i = 0; i < pre; ++i) {
+      if (i != skip) {
+        act_copy(p, sm.act_u(i), w.ks, lane);
+        cp_async_mbar_arrive(sm.full(i));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.full(i));
       }
-      cp_async_wait_all();
-      for (int i = 0; i < pre; ++i)
-        if (i != skip) act_permute(p, sm.act_u(i), lane);
-      __syncwarp();  // every lane's permuted units before lane 0's (release) arrivals
-      if (lane == 0)
-        for (int i = 0; i < pre; ++i)
-          if (i != skip) mbar_arrive(sm.full(i));
-    } else {
-      for (int i = 0; i < pre; ++i) {
-        if (i != skip) {
-          act_copy(p, sm.act_u(i), w.ks, lane);
-          cp_async_mbar_arrive(sm.full(i));
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sm.full(i));
-        }
-        w.next();
-      }
+      w.next();
     }
     // phase 3: steady state
     Ring r{pre % sm.stages, pre == sm.stages ? 1u : 0u, sm.stages};
+    bool ok = true;
     for (int i = pre; i < n; ++i) {
       const bool seg_first = (i == 0) || (w.ks == 0);
-      bool ok = true;
       if (side && w.opens(seg_first)) {
         sr.next();
         ok = mbar_wait(sm.sempty(sr.slot), sr.phase ^ 1u, p.err, kErrTimeoutEmpty, p.wait_ns);
-        ok = __all_sync(0xFFFFFFFFu, ok && *sm.abort_word() == 0u);
         if (!ok) break;
         if (lane == 0) side_copy(p, sm, sr.slot, w, pol);
-        spend.issued(sr.slot, sr.phase);
+        pd.side(sr.slot, sr.phase);
       }
       ok = mbar_wait(sm.empty(r.slot), r.phase ^ 1u, p.err, kErrTimeoutEmpty, p.wait_ns);
-      ok = __all_sync(0xFFFFFFFFu, ok && *sm.abort_word() == 0u);
       if (!ok) break;
+      const uint32_t full = sm.full(r.slot);
       if (i != skip) {
-        const uint32_t full = sm.full(r.slot);
-        if constexpr (kPermuteAct) {  // weights first, then the activations' round trip
-          if (lane == 0) {
-            mbar_expect_tx(full, kStageB);
-            weight_copy(p, sm, r.slot, w, pol);
-          }
-          act_copy(p, sm.act_u(r.slot), w.ks, lane);
-          cp_async_wait_all();
-          act_permute(p, sm.act_u(r.slot), lane);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(full);
-        } else {
-          act_copy(p, sm.act_u(r.slot), w.ks, lane);
-          cp_async_mbar_arrive(full);
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive_expect_tx(full, kStageB);
-            weight_copy(p, sm, r.slot, w, pol);
-          }
+        act_copy(p, sm.act_u(r.slot), w.ks, lane);
+        cp_async_mbar_arrive(full);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, kStageB);
+          weight_copy(p, sm, r.slot, w, pol);
         }
-        wpend.issued(r.slot, r.phase);
+        pd.weight(r.slot, r.phase);
       }
       r.next();
       w.next();
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    drain(p, sm, wpend, spend, lane);
+    if (!ok && lane == 0) *sm.abort_word() = 1u;
+    return pd;
   }
 
   // ---- per-lane constants.  Consumer warp cw owns the tile's mma row group rg = cw (tile rows
@@ -1080,12 +1020,7 @@ struct Gemv {
     for (int mt = 0; mt < MT; ++mt) {
       if constexpr (kFour) {
         const uint4 v = lsh<uint4>(sh.base + (sh.a + act_off(L, c, mt)));
-        if constexpr (kPermuteAct) {  // pairs (8t+j, 8t+j+4), stored so by the producer
-          b[mt][0][0] = v.x;
-          b[mt][0][1] = v.y;
-          b[mt][1][0] = v.z;
-          b[mt][1][1] = v.w;
-        } else if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
+        if constexpr (FMT == kInt4) {  // pairs (8t+j, 8t+j+4)
           b[mt][0][0] = prmt<0x5410u>(v.x, v.z);
           b[mt][0][1] = prmt<0x7632u>(v.x, v.z);
           b[mt][1][0] = prmt<0x5410u>(v.y, v.w);
@@ -1698,27 +1633,22 @@ struct Gemv {
       const int seg = (spt - w.ks) < (n - i) ? (spt - w.ks) : (n - i);  // stages of this segment
       const int64_t tile = w.tile;
       for (int q = 0; q < seg; ++q) {
-        if (ok) {
-          bool got = true;
-          if (SIDE && w.opens(q == 0)) {
-            sr.next();
-            got = mbar_wait(sm.sfull(sr.slot), sr.phase, p.err, kErrTimeoutFull, p.wait_ns);
-          }
-          if (got) got = mbar_wait(sm.full(r.slot), r.phase, p.err, kErrTimeoutFull, p.wait_ns);
-          ok = __all_sync(0xFFFFFFFFu, got);
-          if (ok) {
-            const Sh sh{sm.base, sm.act_off + r.slot * sm.act_bytes,
-                        sm.side_off + sr.slot * sm.side_bytes};
-            consume_stage(R, L, sm.w(r.slot), sh, tile, w.ks, acc, cacc);
-          } else if (lane == 0) {
-            *sm.abort_word() = 1u;  // before this warp's next (release) arrival
-          }
-        } else if (SIDE && w.opens(q == 0)) {
+        // (every lane of the converged warp sees the same barrier state and the same
+        // %globaltimer value at each step of the wait, so `ok` is the same in all lanes)
+        if (SIDE && w.opens(q == 0)) {
           sr.next();
+          if (ok) ok = mbar_wait(sm.sfull(sr.slot), sr.phase, p.err, kErrTimeoutFull, p.wait_ns);
+        }
+        if (ok) ok = mbar_wait(sm.full(r.slot), r.phase, p.err, kErrTimeoutFull, p.wait_ns);
+        if (ok) {
+          const Sh sh{sm.base, sm.act_off + r.slot * sm.act_bytes,
+                      sm.side_off + sr.slot * sm.side_bytes};
+          consume_stage(R, L, sm.w(r.slot), sh, tile, w.ks, acc, cacc);
         }
         __syncwarp();
-        mbar_arrive_if(sm.empty(r.slot), lane == 0);
-        if (SIDE && w.closes(q == seg - 1)) mbar_arrive_if(sm.sempty(sr.slot), lane == 0);
+        // after a wait ran out, the warp releases nothing more (see produce)
+        mbar_arrive_if(sm.empty(r.slot), ok && lane == 0);
+        if (SIDE && w.closes(q == seg - 1)) mbar_arrive_if(sm.sempty(sr.slot), ok && lane == 0);
         r.next();
         w.next();
       }
@@ -1736,6 +1666,7 @@ struct Gemv {
       zero(acc[0]);
     }
     if (np > 0) arrive_and_reduce(p, pend, np, cw, lane, gs);
+    if (!ok && lane == 0) *sm.abort_word() = 1u;
   }
 };
 
@@ -1778,10 +1709,18 @@ BSG_DEV void gemv_cta(const KParams& p) {
   }
   __syncthreads();
 
+  typename K::Pending pd;
   if (warp == 0) {
-    K::produce(p, sm, s0, s1, lane);
+    pd = K::produce(p, sm, s0, s1, lane);
   } else {
     K::consume(p, sm, s0, s1, warp - 1, lane);
+  }
+  // A wait that ran out anywhere in the CTA: the copy warp waits for what it issued (see
+  // produce) before the CTA's shared memory is given up.
+  __syncthreads();
+  if (warp == 0 && *sm.abort_word() != 0u) {
+    K::drain(p, sm, pd, lane);
+    __syncwarp();  // lane 0's waits end before the warp's aligned cluster barrier
   }
   if (p.cluster >= 2) {
     cluster_sync();  // every CTA of the cluster has stored its partials in the leader
@@ -1790,10 +1729,10 @@ BSG_DEV void gemv_cta(const KParams& p) {
 }
 
 // Tensor-core kernel (the default): products on mma.sync.m16n8k16.
-template <int FMT, bool BF16, int MT, bool ZP, int CPB, bool PA>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT))
     bsgemv_mma_kernel(const __grid_constant__ KParams p) {
-  gemv_cta<Gemv<FMT, BF16, MT, ZP, CPB, PA>>(p);
+  gemv_cta<Gemv<FMT, BF16, MT, ZP, CPB>>(p);
 }
 
 // CUDA-core kernel (BSGEMV_VARIANT_CUDA_CORE): products on fp32 FMAs, COLS = 1 (calls with
@@ -1801,7 +1740,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT))
 template <int FMT, bool BF16, bool ZP, int CPB, int COLS>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(1))
     bsgemv_fma_kernel(const __grid_constant__ KParams p) {
-  gemv_cta<Gemv<FMT, BF16, 1, ZP, CPB, false, COLS>>(p);
+  gemv_cta<Gemv<FMT, BF16, 1, ZP, CPB, COLS>>(p);
 }
 
 }  // namespace bsg

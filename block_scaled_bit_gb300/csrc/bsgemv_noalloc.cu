@@ -119,7 +119,7 @@ extern "C" int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_
   if (major != 10 || minor != 3) return BSGEMV_ERR_UNSUPPORTED;
   bsg::Geometry g;
   int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, kRows, sms, 0, 0,
-                                 BSGEMV_SPLIT_AUTO, 0, &g);
+                                 BSGEMV_SPLIT_AUTO, 0, &g, M);
   if (rc != BSGEMV_OK) return rc;
   if (g.pub.ctas > kMaxCtas || g.pub.tiles > kMaxTiles || g.slot_floats > kMaxSlotFloats)
     return BSGEMV_ERR_SCRATCH_LIMIT;

@@ -36,8 +36,8 @@ def cta0_range(g):
 
 @pytest.mark.parametrize("fmt,act,bs,zp,N,K,M,split", [
     ("int8", "f16", 128, True, 2048, 4096, 4, "stream_k"),     # tiles shared by several CTAs
-    ("int4", "bf16", 32, False, 40000, 2048, 1, "auto"),       # activations permuted by the copy warp
-    ("int4", "f16", 32, True, 40000, 2048, 3, "auto"),         # consumers permute them
+    ("int4", "bf16", 32, False, 40000, 2048, 1, "auto"),       # long CTA ranges, a deep ring
+    ("int4", "f16", 32, True, 40000, 2048, 3, "auto"),
     ("fp8", "f16", 128, False, 512, 2048, 9, "cluster"),       # cluster split, two n8 tiles
     ("nvfp4", "bf16", 16, False, 2048, 2048, 2, "auto"),
 ])
