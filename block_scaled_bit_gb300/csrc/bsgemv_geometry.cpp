@@ -4,7 +4,7 @@
 // and the SM count, never on M of a call, so every M run through one plan takes the same
 // per-row summation order (rows are bit-identical across M).
 //
-// Choices (the reasons are measurements on GB300; see the design notes):
+// Choices (each one the faster of the alternatives measured on GB300, as stated below):
 //   * 64 output columns per CTA tile, 4 consumer warps (one 16-row group each, over a whole
 //     stage) + 1 copy warp, 4 CTAs per SM (3 when max_M > 8, 2 when max_M > 24: more
 //     accumulator registers);

@@ -28,7 +28,7 @@
  *   [P5] "[CUDA] Batched small-M GEMV for MatMulNBits (4-bit/8-bit)" (PR #29451), Description and
  *        review: the standard [N, blocks, blob] weight layout and its packed zero points.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent (the plainest reading consistent with the rest of them):
  *   - int4 packing: two codes per byte, the LOW nibble holds the even k.
  *   - int4 zero points: [N, ceil(nb/2)] bytes, block b in nibble (b & 1) of byte b >> 1 (low nibble
  *     = even block).  int8 zero points: [N, nb] bytes.
