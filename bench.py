@@ -73,6 +73,8 @@ def parse_args():
     # --sweep / --one: plans sized for this many rows (default: the configuration's largest M up
     # to 8 for calls with M <= 8, else its largest M)
     ap.add_argument("--plan-max-M", type=int, default=0, help=argparse.SUPPRESS)
+    # --sweep: output columns per CTA tile of every plan (64 or 128; 0 = the plan's choice)
+    ap.add_argument("--tile-rows", type=int, default=0, help=argparse.SUPPRESS)
     # the dense small-N split-K GEMV against cuBLAS (torch.mm), streamed cold
     ap.add_argument("--dense", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--dense-shape", default=None, help=argparse.SUPPRESS)  # "N,K": one shape
@@ -591,6 +593,9 @@ def run_sweep(args):
                                             case.N, case.K, pm)
                     if args.variant != "auto":
                         assert plans[pm].set_override(variant=bsgemv.VARIANTS[args.variant]) == bsgemv.OK
+                    if args.tile_rows:
+                        rc = plans[pm].set_override(rows_per_tile=args.tile_rows)
+                        assert rc == bsgemv.OK, bsgemv.status_string(rc)
                     if args.autotune:
                         b = bufs[0]
                         plans[pm].autotune(b.A[:pm], b.W, b.scales, b.zp, b.y[:pm], M=pm, reps=10)

@@ -222,8 +222,9 @@ class Plan:
         _check(lib().bsgemv_debug_dequant(self._h, _ptr(W), _ptr(scales), _ptr(zp), _ptr(out),
                                           _stream(stream)), "bsgemv_debug_dequant")
 
-    def set_override(self, variant: int = 0, ctas: int = 0, stages: int = 0) -> int:
-        return lib().bsgemv_plan_set_override(self._h, variant, ctas, 0, stages)
+    def set_override(self, variant: int = 0, ctas: int = 0, stages: int = 0,
+                     rows_per_tile: int = 0) -> int:
+        return lib().bsgemv_plan_set_override(self._h, variant, ctas, rows_per_tile, stages)
 
     def set_split(self, split: str = "auto", cluster: int = 0) -> int:
         """K split of the tiles: "auto", "stream_k" or "cluster" (cluster = CTAs per tile)."""

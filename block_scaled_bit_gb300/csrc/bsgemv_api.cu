@@ -22,7 +22,7 @@ struct bsgemv_plan_s {
   int format = 0;
   int device = -1;
   int sm_count = 0;
-  int variant_override = 0, ctas_override = 0, stages_override = 0;
+  int variant_override = 0, ctas_override = 0, stages_override = 0, rows_override = 0;
   int split = BSGEMV_SPLIT_AUTO, cluster = 0;
   int fault_skip = -1;            // bsgemv_plan_set_test_fault
   uint64_t fault_wait_ns = 0;
@@ -100,16 +100,23 @@ int alloc_workspace(bsgemv_plan_s* p) {
 int rebuild_geometry(bsgemv_plan_s* p) {
   bsg::Geometry geo;
   const int max_M = p->geo.max_M;
+  // the CUDA-core variant runs 64-row tiles
+  const int tile_rows = p->variant_override == BSGEMV_VARIANT_CUDA_CORE
+                            ? (p->rows_override == bsg::kMaxRowsPerTile ? -1 : bsg::kBoxRows)
+                            : p->rows_override;
+  if (tile_rows < 0) return BSGEMV_ERR_UNSUPPORTED;
   int rc = bsg::compute_geometry(p->format, p->geo.block_size, p->geo.has_zp, p->geo.N, p->geo.K,
                                  max_M, p->sm_count, p->ctas_override, p->stages_override,
-                                 p->split, p->cluster, &geo);
+                                 p->split, p->cluster, &geo, max_M, tile_rows);
   if (rc != BSGEMV_OK) return rc;
   std::vector<bsg::Geometry> rows(max_M);
   for (int m = 1; m <= max_M && rc == BSGEMV_OK; ++m)
     rc = bsg::compute_geometry(p->format, p->geo.block_size, p->geo.has_zp, p->geo.N, p->geo.K,
                                max_M, p->sm_count, p->ctas_override, p->stages_override, p->split,
-                               p->cluster, &rows[m - 1], m);
+                               p->cluster, &rows[m - 1], m, tile_rows);
   if (rc != BSGEMV_OK) return rc;
+  // the side boxes' tensor maps are shaped by the tile's rows: encode them again
+  for (auto& e : p->maps) e.valid = false;
   if (p->variant_override == BSGEMV_VARIANT_CUDA_CORE) {
     geo.pub.variant = BSGEMV_VARIANT_CUDA_CORE;
     for (auto& r : rows) r.pub.variant = BSGEMV_VARIANT_CUDA_CORE;
@@ -337,21 +344,25 @@ int bsgemv_debug_dequant(bsgemv_plan_t plan, const void* W, const void* scales, 
 
 int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows_per_tile,
                              int stages) {
-  if (plan == nullptr || variant < 0 || ctas < 0 || stages < 0 || rows_per_tile != 0)
+  if (plan == nullptr || variant < 0 || ctas < 0 || stages < 0 ||
+      (rows_per_tile != 0 && rows_per_tile != bsg::kBoxRows &&
+       rows_per_tile != bsg::kMaxRowsPerTile))
     return BSGEMV_ERR_INVALID_ARG;
   if (variant > BSGEMV_VARIANT_CUDA_CORE) return BSGEMV_ERR_INVALID_ARG;
   // the CUDA-core variant accumulates at most 8 activation rows per lane
   if (variant == BSGEMV_VARIANT_CUDA_CORE && plan->geo.max_M > 8) return BSGEMV_ERR_UNSUPPORTED;
   const int old_c = plan->ctas_override, old_s = plan->stages_override;
-  const int old_v = plan->variant_override;
+  const int old_v = plan->variant_override, old_r = plan->rows_override;
   if (variant) plan->variant_override = variant;
   if (ctas) plan->ctas_override = ctas;
   if (stages) plan->stages_override = stages;
+  if (rows_per_tile) plan->rows_override = rows_per_tile;
   const int rc = rebuild_geometry(plan);
   if (rc != BSGEMV_OK) {
     plan->ctas_override = old_c;
     plan->stages_override = old_s;
     plan->variant_override = old_v;
+    plan->rows_override = old_r;
     rebuild_geometry(plan);
   }
   return rc;

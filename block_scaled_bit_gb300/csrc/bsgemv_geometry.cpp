@@ -5,13 +5,21 @@
 // per-row summation order (rows are bit-identical across M).
 //
 // Choices (each one the faster of the alternatives measured on GB300, as stated below):
-//   * 64 output columns per CTA tile, 4 consumer warps (one 16-row group each, over a whole
-//     stage) + 1 copy warp, 4 CTAs per SM (3 when max_M > 8, 2 when max_M > 24: more
-//     accumulator registers);
-//   * a ring of up to 12 stages of 256 k (128 or 256 weight bytes per row, plus the stage's
-//     activations), as
-//     deep as the shared-memory share of a CTA allows, so that every SM keeps
-//     tens of KB of weight in flight;
+//   * 64 or 128 output columns per CTA tile (one or two 64-row halves), 4 consumer warps (each
+//     one 16-row group of every half, over a whole stage) + 1 copy warp.  Two halves halve the
+//     per-row cost of everything a warp does once per stage and chunk (activation fragments,
+//     barrier waits, side loads, ring bookkeeping) but halve the tiles.  Plans for up to 16 rows
+//     take them when, with 128-row tiles, at most kTallMaxCtasPerTile resident CTAs share a tile
+//     on average and there are at least kTallMinStages stages per resident CTA (measured on
+//     GB300, calls of 1 to 8 rows: int4 151936 x 4096 16 % and 12288 x 4096 22 % faster, NVFP4
+//     248320 x 2048 7 %, int8 12288 x 4096 2-4 %; with 9 to 40 resident CTAs per tile -- int4
+//     4096 x 4096 and 4096 x 12288, int8 / FP8 shapes of 4096 to 8192 columns, FP8 5120 x 17408
+//     -- 3 to 65 % slower: a coarser split with more partial sums per tile);
+//   * 4 CTAs per SM for one half and one n8 activation tile, 3 for up to three n8 tiles or two
+//     halves, 2 for four n8 tiles (accumulator registers and shared memory);
+//   * a ring of up to 12 stages of 128 weight bytes per row (256 k of the 4-bit formats, 128 k of
+//     the 8-bit ones) plus the stage's activations, as deep as the shared-memory share of a CTA
+//     allows, so that every SM keeps tens of KB of weight in flight;
 //   * a side ring of scale / zero-point boxes, each covering 64 bytes of scales per row (4 to
 //     64 stages), so that side data costs one TMA per box instead of copies every stage;
 //   * stream-K: the tiles x stages work is split into equal contiguous ranges over
@@ -26,6 +34,10 @@
 namespace bsg {
 
 namespace {
+// 128-row tiles: when at most this many resident CTAs share a tile on average, and the tiles
+// hold at least this many stages per resident CTA
+constexpr int kTallMaxCtasPerTile = 5;
+constexpr int kTallMinStages = 2;
 constexpr int kSmemPerSm = 233472;       // 228 KB shared memory per SM on sm_100-class parts
 constexpr int kSmemPerBlockMax = 232448; // 227 KB opt-in maximum per CTA
 constexpr int kReservedPerBlock = 1024;  // reserved by the system per resident CTA
@@ -39,10 +51,11 @@ bool is_pow2_block(int bs) {
 
 namespace {
 
-// The geometry for a kernel of `mt` n8 activation tiles (mt >= mt_for_m(max_M)).
+// The geometry for a kernel of `mt` n8 activation tiles (mt >= mt_for_m(max_M)) and `halves`
+// 64-row halves per tile.
 int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
                        int sm_count, int ctas_override, int stages_override, int split,
-                       int cluster, int mt, int rows, Geometry* g) {
+                       int cluster, int mt, int halves, int rows, Geometry* g) {
   if (g == nullptr) return BSGEMV_ERR_INVALID_ARG;
   std::memset(g, 0, sizeof(*g));
   if ((format & ~(0xFF | BSGEMV_ACT_BF16)) != 0) return BSGEMV_ERR_INVALID_ARG;
@@ -71,7 +84,9 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   }
   if (K % 64 != 0 || K % block_size != 0) return BSGEMV_ERR_UNSUPPORTED;
   // TMA coordinates are signed 32-bit; y indices are 64-bit.
-  if (N > (int64_t(1) << 31) - kRowsPerTile || K > (int64_t(1) << 30)) return BSGEMV_ERR_UNSUPPORTED;
+  if (N > (int64_t(1) << 31) - kMaxRowsPerTile || K > (int64_t(1) << 30))
+    return BSGEMV_ERR_UNSUPPORTED;
+  const int rpt = halves * kBoxRows;  // output columns per tile
 
   const bool four = (fmt == kInt4 || fmt == kNvfp4);
   g->fmt = fmt;
@@ -82,9 +97,10 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   g->N = N;
   g->K = K;
   g->kpc = four ? 32 : 16;
-  g->kc = kStageK;
-  g->stage_bytes = stage_bytes(fmt);
+  g->kc = stage_k(fmt, halves);
+  g->stage_bytes = stage_bytes(fmt, halves);
   g->mt_max = mt;
+  g->halves = halves;
   g->scale_es = (fmt == kFp8) ? 4 : (fmt == kNvfp4 ? 1 : 2);
   g->nb_s = static_cast<int>(K / block_size);
   g->scale_pitch = g->nb_s * g->scale_es;
@@ -103,14 +119,14 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   g->zbox_bytes = (fmt == kInt4) ? blocks_per_box / 2 : blocks_per_box;
   const bool side_possible = (g->scale_pitch % 16 == 0) && (!has_zp || g->zp_pitch % 16 == 0);
   g->side_bytes = side_possible
-                      ? static_cast<int>(ceil_div(kRowsPerTile * (kSideScaleBytes +
+                      ? static_cast<int>(ceil_div(rpt * (kSideScaleBytes +
                                                                   (has_zp ? g->zbox_bytes : 0)),
                                                   128) * 128)
                       : 0;
-  g->slot_floats = g->mt_max * 32 * 4;
+  g->slot_floats = halves * g->mt_max * 32 * 4;
 
   const int64_t spt = ceil_div(K, g->kc);
-  const int64_t tiles = ceil_div(N, kRowsPerTile);
+  const int64_t tiles = ceil_div(N, rpt);
   const int64_t total = tiles * spt;
 
   // activation ring bytes, rounded up so that the side ring after it starts 128-byte aligned
@@ -126,7 +142,7 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
     return 1024 + stages * g->stage_bytes + act_ring(stages) + ss * g->side_bytes + red +
            8 * (2 * stages + 9);
   };
-  const int slots_per_sm = ctas_per_sm_for_mt(g->mt_max);
+  const int slots_per_sm = ctas_per_sm_for(g->mt_max, halves);
   const int64_t slots = int64_t(sm_count) * slots_per_sm;
   const int budget_slots = kSmemPerSm / slots_per_sm - kReservedPerBlock;
 
@@ -140,7 +156,7 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   // Reduction buffer: per CTA of the cluster and consumer warp, the fragment lanes that hold
   // output columns below max_M (quad lanes t < red_tq) of each n8 tile.
   g->red_tq = (g->mt_max >= 2) ? 4 : static_cast<int>(std::min<int64_t>(4, ceil_div(max_M, 2)));
-  const int red_warp = g->mt_max * 8 * g->red_tq * 16;
+  const int red_warp = halves * g->mt_max * 8 * g->red_tq * 16;
   auto red_for = [&](int c) { return c >= 2 ? c * kConsumerWarps * red_warp : 0; };
   // Cluster split with an even share per CTA: the ring needs no more stages than the share, and
   // one side box when the share never crosses a box boundary (it divides the box's stages)
@@ -247,7 +263,7 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
 
   bsgemv_geometry& pub = g->pub;
   pub.variant = BSGEMV_VARIANT_MMA;
-  pub.rows_per_tile = kRowsPerTile;
+  pub.rows_per_tile = rpt;
   pub.k_per_stage = g->kc;
   pub.stages = stages;
   pub.consumer_warps = kConsumerWarps;
@@ -278,20 +294,43 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
 
 int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
                      int sm_count, int ctas_override, int stages_override, int split, int cluster,
-                     Geometry* g, int rows) {
+                     Geometry* g, int rows, int tile_rows) {
   const int mt = (max_M >= 1 && max_M <= kMaxM) ? mt_for_m(max_M) : 1;
   if (rows == 0) rows = max_M;
+  if (tile_rows != 0 && tile_rows != kBoxRows && tile_rows != kMaxRowsPerTile)
+    return BSGEMV_ERR_INVALID_ARG;
+  // (128-row tiles: kernels for calls of up to 16 rows only)
+  if (tile_rows == kMaxRowsPerTile && mt > 2) return BSGEMV_ERR_UNSUPPORTED;
+  if (tile_rows == kMaxRowsPerTile)
+    return geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, ctas_override,
+                              stages_override, split, cluster, mt, 2, rows, g);
   int rc = geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, ctas_override,
-                              stages_override, split, cluster, mt, rows, g);
-  if (rc != BSGEMV_OK || mt != 3 || split != BSGEMV_SPLIT_AUTO || ctas_override != 0 ||
-      stages_override != 0)
+                              stages_override, split, cluster, mt, 1, rows, g);
+  if (rc != BSGEMV_OK) return rc;
+  if (tile_rows == 0 && mt <= 2) {
+    // Two halves when the plan's work per resident CTA is long (see the header); decided on the
+    // plan's geometry (rows = max_M) and so the same for every call of the plan.
+    Geometry tall;
+    if (geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, ctas_override,
+                           stages_override, split, cluster, mt, 2, max_M, &tall) == BSGEMV_OK &&
+        tall.pub.tiles * kTallMaxCtasPerTile >= int64_t(sm_count) * tall.pub.ctas_per_sm &&
+        tall.pub.total_stages >= int64_t(kTallMinStages) * sm_count * tall.pub.ctas_per_sm) {
+      if (rows == max_M) {
+        *g = tall;
+        return BSGEMV_OK;
+      }
+      return geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, ctas_override,
+                                stages_override, split, cluster, mt, 2, rows, g);
+    }
+  }
+  if (mt != 3 || split != BSGEMV_SPLIT_AUTO || ctas_override != 0 || stages_override != 0)
     return rc;
   // Plans for 17..24 rows: three n8 tiles at 3 CTAs per SM, unless that residency's shared
   // memory (activation ring of 24 rows, reduction buffer) costs the cluster split that four
   // tiles at 2 CTAs per SM keep, with shares of at most 4 stages (measured on GB300: such small
   // shapes ran 15-25 % faster at 2 CTAs per SM; larger shapes 13-22 % faster at 3).
   Geometry four;
-  if (geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, 0, 0, split, 0, 4,
+  if (geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, 0, 0, split, 0, 4, 1,
                          rows, &four) != BSGEMV_OK)
     return rc;
   const int C4 = four.pub.cluster, C3 = g->pub.cluster;

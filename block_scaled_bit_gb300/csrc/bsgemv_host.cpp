@@ -96,16 +96,16 @@ int encode_maps(const Geometry& g, const void* W, const void* scales, const void
                 OperandMaps* m) {
   std::memset(m, 0, sizeof(*m));
   const int64_t row_bytes = (g.fmt == kInt4 || g.fmt == kNvfp4) ? g.K / 2 : g.K;
-  int rc = encode_u8(&m->tm_w, W, row_bytes, g.N, row_bytes, kBoxRowBytes, kRowsPerTile,
+  int rc = encode_u8(&m->tm_w, W, row_bytes, g.N, row_bytes, kBoxRowBytes, kBoxRows,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BSGEMV_OK) return rc;
   const bool int_zp = (g.fmt == kInt4 || g.fmt == kInt8) && g.has_zp;
   m->side_tma = g.side_bytes > 0 && aligned16(scales) && (!int_zp || aligned16(zp));
   if (m->side_tma) {
     rc = encode_u8(&m->tm_s, scales, g.scale_pitch, g.N, g.scale_pitch, kSideScaleBytes,
-                   kRowsPerTile, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   g.pub.rows_per_tile, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc == BSGEMV_OK && int_zp)
-      rc = encode_u8(&m->tm_z, zp, g.zp_pitch, g.N, g.zp_pitch, g.zbox_bytes, kRowsPerTile,
+      rc = encode_u8(&m->tm_z, zp, g.zp_pitch, g.N, g.zp_pitch, g.zbox_bytes, g.pub.rows_per_tile,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != BSGEMV_OK) m->side_tma = false;  // fall back to direct reads
   }
@@ -147,7 +147,8 @@ void fill_params(const Geometry& g, const OperandMaps& m, const void* A, const v
   k->side_off = g.side_off;
   k->side_bytes = g.side_bytes;
   k->side_slots = g.side_slots;
-  k->side_tx = kRowsPerTile * (kSideScaleBytes + ((int_fmt && g.has_zp) ? g.zbox_bytes : 0));
+  k->side_tx =
+      g.pub.rows_per_tile * (kSideScaleBytes + ((int_fmt && g.has_zp) ? g.zbox_bytes : 0));
   k->zbox_bytes = g.zbox_bytes;
   k->rs_log2 = g.rs_log2;
   k->bar_off = g.bar_off;
@@ -183,15 +184,15 @@ int launch_gemv(const Geometry& g, const KParams& k, cudaStream_t s) {
   const int bm = block_mode(g.fmt, g.block_size);
   switch (g.fmt) {
     case kInt4:
-      return g.bf16 ? launch_int4_bf16(k, mt, g.has_zp, bm, ctas, smem, s)
-                    : launch_int4_f16(k, mt, g.has_zp, bm, ctas, smem, s);
+      return g.bf16 ? launch_int4_bf16(k, mt, g.halves, g.has_zp, bm, ctas, smem, s)
+                    : launch_int4_f16(k, mt, g.halves, g.has_zp, bm, ctas, smem, s);
     case kInt8:
-      return g.bf16 ? launch_int8_bf16(k, mt, g.has_zp, bm, ctas, smem, s)
-                    : launch_int8_f16(k, mt, g.has_zp, bm, ctas, smem, s);
+      return g.bf16 ? launch_int8_bf16(k, mt, g.halves, g.has_zp, bm, ctas, smem, s)
+                    : launch_int8_f16(k, mt, g.halves, g.has_zp, bm, ctas, smem, s);
     case kFp8:
-      return launch_fp8(k, mt, g.bf16, false, bm, ctas, smem, s);
+      return launch_fp8(k, mt, g.halves, g.bf16, ctas, smem, s);
     case kNvfp4:
-      return launch_nvfp4(k, mt, g.bf16, false, bm, ctas, smem, s);
+      return launch_nvfp4(k, mt, g.halves, g.bf16, ctas, smem, s);
   }
   return BSGEMV_ERR_INVALID_ARG;
 }

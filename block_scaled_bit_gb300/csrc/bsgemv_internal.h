@@ -1,10 +1,16 @@
 // bsgemv_internal.h -- host/device shared definitions of the block-scaled GEMV library.
 //
 // Work decomposition (one persistent kernel per call):
-//   * a CTA tile is kRowsPerTile consecutive output columns n (rows of W) over a k-range;
-//   * k is walked in "stages" of kStageK = 256 k: 128 weight bytes per row for the 4-bit formats
-//     (one 128-byte-swizzled TMA box), 256 for the 8-bit formats (two boxes), plus the stage's
-//     activations (cp.async) -- scales and zero points arrive per several stages on a side ring;
+//   * a CTA tile is 64 or 128 consecutive output columns n (rows of W) over a k-range: one or
+//     two "halves" of kBoxRows = 64 rows.  Consumer warp w owns mma row group w (16 rows) of
+//     every half, so with two halves every activation fragment it loads and every stage's
+//     bookkeeping serve 32 rows.  Plans whose work is long per CTA take two halves, plans with
+//     little work per CTA one (finer-grained split; see compute_geometry);
+//   * k is walked in "stages" of 256 k for the 4-bit formats (128 weight bytes per row), of 256 k
+//     (two k-boxes) for the 8-bit formats with one half and 128 k with two: one 128-byte-swizzled
+//     TMA box [64 rows][128 B] per half and k-box (8 KB of weight per stage for the 4-bit formats
+//     with one half, else 16 KB), plus the stage's activations (cp.async) -- scales and zero
+//     points arrive per several stages on a side ring;
 //   * the tiles x stages grid is cut into `ctas` equal contiguous ranges (stream-K), and a tile
 //     whose stages fall into several CTAs is finished by the last CTA to arrive, which adds the
 //     partial sums in CTA order; or, for shapes with few tiles, each tile's stages are split
@@ -24,20 +30,34 @@ namespace bsg {
 
 enum Fmt : int { kInt4 = 1, kInt8 = 2, kFp8 = 3, kNvfp4 = 4 };
 
-constexpr int kRowsPerTile = 64;      // output columns per CTA tile (4 mma row groups of 16)
-constexpr int kConsumerWarps = 4;     // decode + mma warps (one 16-row group each); warp 0 copies
+constexpr int kBoxRows = 64;          // rows of one weight TMA box (one half of a tile)
+constexpr int kMaxHalves = 2;         // halves per tile: 1 (64 rows) or 2 (128 rows)
+constexpr int kMaxRowsPerTile = kMaxHalves * kBoxRows;
+constexpr int kConsumerWarps = 4;     // decode + mma warps (row group w of every half); warp 0
+                                      // copies
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxM = 32;             // activation rows per call: up to four n8 mma tiles
-// CTAs per SM the kernels are built for (their register budget): 4 with one n8 activation tile
-// (M <= 8), 3 with two or three (M <= 24; 128 registers, no spills), 2 with four (M <= 32: at
-// 128 registers some of them spill).
-constexpr int ctas_per_sm_for_mt(int mt) { return mt == 1 ? 4 : mt <= 3 ? 3 : 2; }
+// CTAs per SM the kernels are built for (their register and shared-memory budget).  One half:
+// 4 with one n8 activation tile (M <= 8), 3 with two or three (M <= 24; 128 registers, no
+// spills), 2 with four (M <= 32).  Two halves (M <= 16 only): 3 -- twice the accumulators, and a
+// CTA's two 16 KB stages, activations and side ring fill a third of the SM's shared memory.
+constexpr int ctas_per_sm_for(int mt, int halves) {
+  return halves == 2 ? 3 : (mt == 1 ? 4 : mt <= 3 ? 3 : 2);
+}
 // n8 activation tiles of the kernel a plan is sized for (and of the kernel a call with M rows
 // runs).
 constexpr int mt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 24 ? 3 : 4; }
 constexpr int kBoxRowBytes = 128;     // bytes per row of one weight TMA box (128-byte swizzle)
-constexpr int kStageK = 256;          // k per stage for every format: one 128-byte box per row for
-                                      // the 4-bit formats, two for the 8-bit formats
+// Weight boxes along k per stage: two for the 8-bit formats with one half (so that a stage is
+// 16 KB of weight, 256 k, as for every other case), else one.
+constexpr int stage_kboxes(int fmt, int halves) {
+  return (fmt == kInt4 || fmt == kNvfp4 || halves == 2) ? 1 : 2;
+}
+// k per stage: 128 weight bytes per row and k-box, i.e. 256 k of the 4-bit formats, 128 k of the
+// 8-bit ones per k-box.
+constexpr int stage_k(int fmt, int halves) {
+  return stage_kboxes(fmt, halves) * ((fmt == kInt4 || fmt == kNvfp4) ? 256 : 128);
+}
 constexpr int kMaxStages = 12;
 
 // Error word bits written by kernels that abandon a bounded wait.
@@ -48,9 +68,9 @@ constexpr uint64_t kDefaultWaitNs = 4000000000ull;  // 4 s: far above any legiti
 // Kernel parameters (passed by value as a __grid_constant__; the tensor maps must be 64-byte
 // aligned in parameter space).
 struct KParams {
-  CUtensorMap tm_w;   // W as uint8 [N][row_bytes], box [kRowsPerTile][128], 128B swizzle
-  CUtensorMap tm_s;   // scales as uint8 [N][scale_pitch], box [kRowsPerTile][kSideScaleBytes]
-  CUtensorMap tm_z;   // zero points as uint8 [N][zp_pitch], box [kRowsPerTile][zbox_bytes]
+  CUtensorMap tm_w;   // W as uint8 [N][row_bytes], box [kBoxRows][128], 128B swizzle
+  CUtensorMap tm_s;   // scales as uint8 [N][scale_pitch], box [tile rows][kSideScaleBytes]
+  CUtensorMap tm_z;   // zero points as uint8 [N][zp_pitch], box [tile rows][zbox_bytes]
   const uint16_t* A;       // activations [M][K] (fp16 / bf16 bits)
   const uint8_t* W;
   const uint8_t* scales;   // global copy, read directly when side_tma == 0
@@ -59,6 +79,7 @@ struct KParams {
   const uint16_t* bias;    // [N] bias in the activation dtype added before the rounding, or null
   void* y;
   float* partials;         // [ctas][2][kConsumerWarps][slot_floats] cross-CTA partial sums
+                           // (a slot: every half's fragments of one warp)
   unsigned* counters;      // [tiles][kConsumerWarps] arrival counters, left at zero by every call
   unsigned* err;           // error word
   int64_t N, K;
@@ -94,9 +115,10 @@ struct Geometry {
   int fmt, bf16, has_zp, block_size, max_M;
   int64_t N, K;
   int kpc;                 // k per 16-byte chunk
-  int kc;                  // k per stage (kStageK)
+  int kc;                  // k per stage (stage_k)
   int stage_bytes;         // weight bytes per stage
-  int mt_max;              // 1 or 2 n8 mma tiles
+  int mt_max;              // n8 mma tiles of the kernel sized for max_M (1 .. 4)
+  int halves;              // 64-row halves per tile (1 or 2): pub.rows_per_tile / kBoxRows
   int scale_es;            // bytes per scale element
   int nb_s;
   int scale_pitch, zp_pitch;
@@ -108,10 +130,10 @@ struct Geometry {
   int red_tq;              // cluster split: quad lanes t < red_tq hold output columns < max_M
 };
 
-// Weight bytes of one stage (kRowsPerTile rows x kStageK k), and scale bytes per row of one
-// side box.
-inline int stage_bytes(int fmt) {
-  return kRowsPerTile * ((fmt == kInt4 || fmt == kNvfp4) ? kStageK / 2 : kStageK);
+// Weight bytes of one stage (one [64 rows][128 B] box per half and k-box: 8 or 16 KB), and scale
+// bytes per row of one side box.
+inline int stage_bytes(int fmt, int halves) {
+  return halves * stage_kboxes(fmt, halves) * kBoxRows * kBoxRowBytes;
 }
 constexpr int kSideScaleBytes = 64;
 
@@ -119,17 +141,29 @@ constexpr int kSideScaleBytes = 64;
 // split = enum bsgemv_split, cluster = CTAs per tile for BSGEMV_SPLIT_CLUSTER (0 = chosen).
 // rows (1 .. max_M, 0 = max_M): the layout of the shared-memory ring for a call with that many
 // activation rows; the split, CTA count and residency are those of max_M whatever `rows` is.
+// tile_rows: 64 or 128 output columns per tile, 0 = chosen (128 only for max_M <= 16).
 int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t K, int max_M,
                      int sm_count, int ctas_override, int stages_override, int split, int cluster,
-                     Geometry* g, int rows = 0);
+                     Geometry* g, int rows = 0, int tile_rows = 0);
 
 constexpr int kMaxCluster = 16;     // CTAs per cluster (above 8: non-portable cluster size)
 constexpr int kMaxAutoCluster = 8;  // largest cluster the automatic split picks
 
-// Kernel launchers (one translation unit per weight format; int4 split by activation type).
-// cpb: see block_mode.
-int launch_int4_f16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+// Kernel launchers (one translation unit per weight format; int4 and int8 split by activation
+// type; "wide": calls of 17 to 32 rows; "tall": 128-row tiles, calls of up to 16 rows).
+// cpb: see block_mode.  halves: the plan's 64-row halves per tile.
+int launch_int4_f16(const KParams& p, int mt, int halves, bool zp, int cpb, int ctas, int smem,
                     cudaStream_t s);
+int launch_int4_bf16(const KParams& p, int mt, int halves, bool zp, int cpb, int ctas, int smem,
+                     cudaStream_t s);
+int launch_int8_f16(const KParams& p, int mt, int halves, bool zp, int cpb, int ctas, int smem,
+                    cudaStream_t s);
+int launch_int8_bf16(const KParams& p, int mt, int halves, bool zp, int cpb, int ctas, int smem,
+                     cudaStream_t s);
+int launch_fp8(const KParams& p, int mt, int halves, bool bf16, int ctas, int smem,
+               cudaStream_t s);
+int launch_nvfp4(const KParams& p, int mt, int halves, bool bf16, int ctas, int smem,
+                 cudaStream_t s);
 int launch_int4_f16_wide(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
                          cudaStream_t s);
 int launch_int4_bf16_wide(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
@@ -138,16 +172,16 @@ int launch_int8_f16_wide(const KParams& p, int mt, bool zp, int cpb, int ctas, i
                          cudaStream_t s);
 int launch_int8_bf16_wide(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
                           cudaStream_t s);
-int launch_int4_bf16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
-                     cudaStream_t s);
-int launch_int8_f16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
-                    cudaStream_t s);
-int launch_int8_bf16(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
-                     cudaStream_t s);
-int launch_fp8(const KParams& p, int mt, bool bf16, bool zp, int cpb, int ctas, int smem,
-               cudaStream_t s);
-int launch_nvfp4(const KParams& p, int mt, bool bf16, bool zp, int cpb, int ctas, int smem,
-                 cudaStream_t s);
+int launch_int4_f16_tall(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                         cudaStream_t s);
+int launch_int4_bf16_tall(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                          cudaStream_t s);
+int launch_int8_f16_tall(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                         cudaStream_t s);
+int launch_int8_bf16_tall(const KParams& p, int mt, bool zp, int cpb, int ctas, int smem,
+                          cudaStream_t s);
+int launch_fp8_tall(const KParams& p, int mt, bool bf16, int ctas, int smem, cudaStream_t s);
+int launch_nvfp4_tall(const KParams& p, int mt, bool bf16, int ctas, int smem, cudaStream_t s);
 // The CUDA-core variant (BSGEMV_VARIANT_CUDA_CORE; M <= 8).
 int launch_cc_int4_f16(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s);
 int launch_cc_int4_bf16(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s);

@@ -524,27 +524,32 @@ BSG_DEV void zp_consts(uint32_t zp, uint32_t& zl, uint32_t& zh) {
 // Scale blocks of the weight formats, per 16-byte chunk of a row (k = 32 per chunk for the 4-bit
 // formats, 16 for the 8-bit formats): the kernel's CPB template parameter is the number of
 // chunks per scale block -- 0 when a chunk holds two blocks (int4 with 16-element blocks), 1, 2,
-// 4, or 8 for a block of a whole stage or more (larger blocks, fp8).  NVFP4 folds its scales
+// 4, or 8 for a block of a whole 128-byte box or more (larger blocks, fp8).  NVFP4 folds its scales
 // into the decoded values and uses 1.
 
 // CC > 0 selects the CUDA-core variant: the same copies, rings, decoders and epilogues, but the
 // products are formed by fp32 FMAs on the CUDA cores (each lane over its own k positions of
 // the tile rows it holds, for CC = 1 or 8 activation rows: calls with M = 1, or M <= 8)
 // instead of mma.sync.
-template <int FMT, bool BF16, int MT, bool ZP, int CPB, int CC = 0>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, int H, int CC = 0>
 struct Gemv {
+  static_assert(H == 1 || H == 2, "one or two 64-row halves per tile");
   static_assert(CC == 0 || ((CC == 1 || CC == 8) && MT == 1),
                 "CUDA-core variant: 1 or 8 activation rows, natural activation order");
   static constexpr int kCcCols = CC > 0 ? CC : 1;  // activation rows a CUDA-core lane accumulates
   static constexpr bool kFour = (FMT == kInt4 || FMT == kNvfp4);
   static constexpr int kKpc = kFour ? 32 : 16;  // k per 16-byte chunk
   static constexpr int kSteps = kKpc / 16;      // mma k-steps per chunk
-  static constexpr int kKc = kStageK;            // k per stage
-  static constexpr int kCps = kKc / kKpc;         // 16-byte chunks per row per stage: 8 or 16
-  static constexpr int kSrb = 16 * kCps;          // weight bytes per row per stage: 128 or 256
-  static constexpr int kBoxes = kSrb / kBoxRowBytes;        // weight TMA boxes per stage: 1 or 2
-  static constexpr int kStageB = kRowsPerTile * kSrb;       // weight bytes per stage
-  static constexpr int kBoxB = kRowsPerTile * kBoxRowBytes;  // bytes per weight box (8 KB)
+  static constexpr int kKb = stage_kboxes(FMT, H);  // weight boxes along k per stage (1 or 2)
+  static constexpr int kKc = stage_k(FMT, H);        // k per stage: 256, or 128 (8-bit, 2 halves)
+  static constexpr int kBoxK = kKc / kKb;            // k per box
+  static constexpr int kCps = kBoxK / kKpc;          // 16-byte chunks per row per box: 8
+  static constexpr int kSrb = kKb * kBoxRowBytes;    // weight bytes per row per stage
+  static_assert(kCps * 16 == kBoxRowBytes, "a box is 128 bytes of a row");
+  static constexpr int kH = H;                              // 64-row halves per tile
+  static constexpr int kRows = kH * kBoxRows;               // output columns per tile
+  static constexpr int kBoxB = kBoxRows * kBoxRowBytes;     // bytes per weight box (8 KB)
+  static constexpr int kStageB = kKb * kH * kBoxB;          // weight bytes per stage (8 or 16 KB)
   static constexpr bool kFold = (FMT == kNvfp4);
   static constexpr int kSub = (CPB == 0) ? 2 : 1;  // scale blocks per chunk (int4, 16-element blocks)
   static constexpr int kScaleEs = (FMT == kFp8) ? 4 : (FMT == kNvfp4 ? 1 : 2);
@@ -562,7 +567,9 @@ struct Gemv {
                                 : CPB == 8 ? -1
                                            : (CPB == 1 ? 0 : CPB == 2 ? 1 : 2) + (kFour ? 5 : 4);
 
-  // Shared memory: [W ring: stages x 8 KB][activation ring][side ring][barriers].
+  // Shared memory: [W ring: stages x kStageB (box (k-box j, half h) at (j kH + h) kBoxB)]
+  // [activation ring][side ring]
+  // [cluster reduction buffer][barriers].
   // The weight boxes are 1024-byte aligned (128-byte swizzle atoms).
   struct Smem {
     uint8_t* base;    // generic pointer into the kernel's shared array
@@ -611,9 +618,10 @@ struct Gemv {
     }
   };
 
-  // ---- producer: warp 0.  Lane 0 copies each stage's weight boxes [64 rows][128 B] (one or two TMAs)
-  // (L2 evict-first: the weight is read once) and, once per side box, the scale box [64][64 B]
-  // and zero-point box [64][16 or 32 B] (two more TMAs on the side ring).  All 32 lanes copy the
+  // ---- producer: warp 0.  Lane 0 copies each stage's weight boxes [64 rows][128 B] (one TMA
+  // per half of the tile and k-box; L2 evict-first: the weight is read once) and, once per side
+  // box, the scale box [tile rows][64 B] and zero-point box [tile rows][16 or 32 B] (two more
+  // TMAs on the side ring).  All 32 lanes copy the
   // stage's activations [M][k of the stage] with 16-byte cp.async, tracked by the stage's full
   // barrier (cp.async.mbarrier.arrive).  Rows past N and k past K are zero-filled.
   //
@@ -634,25 +642,29 @@ struct Gemv {
     }
   }
 
-  // The weight boxes of stage (tile, ks) into ring slot i (lane 0).
+  // The weight boxes of stage (tile, ks) into ring slot i (lane 0): one [64 rows][128 B] box
+  // per half of the tile and k-box of the stage.  (A k-box wholly past the row, in the ragged
+  // last stage, is filled with zeros like any out-of-range part of a box.)
   static BSG_DEV void weight_copy(const KParams& p, const Smem& sm, int i, const Walk& w,
                                   uint64_t pol) {
-    const int row = static_cast<int>(w.tile * kRowsPerTile);
+    const int row = static_cast<int>(w.tile * kRows);
 #pragma unroll
-    for (int b = 0; b < kBoxes; ++b)
-      tma_load_2d_hint(sm.w(i) + b * kBoxB, &p.tm_w, w.ks * kSrb + b * kBoxRowBytes, row,
-                       sm.full(i), pol);
+    for (int j = 0; j < kKb; ++j)
+#pragma unroll
+      for (int h = 0; h < kH; ++h)
+        tma_load_2d_hint(sm.w(i) + (j * kH + h) * kBoxB, &p.tm_w,
+                         w.ks * kSrb + j * kBoxRowBytes, row + h * kBoxRows, sm.full(i), pol);
   }
 
   static BSG_DEV void side_copy(const KParams& p, const Smem& sm, int j, const Walk& w,
                                 uint64_t pol) {
     const uint32_t full = sm.sfull(j), dst = sm.side_u(j);
     const int bx = w.ks >> p.rs_log2;
-    const int row = static_cast<int>(w.tile * kRowsPerTile);
+    const int row = static_cast<int>(w.tile * kRows);
     mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.side_tx));
     tma_load_2d_hint(dst, &p.tm_s, bx * kSideScaleBytes, row, full, pol);
     if constexpr (ZP)
-      tma_load_2d_hint(dst + kRowsPerTile * kSideScaleBytes, &p.tm_z, bx * p.zbox_bytes, row, full,
+      tma_load_2d_hint(dst + kRows * kSideScaleBytes, &p.tm_z, bx * p.zbox_bytes, row, full,
                        pol);
   }
 
@@ -780,18 +792,20 @@ struct Gemv {
     return pd;
   }
 
-  // ---- per-lane constants.  Consumer warp cw owns the tile's mma row group rg = cw (tile rows
-  // 16 rg .. 16 rg + 15) over the whole stage (kCps chunks of 16 bytes per row, in boxes of 8);
-  // lane (g, t) holds rows g and g + 8 of the group (rr = 0, 1).
+  // ---- per-lane constants.  Consumer warp cw owns mma row group rg = cw of every half of the
+  // tile (rows 64 h + 16 rg .. 64 h + 16 rg + 15, h < kH) over the whole stage (kCps = 8 chunks
+  // of 16 bytes per row and k-box); lane (g, t) holds rows g and g + 8 of the group (rr = 0, 1).
   struct Lane {
     int rg, lane, g, t;
-    uint32_t w[4];             // ldmatrix.x4 row address of chunk pair j (chunks 2j, 2j + 1) of a
-                               // weight box; box b of the stage adds b * kBoxB
+    uint32_t w[4];             // ldmatrix.x4 row address of chunk pair j (chunks 2j, 2j + 1) in
+                               // the weight box of half 0; half h adds h * kBoxB
     uint32_t act[MT];          // activation fragment offset of chunk 0 (n8 tile mt) in a stage's
                                // activation slot; chunk c adds c * kActChunkB
     uint32_t fsel[2];          // NVFP4: prmt selector of the lane's scale code, chunk parity 0/1
-    uint32_t srow;             // side box: scale row 16 rg + g; row g + 8 adds 8 * kSideScaleBytes
-    uint32_t zrow;             // side box: zero-point row 16 rg + g; row g + 8 adds 8 * kZboxB
+    uint32_t srow;             // side box: scale row 16 rg + g (half 0); row g + 8 adds
+                               // 8 * kSideScaleBytes, half h adds h * kBoxRows * kSideScaleBytes
+    uint32_t zrow;             // side box: zero-point row 16 rg + g (half 0); row g + 8 adds
+                               // 8 * kZboxB, half h adds h * kBoxRows * kZboxB
     uint32_t cact;             // CUDA-core variant: the lane's k positions of a chunk in an
                                // activation row (4 or 8 halves from byte t * kActChunkB / 4)
   };
@@ -823,7 +837,7 @@ struct Gemv {
     L.fsel[0] = 0x11u * static_cast<uint32_t>(L.t >> 1);
     L.fsel[1] = 0x11u * static_cast<uint32_t>(2 + (L.t >> 1));
     L.srow = (16 * L.rg + L.g) * kSideScaleBytes;
-    L.zrow = kRowsPerTile * kSideScaleBytes + (16 * L.rg + L.g) * kZboxB;
+    L.zrow = kRows * kSideScaleBytes + (16 * L.rg + L.g) * kZboxB;
     L.cact = L.t * (kActChunkB / 4);
     return L;
   }
@@ -843,19 +857,19 @@ struct Gemv {
   };
 
   template <class R>
-  static BSG_DEV int64_t row_of(const R& p, const Lane& L, int64_t tile, int rr) {
-    const int64_t n = tile * kRowsPerTile + 16 * L.rg + L.g + 8 * rr;
+  static BSG_DEV int64_t row_of(const R& p, const Lane& L, int64_t tile, int h, int rr) {
+    const int64_t n = tile * kRows + h * kBoxRows + 16 * L.rg + L.g + 8 * rr;
     return n < p.k.N ? n : p.k.N - 1;
   }
 
   // fp32 scales of the lane's 2 rows for NB consecutive blocks from global memory, at absolute
   // block `blk` (the path for scale arrays whose pitch a tensor map cannot describe).
   template <int NB, class R>
-  static BSG_DEV void load_scales(const R& p, const Lane& L, int64_t tile, int blk,
+  static BSG_DEV void load_scales(const R& p, const Lane& L, int64_t tile, int h, int blk,
                                   float (&s)[NB][2]) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const uint8_t* src = p.k.scales + row_of(p, L, tile, rr) * p.k.scale_pitch;
+      const uint8_t* src = p.k.scales + row_of(p, L, tile, h, rr) * p.k.scale_pitch;
 #pragma unroll
       for (int u = 0; u < NB; ++u) {
         const int b = blk + u;
@@ -876,14 +890,15 @@ struct Gemv {
   static constexpr uint32_t kNoZp = (FMT == kInt4) ? 0x88888888u : 0x80808080u;
 
   template <int NB, class R>
-  static BSG_DEV void load_zp(const R& p, const Lane& L, int64_t tile, int blk, uint32_t (&z)[2]) {
+  static BSG_DEV void load_zp(const R& p, const Lane& L, int64_t tile, int h, int blk,
+                              uint32_t (&z)[2]) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       if constexpr (!ZP) {
         z[rr] = kNoZp;
       } else {
         uint32_t v = 0;
-        const uint8_t* src = p.k.zp + row_of(p, L, tile, rr) * p.k.zp_pitch;
+        const uint8_t* src = p.k.zp + row_of(p, L, tile, h, rr) * p.k.zp_pitch;
 #pragma unroll
         for (int u = 0; u < NB; ++u) {
           const int b = blk + u;
@@ -918,9 +933,9 @@ struct Gemv {
   };
 
   template <int NB>
-  static BSG_DEV void load_side(const Lane& L, const Sh& sh, int rel, SideLoad<NB>& v) {
-    const uint32_t sa = sh.s + L.srow + rel * kScaleEs;
-    const uint32_t za0 = sh.s + L.zrow + ((rel * kZpW) >> 3);
+  static BSG_DEV void load_side(const Lane& L, const Sh& sh, int h, int rel, SideLoad<NB>& v) {
+    const uint32_t sa = sh.s + L.srow + h * (kBoxRows * kSideScaleBytes) + rel * kScaleEs;
+    const uint32_t za0 = sh.s + L.zrow + h * (kBoxRows * kZboxB) + ((rel * kZpW) >> 3);
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const uint8_t* a = sh.base + (sa + rr * 8 * kSideScaleBytes);
@@ -998,15 +1013,18 @@ struct Gemv {
   // NVFP4: the replicated f16 E4M3 block scale of the lane's 2 rows for 16-block `blk` (side
   // box block `rel`).
   template <class R>
-  static BSG_DEV void load_fold(const R& p, const Lane& L, const Sh& sh, int64_t tile,
+  static BSG_DEV void load_fold(const R& p, const Lane& L, const Sh& sh, int64_t tile, int h,
                                 int blk, int rel, uint32_t (&f)[2]) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       uint32_t code;
       if constexpr (R::side) {
-        code = lsh<uint8_t>(sh.base + (sh.s + L.srow + rr * 8 * kSideScaleBytes + rel));
+        code = lsh<uint8_t>(sh.base + (sh.s + L.srow + h * (kBoxRows * kSideScaleBytes) +
+                                       rr * 8 * kSideScaleBytes + rel));
       } else {
-        code = (blk < p.k.nb_s) ? __ldg(p.k.scales + row_of(p, L, tile, rr) * p.k.scale_pitch + blk) : 0u;
+        code = (blk < p.k.nb_s)
+                   ? __ldg(p.k.scales + row_of(p, L, tile, h, rr) * p.k.scale_pitch + blk)
+                   : 0u;
       }
       f[rr] = e4m3x2_to_f16x2(code * 0x0101u);
     }
@@ -1039,16 +1057,15 @@ struct Gemv {
     }
   }
 
-  // Decode chunk c (words lo: row g, hi: row g + 8) and multiply into d[u] (u: sub-block when a
-  // chunk holds two scale blocks).  ZC: the first k-step starts from zero instead of
-  // accumulating.  zl/zh: zero-point constants (int formats) or the fold scales (NVFP4) of rows
-  // g, g + 8.
-  template <bool ZC>
-  static BSG_DEV void chunk_mma(const Lane& L, const Sh& ap, int c, uint32_t lo, uint32_t hi,
-                                const uint32_t (&zl)[2], const uint32_t (&zh)[2],
-                                float (&d)[kSub][MT][4]) {
-    uint32_t b[MT][kSteps][2];
-    act_fragment(L, ap, c, b);
+  // Decode chunk words lo (row g), hi (row g + 8) and multiply them with the chunk's activation
+  // fragments b into d[u] (u: sub-block when a chunk holds two scale blocks).  ZC: the first
+  // k-step starts from zero instead of accumulating.  zl/zh: zero-point constants (int formats)
+  // or the fold scales (NVFP4) of rows g, g + 8.
+  template <bool ZC, int NS>
+  static BSG_DEV void chunk_mma(const Lane& L, const uint32_t (&b)[MT][kSteps][2], uint32_t lo,
+                                uint32_t hi, const uint32_t (&zl)[2], const uint32_t (&zh)[2],
+                                float (&d)[NS][MT][4]) {
+    static_assert(NS == kSub, "one accumulator per scale block of the chunk");
     uint32_t a[kSteps][4];
     if constexpr (FMT == kInt4) {
       decode_int4<BF16>(lo, hi, zl[0], zh[0], zl[1], zh[1], a);
@@ -1097,144 +1114,199 @@ struct Gemv {
       for (int i = 0; i < 4; ++i) x[mt][i] = 0.f;
   }
 
-  // Consume one stage: the kCps chunks of row group rg, stage ks of `tile`.  `wa` is the stage's
-  // weight box (shared-window address, for ldmatrix), `ap` its activation slot, `sb` the side
-  // box holding its scales and zero points.
+  // Consume one stage, stage ks of `tile`: per k-box, the kCps = 8 chunks of row group rg in
+  // every half (consume_box; `wa` is the box's weight slot, a shared-window address for ldmatrix,
+  // half h's box at wa + h * kBoxB; `ap` the activation slot and side box; k0 and kb the box's
+  // first k in the row and in the side box).  Each chunk's activation fragment is loaded once
+  // and multiplied with the weights of every half.
   //
   // Scale groups (CPB = chunks per scale block): the chunks are taken in groups that share one
   // shared-memory load of scales and zero points per row -- a pair of chunks for CPB = 1 and 2,
-  // four for CPB = 4, eight for CPB = 8 (blocks of eight chunks or longer), one chunk holding two
-  // blocks for CPB = 0.  Within a block the chunk products are summed on the tensor cores (two
-  // independent chains when a block has four or more chunks) and then scaled into acc.
+  // four for CPB = 4, the whole box for CPB = 8 (blocks of eight chunks or longer), one chunk
+  // holding two blocks for CPB = 0.  Within a block the chunk products are summed on the tensor
+  // cores and then scaled into acc.
   static constexpr int kGC = (CPB == 0) ? 1 : (CPB <= 2 ? 2 : CPB);  // chunks per group
   static constexpr int kGB = (CPB == 0 || CPB == 1) ? 2 : 1;          // blocks per group
 
   template <class R>
   static BSG_DEV void consume_stage(const R& p, const Lane& L, uint32_t wa, const Sh& ap,
-                                    int64_t tile, int ks, float (&acc)[1][MT][4],
-                                    uint64_t (&cacc)[2][kCcCols]) {
+                                    int64_t tile, int ks, float (&acc)[kH][MT][4],
+                                    uint64_t (&cacc)[kH][2][kCcCols]) {
     const int k0 = ks * kKc;                                // first k of the stage in the row
     const int kb = (ks & ((1 << p.rs_log2) - 1)) * kKc;    // ... in the side box
-    uint32_t wl[4];
+    uint32_t wv[kH][4][4];  // ldmatrix words: chunk c, row g in wv[h][c >> 1][2 (c & 1)]
+    // k-box j of the stage: its boxes at wa + j kH kBoxB, its activations kCps chunks further
 #pragma unroll
-    for (int j = 0; j < 4; ++j) wl[j] = wa + L.w[j];
-    // one weight box (8 chunks) at a time: 16 weight registers live
+    for (int j = 0; j < kKb; ++j) {
+      const uint32_t wj = wa + j * kH * kBoxB;
+      const Sh aj{ap.base, ap.a + j * kCps * kActChunkB, ap.s};
+      if constexpr (CC > 0) {
 #pragma unroll
-    for (int bx = 0; bx < kBoxes; ++bx) {
-      uint32_t wv[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (bx == 0) ldsm_x4_at<0>(wl[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
-        else ldsm_x4_at<kBoxB>(wl[j], wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
+        for (int q = 0; q < 4; ++q) load_pair(L, wj, q, wv);
+        consume_box_cc(p, L, wv, aj, tile, k0 + j * kBoxK, kb + j * kBoxK, cacc);
+      } else {
+        consume_box(p, L, wj, wv, aj, tile, k0 + j * kBoxK, kb + j * kBoxK, acc);
       }
-      if constexpr (CC > 0) consume_box_cc(p, L, wv, ap, tile, k0, kb, bx * 8, cacc);
-      else consume_box(p, L, wv, ap, tile, k0, kb, bx * 8, acc);
     }
   }
 
-  // Chunks c0 .. c0 + 7 of the stage (one weight box), from the box's ldmatrix words `wv`:
-  // chunk c0 + c has row g in wv[c >> 1][2 (c & 1)] and row g + 8 in the next word.
+  // The ldmatrix words of chunk pair j (chunks 2j, 2j + 1, rows g and g + 8) of every half.
+  // (ldmatrix is a volatile asm: the loads stay where they are written, so the consumer loop
+  // issues each pair's loads one pair ahead of its use and keeps two pairs of registers live.)
+  static BSG_DEV void load_pair(const Lane& L, uint32_t wa, int j, uint32_t (&wv)[kH][4][4]) {
+    const uint32_t wl = wa + L.w[j];
+    ldsm_x4_at<0>(wl, wv[0][j][0], wv[0][j][1], wv[0][j][2], wv[0][j][3]);
+    if constexpr (kH == 2)
+      ldsm_x4_at<kBoxB>(wl, wv[1][j][0], wv[1][j][1], wv[1][j][2], wv[1][j][3]);
+  }
+
+  // The box's first ldmatrix words: with one half all four pairs at once (16 registers, the
+  // most loads in flight); with two halves the first pair, the others one pair ahead of their use
+  // (prefetch), which keeps 16 registers live instead of 32.
+  static BSG_DEV void first_pairs(const Lane& L, uint32_t wa, uint32_t (&wv)[kH][4][4]) {
+    if constexpr (kH == 1) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) load_pair(L, wa, j, wv);
+    } else {
+      load_pair(L, wa, 0, wv);
+    }
+  }
+
+  // Chunk c is about to be multiplied: with two halves, when it opens a chunk pair, load the next
+  // pair's words.
+  static BSG_DEV void prefetch(const Lane& L, uint32_t wa, int c, uint32_t (&wv)[kH][4][4]) {
+    if constexpr (kH == 2)
+      if ((c & 1) == 0 && (c >> 1) + 1 < 4) load_pair(L, wa, (c >> 1) + 1, wv);
+  }
+
   template <class R>
-  static BSG_DEV void consume_box(const R& p, const Lane& L, const uint32_t (&wv)[4][4],
-                                  const Sh& ap, int64_t tile, int k0,
-                                  int kb, int c0, float (&acc)[1][MT][4]) {
-#define BSG_LO(c) wv[(c) >> 1][2 * ((c) & 1)]
-#define BSG_HI(c) wv[(c) >> 1][2 * ((c) & 1) + 1]
-    uint32_t zl[2], zh[2];
+  static BSG_DEV void consume_box(const R& p, const Lane& L, uint32_t wa,
+                                  uint32_t (&wv)[kH][4][4], const Sh& ap, int64_t tile,
+                                  int k0, int kb, float (&acc)[kH][MT][4]) {
+#define BSG_LO(h, c) wv[h][(c) >> 1][2 * ((c) & 1)]
+#define BSG_HI(h, c) wv[h][(c) >> 1][2 * ((c) & 1) + 1]
+    uint32_t zh[2] = {0u, 0u};
+    first_pairs(L, wa, wv);
     if constexpr (kFold) {
       // the lane's 8 codes of chunk c lie in 16-block (k of the chunk + 8t) / 16 = 2c + t/2
       if constexpr (R::side) {
-        // the stage's 16 scale codes per row in one load; the lane's code picked by prmt
-        uint4 cv[2];
+        // the box's 16 scale codes per row (2 per chunk) in one load per half; the lane's code
+        // picked by prmt
+        uint4 cv[kH][2];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-          cv[rr] = lsh<uint4>(ap.base + (ap.s + L.srow + rr * 8 * kSideScaleBytes + (kb >> 4)));
+        for (int h = 0; h < kH; ++h)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr)
+            cv[h][rr] = lsh<uint4>(ap.base + (ap.s + L.srow + h * (kBoxRows * kSideScaleBytes) +
+                                              rr * 8 * kSideScaleBytes + (kb >> 4)));
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const int cc = c0 + c;
+          prefetch(L, wa, c, wv);
+          uint32_t b[MT][kSteps][2];
+          act_fragment(L, ap, c, b);
 #pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const uint32_t wd = (cc >> 1) == 0 ? cv[rr].x
-                              : (cc >> 1) == 1 ? cv[rr].y
-                              : (cc >> 1) == 2 ? cv[rr].z : cv[rr].w;
-            zl[rr] = e4m3_byte_to_f16x2(wd, L.fsel[cc & 1]);
+          for (int h = 0; h < kH; ++h) {
+            uint32_t f[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const uint32_t wd = (c >> 1) == 0 ? cv[h][rr].x
+                                : (c >> 1) == 1 ? cv[h][rr].y
+                                : (c >> 1) == 2 ? cv[h][rr].z : cv[h][rr].w;
+              f[rr] = e4m3_byte_to_f16x2(wd, L.fsel[c & 1]);
+            }
+            chunk_mma<false>(L, b, BSG_LO(h, c), BSG_HI(h, c), f, zh,
+                             reinterpret_cast<float (&)[1][MT][4]>(acc[h]));
           }
-          chunk_mma<false>(L, ap, cc, BSG_LO(c), BSG_HI(c), zl, zh, acc);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const int d = 2 * (c0 + c) + (L.t >> 1);
-          load_fold(p, L, ap, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
-          chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, acc);
+          prefetch(L, wa, c, wv);
+          uint32_t b[MT][kSteps][2];
+          act_fragment(L, ap, c, b);
+          const int d = 2 * c + (L.t >> 1);
+#pragma unroll
+          for (int h = 0; h < kH; ++h) {
+            uint32_t f[2];
+            load_fold(p, L, ap, tile, h, (k0 >> 4) + d, (kb >> 4) + d, f);
+            chunk_mma<false>(L, b, BSG_LO(h, c), BSG_HI(h, c), f, zh,
+                             reinterpret_cast<float (&)[1][MT][4]>(acc[h]));
+          }
         }
       }
     } else {
-      // side ring: one load per row of the scales and zero points of up to 8 blocks (the whole
-      // box, or half of it for 16-element int4 blocks)
-      constexpr int kBB = (8 / kGC) * kGB;         // scale blocks per weight box
+      // side ring: one load per row and half of the scales and zero points of up to 8 blocks
+      // (the whole box, or half of it for 16-element int4 blocks)
+      constexpr int kBB = (8 / kGC) * kGB;         // scale blocks per box
       constexpr int kSL = kBB < 8 ? kBB : 8;       // blocks per side load
       constexpr int kGpl = kSL / kGB;              // groups per side load
-      SideLoad<kSL> sl;
+      SideLoad<kSL> sl[kH];
 #pragma unroll
       for (int grp = 0; grp < 8 / kGC; ++grp) {
-        const int kg = (c0 + grp * kGC) * kKpc;  // k of the group in the stage
-        uint32_t z[2];
-        float s[kGB][2];
-        if constexpr (R::side) {
-          if (grp % kGpl == 0) {
-            int rel;
-            if constexpr (kBsLog2 >= 0) rel = (kb + kg) >> kBsLog2;
-            else rel = (kb + kg) >> p.bs_log2;
-            load_side<kSL>(L, ap, rel, sl);
+        const int kg = grp * kGC * kKpc;  // k of the group in the box
+        uint32_t z[kH][2];
+        float s[kH][kGB][2];
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+          if constexpr (R::side) {
+            if (grp % kGpl == 0) {
+              int rel;
+              if constexpr (kBsLog2 >= 0) rel = (kb + kg) >> kBsLog2;
+              else rel = (kb + kg) >> p.bs_log2;
+              load_side<kSL>(L, ap, h, rel, sl[h]);
+            }
+            side_group<kGB>(sl[h], (grp % kGpl) * kGB, z[h], s[h]);
+          } else {
+            const int blk = (k0 + kg) >> p.bs_log2;
+            load_zp<kGB>(p, L, tile, h, blk, z[h]);
+            load_scales<kGB>(p, L, tile, h, blk, s[h]);
           }
-          side_group<kGB>(sl, (grp % kGpl) * kGB, z, s);
-        } else {
-          const int blk = (k0 + kg) >> p.bs_log2;
-          load_zp<kGB>(p, L, tile, blk, z);
-          load_scales<kGB>(p, L, tile, blk, s);
         }
+        uint32_t zl[2], zhh[2];
         if constexpr (CPB == 0) {  // one chunk, two blocks: the lane's codes are in block t/2
-          zp_of(z, L.t >> 1, zl, zh);
-          float tmp[2][MT][4];
-          chunk_mma<true>(L, ap, c0 + grp, BSG_LO(grp), BSG_HI(grp), zl, zh, tmp);
-          apply_scales(s[0][0], s[0][1], tmp[0], acc[0]);
-          apply_scales(s[1][0], s[1][1], tmp[1], acc[0]);
+          prefetch(L, wa, grp, wv);
+          uint32_t b[MT][kSteps][2];
+          act_fragment(L, ap, grp, b);
+#pragma unroll
+          for (int h = 0; h < kH; ++h) {
+            zp_of(z[h], L.t >> 1, zl, zhh);
+            float tmp[2][MT][4];
+            chunk_mma<true>(L, b, BSG_LO(h, grp), BSG_HI(h, grp), zl, zhh, tmp);
+            apply_scales(s[h][0][0], s[h][0][1], tmp[0], acc[h]);
+            apply_scales(s[h][1][0], s[h][1][1], tmp[1], acc[h]);
+          }
         } else if constexpr (CPB == 1) {  // two chunks, one block each
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int c = grp * 2 + u;
-            zp_of(z, u, zl, zh);
-            float tmp[1][MT][4];
-            chunk_mma<true>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, tmp);
-            apply_scales(s[u][0], s[u][1], tmp[0], acc[0]);
+            prefetch(L, wa, c, wv);
+            uint32_t b[MT][kSteps][2];
+            act_fragment(L, ap, c, b);
+#pragma unroll
+            for (int h = 0; h < kH; ++h) {
+              zp_of(z[h], u, zl, zhh);
+              float tmp[1][MT][4];
+              chunk_mma<true>(L, b, BSG_LO(h, c), BSG_HI(h, c), zl, zhh, tmp);
+              apply_scales(s[h][u][0], s[h][u][1], tmp[0], acc[h]);
+            }
           }
-        } else if constexpr (CPB == 2) {  // two chunks, one block
-          zp_of(z, 0, zl, zh);
-          float tmp[1][MT][4];
-          const int c = grp * 2;
-          chunk_mma<true>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, tmp);
-          chunk_mma<false>(L, ap, c0 + c + 1, BSG_LO(c + 1), BSG_HI(c + 1), zl, zh, tmp);
-          apply_scales(s[0][0], s[0][1], tmp[0], acc[0]);
-        } else {  // CPB 4 or 8: kGC chunks in one block, two independent mma chains
-          zp_of(z, 0, zl, zh);
-          float t0[1][MT][4], t1[1][MT][4];
+        } else {  // CPB 2, 4 or 8: kGC chunks in one block, one mma chain per half
+          float t[kH][1][MT][4];
 #pragma unroll
           for (int u = 0; u < kGC; ++u) {
             const int c = grp * kGC + u;
-            if (u < 2) {
-              if (u == 0) chunk_mma<true>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, t0);
-              else chunk_mma<true>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, t1);
-            } else {
-              if (u & 1) chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, t1);
-              else chunk_mma<false>(L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, t0);
+            prefetch(L, wa, c, wv);
+            uint32_t b[MT][kSteps][2];
+            act_fragment(L, ap, c, b);
+#pragma unroll
+            for (int h = 0; h < kH; ++h) {
+              zp_of(z[h], 0, zl, zhh);
+              if (u == 0) chunk_mma<true>(L, b, BSG_LO(h, c), BSG_HI(h, c), zl, zhh, t[h]);
+              else chunk_mma<false>(L, b, BSG_LO(h, c), BSG_HI(h, c), zl, zhh, t[h]);
             }
           }
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) t0[0][mt][e] += t1[0][mt][e];
-          apply_scales(s[0][0], s[0][1], t0[0], acc[0]);
+          for (int h = 0; h < kH; ++h) apply_scales(s[h][0][0], s[h][0][1], t[h][0], acc[h]);
         }
       }
     }
@@ -1308,76 +1380,80 @@ struct Gemv {
     }
   }
 
-  // Zero points and scales of scale group `grp` of the weight box whose first chunk is c0 (the
-  // same sources and order as consume_box).
+  // Zero points and scales of scale group `grp` of half h of a box (the same sources and
+  // order as consume_box).
   template <int NS, class R>
-  static BSG_DEV void group_side(const R& p, const Lane& L, const Sh& ap, int64_t tile, int k0,
-                                 int kb, int c0, int grp, SideLoad<NS>& sl, uint32_t (&z)[2],
+  static BSG_DEV void group_side(const R& p, const Lane& L, const Sh& ap, int64_t tile, int h,
+                                 int k0, int kb, int grp, SideLoad<NS>& sl, uint32_t (&z)[2],
                                  float (&s)[kGB][2]) {
-    const int kg = (c0 + grp * kGC) * kKpc;  // k of the group in the stage
+    const int kg = grp * kGC * kKpc;  // k of the group in the box
     if constexpr (R::side) {
       constexpr int kGpl = NS / kGB;  // groups per side load
       if (grp % kGpl == 0) {
         int rel;
         if constexpr (kBsLog2 >= 0) rel = (kb + kg) >> kBsLog2;
         else rel = (kb + kg) >> p.bs_log2;
-        load_side<NS>(L, ap, rel, sl);
+        load_side<NS>(L, ap, h, rel, sl);
       }
       side_group<kGB>(sl, (grp % kGpl) * kGB, z, s);
     } else {
       const int blk = (k0 + kg) >> p.bs_log2;
-      load_zp<kGB>(p, L, tile, blk, z);
-      load_scales<kGB>(p, L, tile, blk, s);
+      load_zp<kGB>(p, L, tile, h, blk, z);
+      load_scales<kGB>(p, L, tile, h, blk, s);
     }
   }
 
-  // Chunks c0 .. c0 + 7 of the stage on the CUDA cores (see chunk_cc).  Every lane's codes of a
-  // chunk lie in one scale block: block t/2 of the chunk when it holds two (16-element int4
-  // blocks).
+  // A box's chunks of every half on the CUDA cores (see chunk_cc), half by half.  Every
+  // lane's codes of a chunk lie in one scale block: block t/2 of the chunk when it holds two
+  // (16-element int4 blocks).
   template <class R>
-  static BSG_DEV void consume_box_cc(const R& p, const Lane& L, const uint32_t (&wv)[4][4],
-                                     const Sh& ap, int64_t tile, int k0, int kb, int c0,
-                                     uint64_t (&cacc)[2][kCcCols]) {
-#define BSG_LO(c) wv[(c) >> 1][2 * ((c) & 1)]
-#define BSG_HI(c) wv[(c) >> 1][2 * ((c) & 1) + 1]
-    uint32_t zl[2], zh[2] = {0u, 0u};
-    if constexpr (kFold) {
-      const float one[2] = {1.f, 1.f};
+  static BSG_DEV void consume_box_cc(const R& p, const Lane& L,
+                                     const uint32_t (&wv)[kH][4][4], const Sh& ap,
+                                     int64_t tile, int k0, int kb,
+                                     uint64_t (&cacc)[kH][2][kCcCols]) {
+#define BSG_LO(c) wv[h][(c) >> 1][2 * ((c) & 1)]
+#define BSG_HI(c) wv[h][(c) >> 1][2 * ((c) & 1) + 1]
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int d = 2 * (c0 + c) + (L.t >> 1);
-        load_fold(p, L, ap, tile, (k0 >> 4) + d, (kb >> 4) + d, zl);
-        chunk_cc(p, L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, one, cacc);
-      }
-    } else {
-      constexpr int kBB = (8 / kGC) * kGB;    // scale blocks per weight box
-      constexpr int kSL = kBB < 8 ? kBB : 8;  // blocks per side load
-      SideLoad<kSL> sl;
+    for (int h = 0; h < kH; ++h) {
+      uint32_t zl[2], zh[2] = {0u, 0u};
+      if constexpr (kFold) {
+        const float one[2] = {1.f, 1.f};
 #pragma unroll
-      for (int grp = 0; grp < 8 / kGC; ++grp) {
-        uint32_t z[2];
-        float s[kGB][2];
-        group_side<kSL>(p, L, ap, tile, k0, kb, c0, grp, sl, z, s);
-        if constexpr (CPB == 0) {  // one chunk, two blocks: the lane's codes are in block t/2
-          const int u = L.t >> 1;
-          zp_of(z, u, zl, zh);
-          const float sc[2] = {u ? s[1][0] : s[0][0], u ? s[1][1] : s[0][1]};
-          chunk_cc(p, L, ap, c0 + grp, BSG_LO(grp), BSG_HI(grp), zl, zh, sc, cacc);
-        } else if constexpr (CPB == 1) {  // two chunks, one block each
+        for (int c = 0; c < 8; ++c) {
+          const int d = 2 * c + (L.t >> 1);
+          load_fold(p, L, ap, tile, h, (k0 >> 4) + d, (kb >> 4) + d, zl);
+          chunk_cc(p, L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, one, cacc[h]);
+        }
+      } else {
+        constexpr int kBB = (8 / kGC) * kGB;    // scale blocks per box
+        constexpr int kSL = kBB < 8 ? kBB : 8;  // blocks per side load
+        SideLoad<kSL> sl;
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = grp * 2 + u;
+        for (int grp = 0; grp < 8 / kGC; ++grp) {
+          uint32_t z[2];
+          float s[kGB][2];
+          group_side<kSL>(p, L, ap, tile, h, k0, kb, grp, sl, z, s);
+          if constexpr (CPB == 0) {  // one chunk, two blocks: the lane's codes are in block t/2
+            const int u = L.t >> 1;
             zp_of(z, u, zl, zh);
-            const float sc[2] = {s[u][0], s[u][1]};
-            chunk_cc(p, L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, sc, cacc);
-          }
-        } else {  // CPB 2, 4 or 8: kGC chunks in one block
-          zp_of(z, 0, zl, zh);
-          const float sc[2] = {s[0][0], s[0][1]};
+            const float sc[2] = {u ? s[1][0] : s[0][0], u ? s[1][1] : s[0][1]};
+            chunk_cc(p, L, ap, grp, BSG_LO(grp), BSG_HI(grp), zl, zh, sc, cacc[h]);
+          } else if constexpr (CPB == 1) {  // two chunks, one block each
 #pragma unroll
-          for (int u = 0; u < kGC; ++u) {
-            const int c = grp * kGC + u;
-            chunk_cc(p, L, ap, c0 + c, BSG_LO(c), BSG_HI(c), zl, zh, sc, cacc);
+            for (int u = 0; u < 2; ++u) {
+              const int c = grp * 2 + u;
+              zp_of(z, u, zl, zh);
+              const float sc[2] = {s[u][0], s[u][1]};
+              chunk_cc(p, L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, sc, cacc[h]);
+            }
+          } else {  // CPB 2, 4 or 8: kGC chunks in one block
+            zp_of(z, 0, zl, zh);
+            const float sc[2] = {s[0][0], s[0][1]};
+#pragma unroll
+            for (int u = 0; u < kGC; ++u) {
+              const int c = grp * kGC + u;
+              chunk_cc(p, L, ap, c, BSG_LO(c), BSG_HI(c), zl, zh, sc, cacc[h]);
+            }
           }
         }
       }
@@ -1391,7 +1467,7 @@ struct Gemv {
   // commutes), and leave in acc the mma fragment layout the epilogues take (tile rows g, g + 8;
   // activation rows 2t, 2t + 1).  The partial sums are cleared for the next segment.
   static BSG_DEV void cc_fragment(const Lane& L, uint64_t (&cacc)[2][kCcCols],
-                                  float (&acc)[1][MT][4]) {
+                                  float (&acc)[MT][4]) {
     float v[2][kCcCols];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr)
@@ -1408,26 +1484,26 @@ struct Gemv {
       for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
         for (int e = 0; e < 2; ++e)
-          acc[0][0][2 * rr + e] = L.t == 0   ? v[rr][e]
+          acc[0][2 * rr + e] = L.t == 0   ? v[rr][e]
                                   : L.t == 1 ? v[rr][2 + e]
                                   : L.t == 2 ? v[rr][4 + e]
                                              : v[rr][6 + e];
     } else {  // one activation row: column 0 is entry 0 (row g) and 2 (row g + 8) of lane t = 0
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        acc[0][0][2 * rr] = L.t == 0 ? v[rr][0] : 0.f;
-        acc[0][0][2 * rr + 1] = 0.f;
+        acc[0][2 * rr] = L.t == 0 ? v[rr][0] : 0.f;
+        acc[0][2 * rr + 1] = 0.f;
       }
     }
   }
 
-  // Store the 4 fp32 results of lane ln's fragment (row group rg, n8 tile mt) as y, after
-  // adding the bias of the output column when the call has one (in fp32, before the one
+  // Store the 4 fp32 results of lane ln's fragment (half h, row group rg, n8 tile mt) as y,
+  // after adding the bias of the output column when the call has one (in fp32, before the one
   // rounding to the activation dtype).
-  static BSG_DEV void store_y(const KParams& p, int64_t tile, int rg, int mt, int ln, const float (&v)[4],
-                              float gs) {
+  static BSG_DEV void store_y(const KParams& p, int64_t tile, int h, int rg, int mt, int ln,
+                              const float (&v)[4], float gs) {
     const int g = ln >> 2, t = ln & 3;
-    const int64_t n0 = tile * kRowsPerTile + 16 * rg + g;
+    const int64_t n0 = tile * kRows + h * kBoxRows + 16 * rg + g;
     const int m0 = mt * 8 + 2 * t;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -1470,15 +1546,17 @@ struct Gemv {
   // for its last tile, so among a tile's contributors only the first can hold it in seg 1 (when
   // its range began in an earlier tile).
   static BSG_DEV void store_partial(const KParams& p, int64_t tile, int64_t my_first_tile, int rg,
-                                    int lane, const float (&acc)[1][MT][4]) {
-    const int slot4 = p.slot_floats / 4;  // float4 per (cta, seg, rg) slot
+                                    int lane, const float (&acc)[kH][MT][4]) {
+    const int slot4 = p.slot_floats / 4;  // float4 per (cta, seg, rg) slot: every half
     const int seg = (tile == my_first_tile) ? 0 : 1;
     float4* mine = reinterpret_cast<float4*>(p.partials) +
                    ((static_cast<int64_t>(blockIdx.x) * 2 + seg) * kConsumerWarps + rg) * slot4;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-      __stcg(mine + mt * 32 + lane,
-             make_float4(acc[0][mt][0], acc[0][mt][1], acc[0][mt][2], acc[0][mt][3]));
+    for (int h = 0; h < kH; ++h)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        __stcg(mine + (h * MT + mt) * 32 + lane,
+               make_float4(acc[h][mt][0], acc[h][mt][1], acc[h][mt][2], acc[h][mt][3]));
   }
 
   // First and last CTA holding stages of `tile`.
@@ -1519,14 +1597,15 @@ struct Gemv {
     const int fseg = (static_cast<int64_t>(first) * T < x0 * G) ? 1 : 0;  // first began earlier
     const float4* part = reinterpret_cast<const float4*>(p.partials);
     // contributors' partials in batches of kBatch independent loads, added in CTA order
-    constexpr int kBatch = 8 / MT;
-    float v[MT][4];
+    constexpr int kF = kH * MT;  // float4 per lane and slot
+    constexpr int kBatch = 8 / kF > 0 ? 8 / kF : 1;
+    float v[kF][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int f = 0; f < kF; ++f)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[mt][e] = 0.f;
+      for (int e = 0; e < 4; ++e) v[f][e] = 0.f;
     for (int i0 = first; i0 <= last; i0 += kBatch) {
-      float4 u[kBatch][MT];
+      float4 u[kBatch][kF];
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int i = i0 + j;
@@ -1534,23 +1613,25 @@ struct Gemv {
         const float4* src =
             part + ((static_cast<int64_t>(i) * 2 + sg) * kConsumerWarps + rg) * slot4 + lane;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-          u[j][mt] = (i <= last) ? __ldcg(src + mt * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int f = 0; f < kF; ++f)
+          u[j][f] = (i <= last) ? __ldcg(src + f * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         if (i0 + j > last) break;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          v[mt][0] += u[j][mt].x;
-          v[mt][1] += u[j][mt].y;
-          v[mt][2] += u[j][mt].z;
-          v[mt][3] += u[j][mt].w;
+        for (int f = 0; f < kF; ++f) {
+          v[f][0] += u[j][f].x;
+          v[f][1] += u[j][f].y;
+          v[f][2] += u[j][f].z;
+          v[f][3] += u[j][f].w;
         }
       }
     }
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) store_y(p, tile, rg, mt, lane, v[mt], gs);
+    for (int h = 0; h < kH; ++h)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) store_y(p, tile, h, rg, mt, lane, v[h * MT + mt], gs);
     if (lane == 0) p.counters[tile * kConsumerWarps + rg] = 0u;  // all arrived: reset for reuse
   }
 
@@ -1559,21 +1640,24 @@ struct Gemv {
   // t < red_tq) into the leader's (rank 0) reduction buffer slot [rank][warp], through
   // distributed shared memory; after the cluster barrier the leader's warps add the slots in rank
   // order (fixed: deterministic) and store y.
-  static BSG_DEV uint32_t red_slot(const KParams& p, const Smem& sm, int rank, int cw, int mt,
-                                   int li) {
+  static BSG_DEV uint32_t red_slot(const KParams& p, const Smem& sm, int rank, int cw, int h,
+                                   int mt, int li) {
     const int per_mt = 8 * p.red_tq;
-    return sm.base_u + p.red_off + ((((rank * kConsumerWarps + cw) * MT + mt) * per_mt) + li) * 16;
+    return sm.base_u + p.red_off +
+           (((((rank * kConsumerWarps + cw) * kH + h) * MT + mt) * per_mt) + li) * 16;
   }
 
   static BSG_DEV void cluster_publish(const KParams& p, const Smem& sm, int cw, const Lane& L,
-                                      const float (&acc)[1][MT][4]) {
+                                      const float (&acc)[kH][MT][4]) {
     if (L.t >= p.red_tq) return;
     const int rank = static_cast<int>(cluster_ctarank());
     const int li = L.g * p.red_tq + L.t;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-      st_cluster_f32x4(mapa_shared(red_slot(p, sm, rank, cw, mt, li), 0), acc[0][mt][0],
-                       acc[0][mt][1], acc[0][mt][2], acc[0][mt][3]);
+    for (int h = 0; h < kH; ++h)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        st_cluster_f32x4(mapa_shared(red_slot(p, sm, rank, cw, h, mt, li), 0), acc[h][mt][0],
+                         acc[h][mt][1], acc[h][mt][2], acc[h][mt][3]);
   }
 
   static BSG_DEV void cluster_reduce(const KParams& p, const Smem& sm, int cw, int lane) {
@@ -1583,18 +1667,20 @@ struct Gemv {
     const int64_t tile = blockIdx.x / p.cluster;
     const float gs = kFold ? __ldg(p.gscale) : 1.0f;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int r = 0; r < p.cluster; ++r) {
-        const float4 u = *reinterpret_cast<const float4*>(
-            sm.base + (red_slot(p, sm, r, cw, mt, li) - sm.base_u));
-        v[0] += u.x;
-        v[1] += u.y;
-        v[2] += u.z;
-        v[3] += u.w;
+    for (int h = 0; h < kH; ++h)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < p.cluster; ++r) {
+          const float4 u = *reinterpret_cast<const float4*>(
+              sm.base + (red_slot(p, sm, r, cw, h, mt, li) - sm.base_u));
+          v[0] += u.x;
+          v[1] += u.y;
+          v[2] += u.z;
+          v[3] += u.w;
+        }
+        store_y(p, tile, h, cw, mt, lane, v, gs);
       }
-      store_y(p, tile, cw, mt, lane, v, gs);
-    }
   }
 
   // ---- consumers: warps 1..4.  The CTA's range is walked tile segment by tile segment; within
@@ -1612,13 +1698,17 @@ struct Gemv {
                                     int cw, int lane) {
     const Lane L = make_lane(p, cw, lane);
     const Run<SIDE> R{p.bs_log2, p.rs_log2, p.zbox_bytes, p};
-    float acc[1][MT][4];
-    zero(acc[0]);
-    uint64_t cacc[2][kCcCols];  // CUDA-core variant's partial sums (unused by the mma variant)
+    float acc[kH][MT][4];
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
+    for (int h = 0; h < kH; ++h) zero(acc[h]);
+    uint64_t cacc[kH][2][kCcCols];  // CUDA-core variant's partial sums (unused by the mma
+                                         // variant)
 #pragma unroll
-      for (int m = 0; m < kCcCols; ++m) cacc[rr][m] = 0ull;
+    for (int h = 0; h < kH; ++h)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int m = 0; m < kCcCols; ++m) cacc[h][rr][m] = 0ull;
     const float gs = kFold ? __ldg(p.gscale) : 1.0f;
     const int spt = p.spt;
     const int n = static_cast<int>(s1 - s0);
@@ -1653,17 +1743,23 @@ struct Gemv {
         w.next();
       }
       i += seg;
-      if constexpr (CC > 0) cc_fragment(L, cacc, acc);
+      if constexpr (CC > 0) {
+#pragma unroll
+        for (int h = 0; h < kH; ++h) cc_fragment(L, cacc[h], acc[h]);
+      }
       if (p.cluster >= 2) {
         cluster_publish(p, sm, cw, L, acc);  // the cluster's leader adds and stores
       } else if (seg == spt) {  // whole: this CTA consumed every stage of the tile
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) store_y(p, tile, cw, mt, lane, acc[0][mt], gs);
+        for (int h = 0; h < kH; ++h)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) store_y(p, tile, h, cw, mt, lane, acc[h][mt], gs);
       } else {  // shared with other CTAs (at most the first and the last segment of the range)
         store_partial(p, tile, first_tile, cw, lane, acc);
         pend[np++ & 1] = tile;
       }
-      zero(acc[0]);
+#pragma unroll
+      for (int h = 0; h < kH; ++h) zero(acc[h]);
     }
     if (np > 0) arrive_and_reduce(p, pend, np, cw, lane, gs);
     if (!ok && lane == 0) *sm.abort_word() = 1u;
@@ -1729,18 +1825,18 @@ BSG_DEV void gemv_cta(const KParams& p) {
 }
 
 // Tensor-core kernel (the default): products on mma.sync.m16n8k16.
-template <int FMT, bool BF16, int MT, bool ZP, int CPB>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(MT))
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, int H>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm_for(MT, H))
     bsgemv_mma_kernel(const __grid_constant__ KParams p) {
-  gemv_cta<Gemv<FMT, BF16, MT, ZP, CPB>>(p);
+  gemv_cta<Gemv<FMT, BF16, MT, ZP, CPB, H>>(p);
 }
 
 // CUDA-core kernel (BSGEMV_VARIANT_CUDA_CORE): products on fp32 FMAs, COLS = 1 (calls with
 // M = 1) or 8 (M <= 8) activation rows per lane.
 template <int FMT, bool BF16, bool ZP, int CPB, int COLS>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm_for_mt(1))
+__global__ void __launch_bounds__(kThreads, ctas_per_sm_for(1, 1))
     bsgemv_fma_kernel(const __grid_constant__ KParams p) {
-  gemv_cta<Gemv<FMT, BF16, 1, ZP, CPB, COLS>>(p);
+  gemv_cta<Gemv<FMT, BF16, 1, ZP, CPB, 1, COLS>>(p);
 }
 
 }  // namespace bsg

@@ -55,10 +55,10 @@ int launch_kernel(Kernel k, AttrRecord& rec, const KParams& p, int ctas, int sme
   return cudaGetLastError() == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
 }
 
-template <int FMT, bool BF16, int MT, bool ZP, int CPB>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, int H>
 int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
   static AttrRecord rec;
-  return launch_kernel(bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB>, rec, p, ctas, smem, s);
+  return launch_kernel(bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, H>, rec, p, ctas, smem, s);
 }
 
 template <int FMT, bool BF16, bool ZP, int CPB, int COLS>
@@ -106,10 +106,10 @@ int launch_fmt_cc(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaSt
 }
 
 // Dispatch over zero points and chunks per scale block (block_mode) for one format, activation
-// type and n8 tile count MT (1 .. 4).
-template <int FMT, bool BF16, int MT>
+// type, n8 tile count MT (1 .. 4) and H halves per tile.
+template <int FMT, bool BF16, int MT, int H = 1>
 int launch_fmt_mt(const KParams& p, bool zp, int cpb, int ctas, int smem, cudaStream_t s) {
-#define BSG_L(ZPV, C) return launch_one<FMT, BF16, MT, ZPV, C>(p, ctas, smem, s)
+#define BSG_L(ZPV, C) return launch_one<FMT, BF16, MT, ZPV, C, H>(p, ctas, smem, s)
 #define BSG_ZP(C) \
   if (zp) BSG_L(true, C); \
   BSG_L(false, C)

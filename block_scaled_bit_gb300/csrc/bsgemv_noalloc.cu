@@ -8,7 +8,7 @@
 // fixed scratch area that is part of the library's device image.
 //
 // The scratch area is the file-scope array below.  Every GPU that loads the library holds it
-// (kScratchBytes, about 5.2 MiB) until the process exits.  Its device address is looked up on
+// (kScratchBytes, about 7.6 MiB) until the process exits.  Its device address is looked up on
 // the first call made with a device current, and again on the first call after that device's
 // context changed (a device reset ends the context the address belonged to); such a first call
 // should happen before any stream capture.  All calls on a device share the one array: two calls
@@ -33,11 +33,14 @@
 
 namespace {
 
-// Largest problem the fixed scratch area serves: up to kMaxCtas persistent CTAs (four per SM of a
-// 152-SM GB300 fit) and up to kMaxTiles tiles of 64 output columns (N <= 524288).
-constexpr int kMaxCtas = 640;
-constexpr int kMaxTiles = 8192;
-constexpr int kMaxSlotFloats = 2 * 32 * 4;  // one warp's partial slot with two n8 tiles
+// Largest problem the fixed scratch area serves: up to kMaxCtas persistent CTAs (the three per SM
+// of a geometry for 16 rows on a 152-SM GB300 fit) and N <= kMaxN output columns (kMaxTiles
+// tiles of 64 columns, or half as many of 128).
+constexpr int kMaxCtas = 480;
+constexpr int64_t kMaxN = 524288;
+constexpr int kMaxTiles = static_cast<int>(kMaxN / bsg::kBoxRows);
+// one warp's slot: two n8 tiles of two halves
+constexpr int kMaxSlotFloats = bsg::kMaxHalves * 2 * 32 * 4;
 constexpr size_t kHeaderBytes = 256;        // error word, padded
 constexpr size_t kCounterBytes = size_t(kMaxTiles) * bsg::kConsumerWarps * sizeof(unsigned);
 constexpr size_t kPartialBytes =
@@ -121,7 +124,8 @@ extern "C" int bsgemv_run_noalloc(int format, int block_size, int has_zp, int64_
   int rc = bsg::compute_geometry(format, block_size, has_zp, N, K, kRows, sms, 0, 0,
                                  BSGEMV_SPLIT_AUTO, 0, &g, M);
   if (rc != BSGEMV_OK) return rc;
-  if (g.pub.ctas > kMaxCtas || g.pub.tiles > kMaxTiles || g.slot_floats > kMaxSlotFloats)
+  if (N > kMaxN || g.pub.ctas > kMaxCtas || g.pub.tiles > kMaxTiles ||
+      g.slot_floats > kMaxSlotFloats)
     return BSGEMV_ERR_SCRATCH_LIMIT;
 
   // The call's arguments: same rules as bsgemv_run.

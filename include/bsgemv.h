@@ -199,7 +199,9 @@ int bsgemv_plan_set_split(bsgemv_plan_t plan, int split, int cluster_size);
  * A/B override for measurements: variant (enum bsgemv_variant, 0 = keep; CUDA_CORE needs a plan
  * with max_M <= 8, else BSGEMV_ERR_UNSUPPORTED), ctas (persistent
  * CTAs of a stream-K split, 0 = keep; under BSGEMV_SPLIT_AUTO a CTA count selects stream-K),
- * rows_per_tile (reserved, must be 0), stages (ring depth, 0 = keep).
+ * rows_per_tile (output columns per CTA tile: 64 or 128, 0 = keep; 128 needs a plan with
+ * max_M <= 16 and the tensor-core variant, else BSGEMV_ERR_UNSUPPORTED), stages (ring depth,
+ * 0 = keep).
  * Changes the summation order, so results are bit-identical only between calls made under the
  * same settings.  Returns BSGEMV_ERR_UNSUPPORTED for a setting the plan cannot run.
  */
@@ -267,9 +269,9 @@ int bsgemv_plan_set_test_fault(bsgemv_plan_t plan, int skip_stage, int64_t wait_
  * a plan sized for 16 rows, whatever its M: a row's result is bit-identical for every M and
  * equal to bsgemv_plan(..., max_M = 16) + bsgemv_run.  Instead of a plan's cudaMalloc'd
  * workspace the cross-CTA reduction uses one fixed scratch area compiled into the library (a
- * file-scope device array of about 5.2 MiB that every GPU loading the library holds until the
+ * file-scope device array of about 7.6 MiB that every GPU loading the library holds until the
  * process exits).  Limits: M <= 16 (BSGEMV_ERR_INVALID_ARG beyond), N <= 524288 output columns
- * and at most 640 persistent CTAs (a 152-SM GB300 uses 456); beyond them the call returns
+ * and at most 480 persistent CTAs (a 152-SM GB300 uses 456); beyond them the call returns
  * BSGEMV_ERR_SCRATCH_LIMIT and does nothing.  The first call on a device looks up the scratch
  * area's device address (with that device current), and so does the first call after the
  * device's context changed (e.g. after cudaDeviceReset); make such a first call before any

@@ -5,19 +5,28 @@
 
 namespace bsg {
 
+#define BSG_STUB_MTH(name) \
+  int name(const KParams&, int, int, bool, int, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
+BSG_STUB_MTH(launch_int4_f16)
+BSG_STUB_MTH(launch_int4_bf16)
+BSG_STUB_MTH(launch_int8_f16)
+BSG_STUB_MTH(launch_int8_bf16)
+#undef BSG_STUB_MTH
 #define BSG_STUB_MT(name) \
   int name(const KParams&, int, bool, int, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
-BSG_STUB_MT(launch_int4_f16)
 BSG_STUB_MT(launch_int4_f16_wide)
 BSG_STUB_MT(launch_int4_bf16_wide)
 BSG_STUB_MT(launch_int8_f16_wide)
 BSG_STUB_MT(launch_int8_bf16_wide)
-BSG_STUB_MT(launch_int4_bf16)
-BSG_STUB_MT(launch_int8_f16)
-BSG_STUB_MT(launch_int8_bf16)
+BSG_STUB_MT(launch_int4_f16_tall)
+BSG_STUB_MT(launch_int4_bf16_tall)
+BSG_STUB_MT(launch_int8_f16_tall)
+BSG_STUB_MT(launch_int8_bf16_tall)
 #undef BSG_STUB_MT
-int launch_fp8(const KParams&, int, bool, bool, int, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
-int launch_nvfp4(const KParams&, int, bool, bool, int, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
+int launch_fp8(const KParams&, int, int, bool, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
+int launch_nvfp4(const KParams&, int, int, bool, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
+int launch_fp8_tall(const KParams&, int, bool, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
+int launch_nvfp4_tall(const KParams&, int, bool, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
 #define BSG_STUB_CC(name) \
   int name(const KParams&, bool, int, int, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
 BSG_STUB_CC(launch_cc_int4_f16)

@@ -1,7 +1,7 @@
 // Host code of the library under -fsanitize=address,undefined, without a GPU: the launch geometry
-// over a sweep of problems and SM counts (every split, override, max_M and per-call row count),
-// the kernel parameters filled from each geometry, and the C ABI's host-side paths (argument
-// errors, NULL handles, the no-device path of bsgemv_plan).  Exits 0 and prints "ok" when every
+// over a sweep of problems and SM counts (every split, override, tile height, max_M and per-call
+// row count), the kernel parameters filled from each geometry, and the C ABI's host-side paths
+// (argument errors, NULL handles, the no-device path of bsgemv_plan).  Exits 0 and prints "ok" when every
 // invariant holds; a sanitizer report makes it fail.  (Compiled and run by
 // tests/test_sanitizers.py; the host code of "[CUDA] Pin FP8 GEMV residency for grids just past
 // two blocks per SM" is tested under UBSan in the same spirit, its Tests section.)
@@ -47,9 +47,11 @@ int main() {
     const int cluster = split == BSGEMV_SPLIT_CLUSTER ? int(next() % 9) : 0;
     const int ctas = (split == BSGEMV_SPLIT_AUTO && next() % 4 == 0) ? 1 + int(next() % 2000) : 0;
     const int stages = next() % 8 == 0 ? 1 + int(next() % bsg::kMaxStages) : 0;
+    const int tile_rows_v[] = {0, 0, 64, 128};
+    const int tile_rows = pick(tile_rows_v, 4);
     bsg::Geometry g;
     const int rc = bsg::compute_geometry(fmt | act, bs, zp, N, K, max_M, sm, ctas, stages, split,
-                                         cluster, &g);
+                                         cluster, &g, 0, tile_rows);
     if (rc != BSGEMV_OK) {
       CHECK(rc == BSGEMV_ERR_UNSUPPORTED);
       continue;
@@ -58,11 +60,22 @@ int main() {
     CHECK(g.pub.stages >= 1 && g.pub.stages <= bsg::kMaxStages);
     CHECK(g.pub.smem_bytes <= 232448 && g.act_off % 1024 == 0 && g.side_off % 128 == 0);
     CHECK(g.pub.cluster == 0 || g.pub.ctas == g.pub.tiles * g.pub.cluster);
+    // tiles of one or two 64-row halves; two only for kernels of up to two n8 tiles
+    CHECK(g.pub.rows_per_tile == 64 * g.halves && (g.halves == 1 || g.halves == 2));
+    CHECK(tile_rows == 0 || g.pub.rows_per_tile == tile_rows);
+    CHECK(g.halves == 1 || g.mt_max <= 2);
+    CHECK(g.pub.tiles * g.pub.rows_per_tile >= N && (g.pub.tiles - 1) * g.pub.rows_per_tile < N);
+    // a stage: one 8 KB box per half and k-box (two k-boxes for 8-bit weights with one half)
+    const bool four = fmt == bsg::kInt4 || fmt == bsg::kNvfp4;
+    CHECK(g.stage_bytes == ((four && g.halves == 1) ? 8192 : 16384));
+    CHECK(g.pub.k_per_stage == ((!four && g.halves == 2) ? 128 : 256));
+    CHECK(g.slot_floats == g.halves * g.mt_max * 128);
     // every call's ring layout keeps the plan's split, CTA count and residency
     for (int rows = 1; rows <= max_M; rows += 1 + int(next() % 5)) {
       bsg::Geometry r;
       CHECK(bsg::compute_geometry(fmt | act, bs, zp, N, K, max_M, sm, ctas, stages, split, cluster,
-                                  &r, rows) == BSGEMV_OK);
+                                  &r, rows, tile_rows) == BSGEMV_OK);
+      CHECK(r.pub.rows_per_tile == g.pub.rows_per_tile && r.halves == g.halves);
       CHECK(r.pub.ctas == g.pub.ctas && r.pub.cluster == g.pub.cluster &&
             r.pub.ctas_per_sm == g.pub.ctas_per_sm && r.pub.total_stages == g.pub.total_stages);
       CHECK(r.pub.stages >= g.pub.stages && r.pub.smem_bytes <= 232448);
@@ -73,10 +86,11 @@ int main() {
       bsg::fill_params(r, maps, nullptr, nullptr, nullptr, nullptr, nullptr, rows, nullptr,
                        nullptr, nullptr, &k);
       CHECK(k.M == rows && k.stages == r.pub.stages && k.skip_stage == -1 && k.wait_ns > 0);
+      CHECK(k.side_tx % r.pub.rows_per_tile == 0);
       ++checked;
     }
     bsgemv_geometry pub;
-    if (split == BSGEMV_SPLIT_AUTO && ctas == 0 && stages == 0) {
+    if (split == BSGEMV_SPLIT_AUTO && ctas == 0 && stages == 0 && tile_rows == 0) {
       CHECK(bsgemv_geometry_for(fmt | act, bs, zp, N, K, max_M, sm, &pub) == BSGEMV_OK);
       CHECK(std::memcmp(&pub, &g.pub, sizeof(pub)) == 0);
     }

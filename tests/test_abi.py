@@ -93,9 +93,21 @@ SHAPES = [("int4", 32, False, 151936, 4096), ("int8", 128, True, 2048, 4096),
 def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
     g = bsgemv.geometry_for(fmt, "f16", bs, zp, N, K, max_M, sms)
     four = fmt in ("int4", "nvfp4")
-    assert g["k_per_stage"] == 256
-    assert g["rows_per_tile"] == 64 and g["consumer_warps"] == 4
-    assert g["tiles"] == -(-N // 64)
+    # 64-row tiles, or 128 (two halves) for plans of up to 16 rows where at most 5 resident CTAs
+    # share a 128-row tile on average and there are at least 2 such stages per resident CTA; a
+    # stage is 256 k, or 128 k for the 8-bit formats with 128-row tiles (16 KB of weight, but
+    # 8 KB for the 4-bit formats with 64-row tiles)
+    rpt = g["rows_per_tile"]
+    assert rpt in (64, 128) and g["consumer_warps"] == 4
+    assert g["k_per_stage"] == (128 if rpt == 128 and not four else 256)
+    assert g["tiles"] == -(-N // rpt)
+    tall_tiles = -(-N // 128)
+    tall_stages = tall_tiles * -(-K // (256 if four else 128))
+    if max_M > 16:
+        assert rpt == 64
+    else:  # (128-row tiles run 3 CTAs per SM)
+        assert (rpt == 128) == (tall_tiles * 5 >= sms * 3 and tall_stages >= 2 * sms * 3)
+        assert rpt == 64 or g["ctas_per_sm"] == 3
     assert g["stages_per_tile"] == -(-K // g["k_per_stage"])
     assert g["total_stages"] == g["tiles"] * g["stages_per_tile"]
     # persistent grid: never more CTAs than stages or than the resident slots
@@ -124,23 +136,32 @@ def test_geometry_predicates(L, fmt, bs, zp, N, K, sms, max_M):
 
 def test_summation_order_independent_of_max_M(L):
     """The per-row summation order is fixed by the work split (CTAs, tiles, stages).  It depends
-    on max_M through the residency class -- 4 CTAs per SM for max_M <= 8, 3 for max_M <= 24,
-    2 for max_M <= 32 (more accumulator registers) -- never on M of a call (not an argument),
-    which gives row bit-identity across M within a plan."""
+    on max_M through the residency class -- with 64-row tiles 4 CTAs per SM for max_M <= 8, 3 for
+    max_M <= 24, 2 for max_M <= 32 (more accumulator registers); with 128-row tiles (plans for up
+    to 16 rows with long work per CTA) 3 for every max_M -- never on M of a call (not an
+    argument), which gives row bit-identity across M within a plan."""
     keys = ("ctas", "tiles", "stages_per_tile", "k_per_stage", "rows_per_tile", "consumer_warps")
+
+    def geo(N, K, max_M):
+        return bsgemv.geometry_for("int4", "f16", 32, False, N, K, max_M, 152)
+
     for N, K in ((4096, 4096), (151936, 4096), (300, 2048)):
+        tall = geo(N, K, 1)["rows_per_tile"] == 128
         # (plans with max_M > 16 also differ by their activation ring, 32 rows per stage, which
         # can change the cluster size that fits: the geometry is the plan's, never the call's)
-        for group in ((1, 2, 5, 8), (9, 12, 16)):
-            ref = bsgemv.geometry_for("int4", "f16", 32, False, N, K, group[0], 152)
+        groups = ((1, 2, 5, 8, 9, 12, 16),) if tall else ((1, 2, 5, 8), (9, 12, 16))
+        for group in groups:
+            ref = geo(N, K, group[0])
             for max_M in group[1:]:
-                g = bsgemv.geometry_for("int4", "f16", 32, False, N, K, max_M, 152)
+                g = geo(N, K, max_M)
                 assert {k: g[k] for k in keys} == {k: ref[k] for k in keys}
-        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 8, 152)["ctas_per_sm"] == 4
-        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 9, 152)["ctas_per_sm"] == 3
-        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 17, 152)["ctas_per_sm"] == 3
-        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 24, 152)["ctas_per_sm"] == 3
-        assert bsgemv.geometry_for("int4", "f16", 32, False, N, K, 25, 152)["ctas_per_sm"] == 2
+        assert geo(N, K, 8)["ctas_per_sm"] == (3 if tall else 4)
+        assert geo(N, K, 9)["ctas_per_sm"] == 3
+        assert geo(N, K, 16)["rows_per_tile"] == (128 if tall else 64)
+        assert geo(N, K, 17)["ctas_per_sm"] == 3 and geo(N, K, 17)["rows_per_tile"] == 64
+        assert geo(N, K, 24)["ctas_per_sm"] == 3
+        assert geo(N, K, 25)["ctas_per_sm"] == 2
+    assert geo(151936, 4096, 1)["rows_per_tile"] == 128  # the lm_head: 1187 tiles, 456 CTAs
 
 
 def test_stream_k_ranges_cover_every_stage_once():
@@ -184,7 +205,8 @@ def test_owner_lookup_without_division():
 
 
 def test_split_choice_on_the_configuration_shapes(L):
-    """Automatic K split at 152 SMs (4 CTAs per SM): shapes with few tiles take a cluster of CTAs
+    """Automatic K split at 152 SMs (4 CTAs per SM with 64-row tiles, 3 with 128-row tiles):
+    shapes with few tiles take a cluster of CTAs
     per tile (reduced in shared memory), shapes with more tiles than resident CTAs stream-K, with
     a whole number of CTAs per tile when the tiles are fewer than the resident CTAs."""
     def split(fmt, bs, zp, N, K, max_M=1):
@@ -193,17 +215,18 @@ def test_split_choice_on_the_configuration_shapes(L):
     assert split("int8", 32, True, 2048, 4096) == (8, 2)     # 32 tiles x 16 stages
     assert split("int8", 128, True, 4096, 12288) == (8, 6)   # 64 tiles x 48 stages
     assert split("fp8", 128, False, 5120, 6144) == (6, 4)    # 80 tiles x 24 stages
-    assert split("int8", 128, True, 12288, 4096)[0] == 0     # 192 tiles: no even split fits
+    # 128-row tiles (96 tiles x 32 stages, 3 CTAs per SM): 4-CTA clusters of 8 stages each
+    assert split("int8", 128, True, 12288, 4096) == (4, 8)
     assert split("fp8", 128, False, 5120, 17408)[0] == 0     # 80 tiles x 68 stages
     assert split("int8", 128, True, 4096, 4096) == (8, 2)    # 64 tiles x 16 stages
     assert split("int8", 128, True, 5120, 2048) == (4, 2)    # 80 tiles x 8 stages
     assert split("fp8", 128, False, 512, 2048) == (8, 1)     # 8 tiles x 8 stages
-    assert split("int4", 32, False, 151936, 4096)[0] == 0    # 2374 tiles: stream-K
+    assert split("int4", 32, False, 151936, 4096)[0] == 0    # 1187 tiles of 128 rows: stream-K
     # plans for max_M = 8: 8-CTA clusters no longer fit next to the activation ring, 4 do
     assert split("fp8", 128, False, 2048, 4096, 8) == (4, 4)  # 32 tiles x 16 stages
-    g = bsgemv.geometry_for("int8", "f16", 128, True, 12288, 4096, 1, 152)
-    assert g["ctas"] == 576                                  # 192 tiles x 3 CTAs
-    assert split("nvfp4", 16, False, 248320, 2048)[0] == 0   # 3880 tiles: stream-K
+    g = bsgemv.geometry_for("fp8", "f16", 128, False, 5120, 17408, 1, 152)
+    assert g["ctas"] == 560                                  # 80 tiles x 7 CTAs
+    assert split("nvfp4", 16, False, 248320, 2048)[0] == 0   # 1940 tiles of 128 rows: stream-K
 
 
 def test_shared_memory_layout_is_aligned_for_every_problem(L):

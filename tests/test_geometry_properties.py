@@ -39,7 +39,11 @@ def test_geometry_is_runnable(p):
         assert K % bs != 0 or K % 64 != 0
         return
     spt, tiles = g["stages_per_tile"], g["tiles"]
-    assert tiles == -(-N // 64) and spt == -(-K // 256) and g["total_stages"] == tiles * spt
+    rpt = g["rows_per_tile"]
+    # k per stage: 256, or 128 for the 8-bit formats with 128-row tiles
+    kc = 128 if rpt == 128 and fmt in ("int8", "fp8") else 256
+    assert g["k_per_stage"] == kc and rpt in (64, 128) and (rpt == 64 or max_M <= 16)
+    assert tiles == -(-N // rpt) and spt == -(-K // kc) and g["total_stages"] == tiles * spt
     slots = sms * g["ctas_per_sm"]
     C = g["cluster"]
     if C:
