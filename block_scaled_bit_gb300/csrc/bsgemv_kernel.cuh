@@ -656,16 +656,29 @@ struct Gemv {
                          w.ks * kSrb + j * kBoxRowBytes, row + h * kBoxRows, sm.full(i), pol);
   }
 
+  // The side boxes of the box holding stage (tile, ks) into side slot j (lane 0).  With one half
+  // they keep the normal L2 policy: a box reads 64 bytes of a row's scales (16 or 32 of its zero
+  // points), and the rest of the row's L2 line, fetched from DRAM with them, is what the next box
+  // of the same rows reads a few stages later (measured on GB300: 1-4 % faster than evict-first,
+  // which loses that rest to the streaming weights and reads it again).  With two halves they are
+  // evict-first like the weights (the normal policy measured 2-4 % slower on the int4 lm_head,
+  // though its DRAM reads fell from 1.055 to 1.011 of the algorithmic bytes).
   static BSG_DEV void side_copy(const KParams& p, const Smem& sm, int j, const Walk& w,
                                 uint64_t pol) {
     const uint32_t full = sm.sfull(j), dst = sm.side_u(j);
     const int bx = w.ks >> p.rs_log2;
     const int row = static_cast<int>(w.tile * kRows);
     mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.side_tx));
-    tma_load_2d_hint(dst, &p.tm_s, bx * kSideScaleBytes, row, full, pol);
-    if constexpr (ZP)
-      tma_load_2d_hint(dst + kRows * kSideScaleBytes, &p.tm_z, bx * p.zbox_bytes, row, full,
-                       pol);
+    if constexpr (kH == 1) {
+      tma_load_2d(dst, &p.tm_s, bx * kSideScaleBytes, row, full);
+      if constexpr (ZP)
+        tma_load_2d(dst + kRows * kSideScaleBytes, &p.tm_z, bx * p.zbox_bytes, row, full);
+    } else {
+      tma_load_2d_hint(dst, &p.tm_s, bx * kSideScaleBytes, row, full, pol);
+      if constexpr (ZP)
+        tma_load_2d_hint(dst + kRows * kSideScaleBytes, &p.tm_z, bx * p.zbox_bytes, row, full,
+                         pol);
+    }
   }
 
   // Failure handling.  Every wait is bounded (KParams::wait_ns).  A consumer warp that gives up
@@ -1731,8 +1744,8 @@ struct Gemv {
         }
         if (ok) ok = mbar_wait(sm.full(r.slot), r.phase, p.err, kErrTimeoutFull, p.wait_ns);
         if (ok) {
-          const Sh sh{sm.base, sm.act_off + r.slot * sm.act_bytes,
-                      sm.side_off + sr.slot * sm.side_bytes};
+          const Sh sh{sm.base, static_cast<uint32_t>(sm.act_off + r.slot * sm.act_bytes),
+                      static_cast<uint32_t>(sm.side_off + sr.slot * sm.side_bytes)};
           consume_stage(R, L, sm.w(r.slot), sh, tile, w.ks, acc, cacc);
         }
         __syncwarp();
