@@ -1109,14 +1109,30 @@ struct Gemv {
       }
   }
 
-  // acc += tmp * s (fragment entries 0, 1: row g; 2, 3: row g + 8).
+  // acc += tmp * s (fragment entries 0, 1: row g; 2, 3: row g + 8).  With two or more n8 tiles
+  // the row's pairs go through packed fp32 FMAs (fma.rn.f32x2: the same rounding per element,
+  // half the instructions once the scale pair is built).
   static BSG_DEV void apply_scales(float s0, float s1, const float (&tmp)[MT][4], float (&acc)[MT][4]) {
+    if constexpr (MT >= 2) {
+      const uint64_t p0 = f32x2(s0, s0), p1 = f32x2(s1, s1);
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      acc[mt][0] = fmaf(tmp[mt][0], s0, acc[mt][0]);
-      acc[mt][1] = fmaf(tmp[mt][1], s0, acc[mt][1]);
-      acc[mt][2] = fmaf(tmp[mt][2], s1, acc[mt][2]);
-      acc[mt][3] = fmaf(tmp[mt][3], s1, acc[mt][3]);
+      for (int mt = 0; mt < MT; ++mt) {
+        uint64_t a01 = f32x2(acc[mt][0], acc[mt][1]), a23 = f32x2(acc[mt][2], acc[mt][3]);
+        fma_f32x2(a01, f32x2(tmp[mt][0], tmp[mt][1]), p0);
+        fma_f32x2(a23, f32x2(tmp[mt][2], tmp[mt][3]), p1);
+        acc[mt][0] = f32x2_lo(a01);
+        acc[mt][1] = f32x2_hi(a01);
+        acc[mt][2] = f32x2_lo(a23);
+        acc[mt][3] = f32x2_hi(a23);
+      }
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        acc[mt][0] = fmaf(tmp[mt][0], s0, acc[mt][0]);
+        acc[mt][1] = fmaf(tmp[mt][1], s0, acc[mt][1]);
+        acc[mt][2] = fmaf(tmp[mt][2], s1, acc[mt][2]);
+        acc[mt][3] = fmaf(tmp[mt][3], s1, acc[mt][3]);
+      }
     }
   }
 
