@@ -1715,11 +1715,13 @@ struct Gemv {
   // ---- consumers: warps 1..4.  The CTA's range is walked tile segment by tile segment; within
   // a segment every stage waits for its slot (and, when it opens one, its side box), is
   // multiplied in, and is released; the segment ends with the epilogue.
+  // SIDE: scales and zero points from the side ring (KParams::side_tma), else from global memory;
+  // a template parameter of the kernel, so that each kernel holds one consumer loop.
+  template <bool SIDE>
   static BSG_DEV void consume(const KParams& p, const Smem& sm, int64_t s0, int64_t s1, int cw,
                               int lane) {
     pdl_wait();  // the epilogues write y and the plan's workspace
-    if (p.side_tma) consume_range<true>(p, sm, s0, s1, cw, lane);
-    else consume_range<false>(p, sm, s0, s1, cw, lane);
+    consume_range<SIDE>(p, sm, s0, s1, cw, lane);
   }
 
   template <bool SIDE>
@@ -1796,7 +1798,7 @@ struct Gemv {
 };
 
 // The body shared by both kernels: one CTA of the persistent grid.
-template <class K>
+template <class K, bool SIDE>
 BSG_DEV void gemv_cta(const KParams& p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned (128-byte swizzle atoms), derived from the shared array so that plain
@@ -1838,7 +1840,7 @@ BSG_DEV void gemv_cta(const KParams& p) {
   if (warp == 0) {
     pd = K::produce(p, sm, s0, s1, lane);
   } else {
-    K::consume(p, sm, s0, s1, warp - 1, lane);
+    K::template consume<SIDE>(p, sm, s0, s1, warp - 1, lane);
   }
   // A wait that ran out anywhere in the CTA: the copy warp waits for what it issued (see
   // produce) before the CTA's shared memory is given up.
@@ -1854,18 +1856,18 @@ BSG_DEV void gemv_cta(const KParams& p) {
 }
 
 // Tensor-core kernel (the default): products on mma.sync.m16n8k16.
-template <int FMT, bool BF16, int MT, bool ZP, int CPB, int H>
+template <int FMT, bool BF16, int MT, bool ZP, int CPB, int H, bool SIDE>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm_for(MT, H))
     bsgemv_mma_kernel(const __grid_constant__ KParams p) {
-  gemv_cta<Gemv<FMT, BF16, MT, ZP, CPB, H>>(p);
+  gemv_cta<Gemv<FMT, BF16, MT, ZP, CPB, H>, SIDE>(p);
 }
 
 // CUDA-core kernel (BSGEMV_VARIANT_CUDA_CORE): products on fp32 FMAs, COLS = 1 (calls with
 // M = 1) or 8 (M <= 8) activation rows per lane.
-template <int FMT, bool BF16, bool ZP, int CPB, int COLS>
+template <int FMT, bool BF16, bool ZP, int CPB, int COLS, bool SIDE>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm_for(1, 1))
     bsgemv_fma_kernel(const __grid_constant__ KParams p) {
-  gemv_cta<Gemv<FMT, BF16, 1, ZP, CPB, 1, COLS>>(p);
+  gemv_cta<Gemv<FMT, BF16, 1, ZP, CPB, 1, COLS>, SIDE>(p);
 }
 
 }  // namespace bsg

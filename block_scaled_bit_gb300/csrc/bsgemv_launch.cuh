@@ -57,14 +57,23 @@ int launch_kernel(Kernel k, AttrRecord& rec, const KParams& p, int ctas, int sme
 
 template <int FMT, bool BF16, int MT, bool ZP, int CPB, int H>
 int launch_one(const KParams& p, int ctas, int smem, cudaStream_t s) {
-  static AttrRecord rec;
-  return launch_kernel(bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, H>, rec, p, ctas, smem, s);
+  // one kernel per source of the scales: the side ring, or global memory (unaligned pitches)
+  static AttrRecord rec_side, rec_global;
+  if (p.side_tma)
+    return launch_kernel(bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, H, true>, rec_side, p, ctas,
+                         smem, s);
+  return launch_kernel(bsgemv_mma_kernel<FMT, BF16, MT, ZP, CPB, H, false>, rec_global, p, ctas,
+                       smem, s);
 }
 
 template <int FMT, bool BF16, bool ZP, int CPB, int COLS>
 int launch_one_cc(const KParams& p, int ctas, int smem, cudaStream_t s) {
-  static AttrRecord rec;
-  return launch_kernel(bsgemv_fma_kernel<FMT, BF16, ZP, CPB, COLS>, rec, p, ctas, smem, s);
+  static AttrRecord rec_side, rec_global;
+  if (p.side_tma)
+    return launch_kernel(bsgemv_fma_kernel<FMT, BF16, ZP, CPB, COLS, true>, rec_side, p, ctas,
+                         smem, s);
+  return launch_kernel(bsgemv_fma_kernel<FMT, BF16, ZP, CPB, COLS, false>, rec_global, p, ctas,
+                       smem, s);
 }
 
 // CUDA-core variant (M <= 8): dispatch over zero points and chunks per scale block; COLS = 1
