@@ -314,7 +314,12 @@ int compute_geometry(int format, int block_size, int has_zp, int64_t N, int64_t 
     if (geometry_for_tiles(format, block_size, has_zp, N, K, max_M, sm_count, ctas_override,
                            stages_override, split, cluster, mt, 2, max_M, &tall) == BSGEMV_OK &&
         tall.pub.tiles * kTallMaxCtasPerTile >= int64_t(sm_count) * tall.pub.ctas_per_sm &&
-        tall.pub.total_stages >= int64_t(kTallMinStages) * sm_count * tall.pub.ctas_per_sm) {
+        tall.pub.total_stages >= int64_t(kTallMinStages) * sm_count * tall.pub.ctas_per_sm &&
+        // ... unless 128-row tiles lose the cluster split that 64-row tiles keep, leaving several
+        // CTAs per tile to a stream-K reduction (measured on GB300, 12288 x 4096 in plans for 16
+        // rows: 64-row tiles in 2-CTA clusters 2-9 % faster than 128-row stream-K for int4, 13-17 %
+        // for int8 at M = 9 and 16)
+        !(tall.pub.cluster == 0 && tall.pub.ctas > tall.pub.tiles && g->pub.cluster >= 2)) {
       if (rows == max_M) {
         *g = tall;
         return BSGEMV_OK;
