@@ -131,7 +131,7 @@ int bsgemv_plan(bsgemv_plan_t* out, int format, int block_size, int has_zp, int6
 /*
  * Enqueue y = A . deq(W)^T for the first M (1 <= M <= max_M) rows of A on `stream`.
  * Pointers as in the layout table above (device memory).  Checks arguments, alignment and the
- * current device, launches one kernel and returns cudaGetLastError's verdict; it does not wait.
+ * current device, launches one kernel and returns cudaGetLastError's result; it does not wait.
  * Results depend only on the plan and the inputs: the same row of A gives bit-identical
  * output for every M, and repeated calls are bit-identical.
  */
