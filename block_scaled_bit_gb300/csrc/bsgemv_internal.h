@@ -4,8 +4,9 @@
 //   * a CTA tile is 64 or 128 consecutive output columns n (rows of W) over a k-range: one or
 //     two "halves" of kBoxRows = 64 rows.  Consumer warp w owns mma row group w (16 rows) of
 //     every half, so with two halves every activation fragment it loads and every stage's
-//     bookkeeping serve 32 rows.  Plans whose work is long per CTA take two halves, plans with
-//     little work per CTA one (finer-grained split; see compute_geometry);
+//     bookkeeping serve 32 rows.  Plans for up to 16 rows whose 128-row tiles would each be
+//     shared by few resident CTAs take two halves; plans whose tiles are shared by many CTAs keep
+//     one (a finer split of the work; see compute_geometry);
 //   * k is walked in "stages" of 256 k for the 4-bit formats (128 weight bytes per row), of 256 k
 //     (two k-boxes) for the 8-bit formats with one half and 128 k with two: one 128-byte-swizzled
 //     TMA box [64 rows][128 B] per half and k-box (8 KB of weight per stage for the 4-bit formats

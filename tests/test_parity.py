@@ -187,23 +187,59 @@ def test_edge_shapes(torch_cuda, fmt, bs, zp, N, K, M):
     assert_parity(case, run(case))
 
 
-def test_side_data_fallback_matches_tma(torch_cuda):
+@pytest.mark.parametrize("M", [2, 12])
+@pytest.mark.parametrize("rows_per_tile", [64, 128])
+@pytest.mark.parametrize("fmt,bs,zp", [("int8", 32, True), ("int4", 32, True), ("int4", 16, False),
+                                       ("fp8", 128, False), ("nvfp4", 16, False)])
+def test_side_data_fallback_matches_tma(torch_cuda, fmt, bs, zp, rows_per_tile, M):
     """Scales / zero points that cannot be TMA-tiled (misaligned base) are read from global
-    memory; the arithmetic is the same, so the output is bit-identical."""
+    memory (the kernels built for that source); the arithmetic is the same, so the output is
+    bit-identical, for both tile heights and one or two n8 tiles."""
     torch = torch_cuda
-    case = synth.make_case("int8", "f16", 32, True, 300, 2048, 2, 5)
+    case = synth.make_case(fmt, "f16", bs, zp, 300, 2048, M, 5)
     d = bsgemv.upload(case, "cuda")
-    with bsgemv.Plan("int8", "f16", 32, True, case.N, case.K, 2) as plan:
-        plan.run(d.A, d.W, d.scales, d.zp, d.y)
+    with bsgemv.Plan(fmt, "f16", bs, zp, case.N, case.K, 16) as plan:
+        assert plan.set_override(rows_per_tile=rows_per_tile) == bsgemv.OK
+        plan.run(d.A, d.W, d.scales, d.zp, d.y, M=M)
         torch.cuda.synchronize()
         ref = bsgemv.y_bits(d.y)
-        s2 = torch.empty(d.scales.numel() + 1, dtype=torch.int16, device="cuda")[1:]
-        s2.copy_(d.scales.view(-1))
-        z2 = torch.empty(d.zp.numel() + 3, dtype=torch.uint8, device="cuda")[3:]
-        z2.copy_(d.zp.view(-1))
-        assert s2.data_ptr() % 16 != 0 and z2.data_ptr() % 16 != 0
+        # the same bytes one element past a 16-byte boundary
+        es = d.scales.element_size()
+        flat = d.scales.reshape(-1)
+        s2 = torch.empty(flat.numel() + 1, dtype=flat.dtype, device="cuda")[1:]
+        s2.copy_(flat)
+        assert s2.data_ptr() % 16 == es % 16 and s2.data_ptr() % es == 0
+        z2 = d.zp
+        if zp:
+            z2 = torch.empty(d.zp.numel() + 3, dtype=torch.uint8, device="cuda")[3:]
+            z2.copy_(d.zp.view(-1))
+            assert z2.data_ptr() % 16 != 0
         y2 = torch.empty_like(d.y)
-        plan.run(d.A, d.W, s2, z2, y2)
+        plan.run(d.A, d.W, s2, z2, y2, M=M)
+        torch.cuda.synchronize()
+        assert plan.device_status() == bsgemv.OK
+    assert np.array_equal(bsgemv.y_bits(y2), ref)
+    assert_parity(case, ref)
+
+
+@pytest.mark.parametrize("fmt,bs,zp", [("int8", 32, True), ("int4", 16, True), ("fp8", 128, False),
+                                       ("nvfp4", 16, False)])
+def test_side_data_fallback_cuda_core_variant(torch_cuda, fmt, bs, zp):
+    """The CUDA-core variant's kernels for scales read from global memory: bit-identical to its
+    side-ring kernels."""
+    torch = torch_cuda
+    case = synth.make_case(fmt, "bf16", bs, zp, 333, 1024, 5, 6)
+    d = bsgemv.upload(case, "cuda")
+    with bsgemv.Plan(fmt, "bf16", bs, zp, case.N, case.K, 8) as plan:
+        assert plan.set_override(variant=bsgemv.VARIANTS["cuda_core"]) == bsgemv.OK
+        plan.run(d.A, d.W, d.scales, d.zp, d.y, M=5)
+        torch.cuda.synchronize()
+        ref = bsgemv.y_bits(d.y)
+        flat = d.scales.reshape(-1)
+        s2 = torch.empty(flat.numel() + 1, dtype=flat.dtype, device="cuda")[1:]
+        s2.copy_(flat)
+        y2 = torch.empty_like(d.y)
+        plan.run(d.A, d.W, s2, d.zp, y2, M=5)
         torch.cuda.synchronize()
         assert plan.device_status() == bsgemv.OK
     assert np.array_equal(bsgemv.y_bits(y2), ref)
