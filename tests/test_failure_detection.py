@@ -34,20 +34,21 @@ def cta0_range(g):
     return g["total_stages"] // g["ctas"]
 
 
-@pytest.mark.parametrize("fmt,act,bs,zp,N,K,M,split", [
-    ("int8", "f16", 128, True, 2048, 4096, 4, "stream_k"),     # tiles shared by several CTAs
-    ("int4", "bf16", 32, False, 40000, 2048, 1, "auto"),       # long CTA ranges, a deep ring
-    ("int4", "f16", 32, True, 40000, 2048, 3, "auto"),
-    ("fp8", "f16", 128, False, 512, 2048, 9, "cluster"),       # cluster split, two n8 tiles
-    ("nvfp4", "bf16", 16, False, 2048, 2048, 2, "auto"),
+@pytest.mark.parametrize("fmt,act,bs,zp,N,K,M,split,max_M", [
+    ("int8", "f16", 128, True, 2048, 4096, 4, "stream_k", 16),   # tiles shared by several CTAs
+    ("int4", "bf16", 32, False, 40000, 2048, 1, "auto", 16),     # long ranges, 128-row tiles
+    ("int4", "f16", 32, True, 40000, 2048, 3, "auto", 16),
+    ("fp8", "f16", 128, False, 512, 2048, 9, "cluster", 16),     # cluster split, two n8 tiles
+    ("nvfp4", "bf16", 16, False, 2048, 2048, 2, "auto", 16),
+    ("int4", "f16", 32, False, 12288, 4096, 2, "auto", 8),       # 128-row tiles in 4-CTA clusters
 ])
 @pytest.mark.parametrize("where", ["first", "last"])
 def test_a_wait_that_runs_out_is_reported_and_the_plan_recovers(torch_cuda, fmt, act, bs, zp, N,
-                                                                 K, M, split, where):
+                                                                 K, M, split, max_M, where):
     torch = torch_cuda
     case = synth.make_case(fmt, act, bs, zp, N, K, M, 31 + N)
     d = bsgemv.upload(case, "cuda")
-    with bsgemv.Plan(fmt, act, bs, zp, N, K, 16) as plan:
+    with bsgemv.Plan(fmt, act, bs, zp, N, K, max_M) as plan:
         if split == "stream_k":
             assert plan.set_override(ctas=37) == bsgemv.OK
         elif split == "cluster":
