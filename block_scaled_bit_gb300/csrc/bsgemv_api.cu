@@ -267,6 +267,17 @@ namespace {
 
 // A host -> device into the plan's staging buffer, the GEMV, y device -> host, all on `stream`;
 // waits for the stream when `sync`.
+// The device address of pinned host memory (nullptr for pageable memory, device memory, or a
+// mapping the current device cannot use).
+void* host_mapping(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 int run_host_impl(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
                   const void* zp, void* y_host, int M, void* stream, bool sync) {
   if (plan == nullptr || A_host == nullptr || y_host == nullptr) return BSGEMV_ERR_INVALID_ARG;
@@ -291,12 +302,26 @@ int run_host_impl(bsgemv_plan_t plan, const void* A_host, const void* W, const v
   void* dA = plan->stage;
   void* dy = static_cast<char*>(plan->stage) + a_pad;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(dA, A_host, size_t(M) * g.K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  const size_t a_call = size_t(M) * g.K * 2, y_call = size_t(M) * g.N * 2;
+  // Pinned host buffers (16-byte aligned) are copied by kernels through their device mapping:
+  // between the GEMV's kernels a copy kernel overlaps its start-up like they do, where a
+  // copy-engine transfer adds latency of its own.  Other host memory goes by the copy engines.
+  void* A_map = host_mapping(A_host);
+  void* y_map = host_mapping(y_host);
+  const bool by_kernel = A_map != nullptr && y_map != nullptr && aligned(A_map, 16) &&
+                         aligned(y_map, 16);
+  if (by_kernel) {
+    if ((rc = bsg::launch_host_copy(dA, A_map, a_call, plan->sm_count, s)) != BSGEMV_OK) return rc;
+  } else if (cudaMemcpyAsync(dA, A_host, a_call, cudaMemcpyHostToDevice, s) != cudaSuccess) {
     return BSGEMV_ERR_CUDA;
+  }
   rc = bsgemv_run(plan, dA, W, scales, zp, dy, M, stream);
   if (rc != BSGEMV_OK) return rc;
-  if (cudaMemcpyAsync(y_host, dy, size_t(M) * g.N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (by_kernel) {
+    if ((rc = bsg::launch_host_copy(y_map, dy, y_call, plan->sm_count, s)) != BSGEMV_OK) return rc;
+  } else if (cudaMemcpyAsync(y_host, dy, y_call, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
     return BSGEMV_ERR_CUDA;
+  }
   if (!sync) return BSGEMV_OK;
   return cudaStreamSynchronize(s) == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
 }

@@ -244,6 +244,11 @@ struct AttrRecord {
 // The error word of bsgemv_run_noalloc's scratch area on the current device.
 int noalloc_error_word(unsigned** out);
 
+// Copy `bytes` from src to dst with a kernel on stream s (programmatic dependent launch: it waits
+// for the previous kernel in the stream before touching either buffer).  Both 16-byte aligned
+// (else BSGEMV_ERR_MISALIGNED); either may be pinned host memory seen through its device mapping.
+int launch_host_copy(void* dst, const void* src, size_t bytes, int sm_count, cudaStream_t s);
+
 int launch_debug_dequant(int fmt, bool bf16, bool has_zp, int bs, int64_t N, int64_t K,
                          const uint8_t* W, const uint8_t* scales, const uint8_t* zp,
                          const float* gscale, float* out, cudaStream_t s);

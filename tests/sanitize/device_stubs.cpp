@@ -41,5 +41,6 @@ int launch_debug_dequant(int, bool, bool, int, int64_t, int64_t, const uint8_t*,
   return BSGEMV_ERR_CUDA;
 }
 int noalloc_error_word(unsigned**) { return BSGEMV_ERR_CUDA; }
+int launch_host_copy(void*, const void*, size_t, int, cudaStream_t) { return BSGEMV_ERR_CUDA; }
 
 }  // namespace bsg

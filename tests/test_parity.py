@@ -282,6 +282,37 @@ def test_run_host_async_steps_match_device_runs(torch_cuda):
         assert np.array_equal(y_host.numpy().view(np.uint16), ref[:M]), f"M={M}"
 
 
+@pytest.mark.parametrize("memory", ["pinned", "pinned_offset", "pageable"])
+def test_run_host_copies_for_every_kind_of_host_buffer(torch_cuda, memory):
+    """Pinned, 16-byte aligned buffers are copied by kernels through their device mapping (a
+    ragged byte count: M * N * 2 = 6006); a pinned buffer off the 16-byte grid, or pageable
+    memory, by copy-engine transfers.  Every path gives the device run's bits."""
+    torch = torch_cuda
+    case = synth.make_case("int4", "bf16", 32, True, 1001, 1024, 3, 23)
+    d = bsgemv.upload(case, "cuda")
+    a = np.ascontiguousarray(case.A).view(np.int16)
+
+    def host(shape_or_array, fill=None):
+        arr = shape_or_array if fill is None else np.full(shape_or_array, fill, dtype=np.int16)
+        if memory == "pageable":
+            return torch.from_numpy(np.array(arr))
+        if memory == "pinned":
+            return torch.from_numpy(np.array(arr)).pin_memory()
+        flat = torch.empty(arr.size + 1, dtype=torch.int16).pin_memory()[1:]  # 2 bytes off
+        flat.copy_(torch.from_numpy(np.array(arr)).reshape(-1))
+        return flat.view(arr.shape)
+
+    A_host = host(a)
+    y_host = host((3, case.N), fill=-1)
+    with bsgemv.Plan("int4", "bf16", 32, True, case.N, case.K, 4) as plan:
+        plan.run(d.A, d.W, d.scales, d.zp, d.y)
+        torch.cuda.synchronize()
+        ref = bsgemv.y_bits(d.y)
+        plan.run_host(A_host, d.W, d.scales, d.zp, y_host, M=3)
+        assert plan.device_status() == bsgemv.OK
+    assert np.array_equal(y_host.numpy().view(np.uint16), ref)
+
+
 def test_errors_on_device(torch_cuda):
     torch = torch_cuda
     case = synth.make_case("int4", "f16", 32, True, 128, 512, 4, 3)
