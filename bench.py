@@ -552,10 +552,10 @@ def run_ours(args):
            "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": e2e_steps,
            "api": f"bsgemv_run_host_async for each of the {L} calls of a step (pinned host A in, "
-                  "pinned host y out, through the plan's staging buffers: copy kernels reading and "
-                  "writing the pinned buffers through their device mapping), device-resident "
-                  "weights, the step replayed from a CUDA graph, one stream synchronisation per "
-                  "step"}
+                  "pinned host y out: a copy kernel reads A into the plan's staging buffer and "
+                  "the GEMV writes y, both through the pinned buffers' device mapping), "
+                  "device-resident weights, the step replayed from a CUDA graph, one stream "
+                  "synchronisation per step"}
 
     out = None
     if rank == 0:

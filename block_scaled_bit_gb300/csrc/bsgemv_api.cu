@@ -303,9 +303,10 @@ int run_host_impl(bsgemv_plan_t plan, const void* A_host, const void* W, const v
   void* dy = static_cast<char*>(plan->stage) + a_pad;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t a_call = size_t(M) * g.K * 2, y_call = size_t(M) * g.N * 2;
-  // Pinned host buffers (16-byte aligned) are copied by kernels through their device mapping:
-  // between the GEMV's kernels a copy kernel overlaps its start-up like they do, where a
-  // copy-engine transfer adds latency of its own.  Other host memory goes by the copy engines.
+  // Pinned host buffers (16-byte aligned) are used through their device mapping: A is copied
+  // into the staging buffer by a kernel (whose start-up overlaps the neighbouring kernels, where
+  // a copy-engine transfer adds latency of its own) and the GEMV writes y straight into the host
+  // buffer.  Other host memory goes by copy-engine transfers through the staging buffer.
   void* A_map = host_mapping(A_host);
   void* y_map = host_mapping(y_host);
   const bool by_kernel = A_map != nullptr && y_map != nullptr && aligned(A_map, 16) &&
@@ -315,13 +316,10 @@ int run_host_impl(bsgemv_plan_t plan, const void* A_host, const void* W, const v
   } else if (cudaMemcpyAsync(dA, A_host, a_call, cudaMemcpyHostToDevice, s) != cudaSuccess) {
     return BSGEMV_ERR_CUDA;
   }
-  rc = bsgemv_run(plan, dA, W, scales, zp, dy, M, stream);
+  rc = bsgemv_run(plan, dA, W, scales, zp, by_kernel ? y_map : dy, M, stream);
   if (rc != BSGEMV_OK) return rc;
-  if (by_kernel) {
-    if ((rc = bsg::launch_host_copy(y_map, dy, y_call, plan->sm_count, s)) != BSGEMV_OK) return rc;
-  } else if (cudaMemcpyAsync(y_host, dy, y_call, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+  if (!by_kernel && cudaMemcpyAsync(y_host, dy, y_call, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return BSGEMV_ERR_CUDA;
-  }
   if (!sync) return BSGEMV_OK;
   return cudaStreamSynchronize(s) == cudaSuccess ? BSGEMV_OK : BSGEMV_ERR_CUDA;
 }

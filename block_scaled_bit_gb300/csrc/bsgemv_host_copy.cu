@@ -1,9 +1,9 @@
 // bsgemv_host_copy.cu -- copies between pinned host memory and device memory by a kernel, for
 // bsgemv_run_host / bsgemv_run_host_async: the activations of a call into the plan's staging
-// buffer, its outputs back to the caller's host buffer.  A kernel in the stream instead of a
-// copy-engine transfer: consecutive kernels overlap their start-up through programmatic
-// dependent launch, while each copy-engine transfer between kernels costs a few microseconds of
-// its own latency.  The host buffer is read or written through its device mapping (pinned host
+// buffer (the GEMV writes the outputs into the host buffer itself).  A kernel in the stream
+// instead of a copy-engine transfer: consecutive kernels overlap their start-up through
+// programmatic dependent launch, while each copy-engine transfer between kernels costs a few
+// microseconds of its own latency.  The host buffer is read or written through its device mapping (pinned host
 // memory is addressable from the GPU under unified addressing).
 #include <cuda_runtime.h>
 

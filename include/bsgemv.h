@@ -155,9 +155,10 @@ int bsgemv_run_bias(bsgemv_plan_t plan, const void* A, const void* W, const void
  * call returns after the stream has finished (the host buffers are ready on return).  W,
  * scales and zp stay device pointers.  The staging buffer (max_M * (K + N) activation
  * elements) is allocated by the first call and freed by bsgemv_destroy.  When both host
- * buffers are pinned and 16-byte aligned, the two copies are small kernels that read and
- * write them through their device mapping (their start-up overlaps the neighbouring kernels
- * like the GEMV's own); otherwise they are copy-engine transfers (cudaMemcpyAsync).
+ * buffers are pinned and 16-byte aligned they are used through their device mapping: a small
+ * kernel copies A into the staging buffer (its start-up overlaps the neighbouring kernels like
+ * the GEMV's own) and the GEMV writes y straight into y_host; otherwise A and y go through the
+ * staging buffer by copy-engine transfers (cudaMemcpyAsync).
  */
 int bsgemv_run_host(bsgemv_plan_t plan, const void* A_host, const void* W, const void* scales,
                     const void* zp, void* y_host, int M, void* stream);
