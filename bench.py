@@ -706,7 +706,8 @@ def run_sweep(args):
                         "weight_copies": copies, "plan_max_M": plan.max_M,
                         "variant": "cuda_core" if plan.describe()["variant"] == 2 else "mma",
                         "autotuned": bool(args.autotune),
-                        "geometry": {k: plan.describe()[k] for k in ("ctas", "cluster", "stages")}}),
+                        "geometry": {k: plan.describe()[k] for k in ("rows_per_tile", "ctas", "cluster",
+                                                                    "stages", "ctas_per_sm")}}),
                           flush=True)
                     del g
             finally:

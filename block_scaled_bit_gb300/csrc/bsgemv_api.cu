@@ -421,16 +421,24 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
   }
   const bsg::Geometry& g = plan->geo;
 
-  // Candidates: the plan's automatic choice first, stream-K over the default grid and over
-  // 1 .. 4 CTAs per SM, and a thread-block cluster of each size 2 .. 8 per tile.  Candidates the
-  // plan cannot run (a cluster that does not fit) are skipped, and so are repeats of a geometry
-  // already measured.
+  // Candidates, in two rounds.  First the K split under each tile height (the automatic one,
+  // 64 and 128 rows): the plan's automatic choice first, stream-K over the default grid and
+  // over 1 .. 4 CTAs per SM, and a thread-block cluster of each size 2 .. 8 per tile.  Then the
+  // ring depth of the fastest of those: 2, 3, 4, 6, 8 and 12 stages, where the CTAs per SM stay
+  // as they were.  Candidates the plan cannot run (a cluster or a ring that does not fit, 128-row
+  // tiles in a plan for more than 16 rows) are skipped, and so are repeats of a geometry already
+  // measured.
   struct Cand {
-    int split, cluster, ctas;
+    int split, cluster, ctas, rows, stages;
   };
-  std::vector<Cand> cands = {{BSGEMV_SPLIT_AUTO, 0, 0}, {BSGEMV_SPLIT_STREAM_K, 0, 0}};
-  for (int k = 1; k <= 4; ++k) cands.push_back({BSGEMV_SPLIT_STREAM_K, 0, k * plan->sm_count});
-  for (int c = 2; c <= bsg::kMaxAutoCluster; ++c) cands.push_back({BSGEMV_SPLIT_CLUSTER, c, 0});
+  std::vector<Cand> cands;
+  for (int rows : {0, bsg::kBoxRows, bsg::kMaxRowsPerTile}) {
+    cands.push_back({BSGEMV_SPLIT_AUTO, 0, 0, rows, 0});
+    cands.push_back({BSGEMV_SPLIT_STREAM_K, 0, 0, rows, 0});
+    for (int k = 1; k <= 4; ++k) cands.push_back({BSGEMV_SPLIT_STREAM_K, 0, k * plan->sm_count, rows, 0});
+    for (int c = 2; c <= bsg::kMaxAutoCluster; ++c) cands.push_back({BSGEMV_SPLIT_CLUSTER, c, 0, rows, 0});
+  }
+  const int kRingDepths[] = {2, 3, 4, 6, 8, 12};
 
   // The regime the calls run in: back to back on one stream, each on weights that are not in L2.
   // The caller's weight, scales and zero points are copied R - 1 times (R copies >= 3x the L2,
@@ -470,32 +478,47 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
   if (ok) ok = cudaStreamSynchronize(ts) == cudaSuccess;
   rc = ok ? BSGEMV_OK : BSGEMV_ERR_CUDA;
 
-  const int keep_split = plan->split, keep_cluster = plan->cluster, keep_ctas = plan->ctas_override;
+  const Cand keep = {plan->split, plan->cluster, plan->ctas_override, plan->rows_override,
+                     plan->stages_override};
   float best_us = -1.f;
-  Cand best = {keep_split, keep_cluster, keep_ctas};
-  std::vector<std::pair<int, int>> seen;  // (cluster, ctas) of the geometries measured
+  Cand best = keep;
+  int best_per_sm = 0;
+  struct Key {
+    int rows, cluster, ctas, stages;
+    bool operator==(const Key& o) const {
+      return rows == o.rows && cluster == o.cluster && ctas == o.ctas && stages == o.stages;
+    }
+  };
+  std::vector<Key> seen;  // geometries measured
   const int calls = R * reps;
-  for (size_t ci = 0; rc == BSGEMV_OK && ci < cands.size(); ++ci) {
-    const Cand& c = cands[ci];
+  // Time candidate c (back to back, cold weights); a candidate that cannot run or repeats a
+  // measured geometry is skipped.  Keeps the fastest: another geometry must beat the automatic
+  // choice (measured first) by more than 1 %.
+  auto measure = [&](const Cand& c) {
     plan->split = c.split;
     plan->cluster = c.cluster;
     plan->ctas_override = c.ctas;
-    if (rebuild_geometry(plan) != BSGEMV_OK) continue;  // this candidate does not fit
-    const std::pair<int, int> key{plan->geo.pub.cluster, plan->geo.pub.ctas};
-    if (std::find(seen.begin(), seen.end(), key) != seen.end()) continue;
+    plan->rows_override = c.rows;
+    plan->stages_override = c.stages;
+    if (rebuild_geometry(plan) != BSGEMV_OK) return;  // this candidate does not fit
+    const bsgemv_geometry& pg = plan->geo.pub;
+    const Key key{pg.rows_per_tile, pg.cluster, pg.ctas, pg.stages};
+    if (std::find(seen.begin(), seen.end(), key) != seen.end()) return;
     seen.push_back(key);
     // one eager call first: kernel attributes (shared-memory size) are set outside the capture
-    if ((rc = prepare_params(plan, A, W, scales, zp, y, M)) != BSGEMV_OK) break;
-    if ((rc = launch(plan, ts)) != BSGEMV_OK) break;
+    if ((rc = prepare_params(plan, A, W, scales, zp, y, M)) != BSGEMV_OK) return;
+    if ((rc = launch(plan, ts)) != BSGEMV_OK) return;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     if (cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
       rc = BSGEMV_ERR_CUDA;
-      break;
+      return;
     }
+    // calls of M rows, alternating with calls of one row when M > 1: the geometry serves every
+    // M of the plan, and one tuned on its largest M alone can be slower on the smallest
     for (int i = 0; i < calls && rc == BSGEMV_OK; ++i) {
       const Ops& o = ops[i % R];
-      rc = prepare_params(plan, A, o.W, o.s, o.z, y, M);
+      rc = prepare_params(plan, A, o.W, o.s, o.z, y, (i & 1) ? 1 : M);
       if (rc == BSGEMV_OK) rc = launch(plan, ts);
     }
     const bool captured = cudaStreamEndCapture(ts, &graph) == cudaSuccess;
@@ -510,12 +533,30 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
       rc = BSGEMV_ERR_CUDA;
     if (exec) cudaGraphExecDestroy(exec);
     if (graph) cudaGraphDestroy(graph);
-    if (rc != BSGEMV_OK) break;
+    if (rc != BSGEMV_OK) return;
     const float us = ms * 1000.f / (2.f * calls);
-    // another geometry must beat the automatic choice (measured first) by more than 1 %
     if (best_us < 0.f || us < 0.99f * best_us) {
       best_us = us;
       best = c;
+      best_per_sm = pg.ctas_per_sm;
+    }
+  };
+  for (size_t ci = 0; rc == BSGEMV_OK && ci < cands.size(); ++ci) measure(cands[ci]);
+  if (rc == BSGEMV_OK && best_us >= 0.f) {
+    const Cand base = best;
+    const int base_per_sm = best_per_sm;
+    for (int st : kRingDepths) {
+      if (rc != BSGEMV_OK) break;
+      Cand c = base;
+      c.stages = st;
+      // a ring that only fits at fewer CTAs per SM changes the residency as well: not a candidate
+      plan->split = c.split;
+      plan->cluster = c.cluster;
+      plan->ctas_override = c.ctas;
+      plan->rows_override = c.rows;
+      plan->stages_override = c.stages;
+      if (rebuild_geometry(plan) != BSGEMV_OK || plan->geo.pub.ctas_per_sm != base_per_sm) continue;
+      measure(c);
     }
   }
   if (rc != BSGEMV_OK) cudaGetLastError();
@@ -527,10 +568,12 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
   // the fastest candidate (or, after an error, the settings the plan had)
-  if (rc != BSGEMV_OK || best_us < 0.f) best = {keep_split, keep_cluster, keep_ctas};
+  if (rc != BSGEMV_OK || best_us < 0.f) best = keep;
   plan->split = best.split;
   plan->cluster = best.cluster;
   plan->ctas_override = best.ctas;
+  plan->rows_override = best.rows;
+  plan->stages_override = best.stages;
   const int rc2 = rebuild_geometry(plan);
   if (rc != BSGEMV_OK) return rc;
   if (best_us < 0.f) return BSGEMV_ERR_UNSUPPORTED;

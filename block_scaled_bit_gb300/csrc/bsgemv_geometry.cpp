@@ -150,9 +150,10 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   // ends every call with a global last-arriver reduction; a cluster of C CTAs per tile gives each
   // ceil(spt / C) stages and reduces in the leader's shared memory (no atomics, no global
   // round trips).  Automatic choice: the cluster split with the fewest stages per CTA (the
-  // smallest such C) among clusters of at most 8 CTAs that divide the tile's stages evenly,
-  // when that is within one stage of stream-K's, the tiles x C CTAs fit one wave and the
-  // leader's reduction buffer leaves room for a ring of two stages.
+  // smallest such C) among clusters of at most 8 CTAs that divide the tile's stages evenly (or
+  // split it unevenly where that cuts the largest share by a quarter), when that is within one
+  // stage of stream-K's, the tiles x C CTAs fit one wave and the leader's reduction buffer
+  // leaves room for a ring of two stages.
   // Reduction buffer: per CTA of the cluster and consumer warp, the fragment lanes that hold
   // output columns below max_M (quad lanes t < red_tq) of each n8 tile.
   g->red_tq = (g->mt_max >= 2) ? 4 : static_cast<int>(std::min<int64_t>(4, ceil_div(max_M, 2)));
@@ -192,19 +193,27 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
   } else if (split == BSGEMV_SPLIT_CLUSTER || (split == BSGEMV_SPLIT_AUTO && ctas_override == 0)) {
     // (a CTA-count override describes a stream-K grid: it implies stream-K)
     const int64_t sk = ceil_div(total, std::min<int64_t>(total, slots));  // stream-K stages/CTA
-    int64_t best = -1;
+    int64_t best = -1, best_uneven = -1;
+    int C_uneven = 0;
     for (int c = 1; c <= kMaxCluster; ++c) {
       // (a size that does not fit does not end the search: a larger one can still fit, as a
       // share that lies inside one side box needs a single side slot)
       if (!cluster_fits(c)) continue;
-      // automatic: clusters of at most 8 CTAs splitting the tile evenly (measured on GB300:
-      // 16-CTA clusters and uneven shares were slower than stream-K)
-      if (split == BSGEMV_SPLIT_AUTO && (c > kMaxAutoCluster || spt % c != 0)) continue;
+      // automatic: clusters of at most 8 CTAs (measured on GB300: 16-CTA clusters were slower
+      // than stream-K)
+      if (split == BSGEMV_SPLIT_AUTO && c > kMaxAutoCluster) continue;
       const int64_t st = ceil_div(spt, c);
       // automatic: a one-stage share only while the grid stays within half the resident slots
       // (measured on GB300: FP8 4096 x 2048, 512 CTAs of one stage each, 8-17 % slower than 256
       // of two; FP8 512 x 2048 and NVFP4 2048 x 2048, 64 and 256 CTAs, fastest at one stage)
       if (split == BSGEMV_SPLIT_AUTO && st == 1 && tiles * c > slots / 2) continue;
+      if (split == BSGEMV_SPLIT_AUTO && spt % c != 0) {
+        if (best_uneven < 0 || st < best_uneven) {
+          best_uneven = st;
+          C_uneven = c;
+        }
+        continue;
+      }
       if (best < 0 || st < best) {
         best = st;
         C = c;
@@ -213,6 +222,19 @@ int geometry_for_tiles(int format, int block_size, int has_zp, int64_t N, int64_
     // taken when a CTA's share is within one stage of stream-K's, or at most 4 stages (stream-K
     // with a share of one or two stages has many partial sums per tile to add: measured slower)
     if (split == BSGEMV_SPLIT_AUTO && (C == 0 || best > std::max<int64_t>(sk + 1, 4))) C = 0;
+    // automatic: an even cluster split of 4 or more CTAs so taken gives way to a cluster whose
+    // CTAs' shares differ by one stage (the CTA with the extra stage sets the pace) only where
+    // that cuts the largest share by a quarter or more.  Measured on GB300: 4-CTA clusters of 4
+    // stages against 6-CTA clusters of 2-3, where 8-CTA clusters exceed the resident slots: int4
+    // 4096 x 4096 in plans for 16 rows 4-15 % faster at every M, FP8 2048 x 4096 in plans for 9
+    // rows 9 %; 2-CTA clusters of 4 stages against 3-CTA clusters of 2-3 (FP8 8192 x 2048, plans
+    // for 16 rows): up to 33 % slower.  Plans for up to 16 rows only: the residency of plans for
+    // 17 to 24 rows is chosen by the split it keeps, and was measured with even splits.
+    if (split == BSGEMV_SPLIT_AUTO && g->mt_max <= 2 && C >= 4 && C_uneven > 0 &&
+        best_uneven * 4 <= best * 3) {
+      best = best_uneven;
+      C = C_uneven;
+    }
     if (split == BSGEMV_SPLIT_CLUSTER && C == 0) return BSGEMV_ERR_UNSUPPORTED;
   }
   g->red_bytes = red_for(C);

@@ -215,12 +215,15 @@ int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows
 /*
  * Measure this plan's candidate geometries on the device and keep the fastest (the "online
  * profiler" that "[CUDA] Batched small-M GEMV for MatMulNBits (4-bit/8-bit)", review, proposes
- * instead of thresholds tuned on one GPU).  Candidates: the automatic choice, stream-K over the
- * default grid and over 1 .. 4 CTAs per SM, and thread-block clusters of 2 .. 8 CTAs per tile
- * (those that fit).  They are timed in the regime the calls run in: back to back on one stream
- * (a CUDA graph of `reps` (1 .. 100) rounds over R copies of W, scales and zp, R copies >= 3x
- * the L2, at most 8, so that no call finds its weights in L2), with the caller's A and y (y is
- * overwritten).  The copies, a private stream and the graphs are made and freed here.  Another
+ * instead of thresholds tuned on one GPU).  Candidates, in two rounds: first the K split under
+ * each tile height (the automatic one, 64 and 128 rows) -- the automatic choice, stream-K over the
+ * default grid and over 1 .. 4 CTAs per SM, and thread-block clusters of 2 .. 8 CTAs per tile --
+ * then the ring depth of the fastest (2, 3, 4, 6, 8 or 12 stages, at the same CTAs per SM);
+ * candidates the plan cannot run are skipped.  They are timed in the regime the calls run in:
+ * back to back on one stream (a CUDA graph of `reps` (1 .. 100) rounds over R copies of W,
+ * scales and zp, R copies >= 3x the L2, at most 8, so that no call finds its weights in L2),
+ * with the caller's A and y (y is overwritten), calls of M rows alternating with calls of one
+ * row when M > 1 (the chosen geometry serves every M of the plan).  The copies, a private stream and the graphs are made and freed here.  Another
  * geometry replaces the automatic choice only if it is more than 1 % faster.
  * Synchronises `stream` first and returns when done; not for use inside stream capture.
  * Afterwards every call of the plan runs the chosen geometry, so rows stay bit-identical across

@@ -227,6 +227,12 @@ def test_split_choice_on_the_configuration_shapes(L):
     assert split("int4", 32, False, 151936, 4096)[0] == 0    # 1187 tiles of 128 rows: stream-K
     # plans for max_M = 8: 8-CTA clusters no longer fit next to the activation ring, 4 do
     assert split("fp8", 128, False, 2048, 4096, 8) == (4, 4)  # 32 tiles x 16 stages
+    # plans for 16 rows (3 CTAs per SM): 8-CTA clusters exceed the 456 resident CTAs; a 6-CTA
+    # cluster of 2-3 stages per CTA cuts the largest share of the even 4-CTA split by a quarter
+    assert split("int4", 32, False, 4096, 4096, 16) == (6, 3)   # 64 tiles x 16 stages
+    assert split("int4", 32, False, 4096, 4096, 8) == (8, 2)    # 4 CTAs per SM: 8 fit
+    # a smaller cut keeps the even split (6 CTAs of 8 stages, not 7 of 7)
+    assert split("int4", 32, False, 4096, 12288, 16) == (6, 8)  # 64 tiles x 48 stages
     g = bsgemv.geometry_for("fp8", "f16", 128, False, 5120, 17408, 1, 152)
     assert g["ctas"] == 560                                  # 80 tiles x 7 CTAs
     assert split("nvfp4", 16, False, 248320, 2048)[0] == 0   # 1940 tiles of 128 rows: stream-K
