@@ -70,27 +70,37 @@ int query_device(int* dev, int* sms) {
   return BSGEMV_OK;
 }
 
-// (Re)allocate the workspace for the plan's current geometry; zeroed.
-int alloc_workspace(bsgemv_plan_s* p) {
-  const bsgemv_geometry& g = p->geo.pub;
+// The workspace for geometry `geo`, zeroed: the plan's own buffer while it is large enough,
+// else a new one, and the old one is freed only once the new one exists -- so that a failed
+// allocation leaves the plan with its previous geometry and workspace, still usable.  A failed
+// clear leaves the plan without a workspace (its calls return BSGEMV_ERR_CUDA) until a later
+// geometry change succeeds.
+int alloc_workspace(bsgemv_plan_s* p, const bsg::Geometry& geo) {
+  const bsgemv_geometry& g = geo.pub;
   const size_t partial_bytes =
-      size_t(g.ctas) * 2 * bsg::kConsumerWarps * p->geo.slot_floats * sizeof(float);
+      size_t(g.ctas) * 2 * bsg::kConsumerWarps * geo.slot_floats * sizeof(float);
   const size_t counter_bytes = size_t(g.tiles) * bsg::kConsumerWarps * sizeof(unsigned);
   const size_t need = partial_bytes + counter_bytes + 256;
   if (need > p->ws_bytes) {
-    if (p->ws) {
-      cudaDeviceSynchronize();
-      cudaFree(p->ws);
-      p->ws = nullptr;
-      p->ws_bytes = 0;
-    }
-    if (cudaMalloc(&p->ws, need) != cudaSuccess) {
+    void* fresh = nullptr;
+    if (cudaMalloc(&fresh, need) != cudaSuccess) {
       cudaGetLastError();
       return BSGEMV_ERR_CUDA;
     }
+    if (p->ws) {
+      cudaDeviceSynchronize();
+      cudaFree(p->ws);
+    }
+    p->ws = fresh;
     p->ws_bytes = need;
   }
-  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess) return BSGEMV_ERR_CUDA;
+  p->partials = nullptr;
+  p->counters = nullptr;
+  p->err = nullptr;
+  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return BSGEMV_ERR_CUDA;
+  }
   p->partials = static_cast<float*>(p->ws);
   p->counters = reinterpret_cast<unsigned*>(static_cast<char*>(p->ws) + partial_bytes);
   p->err = reinterpret_cast<unsigned*>(static_cast<char*>(p->ws) + partial_bytes + counter_bytes);
@@ -115,15 +125,17 @@ int rebuild_geometry(bsgemv_plan_s* p) {
                                max_M, p->sm_count, p->ctas_override, p->stages_override, p->split,
                                p->cluster, &rows[m - 1], m, tile_rows);
   if (rc != BSGEMV_OK) return rc;
-  // the side boxes' tensor maps are shaped by the tile's rows: encode them again
-  for (auto& e : p->maps) e.valid = false;
   if (p->variant_override == BSGEMV_VARIANT_CUDA_CORE) {
     geo.pub.variant = BSGEMV_VARIANT_CUDA_CORE;
     for (auto& r : rows) r.pub.variant = BSGEMV_VARIANT_CUDA_CORE;
   }
+  // the workspace first: the geometry is taken only once its workspace exists
+  if ((rc = alloc_workspace(p, geo)) != BSGEMV_OK) return rc;
+  // the side boxes' tensor maps are shaped by the tile's rows: encode them again
+  for (auto& e : p->maps) e.valid = false;
   p->geo = geo;
   p->rows.swap(rows);
-  return alloc_workspace(p);
+  return BSGEMV_OK;
 }
 
 // Fill p->params for this call.  The tensor maps are re-encoded only for a new (W, scales, zp).
@@ -169,6 +181,7 @@ int check_device(const bsgemv_plan_s* p) {
 int validate_run(const bsgemv_plan_s* p, const void* A, const void* W, const void* scales,
                  const void* zp, const void* y, int M) {
   if (p == nullptr) return BSGEMV_ERR_INVALID_ARG;
+  if (p->err == nullptr) return BSGEMV_ERR_CUDA;  // no workspace (a failed clear)
   const bsg::Geometry& g = p->geo;
   if (M < 1) return BSGEMV_ERR_INVALID_ARG;
   if (M > g.max_M) return BSGEMV_ERR_M_TOO_LARGE;
@@ -491,20 +504,17 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
   };
   std::vector<Key> seen;  // geometries measured
   const int calls = R * reps;
-  // Time candidate c (back to back, cold weights); a candidate that cannot run or repeats a
-  // measured geometry is skipped.  Keeps the fastest: another geometry must beat the automatic
-  // choice (measured first) by more than 1 %.
-  auto measure = [&](const Cand& c) {
+  // Put candidate c in place; false if the plan cannot run it.
+  auto apply = [&](const Cand& c) {
     plan->split = c.split;
     plan->cluster = c.cluster;
     plan->ctas_override = c.ctas;
     plan->rows_override = c.rows;
     plan->stages_override = c.stages;
-    if (rebuild_geometry(plan) != BSGEMV_OK) return;  // this candidate does not fit
-    const bsgemv_geometry& pg = plan->geo.pub;
-    const Key key{pg.rows_per_tile, pg.cluster, pg.ctas, pg.stages};
-    if (std::find(seen.begin(), seen.end(), key) != seen.end()) return;
-    seen.push_back(key);
+    return rebuild_geometry(plan) == BSGEMV_OK;
+  };
+  // Time the plan's current geometry (back to back, cold weights): µs per call in *us.
+  auto time_current = [&](float* us) {
     // one eager call first: kernel attributes (shared-memory size) are set outside the capture
     if ((rc = prepare_params(plan, A, W, scales, zp, y, M)) != BSGEMV_OK) return;
     if ((rc = launch(plan, ts)) != BSGEMV_OK) return;
@@ -533,8 +543,20 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
       rc = BSGEMV_ERR_CUDA;
     if (exec) cudaGraphExecDestroy(exec);
     if (graph) cudaGraphDestroy(graph);
+    *us = ms * 1000.f / (2.f * calls);
+  };
+  // Time candidate c; a candidate that cannot run or repeats a measured geometry is skipped.
+  // Keeps the fastest: another geometry must beat the automatic choice (measured first) by
+  // more than 1 %.
+  auto measure = [&](const Cand& c) {
+    if (!apply(c)) return;  // this candidate does not fit
+    const bsgemv_geometry& pg = plan->geo.pub;
+    const Key key{pg.rows_per_tile, pg.cluster, pg.ctas, pg.stages};
+    if (std::find(seen.begin(), seen.end(), key) != seen.end()) return;
+    seen.push_back(key);
+    float us = 0.f;
+    time_current(&us);
     if (rc != BSGEMV_OK) return;
-    const float us = ms * 1000.f / (2.f * calls);
     if (best_us < 0.f || us < 0.99f * best_us) {
       best_us = us;
       best = c;
@@ -550,14 +572,32 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
       Cand c = base;
       c.stages = st;
       // a ring that only fits at fewer CTAs per SM changes the residency as well: not a candidate
-      plan->split = c.split;
-      plan->cluster = c.cluster;
-      plan->ctas_override = c.ctas;
-      plan->rows_override = c.rows;
-      plan->stages_override = c.stages;
-      if (rebuild_geometry(plan) != BSGEMV_OK || plan->geo.pub.ctas_per_sm != base_per_sm) continue;
+      if (!apply(c) || plan->geo.pub.ctas_per_sm != base_per_sm) continue;
       measure(c);
     }
+  }
+  // Confirmation: a winner other than the automatic choice is timed again against it, in turn,
+  // twice each, and kept only if it is still more than 1 % faster (one timing of ~20 calls can
+  // be off by more than that: the first round once kept a ring 5 % slower on the NVFP4 lm_head).
+  const Cand& automatic = cands[0];
+  const bool other = best.split != automatic.split || best.cluster != automatic.cluster ||
+                     best.ctas != automatic.ctas || best.rows != automatic.rows ||
+                     best.stages != automatic.stages;
+  if (rc == BSGEMV_OK && best_us >= 0.f && other) {
+    float t_auto = 0.f, t_best = 0.f;
+    int pairs = 0;
+    for (int r = 0; r < 2 && rc == BSGEMV_OK; ++r) {
+      float ua = 0.f, ub = 0.f;
+      if (!apply(automatic)) break;
+      time_current(&ua);
+      if (rc != BSGEMV_OK || !apply(best)) break;
+      time_current(&ub);
+      if (rc != BSGEMV_OK) break;
+      t_auto += ua;
+      t_best += ub;
+      ++pairs;
+    }
+    if (rc == BSGEMV_OK && !(pairs == 2 && t_best < 0.99f * t_auto)) best = automatic;
   }
   if (rc != BSGEMV_OK) cudaGetLastError();
   if (ts) {
@@ -597,6 +637,7 @@ int bsgemv_device_status(bsgemv_plan_t plan, void* stream) {
   unsigned* err = nullptr;
   if (plan != nullptr) {
     err = plan->err;
+    if (err == nullptr) return BSGEMV_ERR_CUDA;  // no workspace (a failed clear)
   } else {
     const int rc = bsg::noalloc_error_word(&err);  // bsgemv_run_noalloc's, current device
     if (rc != BSGEMV_OK) return rc;

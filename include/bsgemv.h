@@ -223,8 +223,10 @@ int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows
  * back to back on one stream (a CUDA graph of `reps` (1 .. 100) rounds over R copies of W,
  * scales and zp, R copies >= 3x the L2, at most 8, so that no call finds its weights in L2),
  * with the caller's A and y (y is overwritten), calls of M rows alternating with calls of one
- * row when M > 1 (the chosen geometry serves every M of the plan).  The copies, a private stream and the graphs are made and freed here.  Another
- * geometry replaces the automatic choice only if it is more than 1 % faster.
+ * row when M > 1 (the chosen geometry serves every M of the plan).  The copies, a private
+ * stream and the graphs are made and freed here.  Another geometry replaces the automatic
+ * choice only if it is more than 1 % faster, in the search and again when the two are timed in
+ * turn, twice each, at the end.
  * Synchronises `stream` first and returns when done; not for use inside stream capture.
  * Afterwards every call of the plan runs the chosen geometry, so rows stay bit-identical across
  * M from then on (results may differ in the last bits from calls made before, as the
