@@ -513,10 +513,11 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
     plan->stages_override = c.stages;
     return rebuild_geometry(plan) == BSGEMV_OK;
   };
-  // Time the plan's current geometry (back to back, cold weights): µs per call in *us.
-  auto time_current = [&](float* us) {
+  // Time the plan's current geometry on calls of m rows (back to back, cold weights): µs per
+  // call in *us.
+  auto time_rows = [&](int m, float* us) {
     // one eager call first: kernel attributes (shared-memory size) are set outside the capture
-    if ((rc = prepare_params(plan, A, W, scales, zp, y, M)) != BSGEMV_OK) return;
+    if ((rc = prepare_params(plan, A, W, scales, zp, y, m)) != BSGEMV_OK) return;
     if ((rc = launch(plan, ts)) != BSGEMV_OK) return;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
@@ -524,11 +525,9 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
       rc = BSGEMV_ERR_CUDA;
       return;
     }
-    // calls of M rows, alternating with calls of one row when M > 1: the geometry serves every
-    // M of the plan, and one tuned on its largest M alone can be slower on the smallest
     for (int i = 0; i < calls && rc == BSGEMV_OK; ++i) {
       const Ops& o = ops[i % R];
-      rc = prepare_params(plan, A, o.W, o.s, o.z, y, (i & 1) ? 1 : M);
+      rc = prepare_params(plan, A, o.W, o.s, o.z, y, m);
       if (rc == BSGEMV_OK) rc = launch(plan, ts);
     }
     const bool captured = cudaStreamEndCapture(ts, &graph) == cudaSuccess;
@@ -544,6 +543,18 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
     if (exec) cudaGraphExecDestroy(exec);
     if (graph) cudaGraphDestroy(graph);
     *us = ms * 1000.f / (2.f * calls);
+  };
+  // The objective: calls of M rows plus, when M > 1, calls of one row, each timed in a graph of
+  // their own -- the geometry serves every M of the plan, and one tuned on its largest M alone
+  // can be slower on the smallest (calls of the two sizes alternating in one graph instead
+  // favour geometries whose ring is the same at every M: a ring fixed at 2 stages won there on
+  // the NVFP4 lm_head, 4 % slower than the automatic one at each M alone).
+  auto time_current = [&](float* us) {
+    time_rows(M, us);
+    if (rc != BSGEMV_OK || M == 1) return;
+    float u1 = 0.f;
+    time_rows(1, &u1);
+    *us += u1;
   };
   // Time candidate c; a candidate that cannot run or repeats a measured geometry is skipped.
   // Keeps the fastest: another geometry must beat the automatic choice (measured first) by
@@ -577,8 +588,8 @@ int bsgemv_plan_autotune(bsgemv_plan_t plan, const void* A, const void* W, const
     }
   }
   // Confirmation: a winner other than the automatic choice is timed again against it, in turn,
-  // twice each, and kept only if it is still more than 1 % faster (one timing of ~20 calls can
-  // be off by more than that: the first round once kept a ring 5 % slower on the NVFP4 lm_head).
+  // twice each, and kept only if it is still more than 1 % faster (one timing of a few tens of
+  // calls can be off by more than that).
   const Cand& automatic = cands[0];
   const bool other = best.split != automatic.split || best.cluster != automatic.cluster ||
                      best.ctas != automatic.ctas || best.rows != automatic.rows ||

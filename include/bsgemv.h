@@ -222,8 +222,8 @@ int bsgemv_plan_set_override(bsgemv_plan_t plan, int variant, int ctas, int rows
  * candidates the plan cannot run are skipped.  They are timed in the regime the calls run in:
  * back to back on one stream (a CUDA graph of `reps` (1 .. 100) rounds over R copies of W,
  * scales and zp, R copies >= 3x the L2, at most 8, so that no call finds its weights in L2),
- * with the caller's A and y (y is overwritten), calls of M rows alternating with calls of one
- * row when M > 1 (the chosen geometry serves every M of the plan).  The copies, a private
+ * with the caller's A and y (y is overwritten): calls of M rows plus, when M > 1, calls of one
+ * row in a graph of their own (the chosen geometry serves every M of the plan).  The copies, a private
  * stream and the graphs are made and freed here.  Another geometry replaces the automatic
  * choice only if it is more than 1 % faster, in the search and again when the two are timed in
  * turn, twice each, at the end.
