@@ -109,7 +109,8 @@ enum bsgemv_split {
   BSGEMV_SPLIT_AUTO = 0,      /* cluster split where its per-CTA work is within one stage of
                                  stream-K's, else stream-K */
   BSGEMV_SPLIT_STREAM_K = 1,  /* the tiles x stages space cut into equal ranges over all CTAs */
-  BSGEMV_SPLIT_CLUSTER = 2    /* each tile split evenly over the CTAs of one cluster */
+  BSGEMV_SPLIT_CLUSTER = 2    /* each tile split over the CTAs of one cluster, shares differing
+                                 by at most one stage */
 };
 
 /*

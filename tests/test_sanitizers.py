@@ -8,7 +8,10 @@ and run:
   row layout), the kernel parameters, and the C ABI's host-side error paths;
 - tests/sanitize/oracle_check.c with the oracle (oracle/bsgemv_oracle.c, without OpenMP): every
   format on small random problems, NaN codes included, and the dense GEMV.
-Both must exit 0 and print "ok" with no sanitizer report.  ("[CUDA] Pin FP8 GEMV residency for
+- tests/sanitize/plan_check.cpp with the same host sources linked against a fake CUDA runtime
+  (tests/sanitize/fake_cuda.cpp) instead of libcudart: the planned entry points end to end on a
+  fake device, failures of cudaMalloc and cudaMemset injected, every launch's pointers checked.
+All must exit 0 and print "ok" with no sanitizer report.  ("[CUDA] Pin FP8 GEMV residency for
 grids just past two blocks per SM", Tests: the host dispatch selectors are tested under UBSan.)
 """
 import os
@@ -55,6 +58,29 @@ def test_host_code_under_sanitizers(tmp_path):
     assert r.returncode == 0, r.stderr[-3000:]
     out = _run(exe, tmp_path)
     assert int(out.split()[1]) > 1000  # geometries checked
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
+def test_plans_on_a_fake_device_under_sanitizers(tmp_path):
+    """The planned entry points' host code linked against a fake CUDA runtime
+    (tests/sanitize/fake_cuda.cpp, no libcudart): plans, calls, a workspace allocation and a
+    clear that fail, the autotuner's choice and its confirmation, the host-buffer paths."""
+    csrc = os.path.join(ROOT, "block_scaled_bit_gb300", "csrc")
+    inc = ["-I", os.path.join(ROOT, "include"), "-I", os.path.join(CUDA, "include")]
+    objs = []
+    for src in ("bsgemv_geometry.cpp", "bsgemv_host.cpp", "bsgemv_api.cu"):
+        obj = str(tmp_path / (src + ".o"))
+        subprocess.run(["g++", "-std=c++17", "-x", "c++", *SAN, *inc, "-c", os.path.join(csrc, src),
+                        "-o", obj], check=True, capture_output=True, text=True)
+        objs.append(obj)
+    exe = str(tmp_path / "plan_check")
+    r = subprocess.run(["g++", "-std=c++17", *SAN, *inc,
+                        os.path.join(ROOT, "tests", "sanitize", "plan_check.cpp"),
+                        os.path.join(ROOT, "tests", "sanitize", "fake_cuda.cpp"), *objs,
+                        "-lpthread", "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    out = _run(exe, tmp_path)
+    assert int(out.split()[1]) > 100  # kernel launches checked
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
