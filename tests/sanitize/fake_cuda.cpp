@@ -69,7 +69,7 @@ using fake::g;
 extern "C" {
 
 cudaError_t cudaGetDevice(int* device) {
-  *device = 0;
+  *device = g.current_device;
   return cudaSuccess;
 }
 
@@ -258,7 +258,8 @@ int gemv(const KParams& k, int mt, int halves, int ctas, int smem) {
   const size_t yb = size_t(k.M) * k.N * 2;
   if (!fake::device_range(k.y, yb) && !fake::pinned_range(k.y, yb)) fake::violation("y unreachable");
   if (smem <= 0 || smem > 232448) fake::violation("shared memory out of range");
-  fake::Launch l{k.M, mt, halves, ctas, k.cluster, k.stages, k.A, k.y, k.partials};
+  if (k.bias && !fake::device_range(k.bias, size_t(k.N) * 2)) fake::violation("bias unreachable");
+  fake::Launch l{k.M, mt, halves, ctas, k.cluster, k.stages, k.A, k.y, k.partials, k.bias};
   fake::charge(l);
   return BSGEMV_OK;
 }

@@ -15,6 +15,7 @@ struct Launch {
   const void* A;
   const void* y;
   const void* partials;
+  const void* bias;
 };
 
 struct State {
@@ -22,6 +23,7 @@ struct State {
   int fail_malloc = 0;   // > 0: the fail_malloc-th cudaMalloc from now fails
   int fail_memset = 0;   // > 0: the fail_memset-th cudaMemset from now fails
   bool memset_broken = false;  // every cudaMemset fails
+  int current_device = 0;      // what cudaGetDevice reports (the fake device is 0)
   std::function<double(const Launch&)> cost;  // µs charged per launch (1 if unset)
   // observation
   long launches = 0, violations = 0, host_copies = 0, memcpy_calls = 0, maps_encoded = 0;

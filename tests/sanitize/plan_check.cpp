@@ -119,8 +119,34 @@ int main() {
   CHECK(run(p, b, 16) == BSGEMV_OK && g.launches == 3 && g.violations == 0);
   CHECK(g.last.ctas == 304 && g.last.cluster == 0);
   CHECK(bsgemv_device_status(p, nullptr) == BSGEMV_OK);
+
+  // splits and the bias epilogue: a forced split shows in the geometry and the launch; a bias
+  // reaches only the call that passes it; a call from another device is refused
+  CHECK(bsgemv_plan_set_split(p, BSGEMV_SPLIT_CLUSTER, 4) == BSGEMV_OK);
+  bsgemv_plan_describe(p, &cur);
+  CHECK(cur.cluster == 4 && cur.ctas == cur.tiles * 4);
+  CHECK(bsgemv_plan_set_split(p, BSGEMV_SPLIT_STREAM_K, 4) == BSGEMV_ERR_INVALID_ARG);
+  CHECK(bsgemv_plan_set_split(p, 7, 0) == BSGEMV_ERR_INVALID_ARG);
+  bsgemv_plan_describe(p, &g0);
+  CHECK(same(cur, g0));  // refused settings change nothing
+  void* bias = fake::device_alloc(kN * 2);
+  CHECK(bias != nullptr);
+  CHECK(bsgemv_run_bias(p, b.A, b.W, b.s, nullptr, bias, b.y, 3, nullptr) == BSGEMV_OK);
+  CHECK(g.last.bias == bias && g.last.cluster == 4 && g.last.M == 3);
+  CHECK(bsgemv_run_bias(p, b.A, b.W, b.s, nullptr, static_cast<char*>(bias) + 1, b.y, 3,
+                        nullptr) == BSGEMV_ERR_MISALIGNED);
+  CHECK(bsgemv_run_bias(p, b.A, b.W, b.s, nullptr, nullptr, b.y, 3, nullptr) ==
+        BSGEMV_ERR_INVALID_ARG);
+  CHECK(run(p, b, 3) == BSGEMV_OK && g.last.bias == nullptr);
+  g.current_device = 1;
+  const long before = g.launches;
+  CHECK(run(p, b, 3) == BSGEMV_ERR_WRONG_DEVICE && g.launches == before);
+  g.current_device = 0;
+  CHECK(bsgemv_plan_set_split(p, BSGEMV_SPLIT_AUTO, 0) == BSGEMV_OK);
+  CHECK(bsgemv_plan_set_override(p, 0, 0, 64, 0) == BSGEMV_OK);
   CHECK(bsgemv_destroy(p) == BSGEMV_OK);
-  CHECK(fake::live_allocations() == own);
+  CHECK(cudaFree(bias) == cudaSuccess);
+  CHECK(fake::live_allocations() == own && g.violations == 0);
 
   // 4. the autotuner: a clearly faster geometry is kept ...
   auto streamk304 = [](const fake::Launch& l) { return l.cluster == 0 && l.ctas == 304; };
